@@ -1,0 +1,203 @@
+"""CPU oracle for the TACO ASH+DS codec and the AGoQ FP8 gradient paths.
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the
+benchmark's CPU-baseline / reference leg may import this package.  The
+product library never calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``taco_oracle.c`` (plain scalar C, double
+precision); this module compiles it with gcc when needed and wraps it with
+numpy arrays.  See the C file's header for the page sections each function
+follows and for the readings taken where the pages are silent.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "taco_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+QMAX = 448.0
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, no CUDA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            lib.oracle_e4m3_decode.restype = ctypes.c_double
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [f32]
+            lib.oracle_fwht.restype = None
+            lib.oracle_fwht.argtypes = [P, i32]
+            lib.oracle_compress.argtypes = [P, i64, i64, i32, f32, f32, P, P, P]
+            lib.oracle_compress_f64.argtypes = [P, i64, i64, i32, f32, f32, P, P, P]
+            lib.oracle_decompress.argtypes = [P, P, P, i64, i64, i32, P]
+            lib.oracle_reduce_shards.argtypes = [i32, P, P, P, i64, i64, i32, f32, f32, P, P, P]
+            lib.oracle_agoq_accumulate.argtypes = [P, P, P, i64, i32]
+            lib.oracle_agoq_reduce.argtypes = [i32, P, P, i64, i32, P, P]
+            lib.oracle_int8_roundtrip.argtypes = [P, i64, i64, i32, P]
+            for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
+                      "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
+                      "oracle_int8_roundtrip"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise ValueError("oracle: invalid shape or argument")
+
+
+def _ptr_array(arrs):
+    return (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+
+
+# ------------------------------------------------------------------ E4M3 --
+
+def e4m3_decode(code: int) -> float:
+    return _load().oracle_e4m3_decode(int(code) & 0xFF)
+
+
+def e4m3_decode_table() -> np.ndarray:
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
+    lib = _load()
+    v = np.asarray(v, dtype=np.float32).reshape(-1)
+    return np.array([lib.oracle_e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+
+
+def fwht(v: np.ndarray) -> np.ndarray:
+    """Unnormalised Sylvester-order Walsh-Hadamard transform of each row."""
+    out = np.array(v, dtype=np.float64, copy=True, order="C")
+    n = out.shape[-1]
+    flat = out.reshape(-1, n)
+    lib = _load()
+    for r in range(flat.shape[0]):
+        lib.oracle_fwht(flat[r].ctypes.data_as(ctypes.c_void_p), n)
+    return out
+
+
+# ------------------------------------------------------------ TACO codec --
+
+def compress(x_bf16: np.ndarray, block: int, e_target: float = 1.0, eps: float = 1e-12):
+    """bf16 bits [rows, d] -> (codes uint8 [rows, d], alpha f32 [rows, d/block], scale f32)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, d = x.shape
+    codes = np.empty((rows, d), dtype=np.uint8)
+    alpha = np.empty((rows, d // block), dtype=np.float32)
+    scale = np.empty((rows, d // block), dtype=np.float32)
+    _check(_load().oracle_compress(_ptr(x), rows, d, block, e_target, eps, _ptr(codes),
+                                   _ptr(alpha), _ptr(scale)))
+    return codes, alpha, scale
+
+
+def compress_f64(x: np.ndarray, block: int, e_target: float = 1.0, eps: float = 1e-12):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, d = x.shape
+    codes = np.empty((rows, d), dtype=np.uint8)
+    alpha = np.empty((rows, d // block), dtype=np.float32)
+    scale = np.empty((rows, d // block), dtype=np.float32)
+    _check(_load().oracle_compress_f64(_ptr(x), rows, d, block, e_target, eps, _ptr(codes),
+                                       _ptr(alpha), _ptr(scale)))
+    return codes, alpha, scale
+
+
+def decompress(codes: np.ndarray, alpha: np.ndarray, scale: np.ndarray, block: int) -> np.ndarray:
+    """-> float64 reconstruction [rows, d]."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    a = np.ascontiguousarray(alpha, dtype=np.float32)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    rows, d = c.shape
+    assert a.size == rows * d // block and s.size == a.size
+    out = np.empty((rows, d), dtype=np.float64)
+    _check(_load().oracle_decompress(_ptr(c), _ptr(a), _ptr(s), rows, d, block, _ptr(out)))
+    return out
+
+
+def reduce_shards(codes, alphas, scales, block: int, e_target: float = 1.0, eps: float = 1e-12):
+    """P compressed shards (lists) -> compressed sum (codes, alpha, scale)."""
+    cs = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes]
+    As = [np.ascontiguousarray(a, dtype=np.float32) for a in alphas]
+    Ss = [np.ascontiguousarray(s, dtype=np.float32) for s in scales]
+    rows, d = cs[0].shape
+    for c, a, s in zip(cs, As, Ss):
+        assert c.shape == (rows, d) and a.size == rows * d // block and s.size == a.size
+    out_c = np.empty((rows, d), dtype=np.uint8)
+    out_a = np.empty((rows, d // block), dtype=np.float32)
+    out_s = np.empty((rows, d // block), dtype=np.float32)
+    _check(_load().oracle_reduce_shards(len(cs), _ptr_array(cs), _ptr_array(As), _ptr_array(Ss),
+                                        rows, d, block, e_target, eps, _ptr(out_c), _ptr(out_a),
+                                        _ptr(out_s)))
+    return out_c, out_a, out_s
+
+
+# ------------------------------------------------------------------ AGoQ --
+
+def agoq_accumulate(codes: np.ndarray, scale: np.ndarray, grad_bf16: np.ndarray, block: int = 128):
+    """Returns the new (codes, scale); the inputs are not modified."""
+    c = np.array(codes, dtype=np.uint8, copy=True).reshape(-1)
+    s = np.array(scale, dtype=np.float32, copy=True).reshape(-1)
+    g = np.ascontiguousarray(grad_bf16, dtype=np.uint16).reshape(-1)
+    assert g.size == c.size and s.size == c.size // block
+    _check(_load().oracle_agoq_accumulate(_ptr(c), _ptr(s), _ptr(g), c.size, block))
+    return c, s
+
+
+def agoq_reduce(codes, scales, block: int = 128):
+    cs = [np.ascontiguousarray(c, dtype=np.uint8).reshape(-1) for c in codes]
+    ss = [np.ascontiguousarray(s, dtype=np.float32).reshape(-1) for s in scales]
+    n = cs[0].size
+    out_c = np.empty(n, dtype=np.uint8)
+    out_s = np.empty(n // block, dtype=np.float32)
+    _check(_load().oracle_agoq_reduce(len(cs), _ptr_array(cs), _ptr_array(ss), n, block,
+                                      _ptr(out_c), _ptr(out_s)))
+    return out_c, out_s
+
+
+def agoq_dequantise(codes: np.ndarray, scale: np.ndarray, block: int = 128) -> np.ndarray:
+    table = e4m3_decode_table()
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1, block)
+    return (table[c] / np.asarray(scale, dtype=np.float64).reshape(-1, 1)).reshape(-1)
+
+
+# --------------------------------------------------------- INT8 baseline --
+
+def int8_roundtrip(x_bf16: np.ndarray, block: int) -> np.ndarray:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, d = x.shape
+    out = np.empty((rows, d), dtype=np.float64)
+    _check(_load().oracle_int8_roundtrip(_ptr(x), rows, d, block, _ptr(out)))
+    return out
