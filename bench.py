@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Benchmark of the TACO ASH+DS FP8 codec hot path on GB300.
+
+One step = one pass of the two-shot AllReduce's on-GPU path over the
+GPT-6.7B-shaped workload (P = 4 shards of bf16 [8192, 4096], block 128):
+fused compress of all four shards (one launch), shard reduce (FP8 -> FP32
+sum -> requantise, one launch), decompress of the result to fp32 (one
+launch).  Inputs are resident in HBM before the timed region and larger than
+L2 (268 MB of bf16 per step), so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is algorithmic HBM bytes moved per
+step (reads + writes of the three kernels) x steps x ranks / max-over-ranks
+time, in GB/s.  Under torchrun each rank runs its own replica on its own
+shards (weak scaling, no data-path collective).
+
+``--impl reference`` times the CPU oracle (the plain reference
+implementation of the method) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ASH+DS FP8 compress/decompress/reduce GB/s and % of GB300 HBM roofline"
+HEADLINE = "gpt6.7b_p4x8192x4096_n128"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csrc", f)
+                  for f in ("codec_kernels.cu", "device_utils.cuh")]
+
+
+def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4) -> dict:
+    """Bytes each kernel must move at minimum, per step."""
+    nb = n // block
+    return {
+        "compress": P * (2 * n + n + 8 * nb),        # bf16 in; codes + alpha + s out
+        "reduce": P * (n + 8 * nb) + (n + 8 * nb),    # P compressed shards in; one out
+        "decompress": (n + 8 * nb) + out_bytes * n,   # codes + scalars in; fp32 out
+    }
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per compress launch from the committed ncu summary, or None
+    once the kernel source has changed since those counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("source_digest") == kernel_source_digest():
+            return t.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, interval_ms: int = 50):
+        self.proc = None
+        self.interval_ms = interval_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": n}
+
+
+def make_inputs(rank: int):
+    from fp8_communication_compression_gb300 import workloads as W
+
+    w = W.WORKLOADS[HEADLINE]
+    shards = []
+    for p in range(w["shards"]):
+        seed = w["seeds"][p] + 1000 * rank
+        shards.append(W.tp_activation(seed, w["rows"], w["d"], channel_scale=w["channel_scale"],
+                                      spikes=w["spikes"], block=w["block"]))
+    return w, np.stack(shards)
+
+
+def cpu_baseline(bits: np.ndarray, w: dict, sample_rows: int) -> dict:
+    """The oracle, as it stands, on the first ``sample_rows`` rows of every
+    shard: compress each shard, reduce, decompress.  Single-threaded."""
+    import oracle
+
+    P, block = bits.shape[0], w["block"]
+    sub = [np.ascontiguousarray(bits[p, :sample_rows]) for p in range(P)]
+    n = sample_rows * w["d"]
+    t0 = time.perf_counter()
+    comp = [oracle.compress(s, block) for s in sub]
+    rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
+    oracle.decompress(rc, ra, rs, block)
+    dt = time.perf_counter() - t0
+    total = sum(algorithmic_bytes(P, n, block).values())
+    return {"value": total / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {sample_rows} of {w['rows']} rows of each of the {P} shards "
+                      f"({P * n} elements compressed, {n} reduced and decompressed), "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    """The reference arm: the CPU oracle timed on bounded samples."""
+    if rank != 0:
+        return
+    from fp8_communication_compression_gb300 import workloads as W
+    import oracle
+
+    oracle.build()
+    w = W.WORKLOADS[HEADLINE]
+    P, block, rows_s = w["shards"], w["block"], args.ref_rows
+    bits = np.stack([W.tp_activation(w["seeds"][p], rows_s, w["d"], channel_scale=True, block=block)
+                     for p in range(P)])
+    n = rows_s * w["d"]
+    step_bytes = sum(algorithmic_bytes(P, n, block).values())
+
+    def step():
+        comp = [oracle.compress(bits[p], block) for p in range(P)]
+        rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
+        oracle.decompress(rc, ra, rs, block)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / 1e9
+    sample = (f"each step: {rows_s} of {w['rows']} rows of each of the {P} shards "
+              f"(compress {P * n}, reduce and decompress {n} elements), single-threaded")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "P": P, "rows": w["rows"], "d": w["d"], "block": block,
+                   "sample_rows": rows_s},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows per shard")
+    ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+
+    from fp8_communication_compression_gb300 import api
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w, bits = make_inputs(rank)
+    P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
+    n = rows * d
+    nbytes = algorithmic_bytes(P, n, block)
+    step_bytes = sum(nbytes.values())
+
+    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    path = api.TwoShotLocal(P, rows, d, block)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        path.run(x)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
+    time.sleep(0.2 if clocks else 0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(K):
+        e = ev[k]
+        e[0].record(stream)
+        path.compress(x)
+        e[1].record(stream)
+        path.reduce()
+        e[2].record(stream)
+        path.decompress()
+        e[3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    # keep the same work running until the clock sampler has a few samples
+    extra = 0
+    t_region = elapsed_ms / 1e3
+    while clocks and t_region < 1.0:
+        path.run(x)
+        extra += 1
+        if extra % 200 == 0:
+            torch.cuda.synchronize()
+            t_region += 200 * elapsed_ms / K / 1e3
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+
+    if dist:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+           for i, name in enumerate(("compress", "reduce", "decompress"))}
+
+    # end to end through the public API with pinned host buffers
+    h_in = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
+    h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+    h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
+    x2 = torch.empty_like(x)
+    for _ in range(3):
+        path.run_host(h_in, h_out, x2)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        path.run_host(h_in, h_out, x2)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    flags = api.taco_device_error(clear=True)
+
+    if rank == 0:
+        peak, peak_src = hbm_peak()
+        value = step_bytes * K * world / (elapsed_ms / 1e3) / 1e9
+        kern = {}
+        for name in ("compress", "reduce", "decompress"):
+            gbs = nbytes[name] / (per[name] / 1e3) / 1e9
+            kern[name] = {"us_per_launch": per[name] * 1e3, "algorithmic_bytes": nbytes[name],
+                          "gbs": gbs, "frac_of_peak": gbs / peak}
+        achieved = kern["compress"]["gbs"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": HEADLINE, "P": P, "rows": rows, "d": d, "block": block,
+                       "bytes_per_step": step_bytes,
+                       "input_bf16_bytes_per_step": 2 * P * n,
+                       "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": f"taco_compress_kernel<{block}>",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": committed_traffic(), "peak_source": peak_src},
+            "kernels": kern,
+            "step_frac_of_peak": value / world / peak,
+            "e2e": {"value": step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
+                    "api": "TwoShotLocal.run_host (pinned host in/out)"},
+            "gpu_launches": 3 * K,
+            "clocks": clk,
+            "watchdog_flags": flags,
+        }
+        if clk:
+            line["clocks"]["window"] = (f"timed region plus {extra} further identical steps"
+                                        if extra else "timed region")
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(bits, w, args.cpu_rows)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,13 @@
+"""GB300-native (sm_103a) FP8 communication compression.
+
+TACO's fused ASH + DS FP8 block compressor for tensor-parallel intermediate
+tensors, its inverse, the local reduce of the two-shot AllReduce, and AGoQ's
+FP8 gradient accumulation and reduce, as a C-ABI library (libtaco.so,
+include/taco.h) with a thin Python binding.
+"""
+
+from .api import (TwoShotLocal, agoq_fp8_accumulate, agoq_reduce_shards, taco_compress,
+                  taco_decompress, taco_device_error, taco_reduce_shards)
+
+__all__ = ["taco_compress", "taco_decompress", "taco_reduce_shards", "agoq_fp8_accumulate",
+           "agoq_reduce_shards", "taco_device_error", "TwoShotLocal"]

@@ -1,0 +1,221 @@
+"""Python binding of the C ABI, with the same names.
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, outputs are allocated with torch when the caller passes none,
+and the raw device pointers plus the current CUDA stream are handed to
+libtaco.so.  Every step of the codec runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import torch
+
+from . import _lib
+
+E_TARGET = 1.0
+EPS = 1e-12
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, numel: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+_U8 = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _shape2(x: torch.Tensor):
+    if x.dim() < 1:
+        raise ValueError("tensor must have at least one dimension")
+    d = x.shape[-1]
+    return x.numel() // d if d else 0, d
+
+
+def taco_compress(x: torch.Tensor, block: int = 128, e_target: float = E_TARGET, eps: float = EPS,
+                  codes: torch.Tensor | None = None, alpha: torch.Tensor | None = None,
+                  scale: torch.Tensor | None = None, stream=None):
+    """bf16 [..., d] -> (codes uint8 [..., d], alpha fp32 [nb], scale fp32 [nb])."""
+    _need(x, "x", _BF16)
+    rows, d = _shape2(x)
+    nb = rows * d // block if block else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if alpha is None:
+        alpha = torch.empty(nb, dtype=torch.float32, device=x.device)
+    if scale is None:
+        scale = torch.empty(nb, dtype=torch.float32, device=x.device)
+    _need(codes, "codes", _U8, x.numel())
+    _need(alpha, "alpha", (torch.float32,))
+    _need(scale, "scale", (torch.float32,))
+    st = _lib.load().taco_compress(x.data_ptr(), rows, d, block, e_target, eps, codes.data_ptr(),
+                                   alpha.data_ptr(), scale.data_ptr(), _stream_handle(stream))
+    _lib.check("taco_compress", st)
+    return codes, alpha, scale
+
+
+def taco_decompress(codes: torch.Tensor, alpha: torch.Tensor, scale: torch.Tensor, block: int = 128,
+                    out_dtype: torch.dtype = torch.float32, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """(codes [..., d], alpha, scale) -> reconstruction [..., d] in fp32 or bf16."""
+    _need(codes, "codes", _U8)
+    _need(alpha, "alpha", (torch.float32,))
+    _need(scale, "scale", (torch.float32,))
+    rows, d = _shape2(codes)
+    if out is None:
+        out = torch.empty(codes.shape, dtype=out_dtype, device=codes.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), codes.numel())
+    st = _lib.load().taco_decompress(codes.data_ptr(), alpha.data_ptr(), scale.data_ptr(), rows, d,
+                                     block, out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                     _stream_handle(stream))
+    _lib.check("taco_decompress", st)
+    return out
+
+
+def taco_reduce_shards(codes: Sequence[torch.Tensor], alpha: Sequence[torch.Tensor],
+                       scale: Sequence[torch.Tensor], block: int = 128, e_target: float = E_TARGET,
+                       eps: float = EPS, out_codes: torch.Tensor | None = None,
+                       out_alpha: torch.Tensor | None = None, out_scale: torch.Tensor | None = None,
+                       stream=None):
+    """Compressed sum of P compressed shards (two-shot local reduce)."""
+    P = len(codes)
+    if not (len(alpha) == P and len(scale) == P) or P == 0:
+        raise ValueError("codes, alpha and scale must be non-empty lists of equal length")
+    for p in range(P):
+        _need(codes[p], f"codes[{p}]", _U8, codes[0].numel())
+        _need(alpha[p], f"alpha[{p}]", (torch.float32,))
+        _need(scale[p], f"scale[{p}]", (torch.float32,))
+    rows, d = _shape2(codes[0])
+    dev = codes[0].device
+    if out_codes is None:
+        out_codes = torch.empty(codes[0].shape, dtype=torch.uint8, device=dev)
+    if out_alpha is None:
+        out_alpha = torch.empty_like(alpha[0])
+    if out_scale is None:
+        out_scale = torch.empty_like(scale[0])
+    cp, _k1 = _lib.ptr_array([c.data_ptr() for c in codes])
+    ap, _k2 = _lib.ptr_array([a.data_ptr() for a in alpha])
+    sp, _k3 = _lib.ptr_array([s.data_ptr() for s in scale])
+    st = _lib.load().taco_reduce_shards(P, cp, ap, sp, rows, d, block, e_target, eps,
+                                        out_codes.data_ptr(), out_alpha.data_ptr(),
+                                        out_scale.data_ptr(), _stream_handle(stream))
+    _lib.check("taco_reduce_shards", st)
+    return out_codes, out_alpha, out_scale
+
+
+def agoq_fp8_accumulate(main_codes: torch.Tensor, main_scale: torch.Tensor, grad: torch.Tensor,
+                        block: int = 128, stream=None):
+    """In place: main <- requantise(dequantise(main) + grad)."""
+    _need(main_codes, "main_codes", _U8)
+    _need(main_scale, "main_scale", (torch.float32,))
+    _need(grad, "grad", _BF16, main_codes.numel())
+    st = _lib.load().agoq_fp8_accumulate(main_codes.data_ptr(), main_scale.data_ptr(), grad.data_ptr(),
+                                         main_codes.numel(), block, _stream_handle(stream))
+    _lib.check("agoq_fp8_accumulate", st)
+    return main_codes, main_scale
+
+
+def agoq_reduce_shards(codes: Sequence[torch.Tensor], scale: Sequence[torch.Tensor], block: int = 128,
+                       out_codes: torch.Tensor | None = None, out_scale: torch.Tensor | None = None,
+                       stream=None):
+    P = len(codes)
+    if len(scale) != P or P == 0:
+        raise ValueError("codes and scale must be non-empty lists of equal length")
+    n = codes[0].numel()
+    for p in range(P):
+        _need(codes[p], f"codes[{p}]", _U8, n)
+        _need(scale[p], f"scale[{p}]", (torch.float32,))
+    if out_codes is None:
+        out_codes = torch.empty(n, dtype=torch.uint8, device=codes[0].device)
+    if out_scale is None:
+        out_scale = torch.empty(n // block, dtype=torch.float32, device=codes[0].device)
+    cp, _k1 = _lib.ptr_array([c.data_ptr() for c in codes])
+    sp, _k2 = _lib.ptr_array([s.data_ptr() for s in scale])
+    st = _lib.load().agoq_reduce_shards(P, cp, sp, n, block, out_codes.data_ptr(), out_scale.data_ptr(),
+                                        _stream_handle(stream))
+    _lib.check("agoq_reduce_shards", st)
+    return out_codes, out_scale
+
+
+def taco_device_error(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))
+    return int(v.value)
+
+
+class TwoShotLocal:
+    """The two-shot AllReduce's on-GPU path for P shards of [rows, d]:
+    compress all shards in one call, reduce them, decompress the result.
+    Buffers are allocated once; ``run`` only launches the three kernels."""
+
+    def __init__(self, P: int, rows: int, d: int, block: int = 128, device="cuda",
+                 e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32):
+        self.P, self.rows, self.d, self.block = P, rows, d, block
+        self.e_target, self.eps = e_target, eps
+        nb = rows * d // block
+        self.codes = torch.empty((P, rows, d), dtype=torch.uint8, device=device)
+        self.alpha = torch.empty((P, nb), dtype=torch.float32, device=device)
+        self.scale = torch.empty((P, nb), dtype=torch.float32, device=device)
+        self.r_codes = torch.empty((rows, d), dtype=torch.uint8, device=device)
+        self.r_alpha = torch.empty(nb, dtype=torch.float32, device=device)
+        self.r_scale = torch.empty(nb, dtype=torch.float32, device=device)
+        self.out = torch.empty((rows, d), dtype=out_dtype, device=device)
+        self._shard_codes = list(self.codes)
+        self._shard_alpha = list(self.alpha)
+        self._shard_scale = list(self.scale)
+
+    def bytes_per_step(self) -> dict:
+        n = self.rows * self.d
+        nb = n // self.block
+        return {
+            "compress": self.P * (2 * n + n + 8 * nb),
+            "reduce": self.P * (n + 8 * nb) + n + 8 * nb,
+            "decompress": n + 8 * nb + n * self.out.element_size(),
+        }
+
+    def compress(self, x: torch.Tensor, stream=None):
+        return taco_compress(x, self.block, self.e_target, self.eps, self.codes, self.alpha,
+                             self.scale, stream=stream)
+
+    def reduce(self, stream=None):
+        return taco_reduce_shards(self._shard_codes, self._shard_alpha, self._shard_scale, self.block,
+                                  self.e_target, self.eps, self.r_codes, self.r_alpha, self.r_scale,
+                                  stream=stream)
+
+    def decompress(self, stream=None) -> torch.Tensor:
+        return taco_decompress(self.r_codes, self.r_alpha, self.r_scale, self.block, out=self.out,
+                               stream=stream)
+
+    def run(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        """x: bf16 [P, rows, d] on the device -> fp32/bf16 [rows, d]."""
+        self.compress(x, stream)
+        self.reduce(stream)
+        return self.decompress(stream)
+
+    def run_host(self, x_host: torch.Tensor, out_host: torch.Tensor, x_dev: torch.Tensor,
+                 stream=None) -> torch.Tensor:
+        """Host-buffer variant: copies the pinned bf16 input [P, rows, d] to
+        ``x_dev``, runs the path, and copies the result into the pinned
+        ``out_host``, all asynchronously on the stream."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            x_dev.copy_(x_host, non_blocking=True)
+            self.run(x_dev, s)
+            out_host.copy_(self.out, non_blocking=True)
+        return out_host

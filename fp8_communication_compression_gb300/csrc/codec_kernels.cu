@@ -1,0 +1,557 @@
+// Fused ASH + DS FP8 compressor and its inverse for sm_103a.
+//
+// TACO (gist.science summary of arXiv 2604.24088), 2.B.1 - 2.B.3: per block,
+// energy -> adaptive pre-scale alpha -> orthogonal Hadamard rotation ->
+// post-scale s keeping values inside +-448 -> E4M3 codes, fused into one
+// kernel with no intermediate global-memory round trip; decompression
+// inverts the rotation with both scales.
+//
+// Design (GB300):
+//  * The tensor is viewed as nrows rows of 128 elements.  One consumer
+//    thread owns one row in registers, so the 7 butterfly stages of a
+//    128-point Walsh-Hadamard transform are plain register FADDs with no
+//    shuffles.  A 256-element block spans two adjacent lanes and needs one
+//    extra __shfl_xor stage.
+//  * Every warp is an independent pipeline over 32-row tiles: lane 0 keeps
+//    three TMA loads (cp.async.bulk.tensor, 128-byte swizzle) in flight
+//    into the warp's own ring of mbarrier-guarded stages and refills a
+//    stage as soon as the warp has read it.  The swizzle makes each lane's
+//    row reads bank-conflict free.  No producer warp and no cross-warp
+//    barrier: 8 warps per CTA leave 255 registers per thread.
+//  * Each warp writes its 32 output rows into its own swizzled staging
+//    buffer and stores them with TMA tensor stores.
+//  * Persistent grid: one CTA per SM, warp tiles handed out round-robin.
+//  * Every mbarrier wait is time-limited (device_utils.cuh); a wait that
+//    runs out sets a flag readable through taco_device_error().
+
+#include <cfloat>
+#include <mutex>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace taco {
+
+__device__ unsigned int g_codec_error;
+
+constexpr int kWarps = 8;              // warps per CTA, each an independent pipeline
+constexpr int kThreads = kWarps * 32;
+constexpr int kWarpRows = 32;          // rows per warp tile, one per lane
+constexpr int kStages = 3;             // TMA ring depth per warp
+constexpr uint32_t kErrCompress = 1u;
+constexpr uint32_t kErrDecompress = 2u;
+
+// compress, per warp: kStages x (two 128-byte-wide halves of 32 rows of
+// bf16) + 32 rows x 128 bytes of codes
+constexpr uint32_t kCHalfBytes = kWarpRows * 128;           // 4 KB
+constexpr uint32_t kCStageBytes = 2 * kCHalfBytes;          // 8 KB
+constexpr uint32_t kCOutBytes = kWarpRows * 128;            // 4 KB
+constexpr uint32_t kCWarpBytes = kStages * kCStageBytes + kCOutBytes;  // 28 KB
+// decompress, per warp: kStages x 32 rows x 128 codes + 32 rows x 512 bytes
+constexpr uint32_t kDStageBytes = kWarpRows * 128;          // 4 KB
+constexpr uint32_t kDOutBytes = kWarpRows * 512;            // 16 KB
+constexpr uint32_t kDWarpBytes = kStages * kDStageBytes + kDOutBytes;  // 28 KB
+static_assert(kCWarpBytes % 1024 == 0 && kDWarpBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+constexpr uint32_t kBarBytes = kWarps * kStages * 8;
+constexpr uint32_t kCSmemBytes = 1024 + kWarps * kCWarpBytes + kBarBytes;
+constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kBarBytes;
+
+template <int NB> struct BlockConst;
+template <> struct BlockConst<128> {
+    static constexpr float c = 0.0883883461356163f;  // fp32(1/sqrt(128))
+    static constexpr float inv_n = 1.0f / 128.0f;
+};
+template <> struct BlockConst<256> {
+    static constexpr float c = 0.0625f;              // 1/sqrt(256), exact
+    static constexpr float inv_n = 1.0f / 256.0f;
+};
+
+// Unnormalised Sylvester-order Walsh-Hadamard transform of 128 registers:
+// for h = 1, 2, ..., 64, pairs (i, i + h) become (a + b, a - b).
+__device__ __forceinline__ void fwht128(float (&v)[128])
+{
+#pragma unroll
+    for (int h = 1; h < 128; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+            if ((i & h) == 0) {
+                const float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+        }
+    }
+}
+
+// Last stage of a 256-point transform across a lane pair: the even lane
+// holds elements 0..127 (a), the odd lane 128..255 (b); even gets a + b,
+// odd gets a - b.
+__device__ __forceinline__ void fwht_pair_stage(float (&v)[128], int lane)
+{
+    const float sgn = (lane & 1) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
+        v[i] = fmaf(sgn, v[i], o);
+    }
+}
+
+// Sum of squares with 16 interleaved accumulators and a final tree, so the
+// fp32 rounding error stays within ~11 ulp of the sum.
+__device__ __forceinline__ float sum_squares128(const float (&v)[128])
+{
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        acc[i] = v[i] * v[i];
+#pragma unroll
+    for (int i = 16; i < 128; ++i)
+        acc[i & 15] = fmaf(v[i], v[i], acc[i & 15]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            acc[i] += acc[i + w];
+    return acc[0];
+}
+
+__device__ __forceinline__ float max_abs128(const float (&v)[128])
+{
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+        m[i & 3] = fmaxf(m[i & 3], fabsf(v[i]));
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// ===================================================================== //
+//                              compressor                               //
+// ===================================================================== //
+
+// Each warp streams its own 32-row tiles: warp tile t covers rows
+// 32t .. 32t + 31; the warps of the grid take tiles round-robin.  Lane 0
+// keeps kStages TMA loads in flight and refills a stage as soon as the warp
+// has read it.
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+    taco_compress_kernel(const __grid_constant__ CUtensorMap x_map,
+                         const __grid_constant__ CUtensorMap c_map, float *__restrict__ alpha_out,
+                         float *__restrict__ scale_out, int64_t nrows, float e_target, float eps)
+{
+    constexpr int G = NB / 128;  // lanes per block
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t wbase = base + warp * kCWarpBytes;
+    const uint32_t outw = wbase + kStages * kCStageBytes;
+    const uint32_t bars = base + kWarps * kCWarpBytes + warp * kStages * 8;
+    const int64_t ntiles = (nrows + kWarpRows - 1) / kWarpRows;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+
+    int issued = 0;
+    if (lane == 0) {
+        tma_prefetch_map(&x_map);
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(bars + 8 * s, 1);
+        fence_barrier_init();
+        for (; issued < kStages && gw + issued * W < ntiles; ++issued) {
+            const int32_t y = static_cast<int32_t>((gw + issued * W) * kWarpRows);
+            const uint32_t dst = wbase + issued * kCStageBytes, full = bars + 8 * issued;
+            mbar_arrive_expect_tx(full, kCStageBytes);
+            tma_load_2d(dst, &x_map, 0, y, full);
+            tma_load_2d(dst + kCHalfBytes, &x_map, 64, y, full);
+        }
+    }
+    __syncwarp();
+
+    const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+    const uint32_t orow = outw + lane * 128;
+    const float c = BlockConst<NB>::c;
+    int it = 0;
+    for (int64_t t = gw; t < ntiles; t += W, ++it) {
+        const int s = it % kStages;
+        // warp-uniform: if any lane's wait runs out, the whole warp stops
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
+            if (lane == 0)
+                atomicOr(&g_codec_error, kErrCompress);
+            break;
+        }
+        // Lane l reads row l of the stage: half h holds elements 64h .. 64h+63,
+        // and 16-byte chunk j of a 128-byte row sits at chunk j ^ (l & 7).
+        const uint32_t rowp = wbase + s * kCStageBytes + lane * 128;
+        float v[128];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 q = lds128(rowp + h * kCHalfBytes + ((static_cast<uint32_t>(j) << 4) ^ swz));
+                const int e = h * 64 + j * 8;
+                v[e + 0] = bf16lo_to_f32(q.x);
+                v[e + 1] = bf16hi_to_f32(q.x);
+                v[e + 2] = bf16lo_to_f32(q.y);
+                v[e + 3] = bf16hi_to_f32(q.y);
+                v[e + 4] = bf16lo_to_f32(q.z);
+                v[e + 5] = bf16hi_to_f32(q.z);
+                v[e + 6] = bf16lo_to_f32(q.w);
+                v[e + 7] = bf16hi_to_f32(q.w);
+            }
+        }
+        // step 1: block energy (x^2 of a bf16 value is exact in fp32); it
+        // consumes every loaded value, so the stage can be refilled after it
+        float ss = sum_squares128(v);
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
+            if (nt < ntiles) {
+                fence_proxy_async_smem();
+                const uint32_t dst = wbase + s * kCStageBytes, full = bars + 8 * s;
+                const int32_t y = static_cast<int32_t>(nt * kWarpRows);
+                mbar_arrive_expect_tx(full, kCStageBytes);
+                tma_load_2d(dst, &x_map, 0, y, full);
+                tma_load_2d(dst + kCHalfBytes, &x_map, 64, y, full);
+                ++issued;
+            }
+        }
+
+        // step 3 (rotation; the alpha and 1/sqrt(n) factors are applied below)
+        fwht128(v);
+        if constexpr (G == 2) {
+            fwht_pair_stage(v, lane);
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+        }
+        float mh = max_abs128(v);
+        if constexpr (G == 2)
+            mh = fmaxf(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 1));
+
+        // step 2: alpha = sqrt(E / (m + eps));  step 4: s = 448 / max|y|
+        const float m = ss * BlockConst<NB>::inv_n;
+        const float alpha = sqrtf(e_target / (m + eps));
+        const float ac = alpha * c;
+        const float M = ac * mh;
+        const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+        float k = ac * scale;
+        if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+                v[i] *= ac;
+            k = scale;
+        }
+
+        // step 5: codes = E4M3(y * s) into the warp's swizzled staging rows
+        if (lane == 0)
+            bulk_wait_read_all();  // the previous store from this buffer is done reading
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = 16 * j;
+            const uint32_t w0 = f32x4_to_e4m3x4(v[e + 0] * k, v[e + 1] * k, v[e + 2] * k, v[e + 3] * k);
+            const uint32_t w1 = f32x4_to_e4m3x4(v[e + 4] * k, v[e + 5] * k, v[e + 6] * k, v[e + 7] * k);
+            const uint32_t w2 = f32x4_to_e4m3x4(v[e + 8] * k, v[e + 9] * k, v[e + 10] * k, v[e + 11] * k);
+            const uint32_t w3 = f32x4_to_e4m3x4(v[e + 12] * k, v[e + 13] * k, v[e + 14] * k, v[e + 15] * k);
+            sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int64_t wrow = t * kWarpRows;
+        if (lane == 0) {
+            tma_store_2d(&c_map, 0, static_cast<int32_t>(wrow), outw);
+            bulk_commit();
+        }
+        const int64_t grow = wrow + lane;
+        if (grow < nrows && (lane % G) == 0) {
+            alpha_out[grow / G] = alpha;
+            scale_out[grow / G] = scale;
+        }
+    }
+    if (lane == 0) {
+        // leave no copy in flight into or out of this CTA's shared memory
+        for (int k = it; k < issued; ++k)
+            mbar_wait(bars + 8 * (k % kStages), (k / kStages) & 1);
+        bulk_wait_all();
+    }
+}
+
+// ===================================================================== //
+//                             decompressor                              //
+// ===================================================================== //
+
+template <int NB, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    taco_decompress_kernel(const __grid_constant__ CUtensorMap c_map,
+                           const __grid_constant__ CUtensorMap o_map, const float *__restrict__ alpha,
+                           const float *__restrict__ scale, int64_t nrows)
+{
+    constexpr int G = NB / 128;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t wbase = base + warp * kDWarpBytes;
+    const uint32_t outw = wbase + kStages * kDStageBytes;
+    const uint32_t bars = base + kWarps * kDWarpBytes + warp * kStages * 8;
+    const int64_t ntiles = (nrows + kWarpRows - 1) / kWarpRows;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+
+    int issued = 0;
+    if (lane == 0) {
+        tma_prefetch_map(&c_map);
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(bars + 8 * s, 1);
+        fence_barrier_init();
+        for (; issued < kStages && gw + issued * W < ntiles; ++issued) {
+            const uint32_t full = bars + 8 * issued;
+            mbar_arrive_expect_tx(full, kDStageBytes);
+            tma_load_2d(wbase + issued * kDStageBytes, &c_map, 0,
+                        static_cast<int32_t>((gw + issued * W) * kWarpRows), full);
+        }
+    }
+    __syncwarp();
+
+    const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+    const float c = BlockConst<NB>::c;
+    int it = 0;
+    for (int64_t t = gw; t < ntiles; t += W, ++it) {
+        const int s = it % kStages;
+        const int64_t wrow = t * kWarpRows;
+        const int64_t grow = wrow + lane;
+        const int64_t blk = (grow < nrows ? grow : nrows - 1) / G;
+        const float a = __ldg(alpha + blk);
+        const float sc = __ldg(scale + blk);
+        // warp-uniform: if any lane's wait runs out, the whole warp stops
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
+            if (lane == 0)
+                atomicOr(&g_codec_error, kErrDecompress);
+            break;
+        }
+        const uint32_t rowp = wbase + s * kDStageBytes + lane * 128;
+        float v[128];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 q = lds128(rowp + ((static_cast<uint32_t>(j) << 4) ^ swz));
+            const int e = 16 * j;
+            e4m3x2_to_f32x2(q.x, v[e + 0], v[e + 1]);
+            e4m3x2_to_f32x2(q.x >> 16, v[e + 2], v[e + 3]);
+            e4m3x2_to_f32x2(q.y, v[e + 4], v[e + 5]);
+            e4m3x2_to_f32x2(q.y >> 16, v[e + 6], v[e + 7]);
+            e4m3x2_to_f32x2(q.z, v[e + 8], v[e + 9]);
+            e4m3x2_to_f32x2(q.z >> 16, v[e + 10], v[e + 11]);
+            e4m3x2_to_f32x2(q.w, v[e + 12], v[e + 13]);
+            e4m3x2_to_f32x2(q.w >> 16, v[e + 14], v[e + 15]);
+        }
+        fwht128(v);  // consumes every decoded value
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
+            if (nt < ntiles) {
+                fence_proxy_async_smem();
+                const uint32_t full = bars + 8 * s;
+                mbar_arrive_expect_tx(full, kDStageBytes);
+                tma_load_2d(wbase + s * kDStageBytes, &c_map, 0, static_cast<int32_t>(nt * kWarpRows), full);
+                ++issued;
+            }
+        }
+        if constexpr (G == 2)
+            fwht_pair_stage(v, lane);
+
+        // out = c H(decode) / (s alpha)
+        const float sa = sc * a;
+        float k = c / sa;
+        if (!(sa <= FLT_MAX) || !(k >= FLT_MIN)) {  // extreme scales: divide in two steps
+            const float inv_s = 1.0f / sc;
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+                v[i] *= inv_s;
+            k = c / a;
+        }
+
+        if (lane == 0)
+            bulk_wait_read_all();
+        __syncwarp();
+        if constexpr (!BF16OUT) {
+            // 4 boxes of 32 floats (128 bytes) x 32 rows
+#pragma unroll
+            for (int ch = 0; ch < 32; ++ch) {
+                const uint32_t b = ch >> 3, j = ch & 7;
+                const uint32_t addr = outw + b * 4096 + lane * 128 + ((j << 4) ^ swz);
+                const int e = 4 * ch;
+                sts128(addr, __float_as_uint(v[e] * k), __float_as_uint(v[e + 1] * k),
+                       __float_as_uint(v[e + 2] * k), __float_as_uint(v[e + 3] * k));
+            }
+        } else {
+            // 2 boxes of 64 bf16 (128 bytes) x 32 rows
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint32_t b = ch >> 3, j = ch & 7;
+                const uint32_t addr = outw + b * 4096 + lane * 128 + ((j << 4) ^ swz);
+                const int e = 8 * ch;
+                sts128(addr, f32x2_to_bf16x2(v[e] * k, v[e + 1] * k),
+                       f32x2_to_bf16x2(v[e + 2] * k, v[e + 3] * k),
+                       f32x2_to_bf16x2(v[e + 4] * k, v[e + 5] * k),
+                       f32x2_to_bf16x2(v[e + 6] * k, v[e + 7] * k));
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            constexpr int nbox = BF16OUT ? 2 : 4;
+            constexpr int box_inner = BF16OUT ? 64 : 32;
+#pragma unroll
+            for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&o_map, b * box_inner, static_cast<int32_t>(wrow), outw + b * 4096);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) {
+        for (int k = it; k < issued; ++k)
+            mbar_wait(bars + 8 * (k % kStages), (k / kStages) & 1);
+        bulk_wait_all();
+    }
+}
+
+// ===================================================================== //
+//                                 host                                  //
+// ===================================================================== //
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <typename K>
+cudaError_t ensure_smem(K kernel, uint32_t bytes, int device, bool *done)
+{
+    if (done[device])
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e == cudaSuccess)
+        done[device] = true;
+    return e;
+}
+
+}  // namespace
+
+int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t inner,
+                         uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                         uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return -1;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float e_target, float eps,
+                            uint8_t *codes, float *alpha, float *scale, cudaStream_t stream)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap xm, cm;
+    if (encode_tensor_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(x_bf16), 128,
+                             nrows, 256, 64, kWarpRows) != 0 ||
+        encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, 128, nrows, 128, 128, 32) != 0)
+        return cudaErrorInvalidValue;
+    const int64_t ctas = (nrows + kWarps * kWarpRows - 1) / (kWarps * kWarpRows);
+    const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
+    static bool set128[kMaxDevices], set256[kMaxDevices];
+    if (block == 128) {
+        if ((e = ensure_smem(taco_compress_kernel<128>, kCSmemBytes, di.device, set128)) != cudaSuccess)
+            return e;
+        taco_compress_kernel<128><<<grid, kThreads, kCSmemBytes, stream>>>(xm, cm, alpha, scale, nrows,
+                                                                          e_target, eps);
+    } else {
+        if ((e = ensure_smem(taco_compress_kernel<256>, kCSmemBytes, di.device, set256)) != cudaSuccess)
+            return e;
+        taco_compress_kernel<256><<<grid, kThreads, kCSmemBytes, stream>>>(xm, cm, alpha, scale, nrows,
+                                                                          e_target, eps);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale,
+                              int64_t nrows, int block, void *out, bool out_bf16, cudaStream_t stream)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap cm, om;
+    int rc = encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(codes), 128,
+                                  nrows, 128, 128, kWarpRows);
+    if (out_bf16)
+        rc |= encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 128, nrows, 256, 64, 32);
+    else
+        rc |= encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, 128, nrows, 512, 32, 32);
+    if (rc != 0)
+        return cudaErrorInvalidValue;
+    const int64_t ctas = (nrows + kWarps * kWarpRows - 1) / (kWarps * kWarpRows);
+    const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
+    static bool s0[kMaxDevices], s1[kMaxDevices], s2[kMaxDevices], s3[kMaxDevices];
+#define TACO_LAUNCH_D(NB, BF, FLAGS)                                                               \
+    do {                                                                                           \
+        if ((e = ensure_smem(taco_decompress_kernel<NB, BF>, kDSmemBytes, di.device, FLAGS)) !=   \
+            cudaSuccess)                                                                           \
+            return e;                                                                              \
+        taco_decompress_kernel<NB, BF>                                                             \
+            <<<grid, kThreads, kDSmemBytes, stream>>>(cm, om, alpha, scale, nrows);        \
+    } while (0)
+    if (block == 128) {
+        if (out_bf16)
+            TACO_LAUNCH_D(128, true, s0);
+        else
+            TACO_LAUNCH_D(128, false, s1);
+    } else {
+        if (out_bf16)
+            TACO_LAUNCH_D(256, true, s2);
+        else
+            TACO_LAUNCH_D(256, false, s3);
+    }
+#undef TACO_LAUNCH_D
+    return cudaGetLastError();
+}
+
+cudaError_t read_codec_error(uint32_t *flags, bool clear)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_codec_error, sizeof v);
+    if (e != cudaSuccess)
+        return e;
+    *flags = v;
+    if (clear) {
+        v = 0;
+        e = cudaMemcpyToSymbol(g_codec_error, &v, sizeof v);
+    }
+    return e;
+}
+
+}  // namespace taco

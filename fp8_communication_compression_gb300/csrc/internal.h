@@ -1,0 +1,48 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace taco {
+
+// Per-device facts the launchers need (cached on first use).
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+cudaError_t current_device_info(DeviceInfo *out);
+
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
+// Returns 0 on success.
+int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t inner,
+                         uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                         uint32_t box_rows);
+
+// Kernels working on the "128-view" of a TACO tensor: nrows rows of 128
+// elements; a block of n elements spans n / 128 consecutive rows.
+cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float e_target, float eps,
+                            uint8_t *codes, float *alpha, float *scale, cudaStream_t stream);
+cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale,
+                              int64_t nrows, int block, void *out, bool out_bf16,
+                              cudaStream_t stream);
+
+// Direct-load kernels (no Hadamard on their path).
+struct ShardPtrs {
+    const uint8_t *codes[16];
+    const float *alpha[16];
+    const float *scale[16];
+};
+cudaError_t launch_taco_reduce(int P, const ShardPtrs &in, int64_t nblocks, int block, float e_target,
+                               float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
+                               cudaStream_t stream);
+cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *grad_bf16, int64_t n,
+                                   int block, cudaStream_t stream);
+cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block, uint8_t *out_codes,
+                               float *out_scale, cudaStream_t stream);
+
+cudaError_t read_codec_error(uint32_t *flags, bool clear);
+
+} // namespace taco

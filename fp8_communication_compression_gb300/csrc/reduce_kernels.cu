@@ -1,0 +1,363 @@
+// Shard reduce (TACO two-shot local step) and AGoQ FP8 gradient kernels for
+// sm_103a.  None of these needs a Hadamard rotation on its path, so they
+// use plain coalesced 16-byte loads: a lane owns 16 consecutive elements of
+// a block, NB / 16 adjacent lanes own one block, and per-block statistics
+// (sum of squares, absolute maximum) are combined with __shfl_xor_sync.
+//
+// TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
+// and H the Sylvester matrix (c H c H = I), shard p decompresses to
+//     x_p = c H (d_p / s_p) / alpha_p,        d_p = decode(codes_p),
+// so the FP32 sum of the P reconstructions is S = c H T with
+//     T = sum_p d_p / (s_p alpha_p).
+// Compressing S (TACO 2.B.1-2.B.2) needs mean(S^2) = |T|^2 / n (Parseval)
+// and the rotation y = c H (alpha' S) = alpha' T, hence
+//     alpha' = sqrt(E / (|T|^2/n + eps)),  s' = 448 / (alpha' max|T|),
+//     codes' = E4M3(alpha' s' T),
+// which is the literal decompress-sum-compress result without either
+// rotation.  (AGoQ 2.B, step 2: the sum is taken in FP32 so that it cannot
+// overflow the FP8 range.)
+
+#include <cfloat>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace taco {
+
+namespace {
+
+constexpr int kEPL = 16;  // elements per lane
+constexpr int kBlockThreads = 256;
+
+__device__ __forceinline__ void decode16(const uint4 q, float (&d)[16])
+{
+    e4m3x2_to_f32x2(q.x, d[0], d[1]);
+    e4m3x2_to_f32x2(q.x >> 16, d[2], d[3]);
+    e4m3x2_to_f32x2(q.y, d[4], d[5]);
+    e4m3x2_to_f32x2(q.y >> 16, d[6], d[7]);
+    e4m3x2_to_f32x2(q.z, d[8], d[9]);
+    e4m3x2_to_f32x2(q.z >> 16, d[10], d[11]);
+    e4m3x2_to_f32x2(q.w, d[12], d[13]);
+    e4m3x2_to_f32x2(q.w >> 16, d[14], d[15]);
+}
+
+__device__ __forceinline__ uint4 encode16(const float (&v)[16], float k)
+{
+    uint4 q;
+    q.x = f32x4_to_e4m3x4(v[0] * k, v[1] * k, v[2] * k, v[3] * k);
+    q.y = f32x4_to_e4m3x4(v[4] * k, v[5] * k, v[6] * k, v[7] * k);
+    q.z = f32x4_to_e4m3x4(v[8] * k, v[9] * k, v[10] * k, v[11] * k);
+    q.w = f32x4_to_e4m3x4(v[12] * k, v[13] * k, v[14] * k, v[15] * k);
+    return q;
+}
+
+template <int LPB> __device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = LPB / 2; o >= 1; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+template <int LPB> __device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = LPB / 2; o >= 1; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float absmax_scale(float mx)
+{
+    return (mx > 0.0f) ? fminf(448.0f / mx, FLT_MAX) : 1.0f;
+}
+
+// Warp-uniform grid-stride loop over lane slots.  Lanes past the end still
+// take part in the shuffles but load and store nothing.
+#define TACO_LANE_LOOP(total)                                                                    \
+    const int64_t _stride = static_cast<int64_t>(gridDim.x) * blockDim.x;                        \
+    for (int64_t _base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);    \
+         _base < (total); _base += _stride)
+
+// ------------------------------------------------------ TACO reduce --
+
+template <int NB, int P>
+__global__ void __launch_bounds__(kBlockThreads)
+    taco_reduce_kernel(const ShardPtrs in, int64_t nblocks, float e_target, float eps,
+                       uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
+                       float *__restrict__ out_scale)
+{
+    constexpr int LPB = NB / kEPL;
+    const int64_t total = nblocks * LPB;
+    const int lane = threadIdx.x & 31;
+    TACO_LANE_LOOP(total)
+    {
+        const int64_t t = _base + lane;
+        const bool valid = t < total;
+        const int64_t blk = valid ? t / LPB : 0;
+        const int part = static_cast<int>(t % LPB);
+        const int64_t off = blk * NB + part * kEPL;
+        uint4 q[P];
+        float w[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            q[p] = valid ? ldg128_stream(in.codes[p] + off) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const float sa = valid ? __ldg(in.scale[p] + blk) * __ldg(in.alpha[p] + blk) : 1.0f;
+            w[p] = (sa <= FLT_MAX) ? 1.0f / sa : (1.0f / __ldg(in.scale[p] + blk)) / __ldg(in.alpha[p] + blk);
+        }
+        float T[kEPL];
+#pragma unroll
+        for (int i = 0; i < kEPL; ++i)
+            T[i] = 0.0f;
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            float d[kEPL];
+            decode16(q[p], d);
+#pragma unroll
+            for (int i = 0; i < kEPL; ++i)
+                T[i] = fmaf(d[i], w[p], T[i]);
+        }
+        float a4[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kEPL; ++i) {
+            a4[i & 3] = fmaf(T[i], T[i], a4[i & 3]);
+            mx = fmaxf(mx, fabsf(T[i]));
+        }
+        const float ss = group_sum<LPB>((a4[0] + a4[1]) + (a4[2] + a4[3]));
+        mx = group_max<LPB>(mx);
+        const float alpha = sqrtf(e_target / (ss * (1.0f / NB) + eps));
+        const float M = alpha * mx;
+        const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+        float k = alpha * scale;
+        if (!(k <= FLT_MAX)) {
+#pragma unroll
+            for (int i = 0; i < kEPL; ++i)
+                T[i] *= alpha;
+            k = scale;
+        }
+        if (valid) {
+            stg128_stream(out_codes + off, encode16(T, k));
+            if (part == 0) {
+                out_alpha[blk] = alpha;
+                out_scale[blk] = scale;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------- AGoQ accumulate --
+
+template <int NB>
+__global__ void __launch_bounds__(kBlockThreads)
+    agoq_accumulate_kernel(uint8_t *__restrict__ codes, float *__restrict__ scale,
+                           const uint16_t *__restrict__ grad, int64_t nblocks)
+{
+    constexpr int LPB = NB / kEPL;
+    const int64_t total = nblocks * LPB;
+    const int lane = threadIdx.x & 31;
+    TACO_LANE_LOOP(total)
+    {
+        const int64_t t = _base + lane;
+        const bool valid = t < total;
+        const int64_t blk = valid ? t / LPB : 0;
+        const int part = static_cast<int>(t % LPB);
+        const int64_t off = blk * NB + part * kEPL;
+        uint4 q = make_uint4(0, 0, 0, 0), g0 = q, g1 = q;
+        float s_old = 1.0f;
+        if (valid) {
+            // codes and scale are rewritten below: coherent loads, not .nc
+            asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                         : "l"(codes + off));
+            g0 = ldg128_stream(grad + off);
+            g1 = ldg128_stream(grad + off + 8);
+            asm volatile("ld.global.f32 %0, [%1];" : "=f"(s_old) : "l"(scale + blk));
+        }
+        const float inv = 1.0f / s_old;
+        float d[kEPL];
+        decode16(q, d);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            d[2 * i] = fmaf(d[2 * i], inv, bf16lo_to_f32(gw[i]));
+            d[2 * i + 1] = fmaf(d[2 * i + 1], inv, bf16hi_to_f32(gw[i]));
+            mx = fmaxf(mx, fmaxf(fabsf(d[2 * i]), fabsf(d[2 * i + 1])));
+        }
+        mx = group_max<LPB>(mx);
+        const float s_new = absmax_scale(mx);
+        if (valid) {
+            stg128_stream(codes + off, encode16(d, s_new));
+            if (part == 0)
+                scale[blk] = s_new;
+        }
+    }
+}
+
+// ----------------------------------------------------- AGoQ reduce --
+
+template <int NB, int P>
+__global__ void __launch_bounds__(kBlockThreads)
+    agoq_reduce_kernel(const ShardPtrs in, int64_t nblocks, uint8_t *__restrict__ out_codes,
+                       float *__restrict__ out_scale)
+{
+    constexpr int LPB = NB / kEPL;
+    const int64_t total = nblocks * LPB;
+    const int lane = threadIdx.x & 31;
+    TACO_LANE_LOOP(total)
+    {
+        const int64_t t = _base + lane;
+        const bool valid = t < total;
+        const int64_t blk = valid ? t / LPB : 0;
+        const int part = static_cast<int>(t % LPB);
+        const int64_t off = blk * NB + part * kEPL;
+        uint4 q[P];
+        float inv[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            q[p] = valid ? ldg128_stream(in.codes[p] + off) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            inv[p] = 1.0f / (valid ? __ldg(in.scale[p] + blk) : 1.0f);
+        float S[kEPL];
+#pragma unroll
+        for (int i = 0; i < kEPL; ++i)
+            S[i] = 0.0f;
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            float d[kEPL];
+            decode16(q[p], d);
+#pragma unroll
+            for (int i = 0; i < kEPL; ++i)
+                S[i] = fmaf(d[i], inv[p], S[i]);
+        }
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kEPL; ++i)
+            mx = fmaxf(mx, fabsf(S[i]));
+        mx = group_max<LPB>(mx);
+        const float s_new = absmax_scale(mx);
+        if (valid) {
+            stg128_stream(out_codes + off, encode16(S, s_new));
+            if (part == 0)
+                out_scale[blk] = s_new;
+        }
+    }
+}
+
+#undef TACO_LANE_LOOP
+
+template <typename K> cudaError_t grid_for(K kernel, int64_t lanes_total, int *grid)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlockThreads, 0);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        per_sm = 1;
+    const int64_t need = (lanes_total + kBlockThreads - 1) / kBlockThreads;
+    const int64_t cap = static_cast<int64_t>(di.num_sms) * per_sm;
+    *grid = static_cast<int>(need < cap ? need : cap);
+    return cudaSuccess;
+}
+
+template <int NB, int P>
+cudaError_t run_taco_reduce(const ShardPtrs &in, int64_t nblocks, float e_target, float eps,
+                            uint8_t *oc, float *oa, float *os, cudaStream_t st)
+{
+    int grid = 0;
+    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
+    if (e != cudaSuccess)
+        return e;
+    taco_reduce_kernel<NB, P><<<grid, kBlockThreads, 0, st>>>(in, nblocks, e_target, eps, oc, oa, os);
+    return cudaGetLastError();
+}
+
+template <int NB, int P>
+cudaError_t run_agoq_reduce(const ShardPtrs &in, int64_t nblocks, uint8_t *oc, float *os, cudaStream_t st)
+{
+    int grid = 0;
+    cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
+    if (e != cudaSuccess)
+        return e;
+    agoq_reduce_kernel<NB, P><<<grid, kBlockThreads, 0, st>>>(in, nblocks, oc, os);
+    return cudaGetLastError();
+}
+
+template <int NB, int... Ps> struct PDispatch;
+template <int NB> struct PDispatch<NB> {
+    static cudaError_t taco(int, const ShardPtrs &, int64_t, float, float, uint8_t *, float *, float *,
+                            cudaStream_t)
+    {
+        return cudaErrorInvalidValue;
+    }
+    static cudaError_t agoq(int, const ShardPtrs &, int64_t, uint8_t *, float *, cudaStream_t)
+    {
+        return cudaErrorInvalidValue;
+    }
+};
+template <int NB, int P0, int... Ps> struct PDispatch<NB, P0, Ps...> {
+    static cudaError_t taco(int P, const ShardPtrs &in, int64_t nb, float e, float eps, uint8_t *oc,
+                            float *oa, float *os, cudaStream_t st)
+    {
+        if (P == P0)
+            return run_taco_reduce<NB, P0>(in, nb, e, eps, oc, oa, os, st);
+        return PDispatch<NB, Ps...>::taco(P, in, nb, e, eps, oc, oa, os, st);
+    }
+    static cudaError_t agoq(int P, const ShardPtrs &in, int64_t nb, uint8_t *oc, float *os, cudaStream_t st)
+    {
+        if (P == P0)
+            return run_agoq_reduce<NB, P0>(in, nb, oc, os, st);
+        return PDispatch<NB, Ps...>::agoq(P, in, nb, oc, os, st);
+    }
+};
+
+template <int NB>
+using AllP = PDispatch<NB, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16>;
+
+}  // namespace
+
+cudaError_t launch_taco_reduce(int P, const ShardPtrs &in, int64_t nblocks, int block, float e_target,
+                               float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
+                               cudaStream_t stream)
+{
+    if (block == 128)
+        return AllP<128>::taco(P, in, nblocks, e_target, eps, out_codes, out_alpha, out_scale, stream);
+    return AllP<256>::taco(P, in, nblocks, e_target, eps, out_codes, out_alpha, out_scale, stream);
+}
+
+cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block, uint8_t *out_codes,
+                               float *out_scale, cudaStream_t stream)
+{
+    const int64_t nblocks = n / block;
+    if (block == 128)
+        return AllP<128>::agoq(P, in, nblocks, out_codes, out_scale, stream);
+    return AllP<256>::agoq(P, in, nblocks, out_codes, out_scale, stream);
+}
+
+cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *grad_bf16, int64_t n,
+                                   int block, cudaStream_t stream)
+{
+    const int64_t nblocks = n / block;
+    const uint16_t *g = static_cast<const uint16_t *>(grad_bf16);
+    int grid = 0;
+    cudaError_t e;
+    if (block == 128) {
+        if ((e = grid_for(agoq_accumulate_kernel<128>, nblocks * (128 / kEPL), &grid)) != cudaSuccess)
+            return e;
+        agoq_accumulate_kernel<128><<<grid, kBlockThreads, 0, stream>>>(codes, scale, g, nblocks);
+    } else {
+        if ((e = grid_for(agoq_accumulate_kernel<256>, nblocks * (256 / kEPL), &grid)) != cudaSuccess)
+            return e;
+        agoq_accumulate_kernel<256><<<grid, kBlockThreads, 0, stream>>>(codes, scale, g, nblocks);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace taco

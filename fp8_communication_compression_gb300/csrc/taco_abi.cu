@@ -1,0 +1,257 @@
+// C ABI of the library (include/taco.h): argument validation on the host,
+// then one kernel launch on the caller's stream.  No allocation, no
+// synchronisation, no exception crosses this boundary.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/taco.h"
+#include "internal.h"
+
+namespace taco {
+
+cudaError_t current_device_info(DeviceInfo *out)
+{
+    constexpr int kMax = 64;
+    static DeviceInfo cache[kMax];
+    static bool ready[kMax];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMax)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+        DeviceInfo di{dev, 0, 0};
+        if ((e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+            return e;
+        cache[dev] = di;
+        ready[dev] = true;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+}  // namespace taco
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [a, a + na) and [b, b + nb) overlap
+bool overlap(const void *a, uint64_t na, const void *b, uint64_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+bool positive_finite(float v) { return std::isfinite(v) && v > 0.0f; }
+
+taco_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TACO_OK : TACO_ERR_CUDA; }
+
+// The 128-element row view used by the TMA kernels must fit int32 tile
+// coordinates.
+constexpr int64_t kMaxRows128 = (int64_t(1) << 31) - 256;
+
+taco_status check_taco_shape(int64_t rows, int64_t d, int32_t block)
+{
+    if (rows < 0 || d <= 0)
+        return TACO_ERR_INVALID_ARG;
+    if (!taco_block_supported(block))
+        return TACO_ERR_UNSUPPORTED;
+    if (d % block != 0)
+        return TACO_ERR_INVALID_ARG;
+    if (rows > 0 && d > INT64_MAX / rows)
+        return TACO_ERR_INVALID_ARG;
+    if (rows * d / 128 > kMaxRows128)
+        return TACO_ERR_UNSUPPORTED;
+    return TACO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *taco_status_string(taco_status s)
+{
+    switch (s) {
+    case TACO_OK:
+        return "ok";
+    case TACO_ERR_INVALID_ARG:
+        return "invalid argument";
+    case TACO_ERR_UNSUPPORTED:
+        return "unsupported block size, shard count or size";
+    case TACO_ERR_MISALIGNED:
+        return "misaligned pointer";
+    case TACO_ERR_CUDA:
+        return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int taco_abi_version(void) { return TACO_ABI_VERSION; }
+
+int taco_block_supported(int32_t block) { return block == 128 || block == 256; }
+
+taco_status taco_compress(const void *x_bf16, int64_t rows, int64_t d, int32_t block, float e_target,
+                          float eps, uint8_t *codes, float *alpha, float *scale, taco_stream_t stream)
+{
+    taco_status st = check_taco_shape(rows, d, block);
+    if (st != TACO_OK)
+        return st;
+    if (!positive_finite(e_target) || !positive_finite(eps))
+        return TACO_ERR_INVALID_ARG;
+    if (rows == 0)
+        return TACO_OK;
+    if (!x_bf16 || !codes || !alpha || !scale)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(codes, 16) || !aligned(alpha, 4) || !aligned(scale, 4))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t n = static_cast<uint64_t>(rows * d), nb = n / block;
+    if (overlap(x_bf16, 2 * n, codes, n) || overlap(x_bf16, 2 * n, alpha, 4 * nb) ||
+        overlap(x_bf16, 2 * n, scale, 4 * nb) || overlap(codes, n, alpha, 4 * nb) ||
+        overlap(codes, n, scale, 4 * nb) || overlap(alpha, 4 * nb, scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_compress(x_bf16, rows * d / 128, block, e_target, eps, codes, alpha,
+                                           scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_decompress(const uint8_t *codes, const float *alpha, const float *scale, int64_t rows,
+                            int64_t d, int32_t block, void *out, int32_t out_is_bf16,
+                            taco_stream_t stream)
+{
+    taco_status st = check_taco_shape(rows, d, block);
+    if (st != TACO_OK)
+        return st;
+    if (rows == 0)
+        return TACO_OK;
+    if (!codes || !alpha || !scale || !out)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(codes, 16) || !aligned(out, 16) || !aligned(alpha, 4) || !aligned(scale, 4))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t n = static_cast<uint64_t>(rows * d), nb = n / block;
+    const uint64_t out_bytes = n * (out_is_bf16 ? 2 : 4);
+    if (overlap(out, out_bytes, codes, n) || overlap(out, out_bytes, alpha, 4 * nb) ||
+        overlap(out, out_bytes, scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_decompress(codes, alpha, scale, rows * d / 128, block, out,
+                                             out_is_bf16 != 0, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes, const float *const *alpha,
+                               const float *const *scale, int64_t rows, int64_t d, int32_t block,
+                               float e_target, float eps, uint8_t *out_codes, float *out_alpha,
+                               float *out_scale, taco_stream_t stream)
+{
+    taco_status st = check_taco_shape(rows, d, block);
+    if (st != TACO_OK)
+        return st;
+    if (P < 1 || P > TACO_MAX_SHARDS)
+        return TACO_ERR_UNSUPPORTED;
+    if (!positive_finite(e_target) || !positive_finite(eps))
+        return TACO_ERR_INVALID_ARG;
+    if (rows == 0)
+        return TACO_OK;
+    if (!codes || !alpha || !scale || !out_codes || !out_alpha || !out_scale)
+        return TACO_ERR_INVALID_ARG;
+    const uint64_t n = static_cast<uint64_t>(rows * d), nb = n / block;
+    if (!aligned(out_codes, 16) || !aligned(out_alpha, 4) || !aligned(out_scale, 4))
+        return TACO_ERR_MISALIGNED;
+    if (overlap(out_codes, n, out_alpha, 4 * nb) || overlap(out_codes, n, out_scale, 4 * nb) ||
+        overlap(out_alpha, 4 * nb, out_scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    taco::ShardPtrs sp{};
+    for (int p = 0; p < P; ++p) {
+        if (!codes[p] || !alpha[p] || !scale[p])
+            return TACO_ERR_INVALID_ARG;
+        if (!aligned(codes[p], 16) || !aligned(alpha[p], 4) || !aligned(scale[p], 4))
+            return TACO_ERR_MISALIGNED;
+        const void *ins[3] = {codes[p], alpha[p], scale[p]};
+        const uint64_t lens[3] = {n, 4 * nb, 4 * nb};
+        for (int i = 0; i < 3; ++i)
+            if (overlap(ins[i], lens[i], out_codes, n) || overlap(ins[i], lens[i], out_alpha, 4 * nb) ||
+                overlap(ins[i], lens[i], out_scale, 4 * nb))
+                return TACO_ERR_INVALID_ARG;
+        sp.codes[p] = codes[p];
+        sp.alpha[p] = alpha[p];
+        sp.scale[p] = scale[p];
+    }
+    return from_cuda(taco::launch_taco_reduce(P, sp, static_cast<int64_t>(nb), block, e_target, eps,
+                                              out_codes, out_alpha, out_scale,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_fp8_accumulate(uint8_t *main_codes, float *main_scale, const void *grad_bf16, int64_t n,
+                                int32_t block, taco_stream_t stream)
+{
+    if (n < 0)
+        return TACO_ERR_INVALID_ARG;
+    if (!taco_block_supported(block))
+        return TACO_ERR_UNSUPPORTED;
+    if (n % block != 0)
+        return TACO_ERR_INVALID_ARG;
+    if (n == 0)
+        return TACO_OK;
+    if (!main_codes || !main_scale || !grad_bf16)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(main_codes, 16) || !aligned(grad_bf16, 16) || !aligned(main_scale, 4))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t nb = static_cast<uint64_t>(n / block);
+    if (overlap(main_codes, n, main_scale, 4 * nb) || overlap(grad_bf16, 2 * n, main_codes, n) ||
+        overlap(grad_bf16, 2 * n, main_scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_agoq_accumulate(main_codes, main_scale, grad_bf16, n, block,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_reduce_shards(int32_t P, const uint8_t *const *codes, const float *const *scale, int64_t n,
+                               int32_t block, uint8_t *out_codes, float *out_scale, taco_stream_t stream)
+{
+    if (n < 0)
+        return TACO_ERR_INVALID_ARG;
+    if (!taco_block_supported(block) || P < 1 || P > TACO_MAX_SHARDS)
+        return TACO_ERR_UNSUPPORTED;
+    if (n % block != 0)
+        return TACO_ERR_INVALID_ARG;
+    if (n == 0)
+        return TACO_OK;
+    if (!codes || !scale || !out_codes || !out_scale)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(out_codes, 16) || !aligned(out_scale, 4))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t nb = static_cast<uint64_t>(n / block);
+    if (overlap(out_codes, n, out_scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    taco::ShardPtrs sp{};
+    for (int p = 0; p < P; ++p) {
+        if (!codes[p] || !scale[p])
+            return TACO_ERR_INVALID_ARG;
+        if (!aligned(codes[p], 16) || !aligned(scale[p], 4))
+            return TACO_ERR_MISALIGNED;
+        if (overlap(codes[p], n, out_codes, n) || overlap(codes[p], n, out_scale, 4 * nb) ||
+            overlap(scale[p], 4 * nb, out_codes, n) || overlap(scale[p], 4 * nb, out_scale, 4 * nb))
+            return TACO_ERR_INVALID_ARG;
+        sp.codes[p] = codes[p];
+        sp.scale[p] = scale[p];
+    }
+    return from_cuda(taco::launch_agoq_reduce(P, sp, n, block, out_codes, out_scale,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_device_error(uint32_t *flags_out, int32_t clear)
+{
+    if (!flags_out)
+        return TACO_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return TACO_ERR_CUDA;
+    return from_cuda(taco::read_codec_error(flags_out, clear != 0));
+}
+
+}  // extern "C"

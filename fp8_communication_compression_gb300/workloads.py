@@ -47,8 +47,9 @@ def _rng(*key: int) -> np.random.Generator:
 
 def f32_to_bf16_bits(x32: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bits."""
-    b = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    b = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32)
+    # finite inputs only: the sum stays below 2^32
+    b = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return b.astype(np.uint16)
 
 

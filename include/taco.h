@@ -1,0 +1,174 @@
+/*
+ * taco.h - C ABI of the GB300 (sm_103a) FP8 communication-compression library.
+ *
+ * The operations follow two web summaries of papers:
+ *   [TACO] "TACO: Efficient Communication Compression of Intermediate Tensors
+ *          for Scalable Tensor-Parallel LLM Training" (gist.science summary
+ *          of arXiv 2604.24088)
+ *   [AGoQ] "AGoQ: Activation and Gradient Quantization for Memory-Efficient
+ *          Distributed Training of LLMs" (gist.science summary of arXiv
+ *          2605.00539)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Memory: every pointer argument is a DEVICE pointer unless stated
+ *    otherwise.  The caller allocates and owns every buffer; the library
+ *    never allocates, frees or synchronises, and keeps no state beyond a
+ *    per-device cache of attributes and kernel settings.
+ *  - Execution: each call validates its arguments on the host, then enqueues
+ *    one kernel on `stream` and returns; results are ready when the stream
+ *    reaches that point.  A NULL stream is the legacy default stream.
+ *  - Layout: tensors are row-major and contiguous.  A "block" is a run of
+ *    `block` consecutive elements of a row; `d % block == 0`, so a tensor
+ *    of rows x d elements holds nb = rows * d / block blocks, stored one after
+ *    another.  Per-block scalars (alpha, scale) are fp32 arrays of nb values
+ *    in the same order.  FP8 codes are E4M3FN bit patterns, one byte each
+ *    (viewable as torch.float8_e4m3fn); bf16 data is passed as raw 16-bit
+ *    patterns.
+ *  - Alignment: bf16, code and fp32 output buffers must be 16-byte aligned;
+ *    alpha and scale arrays 4-byte aligned.
+ *  - Aliasing: outputs must not overlap inputs, except where an argument is
+ *    documented as in/out.
+ *  - Errors: a bad argument returns a status and launches nothing.  A
+ *    failed launch returns TACO_ERR_CUDA.  Nothing aborts and no C++
+ *    exception crosses the ABI.  Kernels never wait without a time limit;
+ *    a wait that runs out records a flag read by taco_device_error().
+ *  - Empty input (rows == 0 or n == 0) returns TACO_OK without a launch.
+ *  - Inputs must be finite; NaN or Inf input gives unspecified codes.
+ */
+#ifndef TACO_H
+#define TACO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that the header needs no
+ * CUDA include. */
+typedef struct CUstream_st *taco_stream_t;
+
+typedef enum {
+    TACO_OK = 0,
+    TACO_ERR_INVALID_ARG = 1, /* null pointer, bad size, overlap, non-positive e_target/eps */
+    TACO_ERR_UNSUPPORTED = 2, /* block size or shard count outside the supported set */
+    TACO_ERR_MISALIGNED = 3,  /* pointer alignment below the stated minimum */
+    TACO_ERR_CUDA = 4,        /* the CUDA runtime reported an error */
+} taco_status;
+
+#define TACO_ABI_VERSION 1
+#define TACO_QMAX 448.0f
+#define TACO_MAX_SHARDS 16
+
+/* Human-readable name of a status; never NULL. */
+const char *taco_status_string(taco_status status);
+
+/* Returns TACO_ABI_VERSION of the loaded library. */
+int taco_abi_version(void);
+
+/* Block sizes the TACO calls accept: 128 and 256. */
+int taco_block_supported(int32_t block);
+
+/*
+ * taco_compress - fused ASH + DS FP8 compressor.
+ * [TACO] 2.B.1 (ASH), 2.B.2 (DS), 2.B.3 (fused operator).  For every block:
+ *   m      = mean(x^2)                          (block energy)
+ *   alpha  = sqrt(e_target / (m + eps))         (pre-transform scale)
+ *   y      = (1/sqrt(block)) H (alpha x)        (Sylvester-order Hadamard)
+ *   scale  = 448 / max|y|   (1 if y == 0)       (post-transform scale)
+ *   codes  = E4M3(y * scale), round to nearest even, saturating at +-448
+ * in one pass, with no intermediate global-memory round trip.
+ *
+ *  x_bf16   in   bf16 [rows, d]
+ *  rows, d       rows >= 0, d > 0, d % block == 0
+ *  block         128 or 256
+ *  e_target      target block energy, > 0 (finite)
+ *  eps           energy floor, > 0 (finite)
+ *  codes    out  uint8 [rows, d] E4M3FN codes
+ *  alpha    out  fp32 [nb]
+ *  scale    out  fp32 [nb]
+ */
+taco_status taco_compress(const void *x_bf16, int64_t rows, int64_t d, int32_t block,
+                          float e_target, float eps, uint8_t *codes, float *alpha,
+                          float *scale, taco_stream_t stream);
+
+/*
+ * taco_decompress - exact inverse of the compressor up to the FP8 rounding.
+ * [TACO] 2.B.2 reconstruction with both scales:
+ *   out = (1/sqrt(block)) H (decode(codes) / scale) / alpha
+ *
+ *  codes, alpha, scale   in   as produced by taco_compress
+ *  out                   out  [rows, d]: fp32, or bf16 (round to nearest
+ *                             even) when out_is_bf16 != 0
+ */
+taco_status taco_decompress(const uint8_t *codes, const float *alpha, const float *scale,
+                            int64_t rows, int64_t d, int32_t block, void *out,
+                            int32_t out_is_bf16, taco_stream_t stream);
+
+/*
+ * taco_reduce_shards - local step of the two-shot AllReduce
+ * ([TACO] 2.B.3 ReduceScatter + AllGather; [AGoQ] 2.B "local reduce in
+ * FP32"): P compressed shards of the same [rows, d] region, all resident in
+ * this GPU's memory, are dequantised, summed in FP32 and requantised with
+ * the compressor above.  Result = compress(sum_p decompress(shard p)); it is
+ * computed in the Hadamard domain, where the sum of the P reconstructions and
+ * the compressor's forward rotation cancel (c H c H = I), so no rotation is
+ * applied.
+ *
+ *  P                      1 .. TACO_MAX_SHARDS
+ *  codes, alpha, scale    in   HOST arrays of P device pointers, shard p
+ *                              laid out as taco_compress's outputs
+ *  out_codes, out_alpha,  out  the compressed sum, same layout
+ *  out_scale
+ */
+taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes,
+                               const float *const *alpha, const float *const *scale,
+                               int64_t rows, int64_t d, int32_t block, float e_target,
+                               float eps, uint8_t *out_codes, float *out_alpha,
+                               float *out_scale, taco_stream_t stream);
+
+/*
+ * agoq_fp8_accumulate - QuanGrad local accumulation, in place.
+ * [AGoQ] 2.B: per block of `block` elements,
+ *   g       = decode(main_codes) / main_scale + grad     (FP32)
+ *   scale'  = 448 / max|g|   (1 if g == 0)
+ *   codes'  = E4M3(g * scale')
+ * A zero gradient is codes 0 with scale 1.
+ *
+ *  main_codes  in/out  uint8 [n]
+ *  main_scale  in/out  fp32 [n / block]
+ *  grad_bf16   in      bf16 [n] micro-batch gradient
+ *  n                   n >= 0, n % block == 0
+ *  block               128 or 256
+ */
+taco_status agoq_fp8_accumulate(uint8_t *main_codes, float *main_scale, const void *grad_bf16,
+                                int64_t n, int32_t block, taco_stream_t stream);
+
+/*
+ * agoq_reduce_shards - precision-preserving all-reduce, local step.
+ * [AGoQ] 2.B step 2: S = sum_p decode(codes_p) / scale_p in FP32, then
+ * requantised per block as in agoq_fp8_accumulate (a sum, not a mean).
+ *
+ *  codes, scale      in   HOST arrays of P device pointers (uint8 [n],
+ *                         fp32 [n / block])
+ *  out_codes         out  uint8 [n]
+ *  out_scale         out  fp32 [n / block]
+ */
+taco_status agoq_reduce_shards(int32_t P, const uint8_t *const *codes, const float *const *scale,
+                               int64_t n, int32_t block, uint8_t *out_codes, float *out_scale,
+                               taco_stream_t stream);
+
+/*
+ * taco_device_error - watchdog flags of the kernels on the current device.
+ * Every in-kernel wait gives up after about a second and sets a bit here
+ * (bit 0: compressor, bit 1: decompressor).  Synchronises the device.  With
+ * clear != 0 the flags are reset to 0 after reading.
+ */
+taco_status taco_device_error(uint32_t *flags_out, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TACO_H */

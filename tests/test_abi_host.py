@@ -1,0 +1,126 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+function include/taco.h declares, and argument validation rejects bad calls
+before any CUDA call is made (the pointers below are never dereferenced)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_communication_compression_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "taco.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+A = 1 << 20  # a fake, 16-byte aligned "device address"; never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)) - {"if"})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_calls_of_the_boundary():
+    names = declared_functions()
+    for n in ("taco_compress", "taco_decompress", "taco_reduce_shards", "agoq_fp8_accumulate",
+              "agoq_reduce_shards", "taco_status_string", "taco_abi_version", "taco_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.taco_abi_version() == 1
+    for s in range(5):
+        assert lib.taco_status_string(s)
+    assert lib.taco_status_string(99) == b"unknown status"
+    assert lib.taco_block_supported(128) and lib.taco_block_supported(256)
+    assert not lib.taco_block_supported(64) and not lib.taco_block_supported(100)
+
+
+def compress(lib, x=A, rows=4, d=256, block=128, e=1.0, eps=1e-12, codes=A * 4, alpha=A * 8,
+             scale=A * 12):
+    return lib.taco_compress(x, rows, d, block, e, eps, codes, alpha, scale, None)
+
+
+def test_compress_validation(lib):
+    assert compress(lib, block=100) == UNSUPPORTED
+    assert compress(lib, block=64) == UNSUPPORTED
+    assert compress(lib, d=200) == INVALID
+    assert compress(lib, rows=-1) == INVALID
+    assert compress(lib, d=0) == INVALID
+    assert compress(lib, e=0.0) == INVALID
+    assert compress(lib, eps=-1.0) == INVALID
+    assert compress(lib, e=float("inf")) == INVALID
+    assert compress(lib, eps=float("nan")) == INVALID
+    assert compress(lib, rows=0) == OK  # empty input: no launch
+    assert compress(lib, x=0) == INVALID
+    assert compress(lib, codes=0) == INVALID
+    assert compress(lib, x=A + 8) == MISALIGNED
+    assert compress(lib, codes=A * 4 + 4) == MISALIGNED
+    assert compress(lib, alpha=A * 8 + 2) == MISALIGNED
+    assert compress(lib, codes=A + 16) == INVALID  # codes overlap the input
+    assert compress(lib, scale=A * 8 + 4) == INVALID  # scale overlaps alpha
+    assert compress(lib, rows=1 << 40, d=1 << 30) == INVALID  # rows * d overflows
+
+
+def test_decompress_validation(lib):
+    f = lambda **k: lib.taco_decompress(k.get("codes", A), k.get("alpha", A * 4), k.get("scale", A * 8),
+                                        k.get("rows", 4), k.get("d", 256), k.get("block", 128),
+                                        k.get("out", A * 12), k.get("bf16", 0), None)
+    assert f(block=512) == UNSUPPORTED
+    assert f(rows=0) == OK
+    assert f(out=0) == INVALID
+    assert f(out=A * 12 + 8) == MISALIGNED
+    assert f(out=A) == INVALID  # output overlaps the codes
+
+
+def test_reduce_validation(lib):
+    def f(P=2, rows=4, d=256, block=128, codes=None, out_codes=A * 64, e=1.0):
+        c = codes if codes is not None else [A * (1 + p) for p in range(P)]
+        cp, k1 = _lib.ptr_array(c)
+        ap, k2 = _lib.ptr_array([A * (20 + p) for p in range(P)])
+        sp, k3 = _lib.ptr_array([A * (40 + p) for p in range(P)])
+        return lib.taco_reduce_shards(P, cp, ap, sp, rows, d, block, e, 1e-12, out_codes, A * 80,
+                                      A * 90, None)
+    assert f(P=0) == UNSUPPORTED
+    assert f(P=17) == UNSUPPORTED
+    assert f(block=64) == UNSUPPORTED
+    assert f(rows=0) == OK
+    assert f(e=-1.0) == INVALID
+    assert f(codes=[A, 0]) == INVALID
+    assert f(codes=[A, A + 8]) == MISALIGNED
+    assert f(out_codes=A) == INVALID  # output overlaps shard 0
+
+
+def test_agoq_validation(lib):
+    acc = lambda n=1024, block=128, c=A, s=A * 4, g=A * 8: lib.agoq_fp8_accumulate(c, s, g, n, block, None)
+    assert acc(block=64) == UNSUPPORTED
+    assert acc(n=1000) == INVALID
+    assert acc(n=-128) == INVALID
+    assert acc(n=0) == OK
+    assert acc(g=A * 8 + 2) == MISALIGNED
+    assert acc(g=A + 512) == INVALID  # grad overlaps codes
+    cp, k1 = _lib.ptr_array([A, A * 2])
+    sp, k2 = _lib.ptr_array([A * 3, A * 4])
+    red = lambda P=2, n=1024, oc=A * 10, os_=A * 12: lib.agoq_reduce_shards(P, cp, sp, n, 128, oc, os_, None)
+    assert red(P=0) == UNSUPPORTED
+    assert red(n=0) == OK
+    assert red(oc=A * 10 + 1) == MISALIGNED
+    assert red(oc=A) == INVALID
+
+
+def test_device_error_rejects_null(lib):
+    assert lib.taco_device_error(None, 0) == INVALID

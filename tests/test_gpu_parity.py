@@ -1,0 +1,278 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Small and ragged cases are compared element by element; the full-size
+GPT-shaped and AGoQ workloads (launched exactly as the benchmark launches
+them) are compared on sampled blocks, which the oracle computes one by one,
+plus properties checked on every block.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+import oracle
+from fp8_communication_compression_gb300 import api
+from fp8_communication_compression_gb300 import workloads as W
+
+from parity import (assert_codes_match, assert_recon_match, assert_scalars_match, gather_blocks,
+                    gather_scalars, sample_blocks, to_dev_bf16, to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def no_watchdog_flags():
+    api.taco_device_error(clear=True)
+    yield
+    assert api.taco_device_error(clear=True) == 0
+
+
+def check_compress(bits: np.ndarray, block: int, e_target=1.0, eps=1e-12):
+    x = to_dev_bf16(bits)
+    c, a, s = api.taco_compress(x, block, e_target, eps)
+    rc, ra, rs = oracle.compress(bits, block, e_target, eps)
+    stats = assert_codes_match(to_host(c), rc)
+    assert_scalars_match(to_host(a), ra, "alpha")
+    assert_scalars_match(to_host(s), rs, "scale")
+    return (c, a, s), stats
+
+
+def check_decompress(c, a, s, block):
+    out = api.taco_decompress(c, a, s, block)
+    ref = oracle.decompress(to_host(c), to_host(a), to_host(s), block)
+    assert_recon_match(to_host(out), ref.reshape(-1), block)
+    outb = api.taco_decompress(c, a, s, block, out_dtype=torch.bfloat16)
+    g = to_host(outb.float()).astype(np.float64).reshape(-1)
+    r = ref.reshape(-1)
+    # bf16 output: round-to-nearest of a value within 1e-6 of the oracle's
+    assert np.all(np.abs(g - r) <= 2.0 ** -8 * np.abs(r) * (1 + 1e-5) + 1e-6 * np.abs(r).max())
+    return out
+
+
+# ------------------------------------------------------------ tiny case --
+
+def test_tiny_round_trip_and_p2_reduce():
+    name, n = "tiny_64x1024_n128", 128
+    shards = []
+    for p in range(2):
+        bits = W.shard_input(name, p)
+        (c, a, s), _ = check_compress(bits, n)
+        check_decompress(c, a, s, n)
+        shards.append((c, a, s))
+    cs, as_, ss = zip(*shards)
+    oc, oa, os_ = api.taco_reduce_shards(list(cs), list(as_), list(ss), n)
+    rc, ra, rs = oracle.reduce_shards([to_host(c) for c in cs], [to_host(a) for a in as_],
+                                      [to_host(s) for s in ss], n)
+    assert_codes_match(to_host(oc), rc, "reduced codes")
+    assert_scalars_match(to_host(oa), ra, "reduced alpha")
+    assert_scalars_match(to_host(os_), rs, "reduced scale")
+    check_decompress(oc, oa, os_, n)
+
+
+# ------------------------------------------------- ragged / multi-tile --
+
+@pytest.mark.parametrize("rows,d,block", [
+    (1, 128, 128), (37, 384, 128), (1000, 256, 128), (1, 256, 256), (33, 512, 256),
+    (500, 1024, 256), (2048, 4096, 128), (16384, 1024, 128), (8192, 2048, 256)])
+def test_codec_shapes(rows, d, block):
+    bits = W.tp_activation(rows * 7 + d, rows, d, channel_scale=True, block=block)
+    (c, a, s), _ = check_compress(bits, block)
+    check_decompress(c, a, s, block)
+
+
+@pytest.mark.parametrize("e_target,eps", [(4.0, 1e-12), (0.25, 1e-6), (1.0, 1e-30)])
+def test_codec_other_parameters(e_target, eps):
+    bits = W.tp_activation(5, 64, 1024, channel_scale=True)
+    (c, a, s), _ = check_compress(bits, 128, e_target, eps)
+    check_decompress(c, a, s, 128)
+
+
+def edge_blocks(n: int) -> np.ndarray:
+    H = scipy.linalg.hadamard(n).astype(np.float32)
+    rng = np.random.default_rng(3)
+    blocks = [
+        np.zeros(n),                                   # zero block
+        -np.zeros(n),                                  # negative zeros
+        np.eye(n)[5] * 1.0,                            # one-hot
+        -np.eye(n)[n - 1] * 0.015625,                  # one-hot, small
+        H[3] * 0.5,                                    # a Hadamard row
+        np.full(n, 2.0),                               # constant
+        np.where(np.arange(n) % 2, -1.0, 1.0) * 3.0,   # alternating signs
+        rng.standard_normal(n) * 1e-39,                # bf16 subnormals
+        rng.standard_normal(n) * 1e-30,                # tiny normals
+        rng.standard_normal(n) * 1e15,                 # large
+        np.concatenate([[1e4], rng.standard_normal(n - 1) * 1e-20]),  # one outlier
+        rng.standard_normal(n) * 448.0,
+        rng.standard_t(3, n) * 0.05,
+    ]
+    return np.stack(blocks).astype(np.float32)
+
+
+@pytest.mark.parametrize("block", [128, 256])
+def test_codec_edge_blocks(block):
+    x = edge_blocks(block)
+    bits = W.f32_to_bf16_bits(x)
+    (c, a, s), _ = check_compress(bits, block)
+    codes = to_host(c).reshape(-1, block)
+    assert np.all((codes[0] & 0x7F) == 0) and np.all((codes[1] & 0x7F) == 0)
+    assert to_host(s)[0] == 1.0 and to_host(s)[1] == 1.0
+    out = check_decompress(c, a, s, block)
+    assert np.all(to_host(out).reshape(-1, block)[:2] == 0.0)
+
+
+# ---------------------------------------------------------------- reduce --
+
+@pytest.mark.parametrize("P,block", [(1, 128), (2, 256), (3, 128), (4, 128), (8, 256), (16, 128)])
+def test_reduce_shard_counts(P, block):
+    rows, d = 96, 1024
+    shards = [api.taco_compress(to_dev_bf16(W.tp_activation(100 + p, rows, d, channel_scale=True,
+                                                           block=block)), block) for p in range(P)]
+    cs, as_, ss = zip(*shards)
+    oc, oa, os_ = api.taco_reduce_shards(list(cs), list(as_), list(ss), block)
+    rc, ra, rs = oracle.reduce_shards([to_host(c) for c in cs], [to_host(a) for a in as_],
+                                      [to_host(s) for s in ss], block)
+    assert_codes_match(to_host(oc), rc, "reduced codes")
+    assert_scalars_match(to_host(oa), ra, "reduced alpha")
+    assert_scalars_match(to_host(os_), rs, "reduced scale")
+
+
+def test_reduce_shard_and_negation_gives_zero_blocks():
+    block = 128
+    c, a, s = api.taco_compress(to_dev_bf16(W.tp_activation(9, 32, 512, block=block)), block)
+    neg = c ^ 0x80
+    oc, oa, os_ = api.taco_reduce_shards([c, neg], [a, a], [s, s], block)
+    assert torch.all((oc & 0x7F) == 0) and torch.all(os_ == 1.0)
+    assert torch.all(oa == np.float32(math.sqrt(1.0 / np.float64(np.float32(1e-12)))))
+
+
+# ------------------------------------------------------------------ AGoQ --
+
+@pytest.mark.parametrize("block", [128, 256])
+def test_agoq_accumulate_steps(block):
+    n = 1 << 16
+    codes = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    scale = torch.ones(n // block, dtype=torch.float32, device="cuda")
+    for k in range(4):
+        g = W.agoq_grad(100 + k, n)
+        prev_c, prev_s = to_host(codes).copy(), to_host(scale).copy()
+        api.agoq_fp8_accumulate(codes, scale, to_dev_bf16(g), block)
+        rc, rs = oracle.agoq_accumulate(prev_c, prev_s, g, block)
+        assert_codes_match(to_host(codes), rc, f"step {k} codes")
+        assert_scalars_match(to_host(scale), rs, f"step {k} scale")
+
+
+def test_agoq_zero_gradient_keeps_zero_buffer():
+    n = 4096
+    codes = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    scale = torch.ones(n // 128, dtype=torch.float32, device="cuda")
+    api.agoq_fp8_accumulate(codes, scale, torch.zeros(n, dtype=torch.bfloat16, device="cuda"))
+    assert torch.all(codes == 0) and torch.all(scale == 1.0)
+
+
+@pytest.mark.parametrize("P,block", [(1, 128), (2, 128), (8, 128), (16, 256)])
+def test_agoq_reduce(P, block):
+    n = 1 << 15
+    shards = []
+    for p in range(P):
+        c = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        s = torch.ones(n // block, dtype=torch.float32, device="cuda")
+        api.agoq_fp8_accumulate(c, s, to_dev_bf16(W.agoq_grad(300 + p, n)), block)
+        shards.append((c, s))
+    cs, ss = zip(*shards)
+    oc, os_ = api.agoq_reduce_shards(list(cs), list(ss), block)
+    rc, rs = oracle.agoq_reduce([to_host(c) for c in cs], [to_host(s) for s in ss], block)
+    assert_codes_match(to_host(oc), rc)
+    assert_scalars_match(to_host(os_), rs, "scale")
+
+
+# ----------------------------------------------- full-size workloads --
+
+def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None, block: int):
+    mag = (codes.reshape(-1, block) & 0x7F)
+    assert not torch.any(mag == 0x7F), "NaN code"
+    if x_bits_dev is not None:
+        nonzero = (x_bits_dev.reshape(-1, block).view(torch.int16) & 0x7FFF).ne(0).any(dim=1)
+        assert torch.all(mag.amax(dim=1)[nonzero] == 0x7E), "a non-zero block misses +-448"
+
+
+def sampled_compress_check(x_dev, bits_host_blocks, c, a, s, blocks, block):
+    rc, ra, rs = oracle.compress(bits_host_blocks, block)
+    assert_codes_match(gather_blocks(c, blocks, block), rc)
+    assert_scalars_match(gather_scalars(a, blocks), ra, "alpha")
+    assert_scalars_match(gather_scalars(s, blocks), rs, "scale")
+
+
+@pytest.mark.parametrize("name", ["gpt2.7b_4096x2560_n128", "gpt6.7b_p4x8192x4096_n128",
+                                  "gpt13b_p8x8192x5120_n256"])
+def test_full_size_two_shot_local_path(name):
+    w = W.WORKLOADS[name]
+    P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
+    bits = np.stack([W.shard_input(name, p) for p in range(P)])
+    x = to_dev_bf16(bits).reshape(P, rows, d)
+    nb = rows * d // block
+    path = api.TwoShotLocal(P, rows, d, block)
+    out = path.run(x)
+    torch.cuda.synchronize()
+    assert_code_properties(path.codes, x, block)
+    assert_code_properties(path.r_codes, None, block)
+    blocks = sample_blocks(nb, 1024, seed=P)
+    # compress: every shard on the sampled blocks
+    for p in range(P):
+        hb = bits[p].reshape(-1, block)[blocks]
+        sampled_compress_check(x[p], hb, path.codes[p], path.alpha[p], path.scale[p], blocks, block)
+    if P > 1:
+        # reduce on the GPU's own compressed shards
+        rc, ra, rs = oracle.reduce_shards([gather_blocks(path.codes[p], blocks, block) for p in range(P)],
+                                          [gather_scalars(path.alpha[p], blocks) for p in range(P)],
+                                          [gather_scalars(path.scale[p], blocks) for p in range(P)], block)
+        assert_codes_match(gather_blocks(path.r_codes, blocks, block), rc, "reduced codes")
+        assert_scalars_match(gather_scalars(path.r_alpha, blocks), ra, "reduced alpha")
+        assert_scalars_match(gather_scalars(path.r_scale, blocks), rs, "reduced scale")
+    # decompress of the (reduced) codes
+    src_c = path.r_codes if P > 1 else path.codes[0]
+    src_a = path.r_alpha if P > 1 else path.alpha[0]
+    src_s = path.r_scale if P > 1 else path.scale[0]
+    if P == 1:
+        out = api.taco_decompress(path.codes[0], path.alpha[0], path.scale[0], block)
+    ref = oracle.decompress(gather_blocks(src_c, blocks, block), gather_scalars(src_a, blocks),
+                            gather_scalars(src_s, blocks), block)
+    assert_recon_match(gather_blocks(out, blocks, block), ref, block)
+
+
+def test_full_size_agoq_accumulate_and_reduce():
+    a = W.AGOQ
+    block, n = a["block"], a["n_main"]
+    nb = n // block
+    blocks = sample_blocks(nb, 2048, seed=5)
+    codes = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    scale = torch.ones(nb, dtype=torch.float32, device="cuda")
+    for k, seed in enumerate(a["grad_seeds"]):
+        g = W.agoq_grad(seed, n)
+        prev_c = gather_blocks(codes, blocks, block)
+        prev_s = gather_scalars(scale, blocks)
+        api.agoq_fp8_accumulate(codes, scale, to_dev_bf16(g), block)
+        rc, rs = oracle.agoq_accumulate(prev_c, prev_s, g.reshape(-1, block)[blocks], block)
+        assert_codes_match(gather_blocks(codes, blocks, block), rc, f"step {k}")
+        assert_scalars_match(gather_scalars(scale, blocks), rs, f"step {k} scale")
+        del g
+    assert_code_properties(codes, None, block)
+    del codes, scale
+    ns = a["n_shard"]
+    shards = []
+    for p in range(a["reduce_P"]):
+        c = torch.zeros(ns, dtype=torch.uint8, device="cuda")
+        s = torch.ones(ns // block, dtype=torch.float32, device="cuda")
+        for k in range(a["micro_batches"]):
+            api.agoq_fp8_accumulate(c, s, to_dev_bf16(W.agoq_shard_grad(p, k, ns)), block)
+        shards.append((c, s))
+    cs, ss = zip(*shards)
+    oc, os_ = api.agoq_reduce_shards(list(cs), list(ss), block)
+    blocks = sample_blocks(ns // block, 2048, seed=6)
+    rc, rs = oracle.agoq_reduce([gather_blocks(c, blocks, block) for c in cs],
+                                [gather_scalars(s, blocks) for s in ss], block)
+    assert_codes_match(gather_blocks(oc, blocks, block), rc, "agoq reduce")
+    assert_scalars_match(gather_scalars(os_, blocks), rs, "agoq reduce scale")
