@@ -107,17 +107,20 @@ __global__ void __launch_bounds__(kBlockThreads)
             const float sa = valid ? __ldg(in.scale[p] + blk) * __ldg(in.alpha[p] + blk) : 1.0f;
             w[p] = (sa <= FLT_MAX) ? 1.0f / sa : (1.0f / __ldg(in.scale[p] + blk)) / __ldg(in.alpha[p] + blk);
         }
+        // Each product is rounded before it is added (no FMA contraction), so
+        // shards that cancel exactly sum to exactly zero.
         float T[kEPL];
+        decode16(q[0], T);
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
-            T[i] = 0.0f;
+            T[i] = __fmul_rn(T[i], w[0]);
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
+        for (int p = 1; p < P; ++p) {
             float d[kEPL];
             decode16(q[p], d);
 #pragma unroll
             for (int i = 0; i < kEPL; ++i)
-                T[i] = fmaf(d[i], w[p], T[i]);
+                T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w[p]));
         }
         float a4[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.0f;
 #pragma unroll
@@ -221,17 +224,19 @@ __global__ void __launch_bounds__(kBlockThreads)
 #pragma unroll
         for (int p = 0; p < P; ++p)
             inv[p] = 1.0f / (valid ? __ldg(in.scale[p] + blk) : 1.0f);
+        // products rounded before the add: exactly cancelling shards give 0
         float S[kEPL];
+        decode16(q[0], S);
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
-            S[i] = 0.0f;
+            S[i] = __fmul_rn(S[i], inv[0]);
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
+        for (int p = 1; p < P; ++p) {
             float d[kEPL];
             decode16(q[p], d);
 #pragma unroll
             for (int i = 0; i < kEPL; ++i)
-                S[i] = fmaf(d[i], inv[p], S[i]);
+                S[i] = __fadd_rn(S[i], __fmul_rn(d[i], inv[p]));
         }
         float mx = 0.0f;
 #pragma unroll

@@ -189,6 +189,15 @@ def test_agoq_reduce(P, block):
     assert_scalars_match(to_host(os_), rs, "scale")
 
 
+def test_agoq_reduce_shard_and_negation_gives_zero():
+    n = 1 << 13
+    c = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    s = torch.ones(n // 128, dtype=torch.float32, device="cuda")
+    api.agoq_fp8_accumulate(c, s, to_dev_bf16(W.agoq_grad(11, n)))
+    oc, os_ = api.agoq_reduce_shards([c, c ^ 0x80], [s, s])
+    assert torch.all((oc & 0x7F) == 0) and torch.all(os_ == 1.0)
+
+
 # ----------------------------------------------- full-size workloads --
 
 def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None, block: int):
