@@ -67,9 +67,18 @@ template <int LPB> __device__ __forceinline__ float group_max(float v)
     return v;
 }
 
-__device__ __forceinline__ float absmax_scale(float mx)
+// AGoQ per-block requantisation scalars from the block's absolute maximum:
+// codes use q = 448 / amax; the stored scale is the dequantisation
+// multiplier m = amax / 448 (both 1 for an all-zero block).
+__device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
 {
-    return (mx > 0.0f) ? fminf(448.0f / mx, FLT_MAX) : 1.0f;
+    if (amax > 0.0f) {
+        q = fminf(448.0f / amax, FLT_MAX);
+        m = amax / 448.0f;
+    } else {
+        q = 1.0f;
+        m = 1.0f;
+    }
 }
 
 // Warp-uniform grid-stride loop over lane slots.  Lanes past the end still
@@ -178,23 +187,25 @@ __global__ void __launch_bounds__(kBlockThreads)
             g1 = ldg128_stream(grad + off + 8);
             asm volatile("ld.global.f32 %0, [%1];" : "=f"(s_old) : "l"(scale + blk));
         }
-        const float inv = 1.0f / s_old;
+        // g = dequantise(main) + grad in FP32: one rounded multiply, then one
+        // rounded add (no fused multiply-add), as the stated arithmetic is.
         float d[kEPL];
         decode16(q, d);
         const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float mx = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            d[2 * i] = fmaf(d[2 * i], inv, bf16lo_to_f32(gw[i]));
-            d[2 * i + 1] = fmaf(d[2 * i + 1], inv, bf16hi_to_f32(gw[i]));
+            d[2 * i] = __fadd_rn(__fmul_rn(d[2 * i], s_old), bf16lo_to_f32(gw[i]));
+            d[2 * i + 1] = __fadd_rn(__fmul_rn(d[2 * i + 1], s_old), bf16hi_to_f32(gw[i]));
             mx = fmaxf(mx, fmaxf(fabsf(d[2 * i]), fabsf(d[2 * i + 1])));
         }
         mx = group_max<LPB>(mx);
-        const float s_new = absmax_scale(mx);
+        float qs, m_new;
+        agoq_scales(mx, qs, m_new);
         if (valid) {
-            stg128_stream(codes + off, encode16(d, s_new));
+            stg128_stream(codes + off, encode16(d, qs));
             if (part == 0)
-                scale[blk] = s_new;
+                scale[blk] = m_new;
         }
     }
 }
@@ -217,37 +228,39 @@ __global__ void __launch_bounds__(kBlockThreads)
         const int part = static_cast<int>(t % LPB);
         const int64_t off = blk * NB + part * kEPL;
         uint4 q[P];
-        float inv[P];
+        float m[P];
 #pragma unroll
         for (int p = 0; p < P; ++p)
             q[p] = valid ? ldg128_stream(in.codes[p] + off) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            inv[p] = 1.0f / (valid ? __ldg(in.scale[p] + blk) : 1.0f);
-        // products rounded before the add: exactly cancelling shards give 0
+            m[p] = valid ? __ldg(in.scale[p] + blk) : 1.0f;
+        // FP32 dequantise (one rounded multiply) and FP32 sum in shard order,
+        // no fused multiply-add: exactly cancelling shards give exactly 0
         float S[kEPL];
         decode16(q[0], S);
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
-            S[i] = __fmul_rn(S[i], inv[0]);
+            S[i] = __fmul_rn(S[i], m[0]);
 #pragma unroll
         for (int p = 1; p < P; ++p) {
             float d[kEPL];
             decode16(q[p], d);
 #pragma unroll
             for (int i = 0; i < kEPL; ++i)
-                S[i] = __fadd_rn(S[i], __fmul_rn(d[i], inv[p]));
+                S[i] = __fadd_rn(S[i], __fmul_rn(d[i], m[p]));
         }
         float mx = 0.0f;
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
             mx = fmaxf(mx, fabsf(S[i]));
         mx = group_max<LPB>(mx);
-        const float s_new = absmax_scale(mx);
+        float qs, m_new;
+        agoq_scales(mx, qs, m_new);
         if (valid) {
-            stg128_stream(out_codes + off, encode16(S, s_new));
+            stg128_stream(out_codes + off, encode16(S, qs));
             if (part == 0)
-                out_scale[blk] = s_new;
+                out_scale[blk] = m_new;
         }
     }
 }

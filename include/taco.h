@@ -130,14 +130,16 @@ taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes,
 
 /*
  * agoq_fp8_accumulate - QuanGrad local accumulation, in place.
- * [AGoQ] 2.B: per block of `block` elements,
- *   g       = decode(main_codes) / main_scale + grad     (FP32)
- *   scale'  = 448 / max|g|   (1 if g == 0)
- *   codes'  = E4M3(g * scale')
- * A zero gradient is codes 0 with scale 1.
+ * [AGoQ] 2.B: per block of `block` elements, in FP32 arithmetic,
+ *   g       = decode(main_codes) * main_scale + grad   (rounded multiply,
+ *                                                       then rounded add)
+ *   codes'  = E4M3(g * (448 / max|g|))
+ *   scale'  = max|g| / 448                             (1 if g == 0)
+ * The stored AGoQ scale is the dequantisation multiplier: an element's
+ * value is decode(code) * scale.  A zero gradient is codes 0 with scale 1.
  *
  *  main_codes  in/out  uint8 [n]
- *  main_scale  in/out  fp32 [n / block]
+ *  main_scale  in/out  fp32 [n / block] dequantisation multipliers
  *  grad_bf16   in      bf16 [n] micro-batch gradient
  *  n                   n >= 0, n % block == 0
  *  block               128 or 256
@@ -147,8 +149,9 @@ taco_status agoq_fp8_accumulate(uint8_t *main_codes, float *main_scale, const vo
 
 /*
  * agoq_reduce_shards - precision-preserving all-reduce, local step.
- * [AGoQ] 2.B step 2: S = sum_p decode(codes_p) / scale_p in FP32, then
- * requantised per block as in agoq_fp8_accumulate (a sum, not a mean).
+ * [AGoQ] 2.B step 2: S = sum_p decode(codes_p) * scale_p, each term a
+ * rounded FP32 multiply, summed in FP32 in shard order, then requantised
+ * per block as in agoq_fp8_accumulate (a sum, not a mean).
  *
  *  codes, scale      in   HOST arrays of P device pointers (uint8 [n],
  *                         fp32 [n / block])

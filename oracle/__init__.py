@@ -32,7 +32,8 @@ def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` next to its source (gcc, no CUDA)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -188,9 +189,11 @@ def agoq_reduce(codes, scales, block: int = 128):
 
 
 def agoq_dequantise(codes: np.ndarray, scale: np.ndarray, block: int = 128) -> np.ndarray:
+    """decode(code) * m per block, as float64 (the stored AGoQ scale m is the
+    dequantisation multiplier max|g| / 448)."""
     table = e4m3_decode_table()
     c = np.asarray(codes, dtype=np.uint8).reshape(-1, block)
-    return (table[c] / np.asarray(scale, dtype=np.float64).reshape(-1, 1)).reshape(-1)
+    return (table[c] * np.asarray(scale, dtype=np.float64).reshape(-1, 1)).reshape(-1)
 
 
 # --------------------------------------------------------- INT8 baseline --

@@ -34,8 +34,14 @@
  *   - Codes: E4M3FN, round to nearest with ties to even, saturating at 448.
  *     The value handed to the encoder is rounded to fp32 first, so the code
  *     decision is taken in the precision the GPU takes it in.
- *   - AGoQ scale: the same per-block absmax convention, s = 448 / max|g|.
  *   - Reduce: a sum (not a mean) of the dequantised shards, in shard order.
+ *   - AGoQ arithmetic is FP32, the precision the AGoQ page gives for the
+ *     all-reduce's local sum (and the one the accumulation is specified in):
+ *     dequantise = one rounded fp32 multiply, sums are sequential fp32 adds
+ *     in shard order, no fused multiply-add.  The stored per-block AGoQ
+ *     scale is the dequantisation multiplier m = max|g| / 448 (1 for an
+ *     all-zero block); codes are E4M3(g * q) with q = 448 / max|g|.
+ *   - Build with -ffp-contract=off so that no compiler fuses a*b+c.
  *
  * Pins: every entry point is checked by the non-GPU tests against facts that
  * do not come from this file (E4M3 against torch's float8_e4m3fn and the
@@ -281,64 +287,82 @@ int oracle_reduce_shards(int P, const uint8_t *const *codes, const float *const 
     return 0;
 }
 
-/* Requantise one block of high-precision values with the absmax scale. */
-static void absmax_quantise(const double *g, int n, uint8_t *codes, float *scale_out)
+/* AGoQ requantisation of one block of fp32 values: q = 448 / max|g| for the
+ * codes, m = max|g| / 448 stored for dequantisation (both fp32 divisions). */
+static void agoq_requantise(const float *g, int n, uint8_t *codes, float *scale_out)
 {
-    double maxabs = 0.0;
-    float s_f;
+    float amax = 0.0f, q = 1.0f, m = 1.0f;
     int i;
     for (i = 0; i < n; ++i)
-        if (fabs(g[i]) > maxabs)
-            maxabs = fabs(g[i]);
-    s_f = ds_scale(maxabs);
-    for (i = 0; i < n; ++i)
-        codes[i] = oracle_e4m3_encode((float)(g[i] * (double)s_f));
-    *scale_out = s_f;
+        if (fabsf(g[i]) > amax)
+            amax = fabsf(g[i]);
+    if (amax > 0.0f) {
+        q = 448.0f / amax;
+        if (!(q <= FLT_MAX))
+            q = FLT_MAX;
+        m = amax / 448.0f;
+    }
+    for (i = 0; i < n; ++i) {
+        const float v = g[i] * q;
+        codes[i] = oracle_e4m3_encode(v);
+    }
+    *scale_out = m;
+}
+
+/* Dequantise one code to FP32: decode (exact) times the block multiplier. */
+static float agoq_dequantise(uint8_t code, float m)
+{
+    const float d = (float)oracle_e4m3_decode(code);
+    const float x = d * m;
+    return x;
 }
 
 /* [AGoQ] 2.B local accumulation, in place: per block,
- *   g = decode(main) / s + grad;  s' = 448 / max|g|;  main' = E4M3(g * s').
- * The dequantised values are held in double (the pages name FP16/BF16 or
- * FP32; double is at least as exact).  n must be a multiple of block. */
+ *   g = dequantise(main) + grad      (FP32: one multiply, then one add)
+ *   main' = requantise(g).
+ * n must be a multiple of block. */
 int oracle_agoq_accumulate(uint8_t *main_codes, float *main_scale, const uint16_t *grad_bf16,
                            int64_t n, int block)
 {
     int64_t nb, k;
     int i;
-    double *g;
+    float *g;
     if (n < 0 || !valid_block(block) || n % block != 0)
         return -1;
     nb = n / block;
-    g = (double *)malloc(sizeof(double) * block);
+    g = (float *)malloc(sizeof(float) * block);
     for (k = 0; k < nb; ++k) {
-        for (i = 0; i < block; ++i)
-            g[i] = oracle_e4m3_decode(main_codes[k * block + i]) / (double)main_scale[k] +
-                   bf16_to_double(grad_bf16[k * block + i]);
-        absmax_quantise(g, block, main_codes + k * block, main_scale + k);
+        for (i = 0; i < block; ++i) {
+            const float deq = agoq_dequantise(main_codes[k * block + i], main_scale[k]);
+            const float grad = (float)bf16_to_double(grad_bf16[k * block + i]);
+            g[i] = deq + grad;
+        }
+        agoq_requantise(g, block, main_codes + k * block, main_scale + k);
     }
     free(g);
     return 0;
 }
 
 /* [AGoQ] 2.B precision-preserving all-reduce, step 2: dequantise the P
- * received FP8 shards, sum in high precision (shard order), requantise. */
+ * received FP8 shards to FP32, sum them in FP32 in shard order, requantise. */
 int oracle_agoq_reduce(int P, const uint8_t *const *codes, const float *const *scale, int64_t n,
                        int block, uint8_t *out_codes, float *out_scale)
 {
     int64_t nb, k;
     int p, i;
-    double *g;
+    float *g;
     if (n < 0 || !valid_block(block) || n % block != 0 || P < 1)
         return -1;
     nb = n / block;
-    g = (double *)malloc(sizeof(double) * block);
+    g = (float *)malloc(sizeof(float) * block);
     for (k = 0; k < nb; ++k) {
-        for (i = 0; i < block; ++i)
-            g[i] = 0.0;
-        for (p = 0; p < P; ++p)
-            for (i = 0; i < block; ++i)
-                g[i] += oracle_e4m3_decode(codes[p][k * block + i]) / (double)scale[p][k];
-        absmax_quantise(g, block, out_codes + k * block, out_scale + k);
+        for (i = 0; i < block; ++i) {
+            float sum = agoq_dequantise(codes[0][k * block + i], scale[0][k]);
+            for (p = 1; p < P; ++p)
+                sum = sum + agoq_dequantise(codes[p][k * block + i], scale[p][k]);
+            g[i] = sum;
+        }
+        agoq_requantise(g, block, out_codes + k * block, out_scale + k);
     }
     free(g);
     return 0;

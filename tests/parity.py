@@ -35,7 +35,10 @@ def ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(sa * ma - sb * mb)
 
 
-def assert_codes_match(gpu: np.ndarray, ref: np.ndarray, what: str = "codes") -> dict:
+def assert_codes_match(gpu: np.ndarray, ref: np.ndarray, what: str = "codes", exact: bool = False) -> dict:
+    if exact:
+        bad = np.flatnonzero(gpu.reshape(-1) != ref.reshape(-1))
+        assert bad.size == 0, f"{what}: {bad.size} codes differ, first at {bad[:5]}"
     d = ulp_distance(gpu, ref)
     same = float(np.mean(d == 0))
     worst = int(d.max()) if d.size else 0
@@ -44,7 +47,10 @@ def assert_codes_match(gpu: np.ndarray, ref: np.ndarray, what: str = "codes") ->
     return {"identical": same, "max_ulp": worst}
 
 
-def assert_scalars_match(gpu: np.ndarray, ref: np.ndarray, what: str, rtol: float = SCALAR_RTOL) -> float:
+def assert_scalars_match(gpu: np.ndarray, ref: np.ndarray, what: str, rtol: float = SCALAR_RTOL,
+                         exact: bool = False) -> float:
+    if exact:
+        assert np.array_equal(gpu.reshape(-1), ref.reshape(-1)), f"{what}: not bit-identical"
     g = gpu.astype(np.float64).reshape(-1)
     r = ref.astype(np.float64).reshape(-1)
     assert np.all(np.isfinite(g)), f"{what}: non-finite"
