@@ -134,10 +134,12 @@ class ClockSampler:
                 "samples": n}
 
 
-def make_inputs(rank: int):
+def make_inputs(rank: int, rows: int | None = None):
     from fp8_communication_compression_gb300 import workloads as W
 
-    w = W.WORKLOADS[HEADLINE]
+    w = dict(W.WORKLOADS[HEADLINE])
+    if rows is not None:
+        w["rows"] = rows
     shards = []
     for p in range(w["shards"]):
         seed = w["seeds"][p] + 1000 * rank
@@ -219,6 +221,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="rows per shard (a smaller case of the same workload, e.g. for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -241,7 +245,7 @@ def main():
 
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    w, bits = make_inputs(rank)
+    w, bits = make_inputs(rank, args.rows)
     P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
     n = rows * d
     nbytes = algorithmic_bytes(P, n, block)
@@ -298,26 +302,28 @@ def main():
            for i, name in enumerate(("compress", "reduce", "decompress"))}
 
     # end to end through the public API with pinned host buffers
-    h_in = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
-    h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
-    h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
-    x2 = torch.empty_like(x)
-    for _ in range(3):
-        path.run_host(h_in, h_out, x2)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        path.run_host(h_in, h_out, x2)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = None
+    if args.e2e_steps > 0:
+        h_in = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
+        h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+        h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
+        x2 = torch.empty_like(x)
+        for _ in range(3):
+            path.run_host(h_in, h_out, x2)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            path.run_host(h_in, h_out, x2)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
     flags = api.taco_device_error(clear=True)
 
     if rank == 0:
@@ -333,7 +339,8 @@ def main():
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": HEADLINE, "P": P, "rows": rows, "d": d, "block": block,
+            "config": {"workload": HEADLINE if args.rows is None else f"{HEADLINE} (rows={rows})",
+                       "P": P, "rows": rows, "d": d, "block": block,
                        "bytes_per_step": step_bytes,
                        "input_bf16_bytes_per_step": 2 * P * n,
                        "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
@@ -343,9 +350,10 @@ def main():
                          "traffic": committed_traffic(), "peak_source": peak_src},
             "kernels": kern,
             "step_frac_of_peak": value / world / peak,
-            "e2e": {"value": step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
-                    "api": "TwoShotLocal.run_host (pinned host in/out)"},
+            "e2e": None if e2e_ms is None else {
+                "value": step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
+                "api": "TwoShotLocal.run_host (pinned host in/out)"},
             "gpu_launches": 3 * K,
             "clocks": clk,
             "watchdog_flags": flags,
