@@ -210,6 +210,74 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def time_launches(torch, fn, reps: int, stream) -> float:
+    """Mean CUDA-event duration (ms) of ``fn`` over ``reps`` launches."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(stream)
+    for i in range(reps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+
+
+def agoq_leg(torch, api, peak: float) -> dict:
+    """AGoQ accumulate over the 2^28-element buffer and the P=8 reduce of
+    2^25-element shards; inputs larger than L2, per-launch CUDA events."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    a = W.AGOQ
+    n, block, P, ns = a["n_main"], a["block"], a["reduce_P"], a["n_shard"]
+    g = torch.from_numpy(W.agoq_grad(a["grad_seeds"][0], n).view(np.int16)).cuda().view(torch.bfloat16)
+    codes = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    scale = torch.ones(n // block, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    api.agoq_fp8_accumulate(codes, scale, g, block)
+    acc_ms = time_launches(torch, lambda: api.agoq_fp8_accumulate(codes, scale, g, block), 4, stream)
+    acc_bytes = n * (1 + 2 + 1) + 2 * 4 * (n // block)
+    del codes, scale
+    sc = [torch.zeros(ns, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    ss = [torch.ones(ns // block, dtype=torch.float32, device="cuda") for _ in range(P)]
+    for p in range(P):
+        api.agoq_fp8_accumulate(sc[p], ss[p], g[p * ns:(p + 1) * ns], block)
+    oc = torch.empty(ns, dtype=torch.uint8, device="cuda")
+    os_ = torch.empty(ns // block, dtype=torch.float32, device="cuda")
+    api.agoq_reduce_shards(sc, ss, block, oc, os_)
+    red_ms = time_launches(torch, lambda: api.agoq_reduce_shards(sc, ss, block, oc, os_), 5, stream)
+    red_bytes = (P + 1) * (ns + 4 * (ns // block))
+    out = {}
+    for name, ms, b, units in (("accumulate", acc_ms, acc_bytes, f"2^28 elements, n={block}"),
+                               ("reduce", red_ms, red_bytes, f"P={P} x 2^25 elements, n={block}")):
+        gbs = b / (ms / 1e3) / 1e9
+        out[name] = {"us_per_launch": ms * 1e3, "algorithmic_bytes": b, "gbs": gbs,
+                     "frac_of_peak": gbs / peak, "workload": units}
+    return out
+
+
+def gpt13b_leg(torch, api, peak: float) -> dict:
+    """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-kernel
+    CUDA-event times of compress, reduce and decompress."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    name = "gpt13b_p8x8192x5120_n256"
+    w = W.WORKLOADS[name]
+    P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
+    bits = np.stack([W.shard_input(name, p) for p in range(P)])
+    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    del bits
+    path = api.TwoShotLocal(P, rows, d, block)
+    for _ in range(3):
+        path.run(x)
+    stream = torch.cuda.current_stream()
+    ms = {"compress": time_launches(torch, lambda: path.compress(x), 10, stream),
+          "reduce": time_launches(torch, path.reduce, 10, stream),
+          "decompress": time_launches(torch, path.decompress, 10, stream)}
+    nb = algorithmic_bytes(P, rows * d, block)
+    return {k: {"us_per_launch": ms[k] * 1e3, "algorithmic_bytes": nb[k],
+                "gbs": nb[k] / (ms[k] / 1e3) / 1e9, "frac_of_peak": nb[k] / (ms[k] / 1e3) / 1e9 / peak}
+            for k in ms}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,6 +289,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
+    ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
+    ap.add_argument("--gpt13b", action="store_true",
+                    help="also time the GPT-13B-shaped path (P=8, n=256; slow input generation)")
     ap.add_argument("--rows", type=int, default=None,
                     help="rows per shard (a smaller case of the same workload, e.g. for profiling)")
     args = ap.parse_args()
@@ -324,10 +395,19 @@ def main():
             t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
+    peak, peak_src = hbm_peak()
+    extra = {}
+    if rank == 0 and not args.no_agoq:
+        del path, x
+        torch.cuda.empty_cache()
+        extra["agoq"] = agoq_leg(torch, api, peak)
+        torch.cuda.empty_cache()
+    if rank == 0 and args.gpt13b:
+        extra["gpt13b_p8x8192x5120_n256"] = gpt13b_leg(torch, api, peak)
+        torch.cuda.empty_cache()
     flags = api.taco_device_error(clear=True)
 
     if rank == 0:
-        peak, peak_src = hbm_peak()
         value = step_bytes * K * world / (elapsed_ms / 1e3) / 1e9
         kern = {}
         for name in ("compress", "reduce", "decompress"):
@@ -354,6 +434,7 @@ def main():
                 "value": step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
                 "api": "TwoShotLocal.run_host (pinned host in/out)"},
+            "other_workloads": extra,
             "gpu_launches": 3 * K,
             "clocks": clk,
             "watchdog_flags": flags,

@@ -66,18 +66,33 @@ template <> struct BlockConst<256> {
     static constexpr float inv_n = 1.0f / 256.0f;
 };
 
-// Unnormalised Sylvester-order Walsh-Hadamard transform of 128 registers:
-// for h = 1, 2, ..., 64, pairs (i, i + h) become (a + b, a - b).
-__device__ __forceinline__ void fwht128(float (&v)[128])
+// A thread's 128-element row lives in 64 float2 registers: v[k] holds
+// elements 2k and 2k + 1.  The butterfly stage on index bit 0 is done with
+// scalar adds while the row is unpacked; the stages on bits 1..6 pair whole
+// float2 registers and run as packed fp32x2 instructions (sm_100 family),
+// which halves their instruction count.  a - b is computed as
+// fma(b, -1, a): the product is exact, so the result (signed zeros
+// included) is that of the subtraction.
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+
+// Stages h = 2, 4, ..., 64 of the unnormalised Sylvester-order Walsh-
+// Hadamard transform: pairs (i, i + h) become (a + b, a - b).  Together
+// with the bit-0 stage done at unpack time this is the full 128-point
+// transform, in the order h = 1, 2, ..., 64.
+__device__ __forceinline__ void fwht128_upper(float2 (&v)[64])
 {
 #pragma unroll
-    for (int h = 1; h < 128; h <<= 1) {
+    for (int hh = 1; hh < 64; hh <<= 1) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-            if ((i & h) == 0) {
-                const float a = v[i], b = v[i + h];
-                v[i] = a + b;
-                v[i + h] = a - b;
+        for (int k = 0; k < 64; ++k) {
+            if ((k & hh) == 0) {
+                const float2 a = v[k], b = v[k + hh];
+                v[k] = __fadd2_rn(a, b);
+                v[k + hh] = sub2(a, b);
             }
         }
     }
@@ -86,42 +101,52 @@ __device__ __forceinline__ void fwht128(float (&v)[128])
 // Last stage of a 256-point transform across a lane pair: the even lane
 // holds elements 0..127 (a), the odd lane 128..255 (b); even gets a + b,
 // odd gets a - b.
-__device__ __forceinline__ void fwht_pair_stage(float (&v)[128], int lane)
+__device__ __forceinline__ void fwht_pair_stage(float2 (&v)[64], int lane)
 {
-    const float sgn = (lane & 1) ? -1.0f : 1.0f;
+    const float sg = (lane & 1) ? -1.0f : 1.0f;
+    const float2 sgn = make_float2(sg, sg);
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-        const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
-        v[i] = fmaf(sgn, v[i], o);
+    for (int k = 0; k < 64; ++k) {
+        float2 o;
+        o.x = __shfl_xor_sync(0xFFFFFFFFu, v[k].x, 1);
+        o.y = __shfl_xor_sync(0xFFFFFFFFu, v[k].y, 1);
+        v[k] = __ffma2_rn(sgn, v[k], o);
     }
 }
 
-// Sum of squares with 16 interleaved accumulators and a final tree, so the
-// fp32 rounding error stays within ~11 ulp of the sum.
-__device__ __forceinline__ float sum_squares128(const float (&v)[128])
-{
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        acc[i] = v[i] * v[i];
-#pragma unroll
-    for (int i = 16; i < 128; ++i)
-        acc[i & 15] = fmaf(v[i], v[i], acc[i & 15]);
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i)
-            acc[i] += acc[i + w];
-    return acc[0];
-}
-
-__device__ __forceinline__ float max_abs128(const float (&v)[128])
+__device__ __forceinline__ float max_abs128(const float2 (&v)[64])
 {
     float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 128; ++i)
-        m[i & 3] = fmaxf(m[i & 3], fabsf(v[i]));
+    for (int k = 0; k < 64; ++k)
+        m[k & 3] = fmaxf(m[k & 3], fmaxf(fabsf(v[k].x), fabsf(v[k].y)));
     return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// Unpacks 8 bf16 values (one 16-byte chunk) into four float2 registers
+// v[k0 .. k0+3] after the bit-0 butterfly stage, and adds their squares to
+// the packed energy accumulators.
+__device__ __forceinline__ void unpack8_stage1(const uint4 q, float2 (&v)[64], int k0, float2 (&acc)[8],
+                                               bool first)
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float lo = bf16lo_to_f32(w[t]), hi = bf16hi_to_f32(w[t]);
+        const float2 x = make_float2(lo, hi);
+        const int a = (k0 + t) & 7;
+        acc[a] = first ? __fmul2_rn(x, x) : __ffma2_rn(x, x, acc[a]);
+        v[k0 + t] = make_float2(lo + hi, lo - hi);
+    }
+}
+
+// Four float2 pairs times k -> 8 E4M3 codes in two words.
+__device__ __forceinline__ void encode8(const float2 *v, float2 k2, uint32_t &w0, uint32_t &w1)
+{
+    const float2 a = __fmul2_rn(v[0], k2), b = __fmul2_rn(v[1], k2);
+    const float2 c = __fmul2_rn(v[2], k2), d = __fmul2_rn(v[3], k2);
+    w0 = f32x4_to_e4m3x4(a.x, a.y, b.x, b.y);
+    w1 = f32x4_to_e4m3x4(c.x, c.y, d.x, d.y);
 }
 
 // ===================================================================== //
@@ -181,26 +206,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Lane l reads row l of the stage: half h holds elements 64h .. 64h+63,
         // and 16-byte chunk j of a 128-byte row sits at chunk j ^ (l & 7).
         const uint32_t rowp = wbase + s * kCStageBytes + lane * 128;
-        float v[128];
+        float2 v[64];
+        float2 acc[8];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint4 q = lds128(rowp + h * kCHalfBytes + ((static_cast<uint32_t>(j) << 4) ^ swz));
-                const int e = h * 64 + j * 8;
-                v[e + 0] = bf16lo_to_f32(q.x);
-                v[e + 1] = bf16hi_to_f32(q.x);
-                v[e + 2] = bf16lo_to_f32(q.y);
-                v[e + 3] = bf16hi_to_f32(q.y);
-                v[e + 4] = bf16lo_to_f32(q.z);
-                v[e + 5] = bf16hi_to_f32(q.z);
-                v[e + 6] = bf16lo_to_f32(q.w);
-                v[e + 7] = bf16hi_to_f32(q.w);
+                // step 1 (energy, exact squares of bf16 values) and the
+                // bit-0 butterfly stage of step 3
+                unpack8_stage1(q, v, h * 32 + j * 4, acc, h == 0 && j < 2);
             }
         }
-        // step 1: block energy (x^2 of a bf16 value is exact in fp32); it
-        // consumes every loaded value, so the stage can be refilled after it
-        float ss = sum_squares128(v);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i)
+                acc[i] = __fadd2_rn(acc[i], acc[i + w]);
+        float ss = acc[0].x + acc[0].y;
+        // every loaded value has been consumed: refill the stage
         __syncwarp();
         if (lane == 0) {
             const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
@@ -215,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // step 3 (rotation; the alpha and 1/sqrt(n) factors are applied below)
-        fwht128(v);
+        // step 3: remaining butterfly stages (alpha and 1/sqrt(n) are applied below)
+        fwht128_upper(v);
         if constexpr (G == 2) {
             fwht_pair_stage(v, lane);
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
@@ -233,11 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
         float k = ac * scale;
         if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
+            const float2 ac2 = make_float2(ac, ac);
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-                v[i] *= ac;
+            for (int i = 0; i < 64; ++i)
+                v[i] = __fmul2_rn(v[i], ac2);
             k = scale;
         }
+        const float2 k2 = make_float2(k, k);
 
         // step 5: codes = E4M3(y * s) into the warp's swizzled staging rows
         if (lane == 0)
@@ -245,11 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int e = 16 * j;
-            const uint32_t w0 = f32x4_to_e4m3x4(v[e + 0] * k, v[e + 1] * k, v[e + 2] * k, v[e + 3] * k);
-            const uint32_t w1 = f32x4_to_e4m3x4(v[e + 4] * k, v[e + 5] * k, v[e + 6] * k, v[e + 7] * k);
-            const uint32_t w2 = f32x4_to_e4m3x4(v[e + 8] * k, v[e + 9] * k, v[e + 10] * k, v[e + 11] * k);
-            const uint32_t w3 = f32x4_to_e4m3x4(v[e + 12] * k, v[e + 13] * k, v[e + 14] * k, v[e + 15] * k);
+            uint32_t w0, w1, w2, w3;
+            encode8(&v[8 * j], k2, w0, w1);
+            encode8(&v[8 * j + 4], k2, w2, w3);
             sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
         }
         fence_proxy_async_smem();
@@ -326,21 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         const uint32_t rowp = wbase + s * kDStageBytes + lane * 128;
-        float v[128];
+        float2 v[64];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint4 q = lds128(rowp + ((static_cast<uint32_t>(j) << 4) ^ swz));
-            const int e = 16 * j;
-            e4m3x2_to_f32x2(q.x, v[e + 0], v[e + 1]);
-            e4m3x2_to_f32x2(q.x >> 16, v[e + 2], v[e + 3]);
-            e4m3x2_to_f32x2(q.y, v[e + 4], v[e + 5]);
-            e4m3x2_to_f32x2(q.y >> 16, v[e + 6], v[e + 7]);
-            e4m3x2_to_f32x2(q.z, v[e + 8], v[e + 9]);
-            e4m3x2_to_f32x2(q.z >> 16, v[e + 10], v[e + 11]);
-            e4m3x2_to_f32x2(q.w, v[e + 12], v[e + 13]);
-            e4m3x2_to_f32x2(q.w >> 16, v[e + 14], v[e + 15]);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                // 4 codes -> 4 values, then the bit-0 butterfly stage
+                float e0, e1, e2, e3;
+                e4m3x2_to_f32x2(w[t], e0, e1);
+                e4m3x2_to_f32x2(w[t] >> 16, e2, e3);
+                v[8 * j + 2 * t] = make_float2(e0 + e1, e0 - e1);
+                v[8 * j + 2 * t + 1] = make_float2(e2 + e3, e2 - e3);
+            }
         }
-        fwht128(v);  // consumes every decoded value
+        fwht128_upper(v);  // consumes every decoded value
         __syncwarp();
         if (lane == 0) {
             const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
@@ -360,11 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float k = c / sa;
         if (!(sa <= FLT_MAX) || !(k >= FLT_MIN)) {  // extreme scales: divide in two steps
             const float inv_s = 1.0f / sc;
+            const float2 i2 = make_float2(inv_s, inv_s);
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-                v[i] *= inv_s;
+            for (int i = 0; i < 64; ++i)
+                v[i] = __fmul2_rn(v[i], i2);
             k = c / a;
         }
+        const float2 k2 = make_float2(k, k);
 
         if (lane == 0)
             bulk_wait_read_all();
@@ -375,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < 32; ++ch) {
                 const uint32_t b = ch >> 3, j = ch & 7;
                 const uint32_t addr = outw + b * 4096 + lane * 128 + ((j << 4) ^ swz);
-                const int e = 4 * ch;
-                sts128(addr, __float_as_uint(v[e] * k), __float_as_uint(v[e + 1] * k),
-                       __float_as_uint(v[e + 2] * k), __float_as_uint(v[e + 3] * k));
+                const float2 p0 = __fmul2_rn(v[2 * ch], k2), p1 = __fmul2_rn(v[2 * ch + 1], k2);
+                sts128(addr, __float_as_uint(p0.x), __float_as_uint(p0.y), __float_as_uint(p1.x),
+                       __float_as_uint(p1.y));
             }
         } else {
             // 2 boxes of 64 bf16 (128 bytes) x 32 rows
@@ -385,11 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < 16; ++ch) {
                 const uint32_t b = ch >> 3, j = ch & 7;
                 const uint32_t addr = outw + b * 4096 + lane * 128 + ((j << 4) ^ swz);
-                const int e = 8 * ch;
-                sts128(addr, f32x2_to_bf16x2(v[e] * k, v[e + 1] * k),
-                       f32x2_to_bf16x2(v[e + 2] * k, v[e + 3] * k),
-                       f32x2_to_bf16x2(v[e + 4] * k, v[e + 5] * k),
-                       f32x2_to_bf16x2(v[e + 6] * k, v[e + 7] * k));
+                float2 p[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    p[t] = __fmul2_rn(v[4 * ch + t], k2);
+                sts128(addr, f32x2_to_bf16x2(p[0].x, p[0].y), f32x2_to_bf16x2(p[1].x, p[1].y),
+                       f32x2_to_bf16x2(p[2].x, p[2].y), f32x2_to_bf16x2(p[3].x, p[3].y));
             }
         }
         fence_proxy_async_smem();

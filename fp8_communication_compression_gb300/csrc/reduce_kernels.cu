@@ -1,8 +1,10 @@
 // Shard reduce (TACO two-shot local step) and AGoQ FP8 gradient kernels for
 // sm_103a.  None of these needs a Hadamard rotation on its path, so they
-// use plain coalesced 16-byte loads: a lane owns 16 consecutive elements of
-// a block, NB / 16 adjacent lanes own one block, and per-block statistics
-// (sum of squares, absolute maximum) are combined with __shfl_xor_sync.
+// use plain coalesced 16-byte loads: a lane owns 32 consecutive elements of
+// a block, NB / 32 adjacent lanes own one block, per-block statistics (sum
+// of squares, absolute maximum) are combined with __shfl_xor_sync, and the
+// per-shard scalars of a block are fetched once per lane group and
+// broadcast with __shfl_sync.
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -26,29 +28,39 @@ namespace taco {
 
 namespace {
 
-constexpr int kEPL = 16;  // elements per lane
+constexpr int kEPL = 32;  // elements per lane
 constexpr int kBlockThreads = 256;
 
-__device__ __forceinline__ void decode16(const uint4 q, float (&d)[16])
+// 32 codes (two 16-byte words) -> 32 fp32 values (exact)
+__device__ __forceinline__ void decode32(const uint4 (&q)[2], float (&d)[32])
 {
-    e4m3x2_to_f32x2(q.x, d[0], d[1]);
-    e4m3x2_to_f32x2(q.x >> 16, d[2], d[3]);
-    e4m3x2_to_f32x2(q.y, d[4], d[5]);
-    e4m3x2_to_f32x2(q.y >> 16, d[6], d[7]);
-    e4m3x2_to_f32x2(q.z, d[8], d[9]);
-    e4m3x2_to_f32x2(q.z >> 16, d[10], d[11]);
-    e4m3x2_to_f32x2(q.w, d[12], d[13]);
-    e4m3x2_to_f32x2(q.w >> 16, d[14], d[15]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            e4m3x2_to_f32x2(w[j], d[16 * h + 4 * j + 0], d[16 * h + 4 * j + 1]);
+            e4m3x2_to_f32x2(w[j] >> 16, d[16 * h + 4 * j + 2], d[16 * h + 4 * j + 3]);
+        }
+    }
 }
 
-__device__ __forceinline__ uint4 encode16(const float (&v)[16], float k)
+__device__ __forceinline__ void encode32(const float (&v)[32], float k, uint4 (&q)[2])
 {
-    uint4 q;
-    q.x = f32x4_to_e4m3x4(v[0] * k, v[1] * k, v[2] * k, v[3] * k);
-    q.y = f32x4_to_e4m3x4(v[4] * k, v[5] * k, v[6] * k, v[7] * k);
-    q.z = f32x4_to_e4m3x4(v[8] * k, v[9] * k, v[10] * k, v[11] * k);
-    q.w = f32x4_to_e4m3x4(v[12] * k, v[13] * k, v[14] * k, v[15] * k);
-    return q;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *x = v + 16 * h;
+        q[h].x = f32x4_to_e4m3x4(x[0] * k, x[1] * k, x[2] * k, x[3] * k);
+        q[h].y = f32x4_to_e4m3x4(x[4] * k, x[5] * k, x[6] * k, x[7] * k);
+        q[h].z = f32x4_to_e4m3x4(x[8] * k, x[9] * k, x[10] * k, x[11] * k);
+        q[h].w = f32x4_to_e4m3x4(x[12] * k, x[13] * k, x[14] * k, x[15] * k);
+    }
+}
+
+__device__ __forceinline__ void load32_codes(const uint8_t *p, bool valid, uint4 (&q)[2])
+{
+    q[0] = valid ? ldg128_stream(p) : make_uint4(0, 0, 0, 0);
+    q[1] = valid ? ldg128_stream(p + 16) : make_uint4(0, 0, 0, 0);
 }
 
 template <int LPB> __device__ __forceinline__ float group_sum(float v)
@@ -106,27 +118,40 @@ __global__ void __launch_bounds__(kBlockThreads)
         const int64_t blk = valid ? t / LPB : 0;
         const int part = static_cast<int>(t % LPB);
         const int64_t off = blk * NB + part * kEPL;
-        uint4 q[P];
+        uint4 q[P][2];
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            load32_codes(in.codes[p] + off, valid, q[p]);
+        // 1 / (s_p alpha_p): lane `part` of the group computes it for shards
+        // part, part + LPB, ...; the group then shares the values.
+        constexpr int ROUNDS = (P + LPB - 1) / LPB;
+        float wr[ROUNDS];
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int p = r * LPB + part;
+            wr[r] = 1.0f;
+            if (valid && p < P) {
+                const float sc = __ldg(in.scale[p] + blk), al = __ldg(in.alpha[p] + blk);
+                const float sa = sc * al;
+                wr[r] = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
+            }
+        }
+        const int gbase = lane & ~(LPB - 1);
         float w[P];
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            q[p] = valid ? ldg128_stream(in.codes[p] + off) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const float sa = valid ? __ldg(in.scale[p] + blk) * __ldg(in.alpha[p] + blk) : 1.0f;
-            w[p] = (sa <= FLT_MAX) ? 1.0f / sa : (1.0f / __ldg(in.scale[p] + blk)) / __ldg(in.alpha[p] + blk);
-        }
+            w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
         // Each product is rounded before it is added (no FMA contraction), so
         // shards that cancel exactly sum to exactly zero.
         float T[kEPL];
-        decode16(q[0], T);
+        decode32(q[0], T);
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
             T[i] = __fmul_rn(T[i], w[0]);
 #pragma unroll
         for (int p = 1; p < P; ++p) {
             float d[kEPL];
-            decode16(q[p], d);
+            decode32(q[p], d);
 #pragma unroll
             for (int i = 0; i < kEPL; ++i)
                 T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w[p]));
@@ -150,7 +175,10 @@ __global__ void __launch_bounds__(kBlockThreads)
             k = scale;
         }
         if (valid) {
-            stg128_stream(out_codes + off, encode16(T, k));
+            uint4 oq[2];
+            encode32(T, k, oq);
+            stg128_stream(out_codes + off, oq[0]);
+            stg128_stream(out_codes + off + 16, oq[1]);
             if (part == 0) {
                 out_alpha[blk] = alpha;
                 out_scale[blk] = scale;
@@ -176,34 +204,45 @@ __global__ void __launch_bounds__(kBlockThreads)
         const int64_t blk = valid ? t / LPB : 0;
         const int part = static_cast<int>(t % LPB);
         const int64_t off = blk * NB + part * kEPL;
-        uint4 q = make_uint4(0, 0, 0, 0), g0 = q, g1 = q;
+        uint4 q[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        uint4 g[4] = {q[0], q[0], q[0], q[0]};
         float s_old = 1.0f;
         if (valid) {
             // codes and scale are rewritten below: coherent loads, not .nc
-            asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
-                         : "l"(codes + off));
-            g0 = ldg128_stream(grad + off);
-            g1 = ldg128_stream(grad + off + 8);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
+                             : "l"(codes + off + 16 * h));
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                g[h] = ldg128_stream(grad + off + 8 * h);
             asm volatile("ld.global.f32 %0, [%1];" : "=f"(s_old) : "l"(scale + blk));
         }
         // g = dequantise(main) + grad in FP32: one rounded multiply, then one
         // rounded add (no fused multiply-add), as the stated arithmetic is.
         float d[kEPL];
-        decode16(q, d);
-        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        decode32(q, d);
         float mx = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            d[2 * i] = __fadd_rn(__fmul_rn(d[2 * i], s_old), bf16lo_to_f32(gw[i]));
-            d[2 * i + 1] = __fadd_rn(__fmul_rn(d[2 * i + 1], s_old), bf16hi_to_f32(gw[i]));
-            mx = fmaxf(mx, fmaxf(fabsf(d[2 * i]), fabsf(d[2 * i + 1])));
+        for (int h = 0; h < 4; ++h) {
+            const uint32_t gw[4] = {g[h].x, g[h].y, g[h].z, g[h].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = 8 * h + 2 * j;
+                d[e] = __fadd_rn(__fmul_rn(d[e], s_old), bf16lo_to_f32(gw[j]));
+                d[e + 1] = __fadd_rn(__fmul_rn(d[e + 1], s_old), bf16hi_to_f32(gw[j]));
+                mx = fmaxf(mx, fmaxf(fabsf(d[e]), fabsf(d[e + 1])));
+            }
         }
         mx = group_max<LPB>(mx);
         float qs, m_new;
         agoq_scales(mx, qs, m_new);
         if (valid) {
-            stg128_stream(codes + off, encode16(d, qs));
+            uint4 oq[2];
+            encode32(d, qs, oq);
+            stg128_stream(codes + off, oq[0]);
+            stg128_stream(codes + off + 16, oq[1]);
             if (part == 0)
                 scale[blk] = m_new;
         }
@@ -227,25 +266,33 @@ __global__ void __launch_bounds__(kBlockThreads)
         const int64_t blk = valid ? t / LPB : 0;
         const int part = static_cast<int>(t % LPB);
         const int64_t off = blk * NB + part * kEPL;
-        uint4 q[P];
+        uint4 q[P][2];
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            load32_codes(in.codes[p] + off, valid, q[p]);
+        constexpr int ROUNDS = (P + LPB - 1) / LPB;
+        float mr[ROUNDS];
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int p = r * LPB + part;
+            mr[r] = (valid && p < P) ? __ldg(in.scale[p] + blk) : 1.0f;
+        }
+        const int gbase = lane & ~(LPB - 1);
         float m[P];
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            q[p] = valid ? ldg128_stream(in.codes[p] + off) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            m[p] = valid ? __ldg(in.scale[p] + blk) : 1.0f;
+            m[p] = __shfl_sync(0xFFFFFFFFu, mr[p / LPB], gbase + (p % LPB));
         // FP32 dequantise (one rounded multiply) and FP32 sum in shard order,
         // no fused multiply-add: exactly cancelling shards give exactly 0
         float S[kEPL];
-        decode16(q[0], S);
+        decode32(q[0], S);
 #pragma unroll
         for (int i = 0; i < kEPL; ++i)
             S[i] = __fmul_rn(S[i], m[0]);
 #pragma unroll
         for (int p = 1; p < P; ++p) {
             float d[kEPL];
-            decode16(q[p], d);
+            decode32(q[p], d);
 #pragma unroll
             for (int i = 0; i < kEPL; ++i)
                 S[i] = __fadd_rn(S[i], __fmul_rn(d[i], m[p]));
@@ -258,7 +305,10 @@ __global__ void __launch_bounds__(kBlockThreads)
         float qs, m_new;
         agoq_scales(mx, qs, m_new);
         if (valid) {
-            stg128_stream(out_codes + off, encode16(S, qs));
+            uint4 oq[2];
+            encode32(S, qs, oq);
+            stg128_stream(out_codes + off, oq[0]);
+            stg128_stream(out_codes + off + 16, oq[1]);
             if (part == 0)
                 out_scale[blk] = m_new;
         }
