@@ -354,12 +354,12 @@ def main():
         dist.barrier()
     elapsed_ms = start.elapsed_time(end)
     # keep the same work running until the clock sampler has a few samples
-    extra = 0
+    soak = 0
     t_region = elapsed_ms / 1e3
     while clocks and t_region < 1.0:
         path.run(x)
-        extra += 1
-        if extra % 200 == 0:
+        soak += 1
+        if soak % 200 == 0:
             torch.cuda.synchronize()
             t_region += 200 * elapsed_ms / K / 1e3
     torch.cuda.synchronize()
@@ -440,8 +440,8 @@ def main():
             "watchdog_flags": flags,
         }
         if clk:
-            line["clocks"]["window"] = (f"timed region plus {extra} further identical steps"
-                                        if extra else "timed region")
+            line["clocks"]["window"] = (f"timed region plus {soak} further identical steps"
+                                        if soak else "timed region")
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(bits, w, args.cpu_rows)
         print(json.dumps(line), flush=True)
