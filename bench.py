@@ -134,6 +134,27 @@ class ClockSampler:
                 "samples": n}
 
 
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Seed of a shard on ``rank``: each replica draws its own data."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value_ms: float, dist, device=None) -> float:
+    """Largest per-rank time (the job takes as long as its slowest rank)."""
+    if dist is None:
+        return value_ms
+    import torch
+
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Aggregate throughput: every rank moves bytes_per_step per step."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
 def make_inputs(rank: int, rows: int | None = None):
     from fp8_communication_compression_gb300 import workloads as W
 
@@ -142,7 +163,7 @@ def make_inputs(rank: int, rows: int | None = None):
         w["rows"] = rows
     shards = []
     for p in range(w["shards"]):
-        seed = w["seeds"][p] + 1000 * rank
+        seed = replica_seed(w["seeds"][p], rank)
         shards.append(W.tp_activation(seed, w["rows"], w["d"], channel_scale=w["channel_scale"],
                                       spikes=w["spikes"], block=w["block"]))
     return w, np.stack(shards)
@@ -365,10 +386,7 @@ def main():
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
 
-    if dist:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
     per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
            for i, name in enumerate(("compress", "reduce", "decompress"))}
 
@@ -391,10 +409,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     peak, peak_src = hbm_peak()
     extra = {}
     if rank == 0 and not args.no_agoq:
@@ -408,7 +423,7 @@ def main():
     flags = api.taco_device_error(clear=True)
 
     if rank == 0:
-        value = step_bytes * K * world / (elapsed_ms / 1e3) / 1e9
+        value = whole_job_gbs(step_bytes, K, world, elapsed_ms)
         kern = {}
         for name in ("compress", "reduce", "decompress"):
             gbs = nbytes[name] / (per[name] / 1e3) / 1e9
@@ -431,7 +446,7 @@ def main():
             "kernels": kern,
             "step_frac_of_peak": value / world / peak,
             "e2e": None if e2e_ms is None else {
-                "value": step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "value": whole_job_gbs(step_bytes, args.e2e_steps, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
                 "api": "TwoShotLocal.run_host (pinned host in/out)"},
             "other_workloads": extra,

@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
 
+    pdl_wait();
+    pdl_launch_dependents();
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&x_map);
@@ -318,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
 
+    pdl_wait();
+    pdl_launch_dependents();
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&c_map);
@@ -515,15 +519,15 @@ cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float 
     if (block == 128) {
         if ((e = ensure_smem(taco_compress_kernel<128>, kCSmemBytes, di.device, set128)) != cudaSuccess)
             return e;
-        taco_compress_kernel<128><<<grid, kThreads, kCSmemBytes, stream>>>(xm, cm, alpha, scale, nrows,
-                                                                          e_target, eps);
+        e = launch_pdl(taco_compress_kernel<128>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
+                       nrows, e_target, eps);
     } else {
         if ((e = ensure_smem(taco_compress_kernel<256>, kCSmemBytes, di.device, set256)) != cudaSuccess)
             return e;
-        taco_compress_kernel<256><<<grid, kThreads, kCSmemBytes, stream>>>(xm, cm, alpha, scale, nrows,
-                                                                          e_target, eps);
+        e = launch_pdl(taco_compress_kernel<256>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
+                       nrows, e_target, eps);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale,
@@ -550,8 +554,8 @@ cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const fl
         if ((e = ensure_smem(taco_decompress_kernel<NB, BF>, kDSmemBytes, di.device, FLAGS)) !=   \
             cudaSuccess)                                                                           \
             return e;                                                                              \
-        taco_decompress_kernel<NB, BF>                                                             \
-            <<<grid, kThreads, kDSmemBytes, stream>>>(cm, om, alpha, scale, nrows);        \
+        e = launch_pdl(taco_decompress_kernel<NB, BF>, grid, kThreads, kDSmemBytes, stream, cm, om, \
+                       alpha, scale, nrows);                                                       \
     } while (0)
     if (block == 128) {
         if (out_bf16)
@@ -565,7 +569,7 @@ cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const fl
             TACO_LAUNCH_D(256, false, s3);
     }
 #undef TACO_LAUNCH_D
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t read_codec_error(uint32_t *flags, bool clear)

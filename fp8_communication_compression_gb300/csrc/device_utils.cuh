@@ -24,6 +24,22 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start before
+// the previous kernel in its stream has finished; it must not touch that
+// kernel's outputs before pdl_wait() returns (which waits for the previous
+// grid to complete and its memory to be visible).  Without that launch
+// attribute both instructions are no-ops.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream be scheduled once every CTA of this
+// grid has executed it (or exited).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

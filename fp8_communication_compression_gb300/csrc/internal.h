@@ -45,4 +45,25 @@ cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block,
 
 cudaError_t read_codec_error(uint32_t *flags, bool clear);
 
+// Launches `kernel` with programmatic stream serialization allowed, so that
+// it can be scheduled while the previous kernel in the stream drains (every
+// kernel of this library waits for its predecessor with griddepcontrol.wait
+// before reading inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 } // namespace taco

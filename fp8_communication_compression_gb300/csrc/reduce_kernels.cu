@@ -96,6 +96,8 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
 // Warp-uniform grid-stride loop over lane slots.  Lanes past the end still
 // take part in the shuffles but load and store nothing.
 #define TACO_LANE_LOOP(total)                                                                    \
+    pdl_wait();                                                                                  \
+    pdl_launch_dependents();                                                                     \
     const int64_t _stride = static_cast<int64_t>(gridDim.x) * blockDim.x;                        \
     for (int64_t _base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);    \
          _base < (total); _base += _stride)
@@ -343,8 +345,8 @@ cudaError_t run_taco_reduce(const ShardPtrs &in, int64_t nblocks, float e_target
     cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
     if (e != cudaSuccess)
         return e;
-    taco_reduce_kernel<NB, P><<<grid, kBlockThreads, 0, st>>>(in, nblocks, e_target, eps, oc, oa, os);
-    return cudaGetLastError();
+    return launch_pdl(taco_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, e_target, eps, oc,
+                      oa, os);
 }
 
 template <int NB, int P>
@@ -354,8 +356,7 @@ cudaError_t run_agoq_reduce(const ShardPtrs &in, int64_t nblocks, uint8_t *oc, f
     cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
     if (e != cudaSuccess)
         return e;
-    agoq_reduce_kernel<NB, P><<<grid, kBlockThreads, 0, st>>>(in, nblocks, oc, os);
-    return cudaGetLastError();
+    return launch_pdl(agoq_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, oc, os);
 }
 
 template <int NB, int... Ps> struct PDispatch;
@@ -419,13 +420,13 @@ cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *gra
     if (block == 128) {
         if ((e = grid_for(agoq_accumulate_kernel<128>, nblocks * (128 / kEPL), &grid)) != cudaSuccess)
             return e;
-        agoq_accumulate_kernel<128><<<grid, kBlockThreads, 0, stream>>>(codes, scale, g, nblocks);
+        e = launch_pdl(agoq_accumulate_kernel<128>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
     } else {
         if ((e = grid_for(agoq_accumulate_kernel<256>, nblocks * (256 / kEPL), &grid)) != cudaSuccess)
             return e;
-        agoq_accumulate_kernel<256><<<grid, kBlockThreads, 0, stream>>>(codes, scale, g, nblocks);
+        e = launch_pdl(agoq_accumulate_kernel<256>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace taco
