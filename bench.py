@@ -43,14 +43,17 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csr
                   for f in ("codec_kernels.cu", "device_utils.cuh")]
 
 
-def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4) -> dict:
-    """Bytes each kernel must move at minimum, per step."""
+def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: bool = True) -> dict:
+    """Bytes each launch must move at minimum (reads + writes), per step of
+    the two-shot local path over P shards of n elements."""
     nb = n // block
-    return {
-        "compress": P * (2 * n + n + 8 * nb),        # bf16 in; codes + alpha + s out
-        "reduce": P * (n + 8 * nb) + (n + 8 * nb),    # P compressed shards in; one out
-        "decompress": (n + 8 * nb) + out_bytes * n,   # codes + scalars in; fp32 out
-    }
+    comp = P * (2 * n + n + 8 * nb)             # bf16 in; codes + alpha + s out
+    red_in = P * (n + 8 * nb)                   # P compressed shards in
+    red_out = n + 8 * nb                        # the compressed sum out
+    dec_out = out_bytes * n                     # its reconstruction out
+    if fused:
+        return {"compress": comp, "reduce_decompress": red_in + red_out + dec_out}
+    return {"compress": comp, "reduce": red_in + red_out, "decompress": red_out + dec_out}
 
 
 def hbm_peak():
@@ -276,8 +279,9 @@ def agoq_leg(torch, api, peak: float) -> dict:
 
 
 def gpt13b_leg(torch, api, peak: float) -> dict:
-    """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-kernel
-    CUDA-event times of compress, reduce and decompress."""
+    """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
+    CUDA-event times of compress, the fused reduce + decompress, and the
+    separate reduce and decompress."""
     from fp8_communication_compression_gb300 import workloads as W
 
     name = "gpt13b_p8x8192x5120_n256"
@@ -286,14 +290,16 @@ def gpt13b_leg(torch, api, peak: float) -> dict:
     bits = np.stack([W.shard_input(name, p) for p in range(P)])
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     del bits
-    path = api.TwoShotLocal(P, rows, d, block)
+    path = api.TwoShotLocal(P, rows, d, block, fused=True)
     for _ in range(3):
         path.run(x)
     stream = torch.cuda.current_stream()
     ms = {"compress": time_launches(torch, lambda: path.compress(x), 10, stream),
+          "reduce_decompress": time_launches(torch, path.reduce_decompress, 10, stream),
           "reduce": time_launches(torch, path.reduce, 10, stream),
           "decompress": time_launches(torch, path.decompress, 10, stream)}
-    nb = algorithmic_bytes(P, rows * d, block)
+    nb = dict(algorithmic_bytes(P, rows * d, block, fused=True))
+    nb.update(algorithmic_bytes(P, rows * d, block, fused=False))
     return {k: {"us_per_launch": ms[k] * 1e3, "algorithmic_bytes": nb[k],
                 "gbs": nb[k] / (ms[k] / 1e3) / 1e9, "frac_of_peak": nb[k] / (ms[k] / 1e3) / 1e9 / peak}
             for k in ms}
@@ -311,6 +317,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
     ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
+    ap.add_argument("--separate", action="store_true",
+                    help="run reduce and decompress as two launches instead of the fused one")
     ap.add_argument("--gpt13b", action="store_true",
                     help="also time the GPT-13B-shaped path (P=8, n=256; slow input generation)")
     ap.add_argument("--rows", type=int, default=None,
@@ -340,19 +348,21 @@ def main():
     w, bits = make_inputs(rank, args.rows)
     P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
     n = rows * d
-    nbytes = algorithmic_bytes(P, n, block)
-    step_bytes = sum(nbytes.values())
 
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-    path = api.TwoShotLocal(P, rows, d, block)
+    path = api.TwoShotLocal(P, rows, d, block, fused=not args.separate)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
         path.run(x)
     torch.cuda.synchronize()
 
+    launches = path.launches()
+    names = [nm for nm, _ in launches]
+    nbytes = path.bytes_per_step()
+    step_bytes = sum(nbytes.values())
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
     time.sleep(0.2 if clocks else 0)
@@ -363,12 +373,9 @@ def main():
     for k in range(K):
         e = ev[k]
         e[0].record(stream)
-        path.compress(x)
-        e[1].record(stream)
-        path.reduce()
-        e[2].record(stream)
-        path.decompress()
-        e[3].record(stream)
+        for i, (_, fn) in enumerate(launches):
+            fn(x)
+            e[i + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -388,7 +395,7 @@ def main():
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
     per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
-           for i, name in enumerate(("compress", "reduce", "decompress"))}
+           for i, name in enumerate(names)}
 
     # end to end through the public API with pinned host buffers
     e2e_ms = None
@@ -425,7 +432,7 @@ def main():
     if rank == 0:
         value = whole_job_gbs(step_bytes, K, world, elapsed_ms)
         kern = {}
-        for name in ("compress", "reduce", "decompress"):
+        for name in names:
             gbs = nbytes[name] / (per[name] / 1e3) / 1e9
             kern[name] = {"us_per_launch": per[name] * 1e3, "algorithmic_bytes": nbytes[name],
                           "gbs": gbs, "frac_of_peak": gbs / peak}
@@ -436,6 +443,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": HEADLINE if args.rows is None else f"{HEADLINE} (rows={rows})",
                        "P": P, "rows": rows, "d": d, "block": block,
+                       "launches": names,
                        "bytes_per_step": step_bytes,
                        "input_bf16_bytes_per_step": 2 * P * n,
                        "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
@@ -450,7 +458,7 @@ def main():
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
                 "api": "TwoShotLocal.run_host (pinned host in/out)"},
             "other_workloads": extra,
-            "gpu_launches": 3 * K,
+            "gpu_launches": len(launches) * K,
             "clocks": clk,
             "watchdog_flags": flags,
         }

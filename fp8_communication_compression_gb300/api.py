@@ -119,6 +119,42 @@ def taco_reduce_shards(codes: Sequence[torch.Tensor], alpha: Sequence[torch.Tens
     return out_codes, out_alpha, out_scale
 
 
+def taco_reduce_decompress(codes: Sequence[torch.Tensor], alpha: Sequence[torch.Tensor],
+                           scale: Sequence[torch.Tensor], block: int = 128, e_target: float = E_TARGET,
+                           eps: float = EPS, out_codes: torch.Tensor | None = None,
+                           out_alpha: torch.Tensor | None = None, out_scale: torch.Tensor | None = None,
+                           out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                           stream=None):
+    """Compressed sum of P compressed shards and its reconstruction, in one pass."""
+    P = len(codes)
+    if not (len(alpha) == P and len(scale) == P) or P == 0:
+        raise ValueError("codes, alpha and scale must be non-empty lists of equal length")
+    for p in range(P):
+        _need(codes[p], f"codes[{p}]", _U8, codes[0].numel())
+        _need(alpha[p], f"alpha[{p}]", (torch.float32,))
+        _need(scale[p], f"scale[{p}]", (torch.float32,))
+    rows, d = _shape2(codes[0])
+    dev = codes[0].device
+    if out_codes is None:
+        out_codes = torch.empty(codes[0].shape, dtype=torch.uint8, device=dev)
+    if out_alpha is None:
+        out_alpha = torch.empty_like(alpha[0])
+    if out_scale is None:
+        out_scale = torch.empty_like(scale[0])
+    if out is None:
+        out = torch.empty(codes[0].shape, dtype=out_dtype, device=dev)
+    _need(out, "out", (torch.float32, torch.bfloat16), codes[0].numel())
+    cp, _k1 = _lib.ptr_array([c.data_ptr() for c in codes])
+    ap, _k2 = _lib.ptr_array([a.data_ptr() for a in alpha])
+    sp, _k3 = _lib.ptr_array([s.data_ptr() for s in scale])
+    st = _lib.load().taco_reduce_decompress(P, cp, ap, sp, rows, d, block, e_target, eps,
+                                            out_codes.data_ptr(), out_alpha.data_ptr(),
+                                            out_scale.data_ptr(), out.data_ptr(),
+                                            int(out.dtype == torch.bfloat16), _stream_handle(stream))
+    _lib.check("taco_reduce_decompress", st)
+    return out_codes, out_alpha, out_scale, out
+
+
 def agoq_fp8_accumulate(main_codes: torch.Tensor, main_scale: torch.Tensor, grad: torch.Tensor,
                         block: int = 128, stream=None):
     """In place: main <- requantise(dequantise(main) + grad)."""
@@ -165,8 +201,10 @@ class TwoShotLocal:
     Buffers are allocated once; ``run`` only launches the three kernels."""
 
     def __init__(self, P: int, rows: int, d: int, block: int = 128, device="cuda",
-                 e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32):
+                 e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32,
+                 fused: bool = True):
         self.P, self.rows, self.d, self.block = P, rows, d, block
+        self.fused = fused
         self.e_target, self.eps = e_target, eps
         nb = rows * d // block
         self.codes = torch.empty((P, rows, d), dtype=torch.uint8, device=device)
@@ -181,13 +219,21 @@ class TwoShotLocal:
         self._shard_scale = list(self.scale)
 
     def bytes_per_step(self) -> dict:
+        """Algorithmic bytes each launch must move (reads + writes)."""
         n = self.rows * self.d
         nb = n // self.block
-        return {
-            "compress": self.P * (2 * n + n + 8 * nb),
-            "reduce": self.P * (n + 8 * nb) + n + 8 * nb,
-            "decompress": n + 8 * nb + n * self.out.element_size(),
-        }
+        comp = self.P * (2 * n + n + 8 * nb)
+        red_in = self.P * (n + 8 * nb)
+        red_out = n + 8 * nb
+        dec_out = n * self.out.element_size()
+        if self.fused:
+            return {"compress": comp, "reduce_decompress": red_in + red_out + dec_out}
+        return {"compress": comp, "reduce": red_in + red_out, "decompress": red_out + dec_out}
+
+    def reduce_decompress(self, stream=None):
+        return taco_reduce_decompress(self._shard_codes, self._shard_alpha, self._shard_scale,
+                                      self.block, self.e_target, self.eps, self.r_codes, self.r_alpha,
+                                      self.r_scale, self.out, stream=stream)
 
     def compress(self, x: torch.Tensor, stream=None):
         return taco_compress(x, self.block, self.e_target, self.eps, self.codes, self.alpha,
@@ -202,9 +248,19 @@ class TwoShotLocal:
         return taco_decompress(self.r_codes, self.r_alpha, self.r_scale, self.block, out=self.out,
                                stream=stream)
 
+    def launches(self):
+        """The step's launches, in order, as (name, callable taking x)."""
+        if self.fused:
+            return [("compress", self.compress), ("reduce_decompress", lambda x: self.reduce_decompress())]
+        return [("compress", self.compress), ("reduce", lambda x: self.reduce()),
+                ("decompress", lambda x: self.decompress())]
+
     def run(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         """x: bf16 [P, rows, d] on the device -> fp32/bf16 [rows, d]."""
         self.compress(x, stream)
+        if self.fused:
+            self.reduce_decompress(stream)
+            return self.out
         self.reduce(stream)
         return self.decompress(stream)
 

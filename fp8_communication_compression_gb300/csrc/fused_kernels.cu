@@ -1,0 +1,399 @@
+// Fused shard reduce + decompress for sm_103a: the reducing rank of the
+// two-shot AllReduce (TACO, gist.science summary of arXiv 2604.24088, 2.B.3)
+// both sends the compressed reduced shard (AllGather payload) and uses its
+// reconstruction.  One pass writes the compressed sum (codes, alpha, s) and
+// decompress(compressed sum) without reading the reduced codes back.
+//
+// Per warp and 32-row tile (32 / (n/128) blocks):
+//  phase 1  the Hadamard-domain reduce of the shard-reduce kernel: 4 (n=128)
+//           or 8 (n=256) lanes per block, 32 elements per lane, coalesced
+//           16-byte loads of the P shards' codes (double-buffered across the
+//           four sub-steps of a tile when P <= 8), FP32 sum, requantisation.
+//           Codes go to global memory and, swizzled, into the warp's 4 KB
+//           shared-memory tile; alpha and s into a shared array.
+//  phase 2  one lane per 128-element row, exactly the arithmetic of the
+//           decompress kernel (decode, register butterflies, scaling), output
+//           through a swizzled 16 KB staging area and TMA tensor stores.
+
+#include "codec_math.cuh"
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace taco {
+
+namespace {
+
+constexpr int kFWarps = 8;
+constexpr int kFThreads = kFWarps * 32;
+constexpr int kFEPL = 32;                                   // phase 1: elements per lane
+constexpr uint32_t kFCodeTile = 32 * 128;                   // 4 KB per warp
+constexpr uint32_t kFOutBytes = 32 * 512;                   // 16 KB per warp
+constexpr uint32_t kFWarpBytes = kFCodeTile + kFOutBytes;   // 20 KB
+constexpr uint32_t kFScalarBytes = 2 * 32 * 4;              // alpha', s' of up to 32 blocks
+constexpr uint32_t kFSmemBytes = 1024 + kFWarps * (kFWarpBytes + kFScalarBytes);
+static_assert(kFWarpBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+
+__device__ __forceinline__ void decode32(const uint4 (&q)[2], float (&d)[32])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            e4m3x2_to_f32x2(w[j], d[16 * h + 4 * j + 0], d[16 * h + 4 * j + 1]);
+            e4m3x2_to_f32x2(w[j] >> 16, d[16 * h + 4 * j + 2], d[16 * h + 4 * j + 3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void encode32(const float (&v)[32], float k, uint4 (&q)[2])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *x = v + 16 * h;
+        q[h].x = f32x4_to_e4m3x4(x[0] * k, x[1] * k, x[2] * k, x[3] * k);
+        q[h].y = f32x4_to_e4m3x4(x[4] * k, x[5] * k, x[6] * k, x[7] * k);
+        q[h].z = f32x4_to_e4m3x4(x[8] * k, x[9] * k, x[10] * k, x[11] * k);
+        q[h].w = f32x4_to_e4m3x4(x[12] * k, x[13] * k, x[14] * k, x[15] * k);
+    }
+}
+
+template <int LPB> __device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = LPB / 2; o >= 1; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+template <int LPB> __device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = LPB / 2; o >= 1; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Per-lane state of phase 1 for one sub-step: which block, where.
+struct Slot {
+    int64_t blk;
+    int64_t off;
+    int lb;  // block index within the tile
+    bool valid;
+};
+
+template <int NB, int LPB, int BPS>
+__device__ __forceinline__ Slot slot_of(int64_t blk0, int si, int lane, int64_t nblocks)
+{
+    Slot s;
+    s.lb = si * BPS + lane / LPB;
+    s.blk = blk0 + s.lb;
+    s.valid = s.blk < nblocks;
+    s.off = (s.valid ? s.blk : 0) * NB + (lane % LPB) * kFEPL;
+    return s;
+}
+
+template <int P>
+__device__ __forceinline__ void load_shards(const ShardPtrs &in, const Slot &sl, uint4 (&q)[P][2])
+{
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        q[p][0] = sl.valid ? ldg128_stream(in.codes[p] + sl.off) : make_uint4(0, 0, 0, 0);
+        q[p][1] = sl.valid ? ldg128_stream(in.codes[p] + sl.off + 16) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Requantises the lane's 32 Hadamard-domain sums T of one block (see the
+// shard-reduce kernel: alpha' = sqrt(E / (|T|^2/n + eps)), s' = 448 /
+// (alpha' max|T|), codes = E4M3(alpha' s' T)), stores codes and scalars to
+// global memory and to the warp's shared tile.
+template <int NB, int LPB>
+__device__ __forceinline__ void finish_block(float (&T)[32], const Slot &sl, int lane, float e_target,
+                                             float eps, uint8_t *out_codes, float *out_alpha,
+                                             float *out_scale, uint32_t ctile, float *sa_s, float *ss_s)
+{
+    constexpr int G = NB / 128;
+    const int part = lane % LPB;
+    float a4[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kFEPL; ++i) {
+        a4[i & 3] = fmaf(T[i], T[i], a4[i & 3]);
+        mx = fmaxf(mx, fabsf(T[i]));
+    }
+    const float ss = group_sum<LPB>((a4[0] + a4[1]) + (a4[2] + a4[3]));
+    mx = group_max<LPB>(mx);
+    const float alpha = sqrtf(e_target / (ss * (1.0f / NB) + eps));
+    const float M = alpha * mx;
+    const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+    float k = alpha * scale;
+    if (!(k <= FLT_MAX)) {
+#pragma unroll
+        for (int i = 0; i < kFEPL; ++i)
+            T[i] *= alpha;
+        k = scale;
+    }
+    uint4 oq[2];
+    encode32(T, k, oq);
+    if (sl.valid) {
+        stg128_stream(out_codes + sl.off, oq[0]);
+        stg128_stream(out_codes + sl.off + 16, oq[1]);
+        if (part == 0) {
+            out_alpha[sl.blk] = alpha;
+            out_scale[sl.blk] = scale;
+        }
+    }
+    // the lane's 32 codes are 16-byte chunks j0, j0 + 1 of tile row r
+    const int r = sl.lb * G + part / 4;
+    const uint32_t j0 = static_cast<uint32_t>(part % 4) * 2;
+    const uint32_t rsw = static_cast<uint32_t>(r & 7) << 4;
+    sts128(ctile + r * 128 + ((j0 << 4) ^ rsw), oq[0].x, oq[0].y, oq[0].z, oq[0].w);
+    sts128(ctile + r * 128 + (((j0 + 1) << 4) ^ rsw), oq[1].x, oq[1].y, oq[1].z, oq[1].w);
+    if (part == 0) {
+        sa_s[sl.lb] = alpha;
+        ss_s[sl.lb] = scale;
+    }
+}
+
+// Phase 1 for a compile-time shard count.
+template <int NB, int P>
+__device__ __forceinline__ void accumulate_fixed(const ShardPtrs &in, const Slot &sl, const uint4 (&q)[P][2],
+                                                 int lane, float (&T)[32])
+{
+    constexpr int LPB = NB / kFEPL;
+    constexpr int ROUNDS = (P + LPB - 1) / LPB;
+    const int part = lane % LPB;
+    float wr[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int p = r * LPB + part;
+        wr[r] = 1.0f;
+        if (sl.valid && p < P) {
+            const float sc = __ldg(in.scale[p] + sl.blk), al = __ldg(in.alpha[p] + sl.blk);
+            const float sa = sc * al;
+            wr[r] = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
+        }
+    }
+    const int gbase = lane & ~(LPB - 1);
+    float w[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+        w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
+    // products rounded before they are added: exactly cancelling shards give 0
+    decode32(q[0], T);
+#pragma unroll
+    for (int i = 0; i < kFEPL; ++i)
+        T[i] = __fmul_rn(T[i], w[0]);
+#pragma unroll
+    for (int p = 1; p < P; ++p) {
+        float d[kFEPL];
+        decode32(q[p], d);
+#pragma unroll
+        for (int i = 0; i < kFEPL; ++i)
+            T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w[p]));
+    }
+}
+
+// Phase 1 for a run-time shard count (1 .. 16): shard by shard.
+__device__ __forceinline__ void accumulate_any(const ShardPtrs &in, int P, const Slot &sl, float (&T)[32])
+{
+#pragma unroll 1
+    for (int p = 0; p < P; ++p) {
+        uint4 q[2];
+        q[0] = sl.valid ? ldg128_stream(in.codes[p] + sl.off) : make_uint4(0, 0, 0, 0);
+        q[1] = sl.valid ? ldg128_stream(in.codes[p] + sl.off + 16) : make_uint4(0, 0, 0, 0);
+        float w = 1.0f;
+        if (sl.valid) {
+            const float sc = __ldg(in.scale[p] + sl.blk), al = __ldg(in.alpha[p] + sl.blk);
+            const float sa = sc * al;
+            w = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
+        }
+        float d[kFEPL];
+        decode32(q, d);
+        if (p == 0) {
+#pragma unroll
+            for (int i = 0; i < kFEPL; ++i)
+                T[i] = __fmul_rn(d[i], w);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kFEPL; ++i)
+                T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w));
+        }
+    }
+}
+
+// PT > 0: compile-time shard count; PT == 0: run-time P.
+template <int NB, int PT, bool BF16OUT>
+__global__ void __launch_bounds__(kFThreads, 1)
+    taco_reduce_decompress_kernel(const ShardPtrs in, int P, const __grid_constant__ CUtensorMap o_map,
+                                  int64_t nrows, float e_target, float eps, uint8_t *__restrict__ out_codes,
+                                  float *__restrict__ out_alpha, float *__restrict__ out_scale)
+{
+    constexpr int G = NB / 128;       // tile rows per block
+    constexpr int LPB = NB / kFEPL;   // phase-1 lanes per block
+    constexpr int BPS = 32 / LPB;     // blocks per phase-1 sub-step
+    constexpr int BPT = 32 / G;       // blocks per 32-row tile
+    constexpr int SUB = BPT / BPS;    // sub-steps per tile
+    static_assert(SUB == 4, "a 32-row tile is four phase-1 sub-steps");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ctile = base + warp * kFWarpBytes;
+    const uint32_t outw = ctile + kFCodeTile;
+    float *sa_s = reinterpret_cast<float *>(smem_raw + (base - raw) + kFWarps * kFWarpBytes +
+                                            warp * kFScalarBytes);
+    float *ss_s = sa_s + 32;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    if (lane == 0)
+        tma_prefetch_map(&o_map);
+    const int64_t nblocks = nrows / G;
+    const int64_t ntiles = (nrows + 31) / 32;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kFWarps + warp;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kFWarps;
+    const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+
+    for (int64_t t = gw; t < ntiles; t += W) {
+        const int64_t blk0 = t * BPT;
+        // ------------------------------------------------------ phase 1
+        if constexpr (PT > 0 && PT <= 8) {
+            uint4 qa[PT][2], qb[PT][2];
+            Slot sa = slot_of<NB, LPB, BPS>(blk0, 0, lane, nblocks), sb;
+            load_shards<PT>(in, sa, qa);
+#pragma unroll
+            for (int si = 0; si < SUB; si += 2) {
+                sb = slot_of<NB, LPB, BPS>(blk0, si + 1, lane, nblocks);
+                load_shards<PT>(in, sb, qb);
+                float T[kFEPL];
+                accumulate_fixed<NB, PT>(in, sa, qa, lane, T);
+                finish_block<NB, LPB>(T, sa, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
+                                      sa_s, ss_s);
+                if (si + 2 < SUB) {
+                    sa = slot_of<NB, LPB, BPS>(blk0, si + 2, lane, nblocks);
+                    load_shards<PT>(in, sa, qa);
+                }
+                accumulate_fixed<NB, PT>(in, sb, qb, lane, T);
+                finish_block<NB, LPB>(T, sb, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
+                                      sa_s, ss_s);
+            }
+        } else if constexpr (PT > 8) {
+#pragma unroll 1
+            for (int si = 0; si < SUB; ++si) {
+                const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
+                uint4 q[PT][2];
+                load_shards<PT>(in, sl, q);
+                float T[kFEPL];
+                accumulate_fixed<NB, PT>(in, sl, q, lane, T);
+                finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
+                                      sa_s, ss_s);
+            }
+        } else {
+#pragma unroll 1
+            for (int si = 0; si < SUB; ++si) {
+                const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
+                float T[kFEPL];
+                accumulate_any(in, P, sl, T);
+                finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
+                                      sa_s, ss_s);
+            }
+        }
+        __syncwarp();
+
+        // ------------------------------------------------------ phase 2
+        const int lb = lane / G;
+        const float a = sa_s[lb], sc = ss_s[lb];
+        float2 v[64];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            decode16_stage1(lds128(ctile + lane * 128 + ((static_cast<uint32_t>(j) << 4) ^ swz)), v, j);
+        fwht128_upper(v);
+        if constexpr (G == 2)
+            fwht_pair_stage(v, lane);
+        const float2 k2 = decompress_multiplier<NB>(v, sc, a);
+        if (lane == 0)
+            bulk_wait_read_all();
+        __syncwarp();
+        stage_output_row<BF16OUT>(v, k2, outw, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int64_t wrow = t * 32;
+        if (lane == 0) {
+            constexpr int nbox = BF16OUT ? 2 : 4;
+            constexpr int box_inner = BF16OUT ? 64 : 32;
+#pragma unroll
+            for (int b = 0; b < nbox; ++b)
+                tma_store_2d(&o_map, b * box_inner, static_cast<int32_t>(wrow), outw + b * 4096);
+            bulk_commit();
+        }
+        __syncwarp();  // the code tile and scalars are rewritten by the next tile's phase 1
+    }
+    if (lane == 0)
+        bulk_wait_all();
+}
+
+template <int NB, int PT, bool BF> bool g_smem_set[64];
+
+template <int NB, int PT, bool BF>
+cudaError_t run_fused(const ShardPtrs &in, int P, const CUtensorMap &om, int64_t nrows, float e_target,
+                      float eps, uint8_t *oc, float *oa, float *os, cudaStream_t st, const DeviceInfo &di)
+{
+    auto kernel = taco_reduce_decompress_kernel<NB, PT, BF>;
+    if (!g_smem_set<NB, PT, BF>[di.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kFSmemBytes));
+        if (e != cudaSuccess)
+            return e;
+        g_smem_set<NB, PT, BF>[di.device] = true;
+    }
+    const int64_t ctas = (nrows + kFWarps * 32 - 1) / (kFWarps * 32);
+    const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
+    return launch_pdl(kernel, grid, kFThreads, kFSmemBytes, st, in, P, om, nrows, e_target, eps, oc, oa,
+                      os);
+}
+
+template <int NB, bool BF>
+cudaError_t dispatch_p(const ShardPtrs &in, int P, const CUtensorMap &om, int64_t nrows, float e_target,
+                       float eps, uint8_t *oc, float *oa, float *os, cudaStream_t st, const DeviceInfo &di)
+{
+    switch (P) {
+    case 2:
+        return run_fused<NB, 2, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
+    case 4:
+        return run_fused<NB, 4, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
+    case 8:
+        return run_fused<NB, 8, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
+    default:
+        return run_fused<NB, 0, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce_decompress(int P, const ShardPtrs &in, int64_t nrows, int block, float e_target,
+                                     float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
+                                     void *out, bool out_bf16, cudaStream_t stream)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap om;
+    const int rc = out_bf16
+                       ? encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 128, nrows, 256, 64, 32)
+                       : encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, 128, nrows, 512, 32, 32);
+    if (rc != 0)
+        return cudaErrorInvalidValue;
+    if (block == 128)
+        return out_bf16 ? dispatch_p<128, true>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
+                                                stream, di)
+                        : dispatch_p<128, false>(in, P, om, nrows, e_target, eps, out_codes, out_alpha,
+                                                 out_scale, stream, di);
+    return out_bf16 ? dispatch_p<256, true>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
+                                            stream, di)
+                    : dispatch_p<256, false>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
+                                             stream, di);
+}
+
+}  // namespace taco

@@ -38,6 +38,9 @@ struct ShardPtrs {
 cudaError_t launch_taco_reduce(int P, const ShardPtrs &in, int64_t nblocks, int block, float e_target,
                                float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
                                cudaStream_t stream);
+cudaError_t launch_reduce_decompress(int P, const ShardPtrs &in, int64_t nrows, int block, float e_target,
+                                     float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
+                                     void *out, bool out_bf16, cudaStream_t stream);
 cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *grad_bf16, int64_t n,
                                    int block, cudaStream_t stream);
 cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block, uint8_t *out_codes,

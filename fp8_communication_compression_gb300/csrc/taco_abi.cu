@@ -74,6 +74,54 @@ taco_status check_taco_shape(int64_t rows, int64_t d, int32_t block)
     return TACO_OK;
 }
 
+
+// Shared checks of the two reduce entry points; fills `sp`.  `out` (the
+// optional reconstruction of the sum) may be null.
+taco_status check_reduce_args(int32_t P, const uint8_t *const *codes, const float *const *alpha,
+                                     const float *const *scale, int64_t rows, int64_t d, int32_t block,
+                                     float e_target, float eps, const uint8_t *out_codes,
+                                     const float *out_alpha, const float *out_scale, const void *out,
+                                     uint64_t out_bytes_per_elem, taco::ShardPtrs *sp)
+{
+    taco_status st = check_taco_shape(rows, d, block);
+    if (st != TACO_OK)
+        return st;
+    if (P < 1 || P > TACO_MAX_SHARDS)
+        return TACO_ERR_UNSUPPORTED;
+    if (!positive_finite(e_target) || !positive_finite(eps))
+        return TACO_ERR_INVALID_ARG;
+    if (rows == 0)
+        return TACO_OK;
+    if (!codes || !alpha || !scale || !out_codes || !out_alpha || !out_scale)
+        return TACO_ERR_INVALID_ARG;
+    const uint64_t n = static_cast<uint64_t>(rows * d), nb = n / block;
+    if (!aligned(out_codes, 16) || !aligned(out_alpha, 4) || !aligned(out_scale, 4) ||
+        (out && !aligned(out, 16)))
+        return TACO_ERR_MISALIGNED;
+    const void *outs[4] = {out_codes, out_alpha, out_scale, out};
+    const uint64_t olen[4] = {n, 4 * nb, 4 * nb, out ? n * out_bytes_per_elem : 0};
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], olen[i], outs[j], olen[j]))
+                return TACO_ERR_INVALID_ARG;
+    for (int p = 0; p < P; ++p) {
+        if (!codes[p] || !alpha[p] || !scale[p])
+            return TACO_ERR_INVALID_ARG;
+        if (!aligned(codes[p], 16) || !aligned(alpha[p], 4) || !aligned(scale[p], 4))
+            return TACO_ERR_MISALIGNED;
+        const void *ins[3] = {codes[p], alpha[p], scale[p]};
+        const uint64_t lens[3] = {n, 4 * nb, 4 * nb};
+        for (int i = 0; i < 3; ++i)
+            for (int j = 0; j < 4; ++j)
+                if (overlap(ins[i], lens[i], outs[j], olen[j]))
+                    return TACO_ERR_INVALID_ARG;
+        sp->codes[p] = codes[p];
+        sp->alpha[p] = alpha[p];
+        sp->scale[p] = scale[p];
+    }
+    return TACO_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -149,42 +197,30 @@ taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes, const flo
                                float e_target, float eps, uint8_t *out_codes, float *out_alpha,
                                float *out_scale, taco_stream_t stream)
 {
-    taco_status st = check_taco_shape(rows, d, block);
-    if (st != TACO_OK)
-        return st;
-    if (P < 1 || P > TACO_MAX_SHARDS)
-        return TACO_ERR_UNSUPPORTED;
-    if (!positive_finite(e_target) || !positive_finite(eps))
-        return TACO_ERR_INVALID_ARG;
-    if (rows == 0)
-        return TACO_OK;
-    if (!codes || !alpha || !scale || !out_codes || !out_alpha || !out_scale)
-        return TACO_ERR_INVALID_ARG;
-    const uint64_t n = static_cast<uint64_t>(rows * d), nb = n / block;
-    if (!aligned(out_codes, 16) || !aligned(out_alpha, 4) || !aligned(out_scale, 4))
-        return TACO_ERR_MISALIGNED;
-    if (overlap(out_codes, n, out_alpha, 4 * nb) || overlap(out_codes, n, out_scale, 4 * nb) ||
-        overlap(out_alpha, 4 * nb, out_scale, 4 * nb))
-        return TACO_ERR_INVALID_ARG;
     taco::ShardPtrs sp{};
-    for (int p = 0; p < P; ++p) {
-        if (!codes[p] || !alpha[p] || !scale[p])
-            return TACO_ERR_INVALID_ARG;
-        if (!aligned(codes[p], 16) || !aligned(alpha[p], 4) || !aligned(scale[p], 4))
-            return TACO_ERR_MISALIGNED;
-        const void *ins[3] = {codes[p], alpha[p], scale[p]};
-        const uint64_t lens[3] = {n, 4 * nb, 4 * nb};
-        for (int i = 0; i < 3; ++i)
-            if (overlap(ins[i], lens[i], out_codes, n) || overlap(ins[i], lens[i], out_alpha, 4 * nb) ||
-                overlap(ins[i], lens[i], out_scale, 4 * nb))
-                return TACO_ERR_INVALID_ARG;
-        sp.codes[p] = codes[p];
-        sp.alpha[p] = alpha[p];
-        sp.scale[p] = scale[p];
-    }
-    return from_cuda(taco::launch_taco_reduce(P, sp, static_cast<int64_t>(nb), block, e_target, eps,
-                                              out_codes, out_alpha, out_scale,
-                                              reinterpret_cast<cudaStream_t>(stream)));
+    taco_status st = check_reduce_args(P, codes, alpha, scale, rows, d, block, e_target, eps, out_codes,
+                                       out_alpha, out_scale, nullptr, 0, &sp);
+    if (st != TACO_OK || rows == 0)
+        return st;
+    return from_cuda(taco::launch_taco_reduce(P, sp, rows * d / block, block, e_target, eps, out_codes,
+                                              out_alpha, out_scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_reduce_decompress(int32_t P, const uint8_t *const *codes, const float *const *alpha,
+                                   const float *const *scale, int64_t rows, int64_t d, int32_t block,
+                                   float e_target, float eps, uint8_t *out_codes, float *out_alpha,
+                                   float *out_scale, void *out, int32_t out_is_bf16, taco_stream_t stream)
+{
+    taco::ShardPtrs sp{};
+    if (rows > 0 && !out)
+        return TACO_ERR_INVALID_ARG;
+    taco_status st = check_reduce_args(P, codes, alpha, scale, rows, d, block, e_target, eps, out_codes,
+                                       out_alpha, out_scale, out, out_is_bf16 ? 2 : 4, &sp);
+    if (st != TACO_OK || rows == 0)
+        return st;
+    return from_cuda(taco::launch_reduce_decompress(P, sp, rows * d / 128, block, e_target, eps, out_codes,
+                                                    out_alpha, out_scale, out, out_is_bf16 != 0,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 taco_status agoq_fp8_accumulate(uint8_t *main_codes, float *main_scale, const void *grad_bf16, int64_t n,

@@ -129,6 +129,27 @@ taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes,
                                float *out_scale, taco_stream_t stream);
 
 /*
+ * taco_reduce_decompress - taco_reduce_shards and taco_decompress of its
+ * result in one pass.  The rank that reduces in the two-shot AllReduce
+ * ([TACO] 2.B.3) both sends the compressed sum (AllGather payload) and needs
+ * its reconstruction; this call writes both without reading the compressed
+ * sum back.  out_codes / out_alpha / out_scale equal taco_reduce_shards's
+ * outputs and `out` equals taco_decompress of them, bit for bit.
+ *
+ *  P, codes, alpha, scale,          as taco_reduce_shards
+ *  rows, d, block, e_target, eps
+ *  out_codes, out_alpha, out_scale  out  the compressed sum
+ *  out                              out  [rows, d] fp32, or bf16 when
+ *                                        out_is_bf16 != 0
+ */
+taco_status taco_reduce_decompress(int32_t P, const uint8_t *const *codes,
+                                   const float *const *alpha, const float *const *scale,
+                                   int64_t rows, int64_t d, int32_t block, float e_target,
+                                   float eps, uint8_t *out_codes, float *out_alpha,
+                                   float *out_scale, void *out, int32_t out_is_bf16,
+                                   taco_stream_t stream);
+
+/*
  * agoq_fp8_accumulate - QuanGrad local accumulation, in place.
  * [AGoQ] 2.B: per block of `block` elements, in FP32 arithmetic,
  *   g       = decode(main_codes) * main_scale + grad   (rounded multiply,

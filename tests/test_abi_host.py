@@ -124,3 +124,19 @@ def test_agoq_validation(lib):
 
 def test_device_error_rejects_null(lib):
     assert lib.taco_device_error(None, 0) == INVALID
+
+
+def test_reduce_decompress_validation(lib):
+    def f(P=2, rows=4, d=256, block=128, out=A * 100, out_codes=A * 64, bf16=0):
+        cp, k1 = _lib.ptr_array([A * (1 + p) for p in range(P)])
+        ap, k2 = _lib.ptr_array([A * (20 + p) for p in range(P)])
+        sp, k3 = _lib.ptr_array([A * (40 + p) for p in range(P)])
+        return lib.taco_reduce_decompress(P, cp, ap, sp, rows, d, block, 1.0, 1e-12, out_codes, A * 80,
+                                          A * 90, out, bf16, None)
+    assert f(P=17) == UNSUPPORTED
+    assert f(block=512) == UNSUPPORTED
+    assert f(rows=0) == OK
+    assert f(out=0) == INVALID
+    assert f(out=A * 100 + 4) == MISALIGNED
+    assert f(out=A * 64) == INVALID  # reconstruction overlaps the output codes
+    assert f(out=A * 2) == INVALID  # reconstruction overlaps shard 1

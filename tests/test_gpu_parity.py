@@ -149,6 +149,30 @@ def test_reduce_shard_and_negation_gives_zero_blocks():
     assert torch.all(oa == np.float32(math.sqrt(1.0 / np.float64(np.float32(1e-12)))))
 
 
+@pytest.mark.parametrize("P,block,rows,d", [(1, 128, 40, 512), (2, 128, 96, 1024), (3, 256, 33, 512),
+                                         (4, 128, 300, 1024), (8, 256, 64, 1280), (16, 128, 17, 384),
+                                         (4, 256, 1000, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fused_reduce_decompress_equals_the_two_calls(P, block, rows, d, out_dtype):
+    shards = [api.taco_compress(to_dev_bf16(W.tp_activation(200 + p, rows, d, channel_scale=True,
+                                                           block=block)), block) for p in range(P)]
+    cs, as_, ss = map(list, zip(*shards))
+    rc, ra, rs = api.taco_reduce_shards(cs, as_, ss, block)
+    ref_out = api.taco_decompress(rc, ra, rs, block, out_dtype=out_dtype)
+    fc, fa, fs, fout = api.taco_reduce_decompress(cs, as_, ss, block, out_dtype=out_dtype)
+    assert torch.equal(fc, rc) and torch.equal(fa, ra) and torch.equal(fs, rs)
+    assert torch.equal(fout.view(torch.int32 if out_dtype == torch.float32 else torch.int16),
+                       ref_out.view(torch.int32 if out_dtype == torch.float32 else torch.int16))
+    oc, oa, os_ = oracle.reduce_shards([to_host(c) for c in cs], [to_host(a) for a in as_],
+                                       [to_host(s) for s in ss], block)
+    assert_codes_match(to_host(fc), oc, "fused codes")
+    assert_scalars_match(to_host(fa), oa, "fused alpha")
+    assert_scalars_match(to_host(fs), os_, "fused scale")
+    if out_dtype == torch.float32:
+        ref = oracle.decompress(to_host(fc), to_host(fa), to_host(fs), block)
+        assert_recon_match(to_host(fout), ref.reshape(-1), block)
+
+
 # ------------------------------------------------------------------ AGoQ --
 
 @pytest.mark.parametrize("block", [128, 256])
@@ -224,7 +248,7 @@ def test_full_size_two_shot_local_path(name):
     bits = np.stack([W.shard_input(name, p) for p in range(P)])
     x = to_dev_bf16(bits).reshape(P, rows, d)
     nb = rows * d // block
-    path = api.TwoShotLocal(P, rows, d, block)
+    path = api.TwoShotLocal(P, rows, d, block)  # the benchmark's path (fused reduce + decompress)
     out = path.run(x)
     torch.cuda.synchronize()
     assert_code_properties(path.codes, x, block)
