@@ -312,6 +312,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks of the host pipeline")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows per shard")
     ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -403,16 +404,16 @@ def main():
         h_in = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
         h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
         h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
-        x2 = torch.empty_like(x)
+        pipe = api.HostPipeline(P, rows, d, block, chunks=args.e2e_chunks)
         for _ in range(3):
-            path.run_host(h_in, h_out, x2)
+            pipe.run(h_in, h_out)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            path.run_host(h_in, h_out, x2)
+            pipe.run(h_in, h_out)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)
@@ -456,7 +457,7 @@ def main():
             "e2e": None if e2e_ms is None else {
                 "value": whole_job_gbs(step_bytes, args.e2e_steps, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
-                "api": "TwoShotLocal.run_host (pinned host in/out)"},
+                "api": f"HostPipeline.run (pinned host in/out, {pipe.C} row chunks on 3 streams)"},
             "other_workloads": extra,
             "gpu_launches": len(launches) * K,
             "clocks": clk,

@@ -275,3 +275,63 @@ class TwoShotLocal:
             self.run(x_dev, s)
             out_host.copy_(self.out, non_blocking=True)
         return out_host
+
+
+class HostPipeline:
+    """The two-shot local path between pinned HOST buffers, overlapped.
+
+    The rows are split into ``chunks`` equal chunks.  Chunk c is copied in
+    (all P shards) on one stream, compressed and reduced + decompressed on a
+    second, and its result copied out on a third, so host-to-device copies,
+    kernels and device-to-host copies of different chunks run at the same
+    time.  Device buffers are chunk-major and allocated once; the result is
+    identical to ``TwoShotLocal.run`` on the same data."""
+
+    def __init__(self, P: int, rows: int, d: int, block: int = 128, chunks: int = 8, device="cuda",
+                 e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32):
+        while chunks > 1 and rows % chunks:
+            chunks -= 1
+        self.P, self.rows, self.d, self.block, self.C = P, rows, d, block, chunks
+        self.R = rows // chunks
+        self.e_target, self.eps = e_target, eps
+        C, R = chunks, self.R
+        nb = R * d // block
+        self.x = torch.empty((C, P, R, d), dtype=torch.bfloat16, device=device)
+        self.codes = torch.empty((C, P, R, d), dtype=torch.uint8, device=device)
+        self.alpha = torch.empty((C, P, nb), dtype=torch.float32, device=device)
+        self.scale = torch.empty((C, P, nb), dtype=torch.float32, device=device)
+        self.r_codes = torch.empty((C, R, d), dtype=torch.uint8, device=device)
+        self.r_alpha = torch.empty((C, nb), dtype=torch.float32, device=device)
+        self.r_scale = torch.empty((C, nb), dtype=torch.float32, device=device)
+        self.out = torch.empty((C, R, d), dtype=out_dtype, device=device)
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
+        self.ev_in = [torch.cuda.Event() for _ in range(C)]
+        self.ev_done = [torch.cuda.Event() for _ in range(C)]
+        self._lists = [(list(self.codes[c]), list(self.alpha[c]), list(self.scale[c])) for c in range(C)]
+
+    def run(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.Tensor:
+        """x_host: pinned bf16 [P, rows, d]; out_host: pinned [rows, d]."""
+        s_in, s_comp, s_out = self.streams
+        cur = torch.cuda.current_stream()
+        for s in self.streams:
+            s.wait_stream(cur)
+        R = self.R
+        for c in range(self.C):
+            with torch.cuda.stream(s_in):
+                for p in range(self.P):
+                    self.x[c, p].copy_(x_host[p, c * R:(c + 1) * R], non_blocking=True)
+                self.ev_in[c].record(s_in)
+            s_comp.wait_event(self.ev_in[c])
+            codes, alpha, scale = self._lists[c]
+            taco_compress(self.x[c], self.block, self.e_target, self.eps, self.codes[c],
+                          self.alpha[c], self.scale[c], stream=s_comp)
+            taco_reduce_decompress(codes, alpha, scale, self.block, self.e_target, self.eps,
+                                   self.r_codes[c], self.r_alpha[c], self.r_scale[c], self.out[c],
+                                   stream=s_comp)
+            self.ev_done[c].record(s_comp)
+            s_out.wait_event(self.ev_done[c])
+            with torch.cuda.stream(s_out):
+                out_host[c * R:(c + 1) * R].copy_(self.out[c], non_blocking=True)
+        for s in self.streams:
+            cur.wait_stream(s)
+        return out_host

@@ -277,6 +277,22 @@ def test_full_size_two_shot_local_path(name):
     assert_recon_match(gather_blocks(out, blocks, block), ref, block)
 
 
+@pytest.mark.parametrize("P,rows,d,block,chunks", [(4, 512, 1024, 128, 8), (2, 96, 512, 256, 3),
+                                                 (3, 100, 384, 128, 7)])
+def test_host_pipeline_equals_device_path(P, rows, d, block, chunks):
+    bits = np.stack([W.tp_activation(400 + p, rows, d, channel_scale=True, block=block) for p in range(P)])
+    x = to_dev_bf16(bits).reshape(P, rows, d)
+    ref = api.TwoShotLocal(P, rows, d, block).run(x).clone()
+    pipe = api.HostPipeline(P, rows, d, block, chunks=chunks)
+    h_in = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
+    h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+    h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
+    for _ in range(2):
+        pipe.run(h_in, h_out)
+        torch.cuda.synchronize()
+        assert torch.equal(h_out.view(torch.int32), ref.cpu().view(torch.int32))
+
+
 def test_full_size_agoq_accumulate_and_reduce():
     a = W.AGOQ
     block, n = a["block"], a["n_main"]
