@@ -58,9 +58,11 @@ def _load():
             lib.oracle_agoq_accumulate.argtypes = [P, P, P, i64, i32]
             lib.oracle_agoq_reduce.argtypes = [i32, P, P, i64, i32, P, P]
             lib.oracle_int8_roundtrip.argtypes = [P, i64, i64, i32, P]
+            lib.oracle_compress_int8.argtypes = [P, i64, i64, i32, f32, f32, P, P, P]
+            lib.oracle_decompress_int8.argtypes = [P, P, P, i64, i64, i32, P]
             for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
                       "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
-                      "oracle_int8_roundtrip"):
+                      "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -203,4 +205,28 @@ def int8_roundtrip(x_bf16: np.ndarray, block: int) -> np.ndarray:
     rows, d = x.shape
     out = np.empty((rows, d), dtype=np.float64)
     _check(_load().oracle_int8_roundtrip(_ptr(x), rows, d, block, _ptr(out)))
+    return out
+
+
+# ------------------------------------------------------ INT8 ASH + DS ----
+
+def compress_int8(x_bf16: np.ndarray, block: int, e_target: float = 1.0, eps: float = 1e-12):
+    """ASH + DS with INT8 codes: (codes int8 [rows, d], alpha, scale)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, d = x.shape
+    codes = np.empty((rows, d), dtype=np.int8)
+    alpha = np.empty((rows, d // block), dtype=np.float32)
+    scale = np.empty((rows, d // block), dtype=np.float32)
+    _check(_load().oracle_compress_int8(_ptr(x), rows, d, block, e_target, eps, _ptr(codes),
+                                        _ptr(alpha), _ptr(scale)))
+    return codes, alpha, scale
+
+
+def decompress_int8(codes: np.ndarray, alpha: np.ndarray, scale: np.ndarray, block: int) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    a = np.ascontiguousarray(alpha, dtype=np.float32)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    rows, d = c.shape
+    out = np.empty((rows, d), dtype=np.float64)
+    _check(_load().oracle_decompress_int8(_ptr(c), _ptr(a), _ptr(s), rows, d, block, _ptr(out)))
     return out

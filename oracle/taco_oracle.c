@@ -368,6 +368,88 @@ int oracle_agoq_reduce(int P, const uint8_t *const *codes, const float *const *s
     return 0;
 }
 
+/* ------------------------------------------------------- INT8 ASH + DS */
+/* [TACO] 5: the same ASH + DS pipeline with INT8 codes for hardware without
+ * native FP8.  Steps 1-3 are those of compress_block; then
+ *   4. s = fp32(127 / max|y|)   (1 for an all-zero y; clamped to FLT_MAX)
+ *   5. code_i = round-to-nearest-even(fp32(y_i * s)), clamped to [-127, 127]
+ * and the reconstruction is c * H(code / s) / alpha. */
+static void compress_block_int8(const double *x, int n, double e_target, double eps, int8_t *codes,
+                                float *alpha_out, float *scale_out, double *work)
+{
+    double m = 0.0, c = 1.0 / sqrt((double)n), maxabs = 0.0, q;
+    float alpha_f, s_f = 1.0f;
+    int i;
+    for (i = 0; i < n; ++i)
+        m += x[i] * x[i];
+    m /= n;
+    alpha_f = (float)sqrt(e_target / (m + eps));
+    for (i = 0; i < n; ++i)
+        work[i] = (double)alpha_f * x[i];
+    oracle_fwht(work, n);
+    for (i = 0; i < n; ++i) {
+        work[i] *= c;
+        if (fabs(work[i]) > maxabs)
+            maxabs = fabs(work[i]);
+    }
+    if (maxabs > 0.0) {
+        q = 127.0 / maxabs;
+        s_f = q > (double)FLT_MAX ? FLT_MAX : (float)q;
+    }
+    for (i = 0; i < n; ++i) {
+        const float v = (float)(work[i] * (double)s_f);
+        double r = rint((double)v);
+        if (r > 127.0)
+            r = 127.0;
+        if (r < -127.0)
+            r = -127.0;
+        codes[i] = (int8_t)r;
+    }
+    *alpha_out = alpha_f;
+    *scale_out = s_f;
+}
+
+int oracle_compress_int8(const uint16_t *x_bf16, int64_t rows, int64_t d, int block, float e_target,
+                         float eps, int8_t *codes, float *alpha, float *scale)
+{
+    int64_t nb, k;
+    int i;
+    double *x, *work;
+    if (!shape_ok(rows, d, block))
+        return -1;
+    nb = rows * d / block;
+    x = (double *)malloc(sizeof(double) * block);
+    work = (double *)malloc(sizeof(double) * block);
+    for (k = 0; k < nb; ++k) {
+        for (i = 0; i < block; ++i)
+            x[i] = bf16_to_double(x_bf16[k * block + i]);
+        compress_block_int8(x, block, e_target, eps, codes + k * block, alpha + k, scale + k, work);
+    }
+    free(x);
+    free(work);
+    return 0;
+}
+
+int oracle_decompress_int8(const int8_t *codes, const float *alpha, const float *scale, int64_t rows,
+                           int64_t d, int block, double *out)
+{
+    int64_t nb, k;
+    int i;
+    double c = 1.0 / sqrt((double)block);
+    if (!shape_ok(rows, d, block))
+        return -1;
+    nb = rows * d / block;
+    for (k = 0; k < nb; ++k) {
+        double *o = out + k * block;
+        for (i = 0; i < block; ++i)
+            o[i] = (double)codes[k * block + i] / (double)scale[k];
+        oracle_fwht(o, block);
+        for (i = 0; i < block; ++i)
+            o[i] = c * o[i] / (double)alpha[k];
+    }
+    return 0;
+}
+
 /* The uniform INT8 comparison point of [TACO] 2.A: per block of raw x, no
  * transform, q = clamp(rint(x * 127 / amax), -127, 127), x_hat = q * amax / 127
  * (an all-zero block reconstructs to zeros). */

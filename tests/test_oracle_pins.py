@@ -478,3 +478,67 @@ def test_agoq_reduce_of_shard_and_negation_is_zero():
                                   W.agoq_grad(8, n))
     rc, rs = oracle.agoq_reduce([c, c ^ 0x80], [s, s])
     assert np.all(rc & 0x7F == 0) and np.all(rs == 1.0)
+
+
+# ------------------------------------------------------ INT8 ASH + DS ---
+# TACO section 5: the same pipeline with INT8 codes (Q_max = 127).
+
+def test_int8_codec_matches_library_rederivation():
+    n = 128
+    x = W.tp_activation(12, 16, 1024, channel_scale=True, zero_blocks=(3,), block=n)
+    codes, alpha, scale = oracle.compress_int8(x, n)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64).reshape(-1, n)
+    H = scipy.linalg.hadamard(n).astype(np.float64)
+    m = np.mean(xf * xf, axis=1)
+    a = np.sqrt(1.0 / (m + np.float64(np.float32(1e-12)))).astype(np.float32)
+    y = (a.astype(np.float64)[:, None] * xf) @ H.T / math.sqrt(n)
+    M = np.abs(y).max(axis=1)
+    s = np.where(M > 0, 127.0 / np.where(M > 0, M, 1), 1.0).astype(np.float32)
+    ref = np.clip(np.rint((y * s.astype(np.float64)[:, None]).astype(np.float32)), -127, 127)
+    assert np.array_equal(alpha.reshape(-1), a)
+    assert np.max(np.abs(scale.reshape(-1).astype(np.float64) / s - 1)) <= 2 ** -23
+    assert np.mean(codes.reshape(-1, n) == ref) >= 0.9999
+    assert np.max(np.abs(codes.reshape(-1, n).astype(int) - ref)) <= 1
+
+
+def test_int8_codec_closed_forms():
+    n = 128
+    H = scipy.linalg.hadamard(n)
+    xv = np.zeros(n, dtype=np.float32)
+    xv[9] = -0.5
+    c, a, s = oracle.compress_int8(bf16(xv).reshape(1, n), n)
+    assert np.array_equal(c.reshape(-1), np.where(-H[:, 9] < 0, -127, 127))
+    assert np.allclose(oracle.decompress_int8(c, a, s, n).reshape(-1), xv, atol=1e-7)
+    row = (2.0 * H[5]).astype(np.float32)
+    c, a, s = oracle.compress_int8(bf16(row).reshape(1, n), n)
+    expect = np.zeros(n, dtype=np.int8)
+    expect[5] = 127
+    assert np.array_equal(c.reshape(-1), expect)
+    c, a, s = oracle.compress_int8(np.zeros((1, n), np.uint16), n)
+    assert np.all(c == 0) and s[0, 0] == 1.0 and np.all(oracle.decompress_int8(c, a, s, n) == 0)
+
+
+def test_int8_codec_error_within_half_a_step():
+    n = 256
+    x = W.tp_activation(13, 8, 1024, channel_scale=True, block=n)
+    codes, alpha, scale = oracle.compress_int8(x, n)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64).reshape(-1, n)
+    xhat = oracle.decompress_int8(codes, alpha, scale, n).reshape(-1, n)
+    # |code - y s| <= 1/2 per element and the transform is orthonormal
+    lim = 0.5 * math.sqrt(n) / (alpha.reshape(-1).astype(np.float64) * scale.reshape(-1))
+    assert np.all(np.sqrt(np.sum((xhat - xf) ** 2, axis=1)) <= lim * (1 + 1e-6))
+    assert np.abs(codes).max() == 127
+
+
+def test_int8_ash_avoids_the_zero_collapse_of_plain_int8():
+    """TACO sections 2.A and 5: plain per-block INT8 maps most of the dense
+    near-zero values to 0; with the ASH rotation in front they survive."""
+    n = 128
+    x = W.shard_input("tiny_64x1024_n128", 0)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    small = (xf != 0) & (np.abs(xf) < 1e-2)
+    c, a, s = oracle.compress_int8(x, n)
+    ash = oracle.decompress_int8(c, a, s, n)
+    plain = oracle.int8_roundtrip(x, n)
+    assert np.mean(plain[small] == 0) > 0.3
+    assert np.mean(ash[small] == 0) < 0.05
