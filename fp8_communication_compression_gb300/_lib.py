@@ -28,6 +28,8 @@ SIGNATURES = {
     "taco_block_supported": (ctypes.c_int, [_I32]),
     "taco_compress": (ctypes.c_int, [_P, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P]),
     "taco_decompress": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
+    "taco_compress_int8": (ctypes.c_int, [_P, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P]),
+    "taco_decompress_int8": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
     "taco_reduce_shards": (ctypes.c_int, [_I32, _PP, _PP, _PP, _I64, _I64, _I32, _F32, _F32,
                                           _P, _P, _P, _P]),
     "taco_reduce_decompress": (ctypes.c_int, [_I32, _PP, _PP, _PP, _I64, _I64, _I32, _F32, _F32,

@@ -88,6 +88,46 @@ def taco_decompress(codes: torch.Tensor, alpha: torch.Tensor, scale: torch.Tenso
     return out
 
 
+def taco_compress_int8(x: torch.Tensor, block: int = 128, e_target: float = E_TARGET,
+                       eps: float = EPS, codes: torch.Tensor | None = None,
+                       alpha: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                       stream=None):
+    """ASH + DS with INT8 codes: bf16 [..., d] -> (codes int8, alpha, scale)."""
+    _need(x, "x", _BF16)
+    rows, d = _shape2(x)
+    nb = rows * d // block if block else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if alpha is None:
+        alpha = torch.empty(nb, dtype=torch.float32, device=x.device)
+    if scale is None:
+        scale = torch.empty(nb, dtype=torch.float32, device=x.device)
+    _need(codes, "codes", (torch.int8,), x.numel())
+    _need(alpha, "alpha", (torch.float32,))
+    _need(scale, "scale", (torch.float32,))
+    st = _lib.load().taco_compress_int8(x.data_ptr(), rows, d, block, e_target, eps, codes.data_ptr(),
+                                        alpha.data_ptr(), scale.data_ptr(), _stream_handle(stream))
+    _lib.check("taco_compress_int8", st)
+    return codes, alpha, scale
+
+
+def taco_decompress_int8(codes: torch.Tensor, alpha: torch.Tensor, scale: torch.Tensor,
+                         block: int = 128, out_dtype: torch.dtype = torch.float32,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _need(codes, "codes", (torch.int8,))
+    _need(alpha, "alpha", (torch.float32,))
+    _need(scale, "scale", (torch.float32,))
+    rows, d = _shape2(codes)
+    if out is None:
+        out = torch.empty(codes.shape, dtype=out_dtype, device=codes.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), codes.numel())
+    st = _lib.load().taco_decompress_int8(codes.data_ptr(), alpha.data_ptr(), scale.data_ptr(), rows,
+                                          d, block, out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                          _stream_handle(stream))
+    _lib.check("taco_decompress_int8", st)
+    return out
+
+
 def taco_reduce_shards(codes: Sequence[torch.Tensor], alpha: Sequence[torch.Tensor],
                        scale: Sequence[torch.Tensor], block: int = 128, e_target: float = E_TARGET,
                        eps: float = EPS, out_codes: torch.Tensor | None = None,

@@ -66,7 +66,9 @@ constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kBarBytes;
 // keeps kStages TMA loads in flight and refills a stage as soon as the warp
 // has read it.
 
-template <int NB>
+// FMT_INT8: INT8 codes with Q_max = 127 (the fallback format); otherwise
+// E4M3 codes with Q_max = 448.
+template <int NB, bool FMT_INT8>
 __global__ void __launch_bounds__(kThreads, 1)
     taco_compress_kernel(const __grid_constant__ CUtensorMap x_map,
                          const __grid_constant__ CUtensorMap c_map, float *__restrict__ alpha_out,
@@ -164,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = sqrtf(e_target / (m + eps));
         const float ac = alpha * c;
         const float M = ac * mh;
-        const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+        constexpr float kQmax = FMT_INT8 ? 127.0f : 448.0f;
+        const float scale = (M > 0.0f) ? fminf(kQmax / M, FLT_MAX) : 1.0f;
         float k = ac * scale;
         if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
             const float2 ac2 = make_float2(ac, ac);
@@ -182,8 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint32_t w0, w1, w2, w3;
-            encode8(&v[8 * j], k2, w0, w1);
-            encode8(&v[8 * j + 4], k2, w2, w3);
+            if constexpr (FMT_INT8) {
+                encode8_s8(&v[8 * j], k2, w0, w1);
+                encode8_s8(&v[8 * j + 4], k2, w2, w3);
+            } else {
+                encode8(&v[8 * j], k2, w0, w1);
+                encode8(&v[8 * j + 4], k2, w2, w3);
+            }
             sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
         }
         fence_proxy_async_smem();
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                             decompressor                              //
 // ===================================================================== //
 
-template <int NB, bool BF16OUT>
+template <int NB, bool BF16OUT, bool FMT_INT8>
 __global__ void __launch_bounds__(kThreads, 1)
     taco_decompress_kernel(const __grid_constant__ CUtensorMap c_map,
                            const __grid_constant__ CUtensorMap o_map, const float *__restrict__ alpha,
@@ -263,8 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t rowp = wbase + s * kDStageBytes + lane * 128;
         float2 v[64];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            decode16_stage1(lds128(rowp + ((static_cast<uint32_t>(j) << 4) ^ swz)), v, j);
+        for (int j = 0; j < 8; ++j) {
+            const uint4 q = lds128(rowp + ((static_cast<uint32_t>(j) << 4) ^ swz));
+            if constexpr (FMT_INT8)
+                decode16_stage1_s8(q, v, j);
+            else
+                decode16_stage1(q, v, j);
+        }
         fwht128_upper(v);  // consumes every decoded value
         __syncwarp();
         if (lane == 0) {
@@ -363,8 +376,36 @@ int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base
     return r == CUDA_SUCCESS ? 0 : -2;
 }
 
+namespace {
+
+template <int NB, bool I8>
+cudaError_t run_compress(const CUtensorMap &xm, const CUtensorMap &cm, float *alpha, float *scale,
+                         int64_t nrows, float e_target, float eps, int grid, cudaStream_t stream, int device)
+{
+    static bool set[kMaxDevices];
+    cudaError_t e = ensure_smem(taco_compress_kernel<NB, I8>, kCSmemBytes, device, set);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(taco_compress_kernel<NB, I8>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
+                      nrows, e_target, eps);
+}
+
+template <int NB, bool BF, bool I8>
+cudaError_t run_decompress(const CUtensorMap &cm, const CUtensorMap &om, const float *alpha,
+                           const float *scale, int64_t nrows, int grid, cudaStream_t stream, int device)
+{
+    static bool set[kMaxDevices];
+    cudaError_t e = ensure_smem(taco_decompress_kernel<NB, BF, I8>, kDSmemBytes, device, set);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(taco_decompress_kernel<NB, BF, I8>, grid, kThreads, kDSmemBytes, stream, cm, om, alpha,
+                      scale, nrows);
+}
+
+}  // namespace
+
 cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float e_target, float eps,
-                            uint8_t *codes, float *alpha, float *scale, cudaStream_t stream)
+                            uint8_t *codes, float *alpha, float *scale, bool int8_codes, cudaStream_t stream)
 {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
@@ -377,23 +418,16 @@ cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float 
         return cudaErrorInvalidValue;
     const int64_t ctas = (nrows + kWarps * kWarpRows - 1) / (kWarps * kWarpRows);
     const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
-    static bool set128[kMaxDevices], set256[kMaxDevices];
-    if (block == 128) {
-        if ((e = ensure_smem(taco_compress_kernel<128>, kCSmemBytes, di.device, set128)) != cudaSuccess)
-            return e;
-        e = launch_pdl(taco_compress_kernel<128>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
-                       nrows, e_target, eps);
-    } else {
-        if ((e = ensure_smem(taco_compress_kernel<256>, kCSmemBytes, di.device, set256)) != cudaSuccess)
-            return e;
-        e = launch_pdl(taco_compress_kernel<256>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
-                       nrows, e_target, eps);
-    }
-    return e;
+    if (block == 128)
+        return int8_codes ? run_compress<128, true>(xm, cm, alpha, scale, nrows, e_target, eps, grid, stream, di.device)
+                          : run_compress<128, false>(xm, cm, alpha, scale, nrows, e_target, eps, grid, stream,
+                                                     di.device);
+    return int8_codes ? run_compress<256, true>(xm, cm, alpha, scale, nrows, e_target, eps, grid, stream, di.device)
+                      : run_compress<256, false>(xm, cm, alpha, scale, nrows, e_target, eps, grid, stream, di.device);
 }
 
-cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale,
-                              int64_t nrows, int block, void *out, bool out_bf16, cudaStream_t stream)
+cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale, int64_t nrows,
+                              int block, void *out, bool out_bf16, bool int8_codes, cudaStream_t stream)
 {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
@@ -410,28 +444,19 @@ cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const fl
         return cudaErrorInvalidValue;
     const int64_t ctas = (nrows + kWarps * kWarpRows - 1) / (kWarps * kWarpRows);
     const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
-    static bool s0[kMaxDevices], s1[kMaxDevices], s2[kMaxDevices], s3[kMaxDevices];
-#define TACO_LAUNCH_D(NB, BF, FLAGS)                                                               \
-    do {                                                                                           \
-        if ((e = ensure_smem(taco_decompress_kernel<NB, BF>, kDSmemBytes, di.device, FLAGS)) !=   \
-            cudaSuccess)                                                                           \
-            return e;                                                                              \
-        e = launch_pdl(taco_decompress_kernel<NB, BF>, grid, kThreads, kDSmemBytes, stream, cm, om, \
-                       alpha, scale, nrows);                                                       \
-    } while (0)
+    const int dev = di.device;
     if (block == 128) {
-        if (out_bf16)
-            TACO_LAUNCH_D(128, true, s0);
-        else
-            TACO_LAUNCH_D(128, false, s1);
-    } else {
-        if (out_bf16)
-            TACO_LAUNCH_D(256, true, s2);
-        else
-            TACO_LAUNCH_D(256, false, s3);
+        if (int8_codes)
+            return out_bf16 ? run_decompress<128, true, true>(cm, om, alpha, scale, nrows, grid, stream, dev)
+                            : run_decompress<128, false, true>(cm, om, alpha, scale, nrows, grid, stream, dev);
+        return out_bf16 ? run_decompress<128, true, false>(cm, om, alpha, scale, nrows, grid, stream, dev)
+                        : run_decompress<128, false, false>(cm, om, alpha, scale, nrows, grid, stream, dev);
     }
-#undef TACO_LAUNCH_D
-    return e;
+    if (int8_codes)
+        return out_bf16 ? run_decompress<256, true, true>(cm, om, alpha, scale, nrows, grid, stream, dev)
+                        : run_decompress<256, false, true>(cm, om, alpha, scale, nrows, grid, stream, dev);
+    return out_bf16 ? run_decompress<256, true, false>(cm, om, alpha, scale, nrows, grid, stream, dev)
+                    : run_decompress<256, false, false>(cm, om, alpha, scale, nrows, grid, stream, dev);
 }
 
 cudaError_t read_codec_error(uint32_t *flags, bool clear)

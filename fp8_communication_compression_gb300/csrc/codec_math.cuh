@@ -103,6 +103,54 @@ __device__ __forceinline__ void encode8(const float2 *v, float2 k2, uint32_t &w0
     w1 = f32x4_to_e4m3x4(c.x, c.y, d.x, d.y);
 }
 
+// ---- INT8 codes (the fallback format for hardware without native FP8) ----
+
+// Four fp32 values (already scaled into [-127, 127]) -> four int8 codes,
+// round to nearest even, packed little-endian.
+__device__ __forceinline__ uint32_t f32x4_to_s8x4(float a, float b, float c, float d)
+{
+    const int ia = __float2int_rn(a), ib = __float2int_rn(b);
+    const int ic = __float2int_rn(c), id = __float2int_rn(d);
+    const uint32_t lo = __byte_perm(ia, ib, 0x0040), hi = __byte_perm(ic, id, 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ void encode8_s8(const float2 *v, float2 k2, uint32_t &w0, uint32_t &w1)
+{
+    const float2 a = __fmul2_rn(v[0], k2), b = __fmul2_rn(v[1], k2);
+    const float2 c = __fmul2_rn(v[2], k2), d = __fmul2_rn(v[3], k2);
+    w0 = f32x4_to_s8x4(a.x, a.y, b.x, b.y);
+    w1 = f32x4_to_s8x4(c.x, c.y, d.x, d.y);
+}
+
+// Four int8 codes -> four fp32 values, exactly: the biased byte b + 128 is
+// placed in the low mantissa bits of 2^23, and 2^23 + 128 is subtracted.
+__device__ __forceinline__ void s8x4_to_f32x4(uint32_t w, float2 &lo, float2 &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 bias = make_float2(8388736.0f, 8388736.0f);
+    const float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
+    const float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
+    lo = __fadd2_rn(a, make_float2(-bias.x, -bias.y));
+    hi = __fadd2_rn(b, make_float2(-bias.x, -bias.y));
+}
+
+// Decodes one 16-byte chunk of 16 INT8 codes into v[8 j .. 8 j + 7] after
+// the bit-0 butterfly stage.
+__device__ __forceinline__ void decode16_stage1_s8(const uint4 q, float2 (&v)[64], int j)
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        float2 e01, e23;
+        s8x4_to_f32x4(w[t], e01, e23);
+        v[8 * j + 2 * t] = make_float2(e01.x + e01.y, e01.x - e01.y);
+        v[8 * j + 2 * t + 1] = make_float2(e23.x + e23.y, e23.x - e23.y);
+    }
+}
+
 // Decodes one 16-byte chunk of 16 codes (row elements 16 j .. 16 j + 15)
 // into v[8 j .. 8 j + 7] after the bit-0 butterfly stage.
 __device__ __forceinline__ void decode16_stage1(const uint4 q, float2 (&v)[64], int j)

@@ -23,10 +23,12 @@ int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base
 
 // Kernels working on the "128-view" of a TACO tensor: nrows rows of 128
 // elements; a block of n elements spans n / 128 consecutive rows.
+// int8_codes selects the INT8 code format (Q_max 127) instead of E4M3.
 cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float e_target, float eps,
-                            uint8_t *codes, float *alpha, float *scale, cudaStream_t stream);
+                            uint8_t *codes, float *alpha, float *scale, bool int8_codes,
+                            cudaStream_t stream);
 cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const float *scale,
-                              int64_t nrows, int block, void *out, bool out_bf16,
+                              int64_t nrows, int block, void *out, bool out_bf16, bool int8_codes,
                               cudaStream_t stream);
 
 // Direct-load kernels (no Hadamard on their path).

@@ -147,8 +147,9 @@ int taco_abi_version(void) { return TACO_ABI_VERSION; }
 
 int taco_block_supported(int32_t block) { return block == 128 || block == 256; }
 
-taco_status taco_compress(const void *x_bf16, int64_t rows, int64_t d, int32_t block, float e_target,
-                          float eps, uint8_t *codes, float *alpha, float *scale, taco_stream_t stream)
+static taco_status compress_any(const void *x_bf16, int64_t rows, int64_t d, int32_t block, float e_target,
+                                float eps, uint8_t *codes, float *alpha, float *scale, bool int8_codes,
+                                taco_stream_t stream)
 {
     taco_status st = check_taco_shape(rows, d, block);
     if (st != TACO_OK)
@@ -167,12 +168,25 @@ taco_status taco_compress(const void *x_bf16, int64_t rows, int64_t d, int32_t b
         overlap(codes, n, scale, 4 * nb) || overlap(alpha, 4 * nb, scale, 4 * nb))
         return TACO_ERR_INVALID_ARG;
     return from_cuda(taco::launch_compress(x_bf16, rows * d / 128, block, e_target, eps, codes, alpha,
-                                           scale, reinterpret_cast<cudaStream_t>(stream)));
+                                           scale, int8_codes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-taco_status taco_decompress(const uint8_t *codes, const float *alpha, const float *scale, int64_t rows,
-                            int64_t d, int32_t block, void *out, int32_t out_is_bf16,
-                            taco_stream_t stream)
+taco_status taco_compress(const void *x_bf16, int64_t rows, int64_t d, int32_t block, float e_target,
+                          float eps, uint8_t *codes, float *alpha, float *scale, taco_stream_t stream)
+{
+    return compress_any(x_bf16, rows, d, block, e_target, eps, codes, alpha, scale, false, stream);
+}
+
+taco_status taco_compress_int8(const void *x_bf16, int64_t rows, int64_t d, int32_t block, float e_target,
+                               float eps, int8_t *codes, float *alpha, float *scale, taco_stream_t stream)
+{
+    return compress_any(x_bf16, rows, d, block, e_target, eps, reinterpret_cast<uint8_t *>(codes), alpha,
+                        scale, true, stream);
+}
+
+static taco_status decompress_any(const uint8_t *codes, const float *alpha, const float *scale, int64_t rows,
+                                  int64_t d, int32_t block, void *out, int32_t out_is_bf16, bool int8_codes,
+                                  taco_stream_t stream)
 {
     taco_status st = check_taco_shape(rows, d, block);
     if (st != TACO_OK)
@@ -189,7 +203,23 @@ taco_status taco_decompress(const uint8_t *codes, const float *alpha, const floa
         overlap(out, out_bytes, scale, 4 * nb))
         return TACO_ERR_INVALID_ARG;
     return from_cuda(taco::launch_decompress(codes, alpha, scale, rows * d / 128, block, out,
-                                             out_is_bf16 != 0, reinterpret_cast<cudaStream_t>(stream)));
+                                             out_is_bf16 != 0, int8_codes,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_decompress(const uint8_t *codes, const float *alpha, const float *scale, int64_t rows,
+                            int64_t d, int32_t block, void *out, int32_t out_is_bf16,
+                            taco_stream_t stream)
+{
+    return decompress_any(codes, alpha, scale, rows, d, block, out, out_is_bf16, false, stream);
+}
+
+taco_status taco_decompress_int8(const int8_t *codes, const float *alpha, const float *scale, int64_t rows,
+                                 int64_t d, int32_t block, void *out, int32_t out_is_bf16,
+                                 taco_stream_t stream)
+{
+    return decompress_any(reinterpret_cast<const uint8_t *>(codes), alpha, scale, rows, d, block, out,
+                          out_is_bf16, true, stream);
 }
 
 taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes, const float *const *alpha,

@@ -107,6 +107,22 @@ taco_status taco_decompress(const uint8_t *codes, const float *alpha, const floa
                             int32_t out_is_bf16, taco_stream_t stream);
 
 /*
+ * taco_compress_int8 / taco_decompress_int8 - the same ASH + DS codec with
+ * INT8 codes, the fallback [TACO] 5 names for hardware without native FP8:
+ *   scale  = 127 / max|y|   (1 if y == 0)
+ *   codes  = round-to-nearest-even(y * scale), in [-127, 127]
+ *   out    = (1/sqrt(block)) H (codes / scale) / alpha
+ * Arguments, layouts and errors as taco_compress / taco_decompress; codes
+ * are int8 [rows, d].
+ */
+taco_status taco_compress_int8(const void *x_bf16, int64_t rows, int64_t d, int32_t block,
+                               float e_target, float eps, int8_t *codes, float *alpha,
+                               float *scale, taco_stream_t stream);
+taco_status taco_decompress_int8(const int8_t *codes, const float *alpha, const float *scale,
+                                 int64_t rows, int64_t d, int32_t block, void *out,
+                                 int32_t out_is_bf16, taco_stream_t stream);
+
+/*
  * taco_reduce_shards - local step of the two-shot AllReduce
  * ([TACO] 2.B.3 ReduceScatter + AllGather; [AGoQ] 2.B "local reduce in
  * FP32"): P compressed shards of the same [rows, d] region, all resident in

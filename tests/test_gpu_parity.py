@@ -124,6 +124,41 @@ def test_codec_edge_blocks(block):
     assert np.all(to_host(out).reshape(-1, block)[:2] == 0.0)
 
 
+# ------------------------------------------------------ INT8 ASH + DS --
+
+@pytest.mark.parametrize("rows,d,block", [(64, 1024, 128), (37, 384, 128), (33, 512, 256),
+                                          (4096, 2048, 128), (2048, 2560, 256)])
+def test_int8_codec(rows, d, block):
+    bits = W.tp_activation(rows + 3 * d, rows, d, channel_scale=True, zero_blocks=(1,), block=block)
+    c, a, s = api.taco_compress_int8(to_dev_bf16(bits), block)
+    rc, ra, rs = oracle.compress_int8(bits, block)
+    g = to_host(c).astype(np.int32).reshape(-1)
+    r = rc.astype(np.int32).reshape(-1)
+    assert np.abs(g).max() <= 127 and np.abs(g - r).max() <= 1 and np.mean(g == r) >= 0.9999
+    assert_scalars_match(to_host(a), ra, "alpha")
+    assert_scalars_match(to_host(s), rs, "scale")
+    out = api.taco_decompress_int8(c, a, s, block)
+    ref = oracle.decompress_int8(to_host(c), to_host(a), to_host(s), block)
+    assert_recon_match(to_host(out), ref.reshape(-1), block)
+    outb = api.taco_decompress_int8(c, a, s, block, out_dtype=torch.bfloat16)
+    gb = to_host(outb.float()).astype(np.float64).reshape(-1)
+    assert np.all(np.abs(gb - ref.reshape(-1)) <= 2.0 ** -8 * np.abs(ref.reshape(-1)) * (1 + 1e-5)
+                  + 1e-6 * np.abs(ref).max())
+
+
+def test_int8_codec_edge_blocks():
+    for block in (128, 256):
+        bits = W.f32_to_bf16_bits(edge_blocks(block))
+        c, a, s = api.taco_compress_int8(to_dev_bf16(bits), block)
+        rc, ra, rs = oracle.compress_int8(bits, block)
+        g = to_host(c).astype(np.int32).reshape(-1)
+        assert np.abs(g - rc.astype(np.int32).reshape(-1)).max() <= 1
+        assert_scalars_match(to_host(a), ra, "alpha")
+        assert_scalars_match(to_host(s), rs, "scale")
+        out = api.taco_decompress_int8(c, a, s, block)
+        assert np.all(to_host(out).reshape(-1, block)[:2] == 0.0)
+
+
 # ---------------------------------------------------------------- reduce --
 
 @pytest.mark.parametrize("P,block", [(1, 128), (2, 256), (3, 128), (4, 128), (8, 256), (16, 128)])
