@@ -17,6 +17,25 @@ CODE_MATCH = 0.9999
 SCALAR_RTOL = 1e-6
 RECON_RTOL = 1e-6
 
+# Statistics of the comparisons made during a test session, written out as
+# JSON at the end when TACO_PARITY_REPORT names a file (see conftest.py).
+REPORT: dict = {}
+_CURRENT = {"test": "?"}
+
+
+def _record(kind: str, what: str, value) -> None:
+    entry = REPORT.setdefault(_CURRENT["test"], {})
+    key = f"{kind}:{what}"
+    old = entry.get(key)
+    if isinstance(value, dict):
+        if old is None:
+            entry[key] = dict(value)
+        else:
+            old["identical"] = min(old["identical"], value["identical"])
+            old["max_ulp"] = max(old["max_ulp"], value["max_ulp"])
+    else:
+        entry[key] = value if old is None else max(old, value)
+
 
 def to_dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
@@ -44,7 +63,9 @@ def assert_codes_match(gpu: np.ndarray, ref: np.ndarray, what: str = "codes", ex
     worst = int(d.max()) if d.size else 0
     assert not np.any((gpu.reshape(-1) & 0x7F) == 0x7F), f"{what}: NaN code emitted"
     assert same >= CODE_MATCH and worst <= 1, f"{what}: identical {same:.6f}, max ULP {worst}"
-    return {"identical": same, "max_ulp": worst}
+    stats = {"identical": same, "max_ulp": worst}
+    _record("codes", what, stats)
+    return stats
 
 
 def assert_scalars_match(gpu: np.ndarray, ref: np.ndarray, what: str, rtol: float = SCALAR_RTOL,
@@ -57,6 +78,7 @@ def assert_scalars_match(gpu: np.ndarray, ref: np.ndarray, what: str, rtol: floa
     err = np.abs(g - r) / np.where(r == 0, 1.0, np.abs(r))
     worst = float(err.max()) if err.size else 0.0
     assert worst <= rtol, f"{what}: max relative error {worst:.3e} at block {int(err.argmax())}"
+    _record("scalar_max_rel", what, worst)
     return worst
 
 
@@ -70,6 +92,7 @@ def assert_recon_match(gpu: np.ndarray, ref: np.ndarray, block: int, what: str =
     bmax = np.abs(r).max(axis=1)
     berr = np.abs(g - r).max(axis=1)
     assert np.all(berr <= rtol * bmax), f"{what}: block max error {float((berr / np.where(bmax == 0, 1, bmax)).max()):.3e}"
+    _record("recon_rel_l2", what, rel)
     return rel
 
 
