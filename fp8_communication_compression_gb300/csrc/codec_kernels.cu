@@ -151,15 +151,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // step 3: remaining butterfly stages (alpha and 1/sqrt(n) are applied below)
-        fwht128_upper(v);
+        // step 3: remaining butterfly stages (alpha and 1/sqrt(n) are applied
+        // below; at n = 128 the last stage is fused with that scaling)
+        float mh;
         if constexpr (G == 2) {
+            fwht128_upper(v);
             fwht_pair_stage(v, lane);
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-        }
-        float mh = max_abs128(v);
-        if constexpr (G == 2)
+            mh = max_abs128(v);
             mh = fmaxf(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 1));
+        } else {
+            fwht128_upper_but_last(v);
+            mh = max_abs_last_stage(v);
+        }
 
         // step 2: alpha = sqrt(E / (m + eps));  step 4: s = 448 / max|y|
         const float m = ss * BlockConst<NB>::inv_n;
@@ -177,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             k = scale;
         }
         const float2 k2 = make_float2(k, k);
+        if constexpr (G == 1)
+            last_stage_scaled(v, k2);  // v now holds y * s
 
         // step 5: codes = E4M3(y * s) into the warp's swizzled staging rows
         if (lane == 0)
@@ -185,9 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint32_t w0, w1, w2, w3;
-            if constexpr (FMT_INT8) {
+            if constexpr (FMT_INT8 && G == 1) {
+                encode8_s8_prescaled(&v[8 * j], w0, w1);
+                encode8_s8_prescaled(&v[8 * j + 4], w2, w3);
+            } else if constexpr (FMT_INT8) {
                 encode8_s8(&v[8 * j], k2, w0, w1);
                 encode8_s8(&v[8 * j + 4], k2, w2, w3);
+            } else if constexpr (G == 1) {
+                encode8_prescaled(&v[8 * j], w0, w1);
+                encode8_prescaled(&v[8 * j + 4], w2, w3);
             } else {
                 encode8(&v[8 * j], k2, w0, w1);
                 encode8(&v[8 * j + 4], k2, w2, w3);
@@ -278,7 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 decode16_stage1(q, v, j);
         }
-        fwht128_upper(v);  // consumes every decoded value
+        if constexpr (G == 2)
+            fwht128_upper(v);  // consumes every decoded value
+        else
+            fwht128_upper_but_last(v);  // the last stage is fused with the scaling below
         __syncwarp();
         if (lane == 0) {
             const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
@@ -295,10 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // out = c H(decode) / (s alpha)
         const float2 k2 = decompress_multiplier<NB>(v, sc, a);
+        if constexpr (G == 1)
+            last_stage_scaled(v, k2);
         if (lane == 0)
             bulk_wait_read_all();
         __syncwarp();
-        stage_output_row<BF16OUT>(v, k2, outw, lane);
+        stage_output_row<BF16OUT, G == 1>(v, k2, outw, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

@@ -52,6 +52,54 @@ __device__ __forceinline__ void fwht128_upper(float2 (&v)[64])
     }
 }
 
+// Stages h = 2, 4, ..., 32: all but the last stage of the 128-point
+// transform (which pairs v[k] with v[k + 32]).
+__device__ __forceinline__ void fwht128_upper_but_last(float2 (&v)[64])
+{
+#pragma unroll
+    for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            if ((k & hh) == 0) {
+                const float2 a = v[k], b = v[k + hh];
+                v[k] = __fadd2_rn(a, b);
+                v[k + hh] = sub2(a, b);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float2 abs2(float2 a) { return make_float2(fabsf(a.x), fabsf(a.y)); }
+
+// Largest |y| of the full transform, read off the operands of its last
+// stage: max(|a + b|, |a - b|) = |a| + |b|, and fp32 rounding keeps the
+// identity (|round(a + b)| and |round(a - b)| are round(|a| + |b|) and a
+// smaller value).
+__device__ __forceinline__ float max_abs_last_stage(const float2 (&v)[64])
+{
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const float2 t = __fadd2_rn(abs2(v[k]), abs2(v[k + 32]));
+        m[k & 3] = fmaxf(m[k & 3], fmaxf(t.x, t.y));
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// The last stage fused with the multiply by k: v[k] <- (a + b) k and
+// v[k + 32] <- (a - b) k, as fma(b, +-k, a k).
+__device__ __forceinline__ void last_stage_scaled(float2 (&v)[64], float2 k2)
+{
+    const float2 nk2 = make_float2(-k2.x, -k2.y);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const float2 ak = __fmul2_rn(v[k], k2);
+        const float2 b = v[k + 32];
+        v[k] = __ffma2_rn(b, k2, ak);
+        v[k + 32] = __ffma2_rn(b, nk2, ak);
+    }
+}
+
 // Last stage of a 256-point transform across a lane pair: the even lane
 // holds elements 0..127 (a), the odd lane 128..255 (b); even gets a + b,
 // odd gets a - b.
@@ -94,6 +142,13 @@ __device__ __forceinline__ void unpack8_stage1(const uint4 q, float2 (&v)[64], i
     }
 }
 
+// Four float2 pairs (already scaled) -> 8 E4M3 codes in two words.
+__device__ __forceinline__ void encode8_prescaled(const float2 *v, uint32_t &w0, uint32_t &w1)
+{
+    w0 = f32x4_to_e4m3x4(v[0].x, v[0].y, v[1].x, v[1].y);
+    w1 = f32x4_to_e4m3x4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+
 // Four float2 pairs times k -> 8 E4M3 codes in two words.
 __device__ __forceinline__ void encode8(const float2 *v, float2 k2, uint32_t &w0, uint32_t &w1)
 {
@@ -113,6 +168,12 @@ __device__ __forceinline__ uint32_t f32x4_to_s8x4(float a, float b, float c, flo
     const int ic = __float2int_rn(c), id = __float2int_rn(d);
     const uint32_t lo = __byte_perm(ia, ib, 0x0040), hi = __byte_perm(ic, id, 0x0040);
     return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ void encode8_s8_prescaled(const float2 *v, uint32_t &w0, uint32_t &w1)
+{
+    w0 = f32x4_to_s8x4(v[0].x, v[0].y, v[1].x, v[1].y);
+    w1 = f32x4_to_s8x4(v[2].x, v[2].y, v[3].x, v[3].y);
 }
 
 __device__ __forceinline__ void encode8_s8(const float2 *v, float2 k2, uint32_t &w0, uint32_t &w1)
@@ -189,7 +250,8 @@ __device__ __forceinline__ float2 decompress_multiplier(float2 (&v)[64], float s
 // Writes a row of 128 reconstructed values times k2 into a warp's swizzled
 // staging area: fp32 as 4 boxes of 32 floats x 32 rows, or bf16 as 2 boxes
 // of 64 values x 32 rows (each box 4 KB, row `lane` at lane * 128 bytes).
-template <bool BF16OUT>
+// With PRESCALED the values already include the factor and k2 is ignored.
+template <bool BF16OUT, bool PRESCALED = false>
 __device__ __forceinline__ void stage_output_row(const float2 (&v)[64], float2 k2, uint32_t outw, int lane)
 {
     const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
@@ -198,7 +260,8 @@ __device__ __forceinline__ void stage_output_row(const float2 (&v)[64], float2 k
         for (int ch = 0; ch < 32; ++ch) {
             const uint32_t b = ch >> 3, j = ch & 7;
             const uint32_t addr = outw + b * 4096 + lane * 128 + ((j << 4) ^ swz);
-            const float2 p0 = __fmul2_rn(v[2 * ch], k2), p1 = __fmul2_rn(v[2 * ch + 1], k2);
+            const float2 p0 = PRESCALED ? v[2 * ch] : __fmul2_rn(v[2 * ch], k2);
+            const float2 p1 = PRESCALED ? v[2 * ch + 1] : __fmul2_rn(v[2 * ch + 1], k2);
             sts128(addr, __float_as_uint(p0.x), __float_as_uint(p0.y), __float_as_uint(p1.x),
                    __float_as_uint(p1.y));
         }
@@ -210,7 +273,7 @@ __device__ __forceinline__ void stage_output_row(const float2 (&v)[64], float2 k
             float2 p[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                p[t] = __fmul2_rn(v[4 * ch + t], k2);
+                p[t] = PRESCALED ? v[4 * ch + t] : __fmul2_rn(v[4 * ch + t], k2);
             sts128(addr, f32x2_to_bf16x2(p[0].x, p[0].y), f32x2_to_bf16x2(p[1].x, p[1].y),
                    f32x2_to_bf16x2(p[2].x, p[2].y), f32x2_to_bf16x2(p[3].x, p[3].y));
         }

@@ -308,14 +308,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             decode16_stage1(lds128(ctile + lane * 128 + ((static_cast<uint32_t>(j) << 4) ^ swz)), v, j);
-        fwht128_upper(v);
-        if constexpr (G == 2)
+        // exactly the decompress kernel's arithmetic
+        if constexpr (G == 2) {
+            fwht128_upper(v);
             fwht_pair_stage(v, lane);
+        } else {
+            fwht128_upper_but_last(v);
+        }
         const float2 k2 = decompress_multiplier<NB>(v, sc, a);
+        if constexpr (G == 1)
+            last_stage_scaled(v, k2);
         if (lane == 0)
             bulk_wait_read_all();
         __syncwarp();
-        stage_output_row<BF16OUT>(v, k2, outw, lane);
+        stage_output_row<BF16OUT, G == 1>(v, k2, outw, lane);
         fence_proxy_async_smem();
         __syncwarp();
         const int64_t wrow = t * 32;
