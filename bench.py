@@ -43,7 +43,7 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csr
                   for f in ("codec_kernels.cu", "device_utils.cuh")]
 
 
-def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: bool = True) -> dict:
+def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: bool = False) -> dict:
     """Bytes each launch must move at minimum (reads + writes), per step of
     the two-shot local path over P shards of n elements."""
     nb = n // block
@@ -318,8 +318,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
     ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
-    ap.add_argument("--separate", action="store_true",
-                    help="run reduce and decompress as two launches instead of the fused one")
+    ap.add_argument("--fused", action="store_true",
+                    help="run reduce and decompress as one fused launch instead of two")
     ap.add_argument("--gpt13b", action="store_true",
                     help="also time the GPT-13B-shaped path (P=8, n=256; slow input generation)")
     ap.add_argument("--rows", type=int, default=None,
@@ -351,7 +351,7 @@ def main():
     n = rows * d
 
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-    path = api.TwoShotLocal(P, rows, d, block, fused=not args.separate)
+    path = api.TwoShotLocal(P, rows, d, block, fused=args.fused)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):

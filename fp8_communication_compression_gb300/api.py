@@ -237,12 +237,13 @@ def taco_device_error(clear: bool = True) -> int:
 
 class TwoShotLocal:
     """The two-shot AllReduce's on-GPU path for P shards of [rows, d]:
-    compress all shards in one call, reduce them, decompress the result.
-    Buffers are allocated once; ``run`` only launches the three kernels."""
+    compress all shards in one call, reduce them, decompress the result
+    (two launches, or one fused reduce + decompress launch with
+    ``fused=True``).  Buffers are allocated once; ``run`` only launches."""
 
     def __init__(self, P: int, rows: int, d: int, block: int = 128, device="cuda",
                  e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32,
-                 fused: bool = True):
+                 fused: bool = False):
         self.P, self.rows, self.d, self.block = P, rows, d, block
         self.fused = fused
         self.e_target, self.eps = e_target, eps

@@ -18,6 +18,7 @@
 #include "codec_math.cuh"
 #include "device_utils.cuh"
 #include "internal.h"
+#include "reduce_math.cuh"
 
 namespace taco {
 
@@ -32,47 +33,6 @@ constexpr uint32_t kFWarpBytes = kFCodeTile + kFOutBytes;   // 20 KB
 constexpr uint32_t kFScalarBytes = 2 * 32 * 4;              // alpha', s' of up to 32 blocks
 constexpr uint32_t kFSmemBytes = 1024 + kFWarps * (kFWarpBytes + kFScalarBytes);
 static_assert(kFWarpBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-
-__device__ __forceinline__ void decode32(const uint4 (&q)[2], float (&d)[32])
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t w[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            e4m3x2_to_f32x2(w[j], d[16 * h + 4 * j + 0], d[16 * h + 4 * j + 1]);
-            e4m3x2_to_f32x2(w[j] >> 16, d[16 * h + 4 * j + 2], d[16 * h + 4 * j + 3]);
-        }
-    }
-}
-
-__device__ __forceinline__ void encode32(const float (&v)[32], float k, uint4 (&q)[2])
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float *x = v + 16 * h;
-        q[h].x = f32x4_to_e4m3x4(x[0] * k, x[1] * k, x[2] * k, x[3] * k);
-        q[h].y = f32x4_to_e4m3x4(x[4] * k, x[5] * k, x[6] * k, x[7] * k);
-        q[h].z = f32x4_to_e4m3x4(x[8] * k, x[9] * k, x[10] * k, x[11] * k);
-        q[h].w = f32x4_to_e4m3x4(x[12] * k, x[13] * k, x[14] * k, x[15] * k);
-    }
-}
-
-template <int LPB> __device__ __forceinline__ float group_sum(float v)
-{
-#pragma unroll
-    for (int o = LPB / 2; o >= 1; o >>= 1)
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-
-template <int LPB> __device__ __forceinline__ float group_max(float v)
-{
-#pragma unroll
-    for (int o = LPB / 2; o >= 1; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
 
 // Per-lane state of phase 1 for one sub-step: which block, where.
 struct Slot {
@@ -103,37 +63,19 @@ __device__ __forceinline__ void load_shards(const ShardPtrs &in, const Slot &sl,
     }
 }
 
-// Requantises the lane's 32 Hadamard-domain sums T of one block (see the
-// shard-reduce kernel: alpha' = sqrt(E / (|T|^2/n + eps)), s' = 448 /
-// (alpha' max|T|), codes = E4M3(alpha' s' T)), stores codes and scalars to
-// global memory and to the warp's shared tile.
+// Requantises the lane's 32 Hadamard-domain sums T of one block (exactly as
+// the shard-reduce kernel), stores codes and scalars to global memory and
+// to the warp's shared tile.
 template <int NB, int LPB>
-__device__ __forceinline__ void finish_block(float (&T)[32], const Slot &sl, int lane, float e_target,
+__device__ __forceinline__ void finish_block(float2 (&T)[16], const Slot &sl, int lane, float e_target,
                                              float eps, uint8_t *out_codes, float *out_alpha,
                                              float *out_scale, uint32_t ctile, float *sa_s, float *ss_s)
 {
     constexpr int G = NB / 128;
     const int part = lane % LPB;
-    float a4[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kFEPL; ++i) {
-        a4[i & 3] = fmaf(T[i], T[i], a4[i & 3]);
-        mx = fmaxf(mx, fabsf(T[i]));
-    }
-    const float ss = group_sum<LPB>((a4[0] + a4[1]) + (a4[2] + a4[3]));
-    mx = group_max<LPB>(mx);
-    const float alpha = sqrtf(e_target / (ss * (1.0f / NB) + eps));
-    const float M = alpha * mx;
-    const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
-    float k = alpha * scale;
-    if (!(k <= FLT_MAX)) {
-#pragma unroll
-        for (int i = 0; i < kFEPL; ++i)
-            T[i] *= alpha;
-        k = scale;
-    }
     uint4 oq[2];
-    encode32(T, k, oq);
+    float alpha, scale;
+    recompress<NB, LPB>(T, e_target, eps, oq, alpha, scale);
     if (sl.valid) {
         stg128_stream(out_codes + sl.off, oq[0]);
         stg128_stream(out_codes + sl.off + 16, oq[1]);
@@ -154,10 +96,10 @@ __device__ __forceinline__ void finish_block(float (&T)[32], const Slot &sl, int
     }
 }
 
-// Phase 1 for a compile-time shard count.
+// Phase 1 for a compile-time shard count (the shard-reduce kernel's math).
 template <int NB, int P>
 __device__ __forceinline__ void accumulate_fixed(const ShardPtrs &in, const Slot &sl, const uint4 (&q)[P][2],
-                                                 int lane, float (&T)[32])
+                                                 int lane, float2 (&T)[16])
 {
     constexpr int LPB = NB / kFEPL;
     constexpr int ROUNDS = (P + LPB - 1) / LPB;
@@ -166,58 +108,26 @@ __device__ __forceinline__ void accumulate_fixed(const ShardPtrs &in, const Slot
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) {
         const int p = r * LPB + part;
-        wr[r] = 1.0f;
-        if (sl.valid && p < P) {
-            const float sc = __ldg(in.scale[p] + sl.blk), al = __ldg(in.alpha[p] + sl.blk);
-            const float sa = sc * al;
-            wr[r] = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
-        }
+        const bool ok = sl.valid && p < P;
+        wr[r] = shard_weight(ok ? __ldg(in.scale[p] + sl.blk) : 1.0f, ok ? __ldg(in.alpha[p] + sl.blk) : 1.0f);
     }
     const int gbase = lane & ~(LPB - 1);
     float w[P];
 #pragma unroll
     for (int p = 0; p < P; ++p)
         w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
-    // products rounded before they are added: exactly cancelling shards give 0
-    decode32(q[0], T);
-#pragma unroll
-    for (int i = 0; i < kFEPL; ++i)
-        T[i] = __fmul_rn(T[i], w[0]);
-#pragma unroll
-    for (int p = 1; p < P; ++p) {
-        float d[kFEPL];
-        decode32(q[p], d);
-#pragma unroll
-        for (int i = 0; i < kFEPL; ++i)
-            T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w[p]));
-    }
+    weighted_sum<P>(q, w, T);
 }
 
-// Phase 1 for a run-time shard count (1 .. 16): shard by shard.
-__device__ __forceinline__ void accumulate_any(const ShardPtrs &in, int P, const Slot &sl, float (&T)[32])
+// Phase 1 for a run-time shard count (1 .. 16): shard by shard, same rounding.
+__device__ __forceinline__ void accumulate_any(const ShardPtrs &in, int P, const Slot &sl, float2 (&T)[16])
 {
 #pragma unroll 1
     for (int p = 0; p < P; ++p) {
         uint4 q[2];
-        q[0] = sl.valid ? ldg128_stream(in.codes[p] + sl.off) : make_uint4(0, 0, 0, 0);
-        q[1] = sl.valid ? ldg128_stream(in.codes[p] + sl.off + 16) : make_uint4(0, 0, 0, 0);
-        float w = 1.0f;
-        if (sl.valid) {
-            const float sc = __ldg(in.scale[p] + sl.blk), al = __ldg(in.alpha[p] + sl.blk);
-            const float sa = sc * al;
-            w = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
-        }
-        float d[kFEPL];
-        decode32(q, d);
-        if (p == 0) {
-#pragma unroll
-            for (int i = 0; i < kFEPL; ++i)
-                T[i] = __fmul_rn(d[i], w);
-        } else {
-#pragma unroll
-            for (int i = 0; i < kFEPL; ++i)
-                T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w));
-        }
+        load32_codes(in.codes[p] + sl.off, sl.valid, q);
+        const float w = sl.valid ? shard_weight(__ldg(in.scale[p] + sl.blk), __ldg(in.alpha[p] + sl.blk)) : 1.0f;
+        weighted_sum_step(q, w, p == 0, T);
     }
 }
 
@@ -266,7 +176,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             for (int si = 0; si < SUB; si += 2) {
                 sb = slot_of<NB, LPB, BPS>(blk0, si + 1, lane, nblocks);
                 load_shards<PT>(in, sb, qb);
-                float T[kFEPL];
+                float2 T[16];
                 accumulate_fixed<NB, PT>(in, sa, qa, lane, T);
                 finish_block<NB, LPB>(T, sa, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
                                       sa_s, ss_s);
@@ -284,7 +194,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
                 uint4 q[PT][2];
                 load_shards<PT>(in, sl, q);
-                float T[kFEPL];
+                float2 T[16];
                 accumulate_fixed<NB, PT>(in, sl, q, lane, T);
                 finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
                                       sa_s, ss_s);
@@ -293,7 +203,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll 1
             for (int si = 0; si < SUB; ++si) {
                 const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
-                float T[kFEPL];
+                float2 T[16];
                 accumulate_any(in, P, sl, T);
                 finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
                                       sa_s, ss_s);

@@ -4,7 +4,8 @@
 // a block, NB / 32 adjacent lanes own one block, per-block statistics (sum
 // of squares, absolute maximum) are combined with __shfl_xor_sync, and the
 // per-shard scalars of a block are fetched once per lane group and
-// broadcast with __shfl_sync.
+// broadcast with __shfl_sync.  The two reduces keep the next grid-stride
+// slot's loads in flight while they compute the current one.
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -23,61 +24,13 @@
 
 #include "device_utils.cuh"
 #include "internal.h"
+#include "reduce_math.cuh"
 
 namespace taco {
 
 namespace {
 
-constexpr int kEPL = 32;  // elements per lane
 constexpr int kBlockThreads = 256;
-
-// 32 codes (two 16-byte words) -> 32 fp32 values (exact)
-__device__ __forceinline__ void decode32(const uint4 (&q)[2], float (&d)[32])
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t w[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            e4m3x2_to_f32x2(w[j], d[16 * h + 4 * j + 0], d[16 * h + 4 * j + 1]);
-            e4m3x2_to_f32x2(w[j] >> 16, d[16 * h + 4 * j + 2], d[16 * h + 4 * j + 3]);
-        }
-    }
-}
-
-__device__ __forceinline__ void encode32(const float (&v)[32], float k, uint4 (&q)[2])
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float *x = v + 16 * h;
-        q[h].x = f32x4_to_e4m3x4(x[0] * k, x[1] * k, x[2] * k, x[3] * k);
-        q[h].y = f32x4_to_e4m3x4(x[4] * k, x[5] * k, x[6] * k, x[7] * k);
-        q[h].z = f32x4_to_e4m3x4(x[8] * k, x[9] * k, x[10] * k, x[11] * k);
-        q[h].w = f32x4_to_e4m3x4(x[12] * k, x[13] * k, x[14] * k, x[15] * k);
-    }
-}
-
-__device__ __forceinline__ void load32_codes(const uint8_t *p, bool valid, uint4 (&q)[2])
-{
-    q[0] = valid ? ldg128_stream(p) : make_uint4(0, 0, 0, 0);
-    q[1] = valid ? ldg128_stream(p + 16) : make_uint4(0, 0, 0, 0);
-}
-
-template <int LPB> __device__ __forceinline__ float group_sum(float v)
-{
-#pragma unroll
-    for (int o = LPB / 2; o >= 1; o >>= 1)
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-
-template <int LPB> __device__ __forceinline__ float group_max(float v)
-{
-#pragma unroll
-    for (int o = LPB / 2; o >= 1; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
 
 // AGoQ per-block requantisation scalars from the block's absolute maximum:
 // codes use q = 448 / amax; the stored scale is the dequantisation
@@ -93,16 +46,82 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
     }
 }
 
-// Warp-uniform grid-stride loop over lane slots.  Lanes past the end still
-// take part in the shuffles but load and store nothing.
-#define TACO_LANE_LOOP(total)                                                                    \
-    pdl_wait();                                                                                  \
-    pdl_launch_dependents();                                                                     \
-    const int64_t _stride = static_cast<int64_t>(gridDim.x) * blockDim.x;                        \
-    for (int64_t _base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);    \
-         _base < (total); _base += _stride)
+template <int NB, int P> __host__ __device__ constexpr int rounds_of()
+{
+    return (P + NB / kLaneElems - 1) / (NB / kLaneElems);
+}
+
+// One grid-stride slot of a lane: its block, offset, and the loads.
+template <int P, int ROUNDS> struct RedSlot {
+    uint4 q[P][2];
+    float sc[ROUNDS];  // scale (TACO) or dequantisation multiplier (AGoQ) of shard r * LPB + part
+    float al[ROUNDS];  // alpha of that shard (TACO only)
+    int64_t blk, off;
+    bool valid;
+};
+
+template <int NB, int P, bool WITH_ALPHA>
+__device__ __forceinline__ void load_slot(const ShardPtrs &in, int64_t base, int lane, int64_t total,
+                                          RedSlot<P, rounds_of<NB, P>()> &s)
+{
+    constexpr int LPB = NB / kLaneElems;
+    const int part = lane % LPB;
+    const int64_t t = base + lane;
+    s.valid = t < total;
+    s.blk = s.valid ? t / LPB : 0;
+    s.off = s.blk * NB + part * kLaneElems;
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+        load32_codes(in.codes[p] + s.off, s.valid, s.q[p]);
+#pragma unroll
+    for (int r = 0; r < rounds_of<NB, P>(); ++r) {
+        const int p = r * LPB + part;
+        const bool ok = s.valid && p < P;
+        s.sc[r] = ok ? __ldg(in.scale[p] + s.blk) : 1.0f;
+        s.al[r] = (WITH_ALPHA && ok) ? __ldg(in.alpha[p] + s.blk) : 1.0f;
+    }
+}
+
+// Per-shard factors for every shard of the lane's block, from the values the
+// lane group loaded (lane `part` holds shards part, part + LPB, ...).
+template <int LPB, int P, int ROUNDS>
+__device__ __forceinline__ void share_factors(const float (&mine)[ROUNDS], int lane, float (&f)[P])
+{
+    const int gbase = lane & ~(LPB - 1);
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+        f[p] = __shfl_sync(0xFFFFFFFFu, mine[p / LPB], gbase + (p % LPB));
+}
 
 // ------------------------------------------------------ TACO reduce --
+
+template <int NB, int P>
+__device__ __forceinline__ void taco_reduce_slot(const RedSlot<P, rounds_of<NB, P>()> &s, int lane,
+                                                 float e_target, float eps, uint8_t *out_codes,
+                                                 float *out_alpha, float *out_scale)
+{
+    constexpr int LPB = NB / kLaneElems;
+    constexpr int ROUNDS = rounds_of<NB, P>();
+    float wr[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r)
+        wr[r] = shard_weight(s.sc[r], s.al[r]);
+    float w[P];
+    share_factors<LPB, P, ROUNDS>(wr, lane, w);
+    float2 T[16];
+    weighted_sum<P>(s.q, w, T);
+    uint4 oq[2];
+    float alpha, scale;
+    recompress<NB, LPB>(T, e_target, eps, oq, alpha, scale);
+    if (s.valid) {
+        stg128_stream(out_codes + s.off, oq[0]);
+        stg128_stream(out_codes + s.off + 16, oq[1]);
+        if (lane % LPB == 0) {
+            out_alpha[s.blk] = alpha;
+            out_scale[s.blk] = scale;
+        }
+    }
+}
 
 template <int NB, int P>
 __global__ void __launch_bounds__(kBlockThreads)
@@ -110,82 +129,91 @@ __global__ void __launch_bounds__(kBlockThreads)
                        uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
                        float *__restrict__ out_scale)
 {
-    constexpr int LPB = NB / kEPL;
+    constexpr int LPB = NB / kLaneElems;
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
-    TACO_LANE_LOOP(total)
-    {
-        const int64_t t = _base + lane;
-        const bool valid = t < total;
-        const int64_t blk = valid ? t / LPB : 0;
-        const int part = static_cast<int>(t % LPB);
-        const int64_t off = blk * NB + part * kEPL;
-        uint4 q[P][2];
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            load32_codes(in.codes[p] + off, valid, q[p]);
-        // 1 / (s_p alpha_p): lane `part` of the group computes it for shards
-        // part, part + LPB, ...; the group then shares the values.
-        constexpr int ROUNDS = (P + LPB - 1) / LPB;
-        float wr[ROUNDS];
-#pragma unroll
-        for (int r = 0; r < ROUNDS; ++r) {
-            const int p = r * LPB + part;
-            wr[r] = 1.0f;
-            if (valid && p < P) {
-                const float sc = __ldg(in.scale[p] + blk), al = __ldg(in.alpha[p] + blk);
-                const float sa = sc * al;
-                wr[r] = (sa <= FLT_MAX) ? __frcp_rn(sa) : __frcp_rn(sc) / al;
-            }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+    // warp-uniform ping-pong over grid-stride slots: the next slot's loads
+    // are in flight while the current one is computed
+    RedSlot<P, rounds_of<NB, P>()> a, b;
+    if constexpr (P > 8) {  // no room for two slots of loads in registers
+        for (; base < total; base += stride) {
+            load_slot<NB, P, true>(in, base, lane, total, a);
+            taco_reduce_slot<NB, P>(a, lane, e_target, eps, out_codes, out_alpha, out_scale);
         }
-        const int gbase = lane & ~(LPB - 1);
-        float w[P];
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
-        // Each product is rounded before it is added (no FMA contraction), so
-        // shards that cancel exactly sum to exactly zero.
-        float T[kEPL];
-        decode32(q[0], T);
-#pragma unroll
-        for (int i = 0; i < kEPL; ++i)
-            T[i] = __fmul_rn(T[i], w[0]);
-#pragma unroll
-        for (int p = 1; p < P; ++p) {
-            float d[kEPL];
-            decode32(q[p], d);
-#pragma unroll
-            for (int i = 0; i < kEPL; ++i)
-                T[i] = __fadd_rn(T[i], __fmul_rn(d[i], w[p]));
+        return;
+    }
+    load_slot<NB, P, true>(in, base, lane, total, a);
+    while (base < total) {
+        load_slot<NB, P, true>(in, base + stride, lane, total, b);
+        taco_reduce_slot<NB, P>(a, lane, e_target, eps, out_codes, out_alpha, out_scale);
+        base += stride;
+        if (base >= total)
+            break;
+        load_slot<NB, P, true>(in, base + stride, lane, total, a);
+        taco_reduce_slot<NB, P>(b, lane, e_target, eps, out_codes, out_alpha, out_scale);
+        base += stride;
+    }
+}
+
+// ----------------------------------------------------- AGoQ reduce --
+
+template <int NB, int P>
+__device__ __forceinline__ void agoq_reduce_slot(const RedSlot<P, rounds_of<NB, P>()> &s, int lane,
+                                                 uint8_t *out_codes, float *out_scale)
+{
+    constexpr int LPB = NB / kLaneElems;
+    float m[P];
+    share_factors<LPB, P, rounds_of<NB, P>()>(s.sc, lane, m);
+    // FP32 dequantise (one rounded multiply) and FP32 sum in shard order
+    float2 S[16];
+    weighted_sum<P>(s.q, m, S);
+    const float mx = group_max<LPB>(lane_max_abs(S));
+    float qs, m_new;
+    agoq_scales(mx, qs, m_new);
+    uint4 oq[2];
+    encode32_f2(S, qs, oq);
+    if (s.valid) {
+        stg128_stream(out_codes + s.off, oq[0]);
+        stg128_stream(out_codes + s.off + 16, oq[1]);
+        if (lane % LPB == 0)
+            out_scale[s.blk] = m_new;
+    }
+}
+
+template <int NB, int P>
+__global__ void __launch_bounds__(kBlockThreads)
+    agoq_reduce_kernel(const ShardPtrs in, int64_t nblocks, uint8_t *__restrict__ out_codes,
+                       float *__restrict__ out_scale)
+{
+    constexpr int LPB = NB / kLaneElems;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t total = nblocks * LPB;
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+    RedSlot<P, rounds_of<NB, P>()> a, b;
+    if constexpr (P > 8) {  // no room for two slots of loads in registers
+        for (; base < total; base += stride) {
+            load_slot<NB, P, false>(in, base, lane, total, a);
+            agoq_reduce_slot<NB, P>(a, lane, out_codes, out_scale);
         }
-        float a4[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kEPL; ++i) {
-            a4[i & 3] = fmaf(T[i], T[i], a4[i & 3]);
-            mx = fmaxf(mx, fabsf(T[i]));
-        }
-        const float ss = group_sum<LPB>((a4[0] + a4[1]) + (a4[2] + a4[3]));
-        mx = group_max<LPB>(mx);
-        const float alpha = sqrtf(e_target / (ss * (1.0f / NB) + eps));
-        const float M = alpha * mx;
-        const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
-        float k = alpha * scale;
-        if (!(k <= FLT_MAX)) {
-#pragma unroll
-            for (int i = 0; i < kEPL; ++i)
-                T[i] *= alpha;
-            k = scale;
-        }
-        if (valid) {
-            uint4 oq[2];
-            encode32(T, k, oq);
-            stg128_stream(out_codes + off, oq[0]);
-            stg128_stream(out_codes + off + 16, oq[1]);
-            if (part == 0) {
-                out_alpha[blk] = alpha;
-                out_scale[blk] = scale;
-            }
-        }
+        return;
+    }
+    load_slot<NB, P, false>(in, base, lane, total, a);
+    while (base < total) {
+        load_slot<NB, P, false>(in, base + stride, lane, total, b);
+        agoq_reduce_slot<NB, P>(a, lane, out_codes, out_scale);
+        base += stride;
+        if (base >= total)
+            break;
+        load_slot<NB, P, false>(in, base + stride, lane, total, a);
+        agoq_reduce_slot<NB, P>(b, lane, out_codes, out_scale);
+        base += stride;
     }
 }
 
@@ -196,16 +224,19 @@ __global__ void __launch_bounds__(kBlockThreads)
     agoq_accumulate_kernel(uint8_t *__restrict__ codes, float *__restrict__ scale,
                            const uint16_t *__restrict__ grad, int64_t nblocks)
 {
-    constexpr int LPB = NB / kEPL;
+    constexpr int LPB = NB / kLaneElems;
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
-    TACO_LANE_LOOP(total)
-    {
-        const int64_t t = _base + lane;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
+         base += stride) {
+        const int64_t t = base + lane;
         const bool valid = t < total;
         const int64_t blk = valid ? t / LPB : 0;
-        const int part = static_cast<int>(t % LPB);
-        const int64_t off = blk * NB + part * kEPL;
+        const int part = lane % LPB;
+        const int64_t off = blk * NB + part * kLaneElems;
         uint4 q[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
         uint4 g[4] = {q[0], q[0], q[0], q[0]};
         float s_old = 1.0f;
@@ -223,26 +254,24 @@ __global__ void __launch_bounds__(kBlockThreads)
         }
         // g = dequantise(main) + grad in FP32: one rounded multiply, then one
         // rounded add (no fused multiply-add), as the stated arithmetic is.
-        float d[kEPL];
-        decode32(q, d);
-        float mx = 0.0f;
+        float2 d[16];
+        decode32_f2(q, d);
+        const float2 s2 = make_float2(s_old, s_old);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const uint32_t gw[4] = {g[h].x, g[h].y, g[h].z, g[h].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int e = 8 * h + 2 * j;
-                d[e] = __fadd_rn(__fmul_rn(d[e], s_old), bf16lo_to_f32(gw[j]));
-                d[e + 1] = __fadd_rn(__fmul_rn(d[e + 1], s_old), bf16hi_to_f32(gw[j]));
-                mx = fmaxf(mx, fmaxf(fabsf(d[e]), fabsf(d[e + 1])));
+                const float2 gr = make_float2(bf16lo_to_f32(gw[j]), bf16hi_to_f32(gw[j]));
+                d[4 * h + j] = __fadd2_rn(__fmul2_rn(d[4 * h + j], s2), gr);
             }
         }
-        mx = group_max<LPB>(mx);
+        const float mx = group_max<LPB>(lane_max_abs(d));
         float qs, m_new;
         agoq_scales(mx, qs, m_new);
         if (valid) {
             uint4 oq[2];
-            encode32(d, qs, oq);
+            encode32_f2(d, qs, oq);
             stg128_stream(codes + off, oq[0]);
             stg128_stream(codes + off + 16, oq[1]);
             if (part == 0)
@@ -250,74 +279,6 @@ __global__ void __launch_bounds__(kBlockThreads)
         }
     }
 }
-
-// ----------------------------------------------------- AGoQ reduce --
-
-template <int NB, int P>
-__global__ void __launch_bounds__(kBlockThreads)
-    agoq_reduce_kernel(const ShardPtrs in, int64_t nblocks, uint8_t *__restrict__ out_codes,
-                       float *__restrict__ out_scale)
-{
-    constexpr int LPB = NB / kEPL;
-    const int64_t total = nblocks * LPB;
-    const int lane = threadIdx.x & 31;
-    TACO_LANE_LOOP(total)
-    {
-        const int64_t t = _base + lane;
-        const bool valid = t < total;
-        const int64_t blk = valid ? t / LPB : 0;
-        const int part = static_cast<int>(t % LPB);
-        const int64_t off = blk * NB + part * kEPL;
-        uint4 q[P][2];
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            load32_codes(in.codes[p] + off, valid, q[p]);
-        constexpr int ROUNDS = (P + LPB - 1) / LPB;
-        float mr[ROUNDS];
-#pragma unroll
-        for (int r = 0; r < ROUNDS; ++r) {
-            const int p = r * LPB + part;
-            mr[r] = (valid && p < P) ? __ldg(in.scale[p] + blk) : 1.0f;
-        }
-        const int gbase = lane & ~(LPB - 1);
-        float m[P];
-#pragma unroll
-        for (int p = 0; p < P; ++p)
-            m[p] = __shfl_sync(0xFFFFFFFFu, mr[p / LPB], gbase + (p % LPB));
-        // FP32 dequantise (one rounded multiply) and FP32 sum in shard order,
-        // no fused multiply-add: exactly cancelling shards give exactly 0
-        float S[kEPL];
-        decode32(q[0], S);
-#pragma unroll
-        for (int i = 0; i < kEPL; ++i)
-            S[i] = __fmul_rn(S[i], m[0]);
-#pragma unroll
-        for (int p = 1; p < P; ++p) {
-            float d[kEPL];
-            decode32(q[p], d);
-#pragma unroll
-            for (int i = 0; i < kEPL; ++i)
-                S[i] = __fadd_rn(S[i], __fmul_rn(d[i], m[p]));
-        }
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kEPL; ++i)
-            mx = fmaxf(mx, fabsf(S[i]));
-        mx = group_max<LPB>(mx);
-        float qs, m_new;
-        agoq_scales(mx, qs, m_new);
-        if (valid) {
-            uint4 oq[2];
-            encode32(S, qs, oq);
-            stg128_stream(out_codes + off, oq[0]);
-            stg128_stream(out_codes + off + 16, oq[1]);
-            if (part == 0)
-                out_scale[blk] = m_new;
-        }
-    }
-}
-
-#undef TACO_LANE_LOOP
 
 template <typename K> cudaError_t grid_for(K kernel, int64_t lanes_total, int *grid)
 {
@@ -342,7 +303,7 @@ cudaError_t run_taco_reduce(const ShardPtrs &in, int64_t nblocks, float e_target
                             uint8_t *oc, float *oa, float *os, cudaStream_t st)
 {
     int grid = 0;
-    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
+    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * (NB / kLaneElems), &grid);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(taco_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, e_target, eps, oc,
@@ -353,7 +314,7 @@ template <int NB, int P>
 cudaError_t run_agoq_reduce(const ShardPtrs &in, int64_t nblocks, uint8_t *oc, float *os, cudaStream_t st)
 {
     int grid = 0;
-    cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * (NB / kEPL), &grid);
+    cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * (NB / kLaneElems), &grid);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(agoq_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, oc, os);
@@ -418,15 +379,14 @@ cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *gra
     int grid = 0;
     cudaError_t e;
     if (block == 128) {
-        if ((e = grid_for(agoq_accumulate_kernel<128>, nblocks * (128 / kEPL), &grid)) != cudaSuccess)
+        if ((e = grid_for(agoq_accumulate_kernel<128>, nblocks * (128 / kLaneElems), &grid)) != cudaSuccess)
             return e;
-        e = launch_pdl(agoq_accumulate_kernel<128>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
-    } else {
-        if ((e = grid_for(agoq_accumulate_kernel<256>, nblocks * (256 / kEPL), &grid)) != cudaSuccess)
-            return e;
-        e = launch_pdl(agoq_accumulate_kernel<256>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
+        return launch_pdl(agoq_accumulate_kernel<128>, grid, kBlockThreads, 0, stream, codes, scale, g,
+                          nblocks);
     }
-    return e;
+    if ((e = grid_for(agoq_accumulate_kernel<256>, nblocks * (256 / kLaneElems), &grid)) != cudaSuccess)
+        return e;
+    return launch_pdl(agoq_accumulate_kernel<256>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
 }
 
 }  // namespace taco

@@ -283,8 +283,17 @@ def test_full_size_two_shot_local_path(name):
     bits = np.stack([W.shard_input(name, p) for p in range(P)])
     x = to_dev_bf16(bits).reshape(P, rows, d)
     nb = rows * d // block
-    path = api.TwoShotLocal(P, rows, d, block)  # the benchmark's path (fused reduce + decompress)
+    path = api.TwoShotLocal(P, rows, d, block)  # the benchmark's path
     out = path.run(x)
+    if P > 1:  # the fused launch gives the same bits
+        fpath = api.TwoShotLocal(P, rows, d, block, fused=True)
+        fpath.codes.copy_(path.codes)
+        fpath.alpha.copy_(path.alpha)
+        fpath.scale.copy_(path.scale)
+        fout = fpath.reduce_decompress()[3]
+        assert torch.equal(fout.view(torch.int32), out.view(torch.int32))
+        assert torch.equal(fpath.r_codes, path.r_codes)
+        del fpath, fout
     torch.cuda.synchronize()
     assert_code_properties(path.codes, x, block)
     assert_code_properties(path.r_codes, None, block)
