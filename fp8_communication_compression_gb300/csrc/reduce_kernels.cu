@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kBlockThreads)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 gr = make_float2(bf16lo_to_f32(gw[j]), bf16hi_to_f32(gw[j]));
-                d[4 * h + j] = __fadd2_rn(__fmul2_rn(d[4 * h + j], s2), gr);
+                d[4 * h + j] = add2_rounded(mul2_rounded(d[4 * h + j], s2), gr);
             }
         }
         const float mx = group_max<LPB>(lane_max_abs(d));

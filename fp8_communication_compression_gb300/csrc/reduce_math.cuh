@@ -65,7 +65,7 @@ __device__ __forceinline__ void weighted_sum(const uint4 (&q)[P][2], const float
     const float2 w0 = make_float2(w[0], w[0]);
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        S[i] = __fmul2_rn(S[i], w0);
+        S[i] = mul2_rounded(S[i], w0);
 #pragma unroll
     for (int p = 1; p < P; ++p) {
         float2 d[16];
@@ -73,7 +73,7 @@ __device__ __forceinline__ void weighted_sum(const uint4 (&q)[P][2], const float
         const float2 wp = make_float2(w[p], w[p]);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            S[i] = __fadd2_rn(S[i], __fmul2_rn(d[i], wp));
+            S[i] = add2_rounded(S[i], mul2_rounded(d[i], wp));
     }
 }
 
@@ -87,11 +87,11 @@ __device__ __forceinline__ void weighted_sum_step(const uint4 (&q)[2], float w, 
     if (first) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            S[i] = __fmul2_rn(d[i], w2);
+            S[i] = mul2_rounded(d[i], w2);
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            S[i] = __fadd2_rn(S[i], __fmul2_rn(d[i], w2));
+            S[i] = add2_rounded(S[i], mul2_rounded(d[i], w2));
     }
 }
 
