@@ -176,32 +176,20 @@ __device__ __forceinline__ void stg128_stream(void *p, uint4 v)
                  : "memory");
 }
 
-// ------------------------------------------- separately rounded fp32x2 --
-// Packed multiply and add that are never contracted into a fused
-// multiply-add: PTX arithmetic with an explicit rounding modifier is kept
-// as written.  Used where the stated arithmetic rounds the product before
-// the sum (and where exactly cancelling terms must give exactly zero).
+// ------------------------------------------- separately rounded products --
+// a * b + c with the product rounded before the sum, on two lanes of a
+// float2.  __fmul_rn / __fadd_rn are never contracted into a fused
+// multiply-add, so terms that cancel exactly give exactly zero and the
+// result is that of the stated arithmetic.
 
 __device__ __forceinline__ float2 mul2_rounded(float2 a, float2 b)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, z;\n\t"
-        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
+    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
 }
 
 __device__ __forceinline__ float2 add2_rounded(float2 a, float2 b)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, z;\n\t"
-        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
+    return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
 }
 
 // ----------------------------------------------------------- conversions --
