@@ -40,7 +40,7 @@ HEADLINE = "gpt6.7b_p4x8192x4096_n128"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csrc", f)
-                  for f in ("codec_kernels.cu", "device_utils.cuh")]
+                  for f in ("codec_kernels.cu", "codec_math.cuh", "device_utils.cuh")]
 
 
 def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: bool = False) -> dict:

@@ -4,8 +4,10 @@
 // a block, NB / 32 adjacent lanes own one block, per-block statistics (sum
 // of squares, absolute maximum) are combined with __shfl_xor_sync, and the
 // per-shard scalars of a block are fetched once per lane group and
-// broadcast with __shfl_sync.  The two reduces keep the next grid-stride
-// slot's loads in flight while they compute the current one.
+// broadcast with __shfl_sync.  For up to four shards the two reduces keep
+// the next grid-stride slot's loads in flight while they compute the
+// current one (with more shards the second slot's registers would cost more
+// occupancy than the prefetch gains).
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kBlockThreads)
     // warp-uniform ping-pong over grid-stride slots: the next slot's loads
     // are in flight while the current one is computed
     RedSlot<P, rounds_of<NB, P>()> a, b;
-    if constexpr (P > 8) {  // no room for two slots of loads in registers
+    if constexpr (P > 4) {  // two slots of loads would cost occupancy
         for (; base < total; base += stride) {
             load_slot<NB, P, true>(in, base, lane, total, a);
             taco_reduce_slot<NB, P>(a, lane, e_target, eps, out_codes, out_alpha, out_scale);
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kBlockThreads)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
     RedSlot<P, rounds_of<NB, P>()> a, b;
-    if constexpr (P > 8) {  // no room for two slots of loads in registers
+    if constexpr (P > 4) {  // two slots of loads would cost occupancy
         for (; base < total; base += stride) {
             load_slot<NB, P, false>(in, base, lane, total, a);
             agoq_reduce_slot<NB, P>(a, lane, out_codes, out_scale);
