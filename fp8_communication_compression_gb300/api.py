@@ -322,11 +322,17 @@ class HostPipeline:
     """The two-shot local path between pinned HOST buffers, overlapped.
 
     The rows are split into ``chunks`` equal chunks.  Chunk c is copied in
-    (all P shards) on one stream, compressed and reduced + decompressed on a
+    (all P shards) on one stream, compressed, reduced and decompressed on a
     second, and its result copied out on a third, so host-to-device copies,
     kernels and device-to-host copies of different chunks run at the same
-    time.  Device buffers are chunk-major and allocated once; the result is
-    identical to ``TwoShotLocal.run`` on the same data."""
+    time.  Consecutive calls are chained chunk by chunk through events (the
+    next call's copy-in of chunk c waits only for this call's compression of
+    chunk c, its decompression of chunk c only for this call's copy-out of
+    chunk c), so one call's copy-out overlaps the next call's copy-in.  Only
+    the first call waits for work already queued on the caller's stream;
+    every call makes the caller's stream wait for its result.  Device
+    buffers are chunk-major and allocated once; the result is identical to
+    ``TwoShotLocal.run`` on the same data."""
 
     def __init__(self, P: int, rows: int, d: int, block: int = 128, chunks: int = 8, device="cuda",
                  e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32):
@@ -346,19 +352,25 @@ class HostPipeline:
         self.r_scale = torch.empty((C, nb), dtype=torch.float32, device=device)
         self.out = torch.empty((C, R, d), dtype=out_dtype, device=device)
         self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
-        self.ev_in = [torch.cuda.Event() for _ in range(C)]
-        self.ev_done = [torch.cuda.Event() for _ in range(C)]
+        self.ev_in = [torch.cuda.Event() for _ in range(C)]          # chunk copied in
+        self.ev_compressed = [torch.cuda.Event() for _ in range(C)]  # chunk's input consumed
+        self.ev_done = [torch.cuda.Event() for _ in range(C)]        # chunk's result ready
+        self.ev_out = [torch.cuda.Event() for _ in range(C)]         # chunk copied out
+        self._started = False
         self._lists = [(list(self.codes[c]), list(self.alpha[c]), list(self.scale[c])) for c in range(C)]
 
     def run(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.Tensor:
         """x_host: pinned bf16 [P, rows, d]; out_host: pinned [rows, d]."""
         s_in, s_comp, s_out = self.streams
         cur = torch.cuda.current_stream()
-        for s in self.streams:
-            s.wait_stream(cur)
+        if not self._started:
+            for s in self.streams:
+                s.wait_stream(cur)
         R = self.R
         for c in range(self.C):
             with torch.cuda.stream(s_in):
+                if self._started:
+                    s_in.wait_event(self.ev_compressed[c])
                 for p in range(self.P):
                     self.x[c, p].copy_(x_host[p, c * R:(c + 1) * R], non_blocking=True)
                 self.ev_in[c].record(s_in)
@@ -366,13 +378,18 @@ class HostPipeline:
             codes, alpha, scale = self._lists[c]
             taco_compress(self.x[c], self.block, self.e_target, self.eps, self.codes[c],
                           self.alpha[c], self.scale[c], stream=s_comp)
-            taco_reduce_decompress(codes, alpha, scale, self.block, self.e_target, self.eps,
-                                   self.r_codes[c], self.r_alpha[c], self.r_scale[c], self.out[c],
-                                   stream=s_comp)
+            self.ev_compressed[c].record(s_comp)
+            taco_reduce_shards(codes, alpha, scale, self.block, self.e_target, self.eps,
+                               self.r_codes[c], self.r_alpha[c], self.r_scale[c], stream=s_comp)
+            if self._started:
+                s_comp.wait_event(self.ev_out[c])
+            taco_decompress(self.r_codes[c], self.r_alpha[c], self.r_scale[c], self.block,
+                            out=self.out[c], stream=s_comp)
             self.ev_done[c].record(s_comp)
             s_out.wait_event(self.ev_done[c])
             with torch.cuda.stream(s_out):
                 out_host[c * R:(c + 1) * R].copy_(self.out[c], non_blocking=True)
-        for s in self.streams:
-            cur.wait_stream(s)
+                self.ev_out[c].record(s_out)
+        self._started = True
+        cur.wait_stream(s_out)
         return out_host
