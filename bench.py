@@ -278,6 +278,28 @@ def agoq_leg(torch, api, peak: float) -> dict:
     return out
 
 
+def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) -> dict:
+    """The INT8 variant of the codec (compress all shards, decompress one
+    tensor of the same size) on the headline shards, per-launch events."""
+    n = rows * d
+    nb = n // block
+    codes = torch.empty((P, rows, d), dtype=torch.int8, device="cuda")
+    alpha = torch.empty((P, nb), dtype=torch.float32, device="cuda")
+    scale = torch.empty((P, nb), dtype=torch.float32, device="cuda")
+    out = torch.empty((rows, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    comp = lambda: api.taco_compress_int8(x, block, codes=codes, alpha=alpha, scale=scale)
+    dec = lambda: api.taco_decompress_int8(codes[0], alpha[0], scale[0], block, out=out)
+    comp()
+    dec()
+    ms = {"compress_int8": time_launches(torch, comp, 10, stream),
+          "decompress_int8": time_launches(torch, dec, 10, stream)}
+    nbytes = {"compress_int8": P * (2 * n + n + 8 * nb), "decompress_int8": n + 8 * nb + 4 * n}
+    return {k: {"us_per_launch": ms[k] * 1e3, "algorithmic_bytes": nbytes[k],
+                "gbs": nbytes[k] / (ms[k] / 1e3) / 1e9, "frac_of_peak": nbytes[k] / (ms[k] / 1e3) / 1e9 / peak}
+            for k in ms}
+
+
 def gpt13b_leg(torch, api, peak: float) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     CUDA-event times of compress, the fused reduce + decompress, and the
@@ -318,6 +340,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
     ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
+    ap.add_argument("--no-int8", action="store_true", help="skip the INT8-codec leg")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress as one fused launch instead of two")
     ap.add_argument("--gpt13b", action="store_true",
@@ -420,6 +443,8 @@ def main():
         e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     peak, peak_src = hbm_peak()
     extra = {}
+    if rank == 0 and not args.no_int8:
+        extra["int8_" + HEADLINE] = int8_leg(torch, api, x, P, rows, d, block, peak)
     if rank == 0 and not args.no_agoq:
         del path, x
         torch.cuda.empty_cache()

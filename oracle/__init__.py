@@ -60,9 +60,12 @@ def _load():
             lib.oracle_int8_roundtrip.argtypes = [P, i64, i64, i32, P]
             lib.oracle_compress_int8.argtypes = [P, i64, i64, i32, f32, f32, P, P, P]
             lib.oracle_decompress_int8.argtypes = [P, P, P, i64, i64, i32, P]
+            lib.oracle_laaq_quantize.argtypes = [P, i64, i32, i32, P, P]
+            lib.oracle_laaq_dequantize.argtypes = [P, P, i64, i32, i32, P]
             for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
                       "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
-                      "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8"):
+                      "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8",
+                      "oracle_laaq_quantize", "oracle_laaq_dequantize"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -229,4 +232,23 @@ def decompress_int8(codes: np.ndarray, alpha: np.ndarray, scale: np.ndarray, blo
     rows, d = c.shape
     out = np.empty((rows, d), dtype=np.float64)
     _check(_load().oracle_decompress_int8(_ptr(c), _ptr(a), _ptr(s), rows, d, block, _ptr(out)))
+    return out
+
+
+# ------------------------------------------------------------------ LAAQ --
+
+def laaq_quantize(x_bf16: np.ndarray, block: int = 128, bits: int = 4):
+    """bf16 bits [n] -> (packed uint8 [n * bits / 8], scale fp32 [n / block])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1)
+    packed = np.zeros(x.size * bits // 8, dtype=np.uint8)
+    scale = np.empty(x.size // block, dtype=np.float32)
+    _check(_load().oracle_laaq_quantize(_ptr(x), x.size, block, bits, _ptr(packed), _ptr(scale)))
+    return packed, scale
+
+
+def laaq_dequantize(packed: np.ndarray, scale: np.ndarray, n: int, block: int = 128, bits: int = 4):
+    p = np.ascontiguousarray(packed, dtype=np.uint8).reshape(-1)
+    s = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
+    out = np.empty(n, dtype=np.float32)
+    _check(_load().oracle_laaq_dequantize(_ptr(p), _ptr(s), n, block, bits, _ptr(out)))
     return out

@@ -481,3 +481,98 @@ int oracle_int8_roundtrip(const uint16_t *x_bf16, int64_t rows, int64_t d, int b
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ LAAQ */
+/* [AGoQ] 2.A, layer-aware activation quantisation: the activations of the
+ * layers that are quantised are stored block-wise in 4 bits (5, 6 or 8 bits
+ * where the pipeline-stage bit-width compensation grants more memory).
+ * Reading (the page gives no format): per block of `block` elements,
+ *   amax  = max |x|
+ *   qmax  = 2^(bits-1) - 1
+ *   q     = fp32(qmax / amax)          (1 for an all-zero block)
+ *   code  = clamp(round-to-nearest-even(fp32(x * q)), -qmax, qmax)
+ *   m     = fp32(amax / qmax)          (1 for an all-zero block; stored)
+ *   x_hat = fp32(code * m)
+ * Codes are two's complement, packed into a little-endian bit stream:
+ * element i occupies bits [i * bits, (i + 1) * bits) of the buffer, bit j of
+ * the stream being bit (j % 8) of byte j / 8.  All arithmetic is fp32. */
+static int laaq_args_ok(int64_t n, int block, int bits)
+{
+    return n >= 0 && (block == 32 || block == 64 || block == 128 || block == 256) && n % block == 0 &&
+           (bits == 4 || bits == 5 || bits == 6 || bits == 8);
+}
+
+static void put_bits(uint8_t *stream, int64_t bitpos, uint32_t value, int bits)
+{
+    int j;
+    for (j = 0; j < bits; ++j) {
+        const int64_t b = bitpos + j;
+        if ((value >> j) & 1u)
+            stream[b / 8] |= (uint8_t)(1u << (b % 8));
+        else
+            stream[b / 8] &= (uint8_t)~(1u << (b % 8));
+    }
+}
+
+static int32_t get_bits_signed(const uint8_t *stream, int64_t bitpos, int bits)
+{
+    uint32_t v = 0;
+    int j;
+    for (j = 0; j < bits; ++j) {
+        const int64_t b = bitpos + j;
+        v |= (uint32_t)((stream[b / 8] >> (b % 8)) & 1u) << j;
+    }
+    if (v & (1u << (bits - 1)))
+        return (int32_t)v - (int32_t)(1u << bits);
+    return (int32_t)v;
+}
+
+int oracle_laaq_quantize(const uint16_t *x_bf16, int64_t n, int block, int bits, uint8_t *packed,
+                         float *scale)
+{
+    int64_t nb, k;
+    int i;
+    const float qmax = (float)((1 << (bits - 1)) - 1);
+    if (!laaq_args_ok(n, block, bits))
+        return -1;
+    nb = n / block;
+    for (k = 0; k < nb; ++k) {
+        float amax = 0.0f, q = 1.0f, m = 1.0f;
+        for (i = 0; i < block; ++i) {
+            const float v = fabsf((float)bf16_to_double(x_bf16[k * block + i]));
+            if (v > amax)
+                amax = v;
+        }
+        if (amax > 0.0f) {
+            q = qmax / amax;
+            if (!(q <= FLT_MAX))
+                q = FLT_MAX;
+            m = amax / qmax;
+        }
+        for (i = 0; i < block; ++i) {
+            const float v = (float)bf16_to_double(x_bf16[k * block + i]) * q;
+            float r = rintf(v);
+            if (r > qmax)
+                r = qmax;
+            if (r < -qmax)
+                r = -qmax;
+            put_bits(packed, (k * block + i) * (int64_t)bits, (uint32_t)(int32_t)r & ((1u << bits) - 1u),
+                     bits);
+        }
+        scale[k] = m;
+    }
+    return 0;
+}
+
+int oracle_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
+                           float *out)
+{
+    int64_t i;
+    if (!laaq_args_ok(n, block, bits))
+        return -1;
+    for (i = 0; i < n; ++i) {
+        const float c = (float)get_bits_signed(packed, i * (int64_t)bits, bits);
+        out[i] = c * scale[i / block];
+    }
+    return 0;
+}

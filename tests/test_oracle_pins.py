@@ -542,3 +542,61 @@ def test_int8_ash_avoids_the_zero_collapse_of_plain_int8():
     plain = oracle.int8_roundtrip(x, n)
     assert np.mean(plain[small] == 0) > 0.3
     assert np.mean(ash[small] == 0) < 0.05
+
+
+# ------------------------------------------------------------------ LAAQ ---
+# AGoQ section 2.A: block-wise 4-bit activation codes (5, 6, 8 bits under the
+# pipeline-stage compensation), read as symmetric absmax integers packed into
+# a little-endian bit stream, in FP32 arithmetic.
+
+def test_laaq_hand_worked_examples():
+    g = json.load(open(os.path.join(GOLDEN, "laaq_examples.json")))
+    for ex in g["examples"]:
+        x = bf16(ex["x"])
+        packed, scale = oracle.laaq_quantize(x, ex["block"], ex["bits"])
+        assert packed.tolist() == ex["packed"], ex["name"]
+        assert scale[0] == np.float32(ex["scale"]), ex["name"]
+        out = oracle.laaq_dequantize(packed, scale, x.size, ex["block"], ex["bits"])
+        assert np.array_equal(out, (np.array(ex["codes"], np.float32) * scale[0]).astype(np.float32))
+
+
+def laaq_rederive(x_bf16, block, bits):
+    xf = W.bf16_bits_to_f32(x_bf16).reshape(-1, block)
+    qmax = np.float32(2 ** (bits - 1) - 1)
+    amax = np.abs(xf).max(axis=1)
+    with np.errstate(divide="ignore"):
+        q = np.where(amax > 0, qmax / np.where(amax > 0, amax, 1), 1).astype(np.float32)
+        m = np.where(amax > 0, amax / qmax, 1).astype(np.float32)
+    codes = np.clip(np.rint((xf * q[:, None]).astype(np.float32)), -qmax, qmax).astype(np.int64)
+    u = (codes & ((1 << bits) - 1)).reshape(-1)
+    bitarr = ((u[:, None] >> np.arange(bits)) & 1).astype(np.uint8).reshape(-1)
+    return np.packbits(bitarr, bitorder="little"), m, codes
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("block", [32, 128, 256])
+def test_laaq_matches_library_rederivation(bits, block):
+    x = W.tp_activation(30 + bits, 16, 1024, channel_scale=True, zero_blocks=(1,), block=block)
+    packed, scale = oracle.laaq_quantize(x, block, bits)
+    ref_packed, ref_m, codes = laaq_rederive(x, block, bits)
+    assert np.array_equal(packed, ref_packed)
+    assert np.array_equal(scale, ref_m)
+    out = oracle.laaq_dequantize(packed, scale, x.size, block, bits)
+    assert np.array_equal(out, (codes.astype(np.float32) * ref_m[:, None]).astype(np.float32).reshape(-1))
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+def test_laaq_error_within_half_a_step_and_uses_the_full_range(bits):
+    block = 64
+    x = W.tp_activation(40 + bits, 8, 2048, block=block)
+    packed, scale = oracle.laaq_quantize(x, block, bits)
+    out = oracle.laaq_dequantize(packed, scale, x.size, block, bits).reshape(-1, block)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64).reshape(-1, block)
+    step = scale.astype(np.float64)[:, None]
+    amax = np.abs(xf).max(axis=1, keepdims=True)
+    # half a step, plus the fp32 roundings of q, x*q, m and code*m (each at
+    # most 2^-24 relative to values no larger than amax)
+    assert np.all(np.abs(out - xf) <= 0.5 * step + 4 * 2.0 ** -24 * amax * 2)
+    qmax = 2 ** (bits - 1) - 1
+    nz = np.any(xf != 0, axis=1)
+    assert np.all(np.abs(np.rint(out / step)).max(axis=1)[nz] == qmax)
