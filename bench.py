@@ -300,6 +300,48 @@ def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) 
             for k in ms}
 
 
+def laaq_leg(torch, api, peak: float) -> dict:
+    """AGoQ LAAQ activation codec on a GPT-6.7B-shaped activation tensor
+    (bf16 [8192, 4096]), block 128, 4/5/6/8 bits: quantize and dequantize to
+    bf16, per-launch events (inputs larger than L2 are not needed to show the
+    codec: the tensor is 67 MB, so each launch reads a fresh copy from a ring
+    of three)."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    rows, d, block = 8192, 4096, 128
+    n = rows * d
+    xs = [torch.from_numpy(W.tp_activation(600 + i, rows, d, channel_scale=True).view(np.int16))
+          .cuda().view(torch.bfloat16).reshape(-1) for i in range(3)]
+    stream = torch.cuda.current_stream()
+    res = {}
+    for bits in (4, 5, 6, 8):
+        packed = [torch.empty(n * bits // 8, dtype=torch.uint8, device="cuda") for _ in range(3)]
+        scale = [torch.empty(n // block, dtype=torch.float32, device="cuda") for _ in range(3)]
+        out = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        it = {"q": 0, "d": 0}
+
+        def quant():
+            i = it["q"] % 3
+            it["q"] += 1
+            api.agoq_laaq_quantize(xs[i], block, bits, packed[i], scale[i])
+
+        def dequant():
+            i = it["d"] % 3
+            it["d"] += 1
+            api.agoq_laaq_dequantize(packed[i], scale[i], n, block, bits, out=out[i])
+
+        for _ in range(3):
+            quant()
+            dequant()
+        for name, fn, b in (("quantize", quant, 2 * n + n * bits // 8 + 4 * (n // block)),
+                            ("dequantize", dequant, n * bits // 8 + 4 * (n // block) + 2 * n)):
+            ms = time_launches(torch, fn, 12, stream)
+            gbs = b / (ms / 1e3) / 1e9
+            res[f"{name}_{bits}bit"] = {"us_per_launch": ms * 1e3, "algorithmic_bytes": b, "gbs": gbs,
+                                        "frac_of_peak": gbs / peak}
+    return res
+
+
 def gpt13b_leg(torch, api, peak: float) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     CUDA-event times of compress, the fused reduce + decompress, and the
@@ -341,6 +383,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
     ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
     ap.add_argument("--no-int8", action="store_true", help="skip the INT8-codec leg")
+    ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress as one fused launch instead of two")
     ap.add_argument("--gpt13b", action="store_true",
@@ -449,6 +492,9 @@ def main():
         del path, x
         torch.cuda.empty_cache()
         extra["agoq"] = agoq_leg(torch, api, peak)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_laaq:
+        extra["laaq_8192x4096_n128"] = laaq_leg(torch, api, peak)
         torch.cuda.empty_cache()
     if rank == 0 and args.gpt13b:
         extra["gpt13b_p8x8192x5120_n256"] = gpt13b_leg(torch, api, peak)

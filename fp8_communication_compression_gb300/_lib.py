@@ -36,6 +36,8 @@ SIGNATURES = {
                                               _P, _P, _P, _P, _I32, _P]),
     "agoq_fp8_accumulate": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P]),
     "agoq_reduce_shards": (ctypes.c_int, [_I32, _PP, _PP, _I64, _I32, _P, _P, _P]),
+    "agoq_laaq_quantize": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
+    "agoq_laaq_dequantize": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _I32, _P]),
     "taco_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32]),
 }
 

@@ -229,6 +229,39 @@ def agoq_reduce_shards(codes: Sequence[torch.Tensor], scale: Sequence[torch.Tens
     return out_codes, out_scale
 
 
+def agoq_laaq_quantize(x: torch.Tensor, block: int = 128, bits: int = 4,
+                       packed: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                       stream=None):
+    """bf16 activations -> (packed b-bit codes uint8 [n*bits/8], fp32 scale [n/block])."""
+    _need(x, "x", _BF16)
+    n = x.numel()
+    if packed is None:
+        packed = torch.empty(n * bits // 8, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(n // block, dtype=torch.float32, device=x.device)
+    _need(packed, "packed", (torch.uint8,), n * bits // 8)
+    _need(scale, "scale", (torch.float32,))
+    st = _lib.load().agoq_laaq_quantize(x.data_ptr(), n, block, bits, packed.data_ptr(),
+                                        scale.data_ptr(), _stream_handle(stream))
+    _lib.check("agoq_laaq_quantize", st)
+    return packed, scale
+
+
+def agoq_laaq_dequantize(packed: torch.Tensor, scale: torch.Tensor, n: int, block: int = 128,
+                         bits: int = 4, out_dtype: torch.dtype = torch.bfloat16,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _need(packed, "packed", (torch.uint8,), n * bits // 8)
+    _need(scale, "scale", (torch.float32,))
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype, device=packed.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), n)
+    st = _lib.load().agoq_laaq_dequantize(packed.data_ptr(), scale.data_ptr(), n, block, bits,
+                                          out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                          _stream_handle(stream))
+    _lib.check("agoq_laaq_dequantize", st)
+    return out
+
+
 def taco_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))

@@ -48,6 +48,11 @@ cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *gra
 cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block, uint8_t *out_codes,
                                float *out_scale, cudaStream_t stream);
 
+cudaError_t launch_laaq_quantize(const void *x_bf16, int64_t n, int block, int bits, uint8_t *packed,
+                                 float *scale, cudaStream_t stream);
+cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
+                                   void *out, bool out_bf16, cudaStream_t stream);
+
 cudaError_t read_codec_error(uint32_t *flags, bool clear);
 
 // Launches `kernel` with programmatic stream serialization allowed, so that

@@ -310,6 +310,54 @@ taco_status agoq_reduce_shards(int32_t P, const uint8_t *const *codes, const flo
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static taco_status check_laaq(int64_t n, int32_t block, int32_t bits)
+{
+    if (n < 0)
+        return TACO_ERR_INVALID_ARG;
+    if (!(block == 32 || block == 64 || block == 128 || block == 256) ||
+        !(bits == 4 || bits == 5 || bits == 6 || bits == 8))
+        return TACO_ERR_UNSUPPORTED;
+    if (n % block != 0)
+        return TACO_ERR_INVALID_ARG;
+    return TACO_OK;
+}
+
+taco_status agoq_laaq_quantize(const void *x_bf16, int64_t n, int32_t block, int32_t bits, uint8_t *packed,
+                               float *scale, taco_stream_t stream)
+{
+    taco_status st = check_laaq(n, block, bits);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if (!x_bf16 || !packed || !scale)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(packed, 16) || !aligned(scale, 4))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t nb = static_cast<uint64_t>(n / block), pb = static_cast<uint64_t>(n) * bits / 8;
+    if (overlap(x_bf16, 2 * n, packed, pb) || overlap(x_bf16, 2 * n, scale, 4 * nb) ||
+        overlap(packed, pb, scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_laaq_quantize(x_bf16, n, block, bits, packed, scale,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
+                                 int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream)
+{
+    taco_status st = check_laaq(n, block, bits);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if (!packed || !scale || !out)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(packed, 16) || !aligned(scale, 4) || !aligned(out, 16))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t nb = static_cast<uint64_t>(n / block), pb = static_cast<uint64_t>(n) * bits / 8;
+    const uint64_t ob = static_cast<uint64_t>(n) * (out_is_bf16 ? 2 : 4);
+    if (overlap(out, ob, packed, pb) || overlap(out, ob, scale, 4 * nb))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_laaq_dequantize(packed, scale, n, block, bits, out, out_is_bf16 != 0,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 taco_status taco_device_error(uint32_t *flags_out, int32_t clear)
 {
     if (!flags_out)

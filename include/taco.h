@@ -200,6 +200,31 @@ taco_status agoq_reduce_shards(int32_t P, const uint8_t *const *codes, const flo
                                taco_stream_t stream);
 
 /*
+ * agoq_laaq_quantize / agoq_laaq_dequantize - block-wise activation codec of
+ * AGoQ's layer-aware activation quantisation ([AGoQ] 2.A: 4-bit codes, with
+ * 5, 6 or 8 bits where the pipeline-stage compensation allows).  Per block,
+ * in fp32 with every operation rounded:
+ *   amax = max|x|,  qmax = 2^(bits-1) - 1,  q = qmax / amax,
+ *   code = clamp(round-to-nearest-even(x * q), -qmax, qmax),
+ *   scale = amax / qmax (1 for an all-zero block),  x_hat = code * scale.
+ * Codes are two's complement, packed little-endian: element i occupies bits
+ * i*bits .. i*bits + bits - 1 of `packed` (bit j is bit j % 8 of byte j / 8).
+ *
+ *  x_bf16   in   bf16 [n], 16-byte aligned
+ *  n             n >= 0, n % block == 0
+ *  block         32, 64, 128 or 256
+ *  bits          4, 5, 6 or 8
+ *  packed   out  uint8 [n * bits / 8], 16-byte aligned
+ *  scale    out  fp32 [n / block]
+ *  out      out  [n] fp32, or bf16 (round to nearest even) when out_is_bf16
+ */
+taco_status agoq_laaq_quantize(const void *x_bf16, int64_t n, int32_t block, int32_t bits,
+                               uint8_t *packed, float *scale, taco_stream_t stream);
+taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n,
+                                 int32_t block, int32_t bits, void *out, int32_t out_is_bf16,
+                                 taco_stream_t stream);
+
+/*
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
  * (bit 0: compressor, bit 1: decompressor).  Synchronises the device.  With

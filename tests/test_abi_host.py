@@ -140,3 +140,19 @@ def test_reduce_decompress_validation(lib):
     assert f(out=A * 100 + 4) == MISALIGNED
     assert f(out=A * 64) == INVALID  # reconstruction overlaps the output codes
     assert f(out=A * 2) == INVALID  # reconstruction overlaps shard 1
+
+
+def test_laaq_validation(lib):
+    q = lambda n=1024, block=128, bits=4, x=A, p=A * 4, s=A * 8: lib.agoq_laaq_quantize(x, n, block, bits, p, s, None)
+    assert q(bits=3) == UNSUPPORTED
+    assert q(bits=7) == UNSUPPORTED
+    assert q(block=16) == UNSUPPORTED
+    assert q(n=1000) == INVALID
+    assert q(n=0) == OK
+    assert q(p=A * 4 + 8) == MISALIGNED
+    assert q(p=A + 64) == INVALID  # packed codes overlap the input
+    d = lambda n=1024, out=A * 16, bf=1: lib.agoq_laaq_dequantize(A * 4, A * 8, n, 128, 4, out, bf, None)
+    assert d(out=0) == INVALID
+    assert d(out=A * 16 + 2) == MISALIGNED
+    assert d(out=A * 4) == INVALID  # output overlaps the packed codes
+    assert d(n=0) == OK

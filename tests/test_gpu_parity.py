@@ -258,6 +258,24 @@ def test_agoq_reduce_shard_and_negation_gives_zero():
     assert torch.all((oc & 0x7F) == 0) and torch.all(os_ == 1.0)
 
 
+# ------------------------------------------------------------------ LAAQ --
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_laaq_codec_is_bit_identical_to_the_oracle(bits, block):
+    n = 96 * 1024 + 3 * 256  # several grid strides and a ragged tail of blocks
+    x = W.tp_activation(500 + bits, n // 256, 256, channel_scale=True, zero_blocks=(2,), block=block)
+    packed, scale = api.agoq_laaq_quantize(to_dev_bf16(x).reshape(-1), block, bits)
+    rp, rs = oracle.laaq_quantize(x, block, bits)
+    assert np.array_equal(to_host(packed), rp)
+    assert np.array_equal(to_host(scale), rs)
+    out32 = api.agoq_laaq_dequantize(packed, scale, n, block, bits, out_dtype=torch.float32)
+    ref = oracle.laaq_dequantize(rp, rs, n, block, bits)
+    assert np.array_equal(to_host(out32), ref)
+    out16 = api.agoq_laaq_dequantize(packed, scale, n, block, bits, out_dtype=torch.bfloat16)
+    assert np.array_equal(to_host(out16.view(torch.int16)).view(np.uint16), W.f32_to_bf16_bits(ref))
+
+
 # ----------------------------------------------- full-size workloads --
 
 def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None, block: int):
