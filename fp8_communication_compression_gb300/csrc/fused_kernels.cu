@@ -75,7 +75,7 @@ __device__ __forceinline__ void finish_block(float2 (&T)[16], const Slot &sl, in
     const int part = lane % LPB;
     uint4 oq[2];
     float alpha, scale;
-    recompress<NB, LPB>(T, e_target, eps, oq, alpha, scale);
+    recompress<NB, LPB, 16>(T, e_target, eps, oq, alpha, scale);
     if (sl.valid) {
         stg128_stream(out_codes + sl.off, oq[0]);
         stg128_stream(out_codes + sl.off + 16, oq[1]);
@@ -116,7 +116,7 @@ __device__ __forceinline__ void accumulate_fixed(const ShardPtrs &in, const Slot
 #pragma unroll
     for (int p = 0; p < P; ++p)
         w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
-    weighted_sum<P>(q, w, T);
+    weighted_sum<P, 16>(q, w, T);
 }
 
 // Phase 1 for a run-time shard count (1 .. 16): shard by shard, same rounding.
@@ -127,7 +127,7 @@ __device__ __forceinline__ void accumulate_any(const ShardPtrs &in, int P, const
         uint4 q[2];
         load32_codes(in.codes[p] + sl.off, sl.valid, q);
         const float w = sl.valid ? shard_weight(__ldg(in.scale[p] + sl.blk), __ldg(in.alpha[p] + sl.blk)) : 1.0f;
-        weighted_sum_step(q, w, p == 0, T);
+        weighted_sum_step<16>(q, w, p == 0, T);
     }
 }
 

@@ -1,13 +1,13 @@
 // Shard reduce (TACO two-shot local step) and AGoQ FP8 gradient kernels for
 // sm_103a.  None of these needs a Hadamard rotation on its path, so they
-// use plain coalesced 16-byte loads: a lane owns 32 consecutive elements of
-// a block, NB / 32 adjacent lanes own one block, per-block statistics (sum
+// use plain coalesced 16-byte loads: a lane owns 32 (or 16) consecutive
+// elements of a block, adjacent lanes own one block, per-block statistics (sum
 // of squares, absolute maximum) are combined with __shfl_xor_sync, and the
 // per-shard scalars of a block are fetched once per lane group and
-// broadcast with __shfl_sync.  For up to four shards the two reduces keep
-// the next grid-stride slot's loads in flight while they compute the
-// current one (with more shards the second slot's registers would cost more
-// occupancy than the prefetch gains).
+// broadcast with __shfl_sync.  The shard reduces use 16 elements per lane
+// when there are more than four shards, and for up to four shards keep the
+// next grid-stride slot's loads in flight while they compute the current
+// one.
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -48,33 +48,45 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
     }
 }
 
+// Elements per lane of the two reduces: 32 for up to four shards; with more
+// shards 16, so that a lane's codes in flight (16 or 32 bytes per shard)
+// leave room for occupancy.  Block statistics are bit-identical in both
+// layouts (reduce_math.cuh).
+template <int P> __host__ __device__ constexpr int elems_per_lane() { return P <= 4 ? 32 : 16; }
+
+template <int NB, int P> __host__ __device__ constexpr int lanes_per_block() { return NB / elems_per_lane<P>(); }
+
 template <int NB, int P> __host__ __device__ constexpr int rounds_of()
 {
-    return (P + NB / kLaneElems - 1) / (NB / kLaneElems);
+    return (P + lanes_per_block<NB, P>() - 1) / lanes_per_block<NB, P>();
 }
 
 // One grid-stride slot of a lane: its block, offset, and the loads.
-template <int P, int ROUNDS> struct RedSlot {
-    uint4 q[P][2];
+template <int P, int ROUNDS, int NF> struct RedSlot {
+    uint4 q[P][NF / 8];
     float sc[ROUNDS];  // scale (TACO) or dequantisation multiplier (AGoQ) of shard r * LPB + part
     float al[ROUNDS];  // alpha of that shard (TACO only)
     int64_t blk, off;
     bool valid;
 };
 
+template <int NB, int P>
+using SlotOf = RedSlot<P, rounds_of<NB, P>(), elems_per_lane<P>() / 2>;
+
 template <int NB, int P, bool WITH_ALPHA>
 __device__ __forceinline__ void load_slot(const ShardPtrs &in, int64_t base, int lane, int64_t total,
-                                          RedSlot<P, rounds_of<NB, P>()> &s)
+                                          SlotOf<NB, P> &s)
 {
-    constexpr int LPB = NB / kLaneElems;
+    constexpr int LPB = lanes_per_block<NB, P>();
+    constexpr int NF = elems_per_lane<P>() / 2;
     const int part = lane % LPB;
     const int64_t t = base + lane;
     s.valid = t < total;
     s.blk = s.valid ? t / LPB : 0;
-    s.off = s.blk * NB + part * kLaneElems;
+    s.off = s.blk * NB + part * elems_per_lane<P>();
 #pragma unroll
     for (int p = 0; p < P; ++p)
-        load32_codes(in.codes[p] + s.off, s.valid, s.q[p]);
+        load_codes<NF>(in.codes[p] + s.off, s.valid, s.q[p]);
 #pragma unroll
     for (int r = 0; r < rounds_of<NB, P>(); ++r) {
         const int p = r * LPB + part;
@@ -95,35 +107,40 @@ __device__ __forceinline__ void share_factors(const float (&mine)[ROUNDS], int l
         f[p] = __shfl_sync(0xFFFFFFFFu, mine[p / LPB], gbase + (p % LPB));
 }
 
-// ------------------------------------------------------ TACO reduce --
-
-template <int NB, int P>
-__device__ __forceinline__ void taco_reduce_slot(const RedSlot<P, rounds_of<NB, P>()> &s, int lane,
-                                                 float e_target, float eps, uint8_t *out_codes,
-                                                 float *out_alpha, float *out_scale)
+// Runs `process` over the lane's grid-stride slots.  For up to four shards
+// the next slot's loads are issued before the current slot is processed
+// (ping-pong); with more shards the second slot's registers would cost more
+// occupancy than the prefetch gains.
+template <int NB, int P, bool WITH_ALPHA, typename F>
+__device__ __forceinline__ void for_each_slot(const ShardPtrs &in, int64_t nblocks, F &&process)
 {
-    constexpr int LPB = NB / kLaneElems;
-    constexpr int ROUNDS = rounds_of<NB, P>();
-    float wr[ROUNDS];
-#pragma unroll
-    for (int r = 0; r < ROUNDS; ++r)
-        wr[r] = shard_weight(s.sc[r], s.al[r]);
-    float w[P];
-    share_factors<LPB, P, ROUNDS>(wr, lane, w);
-    float2 T[16];
-    weighted_sum<P>(s.q, w, T);
-    uint4 oq[2];
-    float alpha, scale;
-    recompress<NB, LPB>(T, e_target, eps, oq, alpha, scale);
-    if (s.valid) {
-        stg128_stream(out_codes + s.off, oq[0]);
-        stg128_stream(out_codes + s.off + 16, oq[1]);
-        if (lane % LPB == 0) {
-            out_alpha[s.blk] = alpha;
-            out_scale[s.blk] = scale;
+    constexpr int LPB = lanes_per_block<NB, P>();
+    const int64_t total = nblocks * LPB;
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+    SlotOf<NB, P> a, b;
+    if constexpr (P > 4) {
+        for (; base < total; base += stride) {
+            load_slot<NB, P, WITH_ALPHA>(in, base, lane, total, a);
+            process(a);
+        }
+    } else {
+        load_slot<NB, P, WITH_ALPHA>(in, base, lane, total, a);
+        while (base < total) {
+            load_slot<NB, P, WITH_ALPHA>(in, base + stride, lane, total, b);
+            process(a);
+            base += stride;
+            if (base >= total)
+                break;
+            load_slot<NB, P, WITH_ALPHA>(in, base + stride, lane, total, a);
+            process(b);
+            base += stride;
         }
     }
 }
+
+// ------------------------------------------------------ TACO reduce --
 
 template <int NB, int P>
 __global__ void __launch_bounds__(kBlockThreads)
@@ -131,92 +148,67 @@ __global__ void __launch_bounds__(kBlockThreads)
                        uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
                        float *__restrict__ out_scale)
 {
-    constexpr int LPB = NB / kLaneElems;
+    constexpr int LPB = lanes_per_block<NB, P>();
+    constexpr int NF = elems_per_lane<P>() / 2;
+    constexpr int ROUNDS = rounds_of<NB, P>();
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-    // warp-uniform ping-pong over grid-stride slots: the next slot's loads
-    // are in flight while the current one is computed
-    RedSlot<P, rounds_of<NB, P>()> a, b;
-    if constexpr (P > 4) {  // two slots of loads would cost occupancy
-        for (; base < total; base += stride) {
-            load_slot<NB, P, true>(in, base, lane, total, a);
-            taco_reduce_slot<NB, P>(a, lane, e_target, eps, out_codes, out_alpha, out_scale);
+    for_each_slot<NB, P, true>(in, nblocks, [&](const SlotOf<NB, P> &s) {
+        float wr[ROUNDS];
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r)
+            wr[r] = shard_weight(s.sc[r], s.al[r]);
+        float w[P];
+        share_factors<LPB, P, ROUNDS>(wr, lane, w);
+        float2 T[NF];
+        weighted_sum<P, NF>(s.q, w, T);
+        uint4 oq[NF / 8];
+        float alpha, scale;
+        recompress<NB, LPB, NF>(T, e_target, eps, oq, alpha, scale);
+        if (s.valid) {
+#pragma unroll
+            for (int h = 0; h < NF / 8; ++h)
+                stg128_stream(out_codes + s.off + 16 * h, oq[h]);
+            if (lane % LPB == 0) {
+                out_alpha[s.blk] = alpha;
+                out_scale[s.blk] = scale;
+            }
         }
-        return;
-    }
-    load_slot<NB, P, true>(in, base, lane, total, a);
-    while (base < total) {
-        load_slot<NB, P, true>(in, base + stride, lane, total, b);
-        taco_reduce_slot<NB, P>(a, lane, e_target, eps, out_codes, out_alpha, out_scale);
-        base += stride;
-        if (base >= total)
-            break;
-        load_slot<NB, P, true>(in, base + stride, lane, total, a);
-        taco_reduce_slot<NB, P>(b, lane, e_target, eps, out_codes, out_alpha, out_scale);
-        base += stride;
-    }
+    });
 }
 
 // ----------------------------------------------------- AGoQ reduce --
-
-template <int NB, int P>
-__device__ __forceinline__ void agoq_reduce_slot(const RedSlot<P, rounds_of<NB, P>()> &s, int lane,
-                                                 uint8_t *out_codes, float *out_scale)
-{
-    constexpr int LPB = NB / kLaneElems;
-    float m[P];
-    share_factors<LPB, P, rounds_of<NB, P>()>(s.sc, lane, m);
-    // FP32 dequantise (one rounded multiply) and FP32 sum in shard order
-    float2 S[16];
-    weighted_sum<P>(s.q, m, S);
-    const float mx = group_max<LPB>(lane_max_abs(S));
-    float qs, m_new;
-    agoq_scales(mx, qs, m_new);
-    uint4 oq[2];
-    encode32_f2(S, qs, oq);
-    if (s.valid) {
-        stg128_stream(out_codes + s.off, oq[0]);
-        stg128_stream(out_codes + s.off + 16, oq[1]);
-        if (lane % LPB == 0)
-            out_scale[s.blk] = m_new;
-    }
-}
 
 template <int NB, int P>
 __global__ void __launch_bounds__(kBlockThreads)
     agoq_reduce_kernel(const ShardPtrs in, int64_t nblocks, uint8_t *__restrict__ out_codes,
                        float *__restrict__ out_scale)
 {
-    constexpr int LPB = NB / kLaneElems;
+    constexpr int LPB = lanes_per_block<NB, P>();
+    constexpr int NF = elems_per_lane<P>() / 2;
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-    RedSlot<P, rounds_of<NB, P>()> a, b;
-    if constexpr (P > 4) {  // two slots of loads would cost occupancy
-        for (; base < total; base += stride) {
-            load_slot<NB, P, false>(in, base, lane, total, a);
-            agoq_reduce_slot<NB, P>(a, lane, out_codes, out_scale);
+    for_each_slot<NB, P, false>(in, nblocks, [&](const SlotOf<NB, P> &s) {
+        float m[P];
+        share_factors<LPB, P, rounds_of<NB, P>()>(s.sc, lane, m);
+        // FP32 dequantise (one rounded multiply) and FP32 sum in shard order
+        float2 S[NF];
+        weighted_sum<P, NF>(s.q, m, S);
+        const float mx = group_max<LPB>(lane_max_abs<NF>(S));
+        float qs, m_new;
+        agoq_scales(mx, qs, m_new);
+        uint4 oq[NF / 8];
+        encode_codes<NF>(S, qs, oq);
+        if (s.valid) {
+#pragma unroll
+            for (int h = 0; h < NF / 8; ++h)
+                stg128_stream(out_codes + s.off + 16 * h, oq[h]);
+            if (lane % LPB == 0)
+                out_scale[s.blk] = m_new;
         }
-        return;
-    }
-    load_slot<NB, P, false>(in, base, lane, total, a);
-    while (base < total) {
-        load_slot<NB, P, false>(in, base + stride, lane, total, b);
-        agoq_reduce_slot<NB, P>(a, lane, out_codes, out_scale);
-        base += stride;
-        if (base >= total)
-            break;
-        load_slot<NB, P, false>(in, base + stride, lane, total, a);
-        agoq_reduce_slot<NB, P>(b, lane, out_codes, out_scale);
-        base += stride;
-    }
+    });
 }
 
 // ------------------------------------------------- AGoQ accumulate --
@@ -305,7 +297,7 @@ cudaError_t run_taco_reduce(const ShardPtrs &in, int64_t nblocks, float e_target
                             uint8_t *oc, float *oa, float *os, cudaStream_t st)
 {
     int grid = 0;
-    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * (NB / kLaneElems), &grid);
+    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * lanes_per_block<NB, P>(), &grid);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(taco_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, e_target, eps, oc,
@@ -316,7 +308,7 @@ template <int NB, int P>
 cudaError_t run_agoq_reduce(const ShardPtrs &in, int64_t nblocks, uint8_t *oc, float *os, cudaStream_t st)
 {
     int grid = 0;
-    cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * (NB / kLaneElems), &grid);
+    cudaError_t e = grid_for(agoq_reduce_kernel<NB, P>, nblocks * lanes_per_block<NB, P>(), &grid);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(agoq_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, oc, os);

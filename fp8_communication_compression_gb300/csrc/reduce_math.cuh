@@ -13,7 +13,11 @@
 
 namespace taco {
 
-constexpr int kLaneElems = 32;
+constexpr int kLaneElems = 32;  // elements per lane in the default layout
+
+// A lane holds NF float2 registers: 16 (32 elements) or 8 (16 elements).
+// Everything below is written so that a block's statistics come out
+// bit-identical in either layout.
 
 // 16 E4M3 codes -> 8 float2 (element order), exact.
 __device__ __forceinline__ void decode16_f2(const uint4 q, float2 *d)
@@ -26,18 +30,21 @@ __device__ __forceinline__ void decode16_f2(const uint4 q, float2 *d)
     }
 }
 
-__device__ __forceinline__ void decode32_f2(const uint4 (&q)[2], float2 (&d)[16])
+template <int NF> __device__ __forceinline__ void decode_codes(const uint4 (&q)[NF / 8], float2 (&d)[NF])
 {
-    decode16_f2(q[0], d);
-    decode16_f2(q[1], d + 8);
+#pragma unroll
+    for (int h = 0; h < NF / 8; ++h)
+        decode16_f2(q[h], d + 8 * h);
 }
 
-// 32 values times k -> 32 E4M3 codes (two 16-byte words).
-__device__ __forceinline__ void encode32_f2(const float2 (&v)[16], float k, uint4 (&q)[2])
+__device__ __forceinline__ void decode32_f2(const uint4 (&q)[2], float2 (&d)[16]) { decode_codes<16>(q, d); }
+
+// NF float2 values times k -> E4M3 codes (NF / 8 16-byte words).
+template <int NF> __device__ __forceinline__ void encode_codes(const float2 (&v)[NF], float k, uint4 (&q)[NF / 8])
 {
     const float2 k2 = make_float2(k, k);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NF / 8; ++h) {
         float2 p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -49,56 +56,68 @@ __device__ __forceinline__ void encode32_f2(const float2 (&v)[16], float k, uint
     }
 }
 
-__device__ __forceinline__ void load32_codes(const uint8_t *p, bool valid, uint4 (&q)[2])
+__device__ __forceinline__ void encode32_f2(const float2 (&v)[16], float k, uint4 (&q)[2]) { encode_codes<16>(v, k, q); }
+
+template <int NF> __device__ __forceinline__ void load_codes(const uint8_t *p, bool valid, uint4 (&q)[NF / 8])
 {
-    q[0] = valid ? ldg128_stream(p) : make_uint4(0, 0, 0, 0);
-    q[1] = valid ? ldg128_stream(p + 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int h = 0; h < NF / 8; ++h)
+        q[h] = valid ? ldg128_stream(p + 16 * h) : make_uint4(0, 0, 0, 0);
 }
 
+__device__ __forceinline__ void load32_codes(const uint8_t *p, bool valid, uint4 (&q)[2]) { load_codes<16>(p, valid, q); }
+
 // S = sum_p decode(q_p) * w_p over a compile-time number of shards, in shard
-// order; every product is rounded before it is added, so shards that cancel
+// order.  Every product is rounded before it is added (__fmul_rn / __fadd_rn
+// are never contracted into a fused multiply-add), so shards that cancel
 // exactly sum to exactly zero.
-template <int P>
-__device__ __forceinline__ void weighted_sum(const uint4 (&q)[P][2], const float (&w)[P], float2 (&S)[16])
+template <int P, int NF>
+__device__ __forceinline__ void weighted_sum(const uint4 (&q)[P][NF / 8], const float (&w)[P], float2 (&S)[NF])
 {
-    decode32_f2(q[0], S);
+    decode_codes<NF>(q[0], S);
     const float2 w0 = make_float2(w[0], w[0]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < NF; ++i)
         S[i] = mul2_rounded(S[i], w0);
 #pragma unroll
     for (int p = 1; p < P; ++p) {
-        float2 d[16];
-        decode32_f2(q[p], d);
+        float2 d[NF];
+        decode_codes<NF>(q[p], d);
         const float2 wp = make_float2(w[p], w[p]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < NF; ++i)
             S[i] = add2_rounded(S[i], mul2_rounded(d[i], wp));
     }
 }
 
 // Adds shard p (p > 0) or starts the sum (p == 0): the run-time-P form of
 // weighted_sum, with the same rounding.
-__device__ __forceinline__ void weighted_sum_step(const uint4 (&q)[2], float w, bool first, float2 (&S)[16])
+template <int NF>
+__device__ __forceinline__ void weighted_sum_step(const uint4 (&q)[NF / 8], float w, bool first, float2 (&S)[NF])
 {
-    float2 d[16];
-    decode32_f2(q, d);
+    float2 d[NF];
+    decode_codes<NF>(q, d);
     const float2 w2 = make_float2(w, w);
     if (first) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < NF; ++i)
             S[i] = mul2_rounded(d[i], w2);
     } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < NF; ++i)
             S[i] = add2_rounded(S[i], mul2_rounded(d[i], w2));
     }
 }
 
+// Sum over the LPB lanes of a group.  The xor butterfly runs in ascending
+// order (1, 2, 4, ...), which adds aligned neighbours first: with partial
+// sums p_0, p_1, ... in element order the result is the balanced tree
+// ((p_0 + p_1) + (p_2 + p_3)) + ..., whatever the number of partials per
+// lane (floating-point addition is commutative).
 template <int LPB> __device__ __forceinline__ float group_sum(float v)
 {
 #pragma unroll
-    for (int o = LPB / 2; o >= 1; o >>= 1)
+    for (int o = 1; o < LPB; o <<= 1)
         v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
 }
@@ -111,39 +130,46 @@ template <int LPB> __device__ __forceinline__ float group_max(float v)
     return v;
 }
 
-// Largest |value| of the lane's 32 values.
-__device__ __forceinline__ float lane_max_abs(const float2 (&S)[16])
+// Largest |value| of the lane's values.
+template <int NF> __device__ __forceinline__ float lane_max_abs(const float2 (&S)[NF])
 {
     float m[2] = {0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < NF; ++i)
         m[i & 1] = fmaxf(m[i & 1], fmaxf(fabsf(S[i].x), fabsf(S[i].y)));
     return fmaxf(m[0], m[1]);
 }
 
-// Sum of squares of the lane's 32 values (packed accumulators).
-__device__ __forceinline__ float lane_sum_squares(const float2 (&S)[16])
+// Sum of squares of 16 consecutive elements (8 float2), in one fixed order.
+__device__ __forceinline__ float sum_squares16(const float2 *S)
 {
-    float2 a = __fmul2_rn(S[0], S[0]), b = __fmul2_rn(S[1], S[1]);
+    float2 a = __fmul2_rn(S[0], S[0]);
 #pragma unroll
-    for (int i = 2; i < 16; i += 2) {
+    for (int i = 1; i < 8; ++i)
         a = __ffma2_rn(S[i], S[i], a);
-        b = __ffma2_rn(S[i + 1], S[i + 1], b);
-    }
-    const float2 c = __fadd2_rn(a, b);
-    return c.x + c.y;
+    return a.x + a.y;
+}
+
+// The lane's share of the block's sum of squares: its 16-element partials
+// added in pairs (see group_sum for how the lanes' shares combine).
+template <int NF> __device__ __forceinline__ float lane_sum_squares(const float2 (&S)[NF])
+{
+    if constexpr (NF == 8)
+        return sum_squares16(S);
+    else
+        return sum_squares16(S) + sum_squares16(S + 8);
 }
 
 // TACO re-compression of the Hadamard-domain sum T of a block (the lane
-// holds 32 of its values; LPB lanes share the block):
+// holds 2 NF of its values; LPB lanes share the block):
 //   alpha' = sqrt(E / (|T|^2 / n + eps)),  s' = 448 / (alpha' max|T|),
 //   codes  = E4M3(alpha' s' T).
-template <int NB, int LPB>
-__device__ __forceinline__ void recompress(float2 (&T)[16], float e_target, float eps, uint4 (&codes)[2],
+template <int NB, int LPB, int NF>
+__device__ __forceinline__ void recompress(float2 (&T)[NF], float e_target, float eps, uint4 (&codes)[NF / 8],
                                            float &alpha, float &scale)
 {
-    const float ss = group_sum<LPB>(lane_sum_squares(T));
-    const float mx = group_max<LPB>(lane_max_abs(T));
+    const float ss = group_sum<LPB>(lane_sum_squares<NF>(T));
+    const float mx = group_max<LPB>(lane_max_abs<NF>(T));
     alpha = sqrtf(e_target / (ss * (1.0f / NB) + eps));
     const float M = alpha * mx;
     scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
@@ -151,11 +177,11 @@ __device__ __forceinline__ void recompress(float2 (&T)[16], float e_target, floa
     if (!(k <= FLT_MAX)) {
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < NF; ++i)
             T[i] = __fmul2_rn(T[i], a2);
         k = scale;
     }
-    encode32_f2(T, k, codes);
+    encode_codes<NF>(T, k, codes);
 }
 
 // 1 / (s alpha) of shard p's block, the weight of its decoded codes in the
