@@ -303,9 +303,10 @@ def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) 
 def laaq_leg(torch, api, peak: float) -> dict:
     """AGoQ LAAQ activation codec on a GPT-6.7B-shaped activation tensor
     (bf16 [8192, 4096]), block 128, 4/5/6/8 bits: quantize and dequantize to
-    bf16, per-launch events (inputs larger than L2 are not needed to show the
-    codec: the tensor is 67 MB, so each launch reads a fresh copy from a ring
-    of three)."""
+    bf16, timed per launch with events.  One tensor is 67 MB, below the
+    129 MB L2, so launches rotate over a ring of three inputs and outputs
+    (201 MB of inputs): each launch reads a tensor the previous two launches
+    did not touch."""
     from fp8_communication_compression_gb300 import workloads as W
 
     rows, d, block = 8192, 4096, 128
