@@ -234,20 +234,39 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-def time_launches(torch, fn, reps: int, stream) -> float:
-    """Mean CUDA-event duration (ms) of ``fn`` over ``reps`` launches."""
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    ev[0].record(stream)
-    for i in range(reps):
+def time_launches(torch, fn, reps: int, stream, replays: int = 3) -> float:
+    """Mean device time (ms) per launch of ``fn``: ``reps`` calls captured in
+    one CUDA graph, and the graph replayed ``replays`` times between two CUDA
+    events on ``stream``.  Replaying a graph keeps the host's per-call launch
+    overhead out of the figure; it matters for launches of a few tens of
+    microseconds, which the host cannot otherwise enqueue as fast as the GPU
+    runs them."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
         fn()
-        ev[i + 1].record(stream)
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            fn()
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    ms = e0.elapsed_time(e1) / (reps * replays)
+    del graph
+    return ms
 
 
 def agoq_leg(torch, api, peak: float) -> dict:
     """AGoQ accumulate over the 2^28-element buffer and the P=8 reduce of
-    2^25-element shards; inputs larger than L2, per-launch CUDA events."""
+    2^25-element shards; inputs larger than L2, timed per launch from graph
+    replays."""
     from fp8_communication_compression_gb300 import workloads as W
 
     a = W.AGOQ
@@ -280,7 +299,8 @@ def agoq_leg(torch, api, peak: float) -> dict:
 
 def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) -> dict:
     """The INT8 variant of the codec (compress all shards, decompress one
-    tensor of the same size) on the headline shards, per-launch events."""
+    tensor of the same size) on the headline shards, timed per launch from
+    graph replays."""
     n = rows * d
     nb = n // block
     codes = torch.empty((P, rows, d), dtype=torch.int8, device="cuda")
@@ -303,7 +323,7 @@ def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) 
 def laaq_leg(torch, api, peak: float) -> dict:
     """AGoQ LAAQ activation codec on a GPT-6.7B-shaped activation tensor
     (bf16 [8192, 4096]), block 128, 4/5/6/8 bits: quantize and dequantize to
-    bf16, timed per launch with events.  One tensor is 67 MB, below the
+    bf16, timed per launch from graph replays.  One tensor is 67 MB, below the
     129 MB L2, so launches rotate over a ring of three inputs and outputs
     (201 MB of inputs): each launch reads a tensor the previous two launches
     did not touch."""
@@ -345,8 +365,8 @@ def laaq_leg(torch, api, peak: float) -> dict:
 
 def gpt13b_leg(torch, api, peak: float) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
-    CUDA-event times of compress, the fused reduce + decompress, and the
-    separate reduce and decompress."""
+    device times (graph replays) of compress, the fused reduce + decompress,
+    and the separate reduce and decompress."""
     from fp8_communication_compression_gb300 import workloads as W
 
     name = "gpt13b_p8x8192x5120_n256"

@@ -266,14 +266,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
 
     const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+    // the block scalars of a tile are loaded one tile ahead
+    auto tile_block = [&](int64_t t) {
+        const int64_t grow = t * kWarpRows + lane;
+        return (grow < nrows ? grow : nrows - 1) / G;
+    };
+    float a_next = 1.0f, sc_next = 1.0f;
+    if (gw < ntiles) {
+        a_next = __ldg(alpha + tile_block(gw));
+        sc_next = __ldg(scale + tile_block(gw));
+    }
     int it = 0;
     for (int64_t t = gw; t < ntiles; t += W, ++it) {
         const int s = it % kStages;
         const int64_t wrow = t * kWarpRows;
-        const int64_t grow = wrow + lane;
-        const int64_t blk = (grow < nrows ? grow : nrows - 1) / G;
-        const float a = __ldg(alpha + blk);
-        const float sc = __ldg(scale + blk);
+        const float a = a_next, sc = sc_next;
+        if (t + W < ntiles) {
+            a_next = __ldg(alpha + tile_block(t + W));
+            sc_next = __ldg(scale + tile_block(t + W));
+        }
         // warp-uniform: if any lane's wait runs out, the whole warp stops
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
             if (lane == 0)

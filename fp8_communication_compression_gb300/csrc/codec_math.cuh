@@ -162,11 +162,16 @@ __device__ __forceinline__ void encode8(const float2 *v, float2 k2, uint32_t &w0
 
 // Four fp32 values (already scaled into [-127, 127]) -> four int8 codes,
 // round to nearest even, packed little-endian.
+// Four values already in [-127.5, 127.5) -> four int8 codes, rounded to
+// nearest even.  Adding 1.5 * 2^23 rounds a value to an integer in the low
+// mantissa bits (the float's unit in the last place is 1 there), and since
+// the low byte of 1.5 * 2^23 is zero, that byte is the two's-complement code.
 __device__ __forceinline__ uint32_t f32x4_to_s8x4(float a, float b, float c, float d)
 {
-    const int ia = __float2int_rn(a), ib = __float2int_rn(b);
-    const int ic = __float2int_rn(c), id = __float2int_rn(d);
-    const uint32_t lo = __byte_perm(ia, ib, 0x0040), hi = __byte_perm(ic, id, 0x0040);
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    const float2 p = __fadd2_rn(make_float2(a, b), magic), q = __fadd2_rn(make_float2(c, d), magic);
+    const uint32_t lo = __byte_perm(__float_as_uint(p.x), __float_as_uint(p.y), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), 0x0040);
     return __byte_perm(lo, hi, 0x5410);
 }
 

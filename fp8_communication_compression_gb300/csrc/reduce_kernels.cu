@@ -54,6 +54,10 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
 // layouts (reduce_math.cuh).
 template <int P> __host__ __device__ constexpr int elems_per_lane() { return P <= 4 ? 32 : 16; }
 
+// Whether a lane keeps its next grid-stride slot's loads in flight while it
+// processes the current one (two slots of registers).
+template <int P> __host__ __device__ constexpr bool prefetch_next() { return P <= 4; }
+
 template <int NB, int P> __host__ __device__ constexpr int lanes_per_block() { return NB / elems_per_lane<P>(); }
 
 template <int NB, int P> __host__ __device__ constexpr int rounds_of()
@@ -120,7 +124,7 @@ __device__ __forceinline__ void for_each_slot(const ShardPtrs &in, int64_t nbloc
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
     SlotOf<NB, P> a, b;
-    if constexpr (P > 4) {
+    if constexpr (!prefetch_next<P>()) {
         for (; base < total; base += stride) {
             load_slot<NB, P, WITH_ALPHA>(in, base, lane, total, a);
             process(a);
