@@ -10,8 +10,13 @@
 // are two's complement in a little-endian bit stream: element i occupies
 // bits i*b .. i*b + b - 1.
 //
+// The clamp never binds (|x q| <= qmax up to one rounding); the kernels
+// round with a magic-number addition instead of conversion instructions.
+//
 // A lane owns 32 consecutive elements of a block; its 32 codes are exactly
-// b 32-bit words of the stream, packed with compile-time shifts.
+// b 32-bit words of the stream, packed with compile-time shifts.  Each lane
+// takes several grid-stride slots per loop trip and issues all of their
+// loads before it processes the first.
 
 #include <cfloat>
 
@@ -25,7 +30,16 @@ namespace {
 
 constexpr int kLThreads = 256;
 
-template <int BITS> __device__ __forceinline__ void pack32(const int (&c)[32], uint32_t (&w)[BITS])
+// Rounding to an integer without a conversion instruction: for |v| < 2^22,
+// the float sum v + 1.5 * 2^23 has a unit in the last place of 1, so the
+// addition rounds v to the nearest integer (ties to even), and the low
+// mantissa bits of the sum hold that integer in two's complement (the low 22
+// bits of 1.5 * 2^23 are zero).
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23, bits 0x4B400000
+
+// Packs the low BITS bits of each of 32 words (the rounded sums above) into
+// the lane's BITS-word stream segment.
+template <int BITS> __device__ __forceinline__ void pack32(const uint32_t (&c)[32], uint32_t (&w)[BITS])
 {
     constexpr uint32_t kMask = (1u << BITS) - 1u;
 #pragma unroll
@@ -33,21 +47,12 @@ template <int BITS> __device__ __forceinline__ void pack32(const int (&c)[32], u
         w[j] = 0u;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const uint32_t u = static_cast<uint32_t>(c[i]) & kMask;
+        const uint32_t u = c[i] & kMask;
         const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
         w[wi] |= u << sh;
         if (sh + BITS > 32)
             w[wi + 1] |= u >> (32 - sh);
     }
-}
-
-template <int BITS> __device__ __forceinline__ int unpack_one(const uint32_t (&w)[BITS], int i)
-{
-    const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
-    uint32_t raw = w[wi] >> sh;
-    if (sh + BITS > 32)
-        raw |= w[wi + 1] << (32 - sh);
-    return static_cast<int>(raw << (32 - BITS)) >> (32 - BITS);  // sign-extend
 }
 
 // The lane's BITS words go to byte offset 4 * BITS * (lane slot): 16-byte
@@ -69,30 +74,9 @@ template <int BITS> __device__ __forceinline__ void store_words(uint8_t *dst, co
     }
 }
 
-template <int BITS> __device__ __forceinline__ void load_words(const uint8_t *src, uint32_t (&w)[BITS])
-{
-    if constexpr (BITS % 4 == 0) {
-#pragma unroll
-        for (int j = 0; j < BITS; j += 4) {
-            const uint4 q = ldg128_stream(src + 4 * j);
-            w[j] = q.x;
-            w[j + 1] = q.y;
-            w[j + 2] = q.z;
-            w[j + 3] = q.w;
-        }
-    } else if constexpr (BITS % 2 == 0) {
-#pragma unroll
-        for (int j = 0; j < BITS; j += 2) {
-            const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src + 4 * j));
-            w[j] = q.x;
-            w[j + 1] = q.y;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < BITS; ++j)
-            w[j] = __ldg(reinterpret_cast<const uint32_t *>(src) + j);
-    }
-}
+// Slots a lane loads before it processes any of them: the loads of both
+// slots (128 bytes of bf16 per lane) are in flight together.
+constexpr int kQuantSlots = 2;
 
 template <int BITS, int NB>
 __global__ void __launch_bounds__(kLThreads)
@@ -100,99 +84,144 @@ __global__ void __launch_bounds__(kLThreads)
                          float *__restrict__ scale)
 {
     constexpr int LPB = NB / 32;
+    constexpr int U = kQuantSlots;
     constexpr float kQmax = static_cast<float>((1 << (BITS - 1)) - 1);
     pdl_wait();
     pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
+    const int part = lane % LPB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
-         base += stride) {
-        const int64_t t = base + lane;
-        const bool valid = t < total;
-        const int64_t blk = valid ? t / LPB : 0;
-        const int part = lane % LPB;
-        const int64_t off = blk * NB + part * 32;
-        uint4 g[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                      make_uint4(0, 0, 0, 0)};
-        if (valid) {
+         base += U * stride) {
+        uint4 g[U][4];
+        int64_t off[U];
+        bool valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t t = base + u * stride + lane;
+            valid[u] = t < total;
+            off[u] = (valid[u] ? t / LPB : 0) * NB + part * 32;
 #pragma unroll
             for (int h = 0; h < 4; ++h)
-                g[h] = ldg128_stream(x + off + 8 * h);
+                g[u][h] = valid[u] ? ldg128_stream(x + off[u] + 8 * h) : make_uint4(0, 0, 0, 0);
         }
-        float v[32];
-        float mx = 0.0f;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const uint32_t gw[4] = {g[h].x, g[h].y, g[h].z, g[h].w};
+        for (int u = 0; u < U; ++u) {
+            float v[32];
+            float mx = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[8 * h + 2 * j] = bf16lo_to_f32(gw[j]);
-                v[8 * h + 2 * j + 1] = bf16hi_to_f32(gw[j]);
-                mx = fmaxf(mx, fmaxf(fabsf(v[8 * h + 2 * j]), fabsf(v[8 * h + 2 * j + 1])));
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t gw[4] = {g[u][h].x, g[u][h].y, g[u][h].z, g[u][h].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[8 * h + 2 * j] = bf16lo_to_f32(gw[j]);
+                    v[8 * h + 2 * j + 1] = bf16hi_to_f32(gw[j]);
+                    mx = fmaxf(mx, fmaxf(fabsf(v[8 * h + 2 * j]), fabsf(v[8 * h + 2 * j + 1])));
+                }
             }
-        }
-        const float amax = group_max<LPB>(mx);
-        float q = 1.0f, m = 1.0f;
-        if (amax > 0.0f) {
-            q = fminf(kQmax / amax, FLT_MAX);
-            m = amax / kQmax;
-        }
-        int c[32];
+            const float amax = group_max<LPB>(mx);
+            float q = 1.0f, m = 1.0f;
+            if (amax > 0.0f) {
+                q = fminf(kQmax / amax, FLT_MAX);
+                m = amax / kQmax;
+            }
+            // |x q| <= qmax up to one rounding, so the clamp to +-qmax never
+            // binds: the nearest integer of qmax (1 + 2^-23) is qmax
+            uint32_t c[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            c[i] = static_cast<int>(fminf(fmaxf(rintf(__fmul_rn(v[i], q)), -kQmax), kQmax));
-        uint32_t w[BITS];
-        pack32<BITS>(c, w);
-        if (valid) {
-            store_words<BITS>(packed + off * BITS / 8, w);
-            if (part == 0)
-                scale[blk] = m;
+            for (int i = 0; i < 32; ++i)
+                c[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[i], q), kRoundMagic));
+            uint32_t w[BITS];
+            pack32<BITS>(c, w);
+            if (valid[u]) {
+                store_words<BITS>(packed + off[u] * BITS / 8, w);
+                if (part == 0)
+                    scale[off[u] / NB] = m;
+            }
         }
     }
 }
 
+// The dequantizer's unit is 8 consecutive codes (BITS bytes of the stream);
+// adjacent lanes take adjacent units, so that a warp's code loads and its
+// 16-byte bf16 stores are both contiguous.  Returns the unit's 8 * BITS bits,
+// code 0 in the lowest.  A second 32-bit word is read only when the unit
+// reaches into it, so no load leaves the stream.
+template <int BITS> __device__ __forceinline__ uint64_t load_unit(const uint8_t *packed, int64_t unit)
+{
+    const int64_t byte = unit * BITS;
+    if constexpr (BITS == 8) {
+        return __ldg(reinterpret_cast<const unsigned long long *>(packed + byte));
+    } else if constexpr (BITS == 4) {
+        return __ldg(reinterpret_cast<const uint32_t *>(packed + byte));
+    } else {
+        const int64_t a = byte & ~static_cast<int64_t>(3);
+        const int sh = 8 * static_cast<int>(byte & 3);
+        const uint32_t lo = __ldg(reinterpret_cast<const uint32_t *>(packed + a));
+        const uint32_t hi = (sh + 8 * BITS > 32) ? __ldg(reinterpret_cast<const uint32_t *>(packed + a + 4)) : 0u;
+        return ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
+    }
+}
+
+// Code i (0..7) of a unit as an exact float: the BITS-bit field with its
+// sign bit flipped is code + 2^(BITS-1) in [0, 2^BITS); placed in the low
+// mantissa bits of 1.5 * 2^23 it gives the float 1.5 * 2^23 + code +
+// 2^(BITS-1), from which one exact subtraction leaves the code.
+template <int BITS> __device__ __forceinline__ float unit_code(uint64_t u, int i)
+{
+    constexpr uint32_t kMask = (1u << BITS) - 1u, kSign = 1u << (BITS - 1);
+    const uint32_t raw = static_cast<uint32_t>(u >> (BITS * i));
+    const float biased = __uint_as_float(((raw & kMask) ^ kSign) | 0x4B400000u);
+    return __fsub_rn(biased, kRoundMagic + static_cast<float>(kSign));
+}
+
+constexpr int kDequantUnits = 8;  // units per lane per loop trip, loads issued together
+
 template <int BITS, int NB, bool BF16OUT>
 __global__ void __launch_bounds__(kLThreads)
-    laaq_dequantize_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
-                           int64_t nblocks, void *__restrict__ out)
+    laaq_dequantize_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale, int64_t n,
+                           void *__restrict__ out)
 {
-    constexpr int LPB = NB / 32;
+    constexpr int U = kDequantUnits;
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t total = nblocks * LPB;
-    const int lane = threadIdx.x & 31;
+    const int64_t units = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
-         base += stride) {
-        const int64_t t = base + lane;
-        if (t >= total)
-            continue;
-        const int64_t blk = t / LPB;
-        const int part = lane % LPB;
-        const int64_t off = blk * NB + part * 32;
-        uint32_t w[BITS];
-        load_words<BITS>(packed + off * BITS / 8, w);
-        const float m = __ldg(scale + blk);
-        float v[32];
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < units;
+         base += U * stride) {
+        uint64_t w[U];
+        float m[U];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = __fmul_rn(static_cast<float>(unpack_one<BITS>(w, i)), m);
-        if constexpr (BF16OUT) {
-            uint16_t *o = static_cast<uint16_t *>(out) + off;
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = base + u * stride;
+            w[u] = 0;
+            m[u] = 1.0f;
+            if (j < units) {
+                w[u] = load_unit<BITS>(packed, j);
+                m[u] = __ldg(scale + j * 8 / NB);
+            }
+        }
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
-                stg128_stream(o + 8 * h, make_uint4(f32x2_to_bf16x2(v[8 * h], v[8 * h + 1]),
-                                                    f32x2_to_bf16x2(v[8 * h + 2], v[8 * h + 3]),
-                                                    f32x2_to_bf16x2(v[8 * h + 4], v[8 * h + 5]),
-                                                    f32x2_to_bf16x2(v[8 * h + 6], v[8 * h + 7])));
-        } else {
-            float *o = static_cast<float *>(out) + off;
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = base + u * stride;
+            if (j >= units)
+                break;
+            float v[8];
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-                stg128_stream(o + 4 * h, make_uint4(__float_as_uint(v[4 * h]), __float_as_uint(v[4 * h + 1]),
-                                                    __float_as_uint(v[4 * h + 2]),
-                                                    __float_as_uint(v[4 * h + 3])));
+            for (int i = 0; i < 8; ++i)
+                v[i] = __fmul_rn(unit_code<BITS>(w[u], i), m[u]);
+            if constexpr (BF16OUT) {
+                stg128_stream(static_cast<uint16_t *>(out) + 8 * j,
+                              make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]),
+                                         f32x2_to_bf16x2(v[4], v[5]), f32x2_to_bf16x2(v[6], v[7])));
+            } else {
+                float *o = static_cast<float *>(out) + 8 * j;
+                stg128_stream(o, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                            __float_as_uint(v[3])));
+                stg128_stream(o + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]),
+                                                __float_as_uint(v[6]), __float_as_uint(v[7])));
+            }
         }
     }
 }
@@ -229,17 +258,17 @@ cudaError_t run_dequantize(const uint8_t *packed, const float *scale, int64_t n,
                            cudaStream_t st)
 {
     int grid = 0;
-    const int64_t nb = n / NB;
+    const int64_t lanes = (n / 8 + kDequantUnits - 1) / kDequantUnits;
     if (bf16) {
-        cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, true>, nb * (NB / 32), &grid);
+        cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, true>, lanes, &grid);
         if (e != cudaSuccess)
             return e;
-        return launch_pdl(laaq_dequantize_kernel<BITS, NB, true>, grid, kLThreads, 0, st, packed, scale, nb, out);
+        return launch_pdl(laaq_dequantize_kernel<BITS, NB, true>, grid, kLThreads, 0, st, packed, scale, n, out);
     }
-    cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, false>, nb * (NB / 32), &grid);
+    cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, false>, lanes, &grid);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(laaq_dequantize_kernel<BITS, NB, false>, grid, kLThreads, 0, st, packed, scale, nb, out);
+    return launch_pdl(laaq_dequantize_kernel<BITS, NB, false>, grid, kLThreads, 0, st, packed, scale, n, out);
 }
 
 template <int BITS>

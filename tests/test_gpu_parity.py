@@ -276,6 +276,23 @@ def test_laaq_codec_is_bit_identical_to_the_oracle(bits, block):
     assert np.array_equal(to_host(out16.view(torch.int16)).view(np.uint16), W.f32_to_bf16_bits(ref))
 
 
+@pytest.mark.parametrize("bits,block", [(4, 128), (5, 32), (6, 256), (8, 64)])
+def test_laaq_codec_many_slots_per_lane(bits, block):
+    """8.4 M elements: more lanes than one grid holds, so each lane takes
+    several grid-stride slots per loop trip, and the last trip is ragged
+    (some of its slots past the end)."""
+    rows, d = 2051, 4096
+    n = rows * d
+    x = W.tp_activation(520 + bits, rows, d, channel_scale=True, zero_blocks=(5,), block=block)
+    packed, scale = api.agoq_laaq_quantize(to_dev_bf16(x).reshape(-1), block, bits)
+    rp, rs = oracle.laaq_quantize(x, block, bits)
+    assert np.array_equal(to_host(packed), rp)
+    assert np.array_equal(to_host(scale), rs)
+    out16 = api.agoq_laaq_dequantize(packed, scale, n, block, bits, out_dtype=torch.bfloat16)
+    ref = oracle.laaq_dequantize(rp, rs, n, block, bits)
+    assert np.array_equal(to_host(out16.view(torch.int16)).view(np.uint16), W.f32_to_bf16_bits(ref))
+
+
 # ----------------------------------------------- full-size workloads --
 
 def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None, block: int):
