@@ -262,6 +262,18 @@ def agoq_laaq_dequantize(packed: torch.Tensor, scale: torch.Tensor, n: int, bloc
     return out
 
 
+def taco_e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 [n] -> E4M3FN codes uint8 [n] (round to nearest even, saturating at +-448)."""
+    _need(x, "x", (torch.float32,))
+    n = x.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=x.device)
+    _need(out, "out", (torch.uint8,), n)
+    st = _lib.load().taco_e4m3_encode(x.data_ptr(), n, out.data_ptr(), _stream_handle(stream))
+    _lib.check("taco_e4m3_encode", st)
+    return out
+
+
 def taco_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))

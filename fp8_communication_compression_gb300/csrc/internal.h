@@ -53,6 +53,8 @@ cudaError_t launch_laaq_quantize(const void *x_bf16, int64_t n, int block, int b
 cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
                                    void *out, bool out_bf16, cudaStream_t stream);
 
+cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *codes, cudaStream_t stream);
+
 cudaError_t read_codec_error(uint32_t *flags, bool clear);
 
 // Launches `kernel` with programmatic stream serialization allowed, so that

@@ -145,22 +145,29 @@ __global__ void __launch_bounds__(kLThreads)
 
 // The dequantizer's unit is 8 consecutive codes (BITS bytes of the stream);
 // adjacent lanes take adjacent units, so that a warp's code loads and its
-// 16-byte bf16 stores are both contiguous.  Returns the unit's 8 * BITS bits,
-// code 0 in the lowest.  A second 32-bit word is read only when the unit
-// reaches into it, so no load leaves the stream.
-template <int BITS> __device__ __forceinline__ uint64_t load_unit(const uint8_t *packed, int64_t unit)
+// 16-byte bf16 stores are both contiguous.  A unit's 8 * BITS bits are held
+// as two 32-bit words, code 0 in the lowest bits of lo.  A second word is
+// read only when the unit reaches into it, so no load leaves the stream.
+struct UnitBits {
+    uint32_t lo, hi;
+};
+
+template <int BITS> __device__ __forceinline__ UnitBits load_unit(const uint8_t *packed, int64_t unit)
 {
     const int64_t byte = unit * BITS;
     if constexpr (BITS == 8) {
-        return __ldg(reinterpret_cast<const unsigned long long *>(packed + byte));
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(packed + byte));
+        return {v.x, v.y};
     } else if constexpr (BITS == 4) {
-        return __ldg(reinterpret_cast<const uint32_t *>(packed + byte));
+        return {__ldg(reinterpret_cast<const uint32_t *>(packed + byte)), 0u};
     } else {
         const int64_t a = byte & ~static_cast<int64_t>(3);
-        const int sh = 8 * static_cast<int>(byte & 3);
-        const uint32_t lo = __ldg(reinterpret_cast<const uint32_t *>(packed + a));
-        const uint32_t hi = (sh + 8 * BITS > 32) ? __ldg(reinterpret_cast<const uint32_t *>(packed + a + 4)) : 0u;
-        return ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
+        const uint32_t sh = 8u * static_cast<uint32_t>(byte & 3);
+        const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(packed + a));
+        // a unit of 5 or 6 bytes starting at byte offset sh / 8 <= 3 of w0
+        // always reaches into the next word
+        const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(packed + a + 4));
+        return {__funnelshift_r(w0, w1, sh), w1 >> sh};
     }
 }
 
@@ -168,11 +175,20 @@ template <int BITS> __device__ __forceinline__ uint64_t load_unit(const uint8_t 
 // sign bit flipped is code + 2^(BITS-1) in [0, 2^BITS); placed in the low
 // mantissa bits of 1.5 * 2^23 it gives the float 1.5 * 2^23 + code +
 // 2^(BITS-1), from which one exact subtraction leaves the code.
-template <int BITS> __device__ __forceinline__ float unit_code(uint64_t u, int i)
+template <int BITS> __device__ __forceinline__ float unit_code(const UnitBits &u, int i)
 {
     constexpr uint32_t kMask = (1u << BITS) - 1u, kSign = 1u << (BITS - 1);
-    const uint32_t raw = static_cast<uint32_t>(u >> (BITS * i));
-    const float biased = __uint_as_float(((raw & kMask) ^ kSign) | 0x4B400000u);
+    const int bit = BITS * i;
+    uint32_t raw;
+    if (bit + BITS <= 32)
+        raw = u.lo >> bit;
+    else if (bit >= 32)
+        raw = u.hi >> (bit - 32);
+    else
+        raw = __funnelshift_r(u.lo, u.hi, bit);
+    // (raw & mask) has no bit in common with 1.5 * 2^23, so the sign flip and
+    // the exponent bits go in with one exclusive or
+    const float biased = __uint_as_float((raw & kMask) ^ (kSign | 0x4B400000u));
     return __fsub_rn(biased, kRoundMagic + static_cast<float>(kSign));
 }
 
@@ -190,12 +206,12 @@ __global__ void __launch_bounds__(kLThreads)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < units;
          base += U * stride) {
-        uint64_t w[U];
+        UnitBits w[U];
         float m[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t j = base + u * stride;
-            w[u] = 0;
+            w[u] = {0u, 0u};
             m[u] = 1.0f;
             if (j < units) {
                 w[u] = load_unit<BITS>(packed, j);

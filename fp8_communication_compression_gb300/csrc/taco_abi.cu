@@ -358,6 +358,21 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream)
+{
+    if (n < 0)
+        return TACO_ERR_INVALID_ARG;
+    if (n == 0)
+        return TACO_OK;
+    if (!x || !codes)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16))
+        return TACO_ERR_MISALIGNED;
+    if (overlap(x, 4 * static_cast<uint64_t>(n), codes, static_cast<uint64_t>(n)))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_e4m3_encode(x, n, codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 taco_status taco_device_error(uint32_t *flags_out, int32_t clear)
 {
     if (!flags_out)

@@ -34,7 +34,8 @@
  *    exception crosses the ABI.  Kernels never wait without a time limit;
  *    a wait that runs out records a flag read by taco_device_error().
  *  - Empty input (rows == 0 or n == 0) returns TACO_OK without a launch.
- *  - Inputs must be finite; NaN or Inf input gives unspecified codes.
+ *  - Inputs must be finite; NaN or Inf input gives unspecified codes
+ *    (taco_e4m3_encode states its own handling of them).
  */
 #ifndef TACO_H
 #define TACO_H
@@ -223,6 +224,21 @@ taco_status agoq_laaq_quantize(const void *x_bf16, int64_t n, int32_t block, int
 taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n,
                                  int32_t block, int32_t bits, void *out, int32_t out_is_bf16,
                                  taco_stream_t stream);
+
+/*
+ * taco_e4m3_encode - the compressor's FP8 encoder on its own ([TACO] 2.A:
+ * the E4M3 format of the codes; 2.B.2: codes are taken with saturation at
+ * the largest finite value).  codes[i] = E4M3FN(x[i]): round to nearest,
+ * ties to even; |x| >= 448 (including +-Inf) gives +-448 (0x7E / 0xFE); a
+ * value that rounds to zero keeps its sign (0x00 / 0x80); NaN gives a NaN
+ * code (0x7F / 0xFF).  This is the conversion that step (5) of
+ * taco_compress applies to y * scale.
+ *
+ *  x        in   fp32 [n], 16-byte aligned
+ *  n             n >= 0
+ *  codes    out  uint8 [n], 16-byte aligned, not overlapping x
+ */
+taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream);
 
 /*
  * taco_device_error - watchdog flags of the kernels on the current device.

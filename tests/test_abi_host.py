@@ -156,3 +156,14 @@ def test_laaq_validation(lib):
     assert d(out=A * 16 + 2) == MISALIGNED
     assert d(out=A * 4) == INVALID  # output overlaps the packed codes
     assert d(n=0) == OK
+
+
+def test_e4m3_encode_validation(lib):
+    f = lambda n=1024, x=A, c=A * 8: lib.taco_e4m3_encode(x, n, c, None)
+    assert f(n=-1) == INVALID
+    assert f(n=0) == OK
+    assert f(x=0) == INVALID
+    assert f(c=0) == INVALID
+    assert f(x=A + 4) == MISALIGNED
+    assert f(c=A * 8 + 8) == MISALIGNED
+    assert f(c=A + 1024) == INVALID  # codes overlap the input

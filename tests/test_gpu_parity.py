@@ -293,6 +293,64 @@ def test_laaq_codec_many_slots_per_lane(bits, block):
     assert np.array_equal(to_host(out16.view(torch.int16)).view(np.uint16), W.f32_to_bf16_bits(ref))
 
 
+# ------------------------------------------------------ E4M3 encoder --
+
+def oracle_e4m3_thresholds() -> np.ndarray:
+    """T[m] (m = 1 .. 126): the bit pattern of the smallest non-negative fp32
+    value that the oracle's encoder maps to a magnitude code >= m.  Found by
+    bisection over the bit patterns of non-negative floats, whose order is
+    the order of their values; the nearest-value encoder is monotone in the
+    value, so one threshold per code describes it on all 2^31 patterns."""
+    T = np.zeros(127, dtype=np.int64)
+    start = 0
+    for m in range(1, 127):
+        lo, hi = start, 0x7F800000  # +Inf saturates to magnitude 126
+        while lo < hi:
+            mid = (lo + hi) // 2
+            v = float(np.array([mid], dtype=np.uint32).view(np.float32)[0])
+            if (oracle.e4m3_encode(v) & 0x7F) >= m:
+                hi = mid
+            else:
+                lo = mid + 1
+        T[m] = start = lo
+    return T
+
+
+def test_e4m3_encoder_matches_the_oracle_on_every_fp32_pattern():
+    """All 2^32 fp32 bit patterns through taco_e4m3_encode (the conversion the
+    codec kernels use), against the oracle's encoder: its per-code thresholds
+    for every non-NaN pattern, and NaN codes for NaN patterns."""
+    T = torch.tensor(oracle_e4m3_thresholds(), dtype=torch.int64, device="cuda")
+    chunk = 1 << 28
+    for c in range(1 << 4):
+        bits = torch.arange(c * chunk, (c + 1) * chunk, dtype=torch.int64, device="cuda")
+        x = torch.where(bits >= 1 << 31, bits - (1 << 32), bits).to(torch.int32).view(torch.float32)
+        codes = api.taco_e4m3_encode(x).to(torch.int64)
+        mag = bits & 0x7FFFFFFF
+        nan = mag > 0x7F800000
+        expect = ((bits >> 31) << 7) | (torch.bucketize(mag, T, right=True) - 1)
+        assert torch.equal(codes[~nan], expect[~nan]), f"chunk {c}"
+        assert torch.all((codes[nan] & 0x7F) == 0x7F), f"chunk {c}: NaN"
+        del bits, x, codes, mag, nan, expect
+
+
+def test_e4m3_encoder_direct_oracle_sample_and_ragged_tail():
+    """A direct check of the thresholds above: random bit patterns and the
+    format's special values, encoded one by one by the oracle, with a length
+    that leaves a ragged tail of 3 values."""
+    g = np.random.default_rng(7)
+    bits = g.integers(0, 1 << 32, size=20003, dtype=np.uint64).astype(np.uint32)
+    special = np.array([0.0, -0.0, 448.0, -448.0, 464.0, 480.0, 1e30, np.inf, -np.inf, 2.0 ** -9,
+                        2.0 ** -10, 2.0 ** -10 * 1.0000001, 0.5 * (416 + 448), -0.5 * (416 + 448)],
+                       dtype=np.float32).view(np.uint32)
+    bits[:special.size] = special
+    v = bits.view(np.float32)
+    v = v[~np.isnan(v)]
+    v = np.ascontiguousarray(v[:len(v) - len(v) % 8 - 5])  # n % 8 == 3
+    got = to_host(api.taco_e4m3_encode(torch.from_numpy(v).cuda()))
+    assert np.array_equal(got, oracle.e4m3_encode_array(v))
+
+
 # ----------------------------------------------- full-size workloads --
 
 def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None, block: int):
