@@ -414,7 +414,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks of the host pipeline")
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="row chunks of the host pipeline")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows per shard")
     ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -566,7 +566,7 @@ def main():
             "e2e": None if e2e_ms is None else {
                 "value": whole_job_gbs(step_bytes, args.e2e_steps, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
-                "api": f"HostPipeline.run (pinned host in/out, {pipe.C} row chunks on 3 streams)"},
+                "api": f"taco_host_pipeline_run via HostPipeline.run (pinned host in/out, {pipe.C} row chunks on 3 streams)"},
             "other_workloads": extra,
             "gpu_launches": len(launches) * K,
             "clocks": clk,

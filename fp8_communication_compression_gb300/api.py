@@ -364,77 +364,52 @@ class TwoShotLocal:
 
 
 class HostPipeline:
-    """The two-shot local path between pinned HOST buffers, overlapped.
+    """The two-shot local path between pinned HOST buffers, overlapped: a
+    handle on the library's native host pipeline (taco_host_pipeline_*).
 
-    The rows are split into ``chunks`` equal chunks.  Chunk c is copied in
-    (all P shards) on one stream, compressed, reduced and decompressed on a
-    second, and its result copied out on a third, so host-to-device copies,
-    kernels and device-to-host copies of different chunks run at the same
-    time.  Consecutive calls are chained chunk by chunk through events (the
-    next call's copy-in of chunk c waits only for this call's compression of
-    chunk c, its decompression of chunk c only for this call's copy-out of
-    chunk c), so one call's copy-out overlaps the next call's copy-in.  Only
-    the first call waits for work already queued on the caller's stream;
-    every call makes the caller's stream wait for its result.  Device
-    buffers are chunk-major and allocated once; the result is identical to
-    ``TwoShotLocal.run`` on the same data."""
+    The rows are split into ``chunks`` chunks (the last may be shorter).
+    For each chunk, one 2-D copy gathers its rows of all P shards to the
+    device, compress, reduce and decompress run on a second stream, and the
+    result is copied back on a third, so copies in, kernels and copies out
+    of different chunks overlap.  Consecutive runs overlap chunk by chunk.
+    The first run is ordered after the work queued on the current stream;
+    every run makes the current stream wait for its result, which equals
+    ``TwoShotLocal.run`` on the same data.  The device workspace is
+    allocated once here (torch), the streams and events by the library."""
 
-    def __init__(self, P: int, rows: int, d: int, block: int = 128, chunks: int = 8, device="cuda",
+    def __init__(self, P: int, rows: int, d: int, block: int = 128, chunks: int = 4, device="cuda",
                  e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32):
-        while chunks > 1 and rows % chunks:
-            chunks -= 1
-        self.P, self.rows, self.d, self.block, self.C = P, rows, d, block, chunks
-        self.R = rows // chunks
-        self.e_target, self.eps = e_target, eps
-        C, R = chunks, self.R
-        nb = R * d // block
-        self.x = torch.empty((C, P, R, d), dtype=torch.bfloat16, device=device)
-        self.codes = torch.empty((C, P, R, d), dtype=torch.uint8, device=device)
-        self.alpha = torch.empty((C, P, nb), dtype=torch.float32, device=device)
-        self.scale = torch.empty((C, P, nb), dtype=torch.float32, device=device)
-        self.r_codes = torch.empty((C, R, d), dtype=torch.uint8, device=device)
-        self.r_alpha = torch.empty((C, nb), dtype=torch.float32, device=device)
-        self.r_scale = torch.empty((C, nb), dtype=torch.float32, device=device)
-        self.out = torch.empty((C, R, d), dtype=out_dtype, device=device)
-        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
-        self.ev_in = [torch.cuda.Event() for _ in range(C)]          # chunk copied in
-        self.ev_compressed = [torch.cuda.Event() for _ in range(C)]  # chunk's input consumed
-        self.ev_done = [torch.cuda.Event() for _ in range(C)]        # chunk's result ready
-        self.ev_out = [torch.cuda.Event() for _ in range(C)]         # chunk copied out
-        self._started = False
-        self._lists = [(list(self.codes[c]), list(self.alpha[c]), list(self.scale[c])) for c in range(C)]
+        self.P, self.rows, self.d, self.block = P, rows, d, block
+        self.e_target, self.eps, self.out_dtype = e_target, eps, out_dtype
+        c = max(1, min(chunks, rows))
+        self.R = -(-rows // c)
+        self.C = -(-rows // self.R)
+        self._h = None
+        lib = _lib.load()
+        h, ws = ctypes.c_void_p(), ctypes.c_uint64()
+        with torch.cuda.device(torch.device(device)):
+            st = lib.taco_host_pipeline_create(P, rows, d, block, chunks, int(out_dtype == torch.bfloat16),
+                                               ctypes.byref(h), ctypes.byref(ws))
+            _lib.check("taco_host_pipeline_create", st)
+            self._h = h
+            self.workspace = torch.empty(ws.value, dtype=torch.uint8, device=device)
 
-    def run(self, x_host: torch.Tensor, out_host: torch.Tensor) -> torch.Tensor:
-        """x_host: pinned bf16 [P, rows, d]; out_host: pinned [rows, d]."""
-        s_in, s_comp, s_out = self.streams
-        cur = torch.cuda.current_stream()
-        if not self._started:
-            for s in self.streams:
-                s.wait_stream(cur)
-        R = self.R
-        for c in range(self.C):
-            with torch.cuda.stream(s_in):
-                if self._started:
-                    s_in.wait_event(self.ev_compressed[c])
-                for p in range(self.P):
-                    self.x[c, p].copy_(x_host[p, c * R:(c + 1) * R], non_blocking=True)
-                self.ev_in[c].record(s_in)
-            s_comp.wait_event(self.ev_in[c])
-            codes, alpha, scale = self._lists[c]
-            taco_compress(self.x[c], self.block, self.e_target, self.eps, self.codes[c],
-                          self.alpha[c], self.scale[c], stream=s_comp)
-            self.ev_compressed[c].record(s_comp)
-            taco_reduce_shards(codes, alpha, scale, self.block, self.e_target, self.eps,
-                               self.r_codes[c], self.r_alpha[c], self.r_scale[c], stream=s_comp)
-            if self._started:
-                s_comp.wait_event(self.ev_out[c])
-            taco_decompress(self.r_codes[c], self.r_alpha[c], self.r_scale[c], self.block,
-                            out=self.out[c], stream=s_comp)
-            self.ev_done[c].record(s_comp)
-            s_out.wait_event(self.ev_done[c])
-            with torch.cuda.stream(s_out):
-                out_host[c * R:(c + 1) * R].copy_(self.out[c], non_blocking=True)
-                self.ev_out[c].record(s_out)
-        self._started = True
-        cur.wait_stream(s_out)
+    def run(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
+        """x_host: pinned bf16 [P, rows, d]; out_host: pinned [rows, d] of out_dtype."""
+        for t, name, dt, shape in ((x_host, "x_host", torch.bfloat16, (self.P, self.rows, self.d)),
+                                   (out_host, "out_host", self.out_dtype, (self.rows, self.d))):
+            if t.device.type != "cpu" or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor {dt} {shape}")
+        st = _lib.load().taco_host_pipeline_run(self._h, x_host.data_ptr(), out_host.data_ptr(),
+                                                self.workspace.data_ptr(), self.e_target, self.eps,
+                                                _stream_handle(stream))
+        _lib.check("taco_host_pipeline_run", st)
         return out_host
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            try:
+                _lib.load().taco_host_pipeline_destroy(self._h)
+            except Exception:
+                pass
+            self._h = None

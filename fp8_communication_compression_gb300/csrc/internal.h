@@ -55,6 +55,17 @@ cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, in
 
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *codes, cudaStream_t stream);
 
+// Chunked host-buffer pipeline of the two-shot local path (host_pipeline.cu).
+struct HostPipeline;
+int host_pipeline_max_chunks();
+cudaError_t host_pipeline_create(int P, int64_t rows, int64_t d, int block, int chunks, bool out_bf16,
+                                 HostPipeline **out, uint64_t *workspace_bytes);
+void host_pipeline_destroy(HostPipeline *p);
+int host_pipeline_device(const HostPipeline *p);
+uint64_t host_pipeline_workspace(const HostPipeline *p);
+cudaError_t host_pipeline_run(HostPipeline *p, const void *x_host, void *out_host, void *workspace, float e_target,
+                              float eps, cudaStream_t stream);
+
 cudaError_t read_codec_error(uint32_t *flags, bool clear);
 
 // Launches `kernel` with programmatic stream serialization allowed, so that

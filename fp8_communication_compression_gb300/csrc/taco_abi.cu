@@ -1,10 +1,13 @@
 // C ABI of the library (include/taco.h): argument validation on the host,
 // then one kernel launch on the caller's stream.  No allocation, no
-// synchronisation, no exception crosses this boundary.
+// synchronisation, no exception crosses this boundary.  The host pipeline
+// calls are the exception their declarations state: a pipeline owns CUDA
+// streams and events, and one run enqueues copies and launches per chunk.
 
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <new>
 
 #include "../../include/taco.h"
 #include "internal.h"
@@ -371,6 +374,64 @@ taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_str
     if (overlap(x, 4 * static_cast<uint64_t>(n), codes, static_cast<uint64_t>(n)))
         return TACO_ERR_INVALID_ARG;
     return from_cuda(taco::launch_e4m3_encode(x, n, codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+struct taco_host_pipeline {
+    taco::HostPipeline *impl;
+};
+
+taco_status taco_host_pipeline_create(int32_t P, int64_t rows, int64_t d, int32_t block, int32_t chunks,
+                                      int32_t out_is_bf16, taco_host_pipeline **pipe_out,
+                                      uint64_t *workspace_bytes)
+{
+    if (!pipe_out || !workspace_bytes)
+        return TACO_ERR_INVALID_ARG;
+    *pipe_out = nullptr;
+    taco_status st = check_taco_shape(rows, d, block);
+    if (st != TACO_OK)
+        return st;
+    if (P < 1 || P > TACO_MAX_SHARDS)
+        return TACO_ERR_UNSUPPORTED;
+    if (rows < 1 || chunks < 1 || chunks > taco::host_pipeline_max_chunks())
+        return TACO_ERR_INVALID_ARG;
+    auto *h = new (std::nothrow) taco_host_pipeline{nullptr};
+    if (!h)
+        return TACO_ERR_CUDA;
+    const int c = static_cast<int>(chunks < rows ? chunks : rows);
+    cudaError_t e = taco::host_pipeline_create(P, rows, d, block, c, out_is_bf16 != 0, &h->impl, workspace_bytes);
+    if (e != cudaSuccess) {
+        delete h;
+        return TACO_ERR_CUDA;
+    }
+    *pipe_out = h;
+    return TACO_OK;
+}
+
+taco_status taco_host_pipeline_run(taco_host_pipeline *pipe, const void *x_host_bf16, void *out_host,
+                                   void *workspace, float e_target, float eps, taco_stream_t stream)
+{
+    if (!pipe || !pipe->impl || !x_host_bf16 || !out_host || !workspace)
+        return TACO_ERR_INVALID_ARG;
+    if (!positive_finite(e_target) || !positive_finite(eps))
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256))
+        return TACO_ERR_MISALIGNED;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TACO_ERR_CUDA;
+    if (dev != taco::host_pipeline_device(pipe->impl))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::host_pipeline_run(pipe->impl, x_host_bf16, out_host, workspace, e_target, eps,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status taco_host_pipeline_destroy(taco_host_pipeline *pipe)
+{
+    if (!pipe)
+        return TACO_ERR_INVALID_ARG;
+    taco::host_pipeline_destroy(pipe->impl);
+    delete pipe;
+    return TACO_OK;
 }
 
 taco_status taco_device_error(uint32_t *flags_out, int32_t clear)

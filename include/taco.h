@@ -14,7 +14,9 @@
  *  - Memory: every pointer argument is a DEVICE pointer unless stated
  *    otherwise.  The caller allocates and owns every buffer; the library
  *    never allocates, frees or synchronises, and keeps no state beyond a
- *    per-device cache of attributes and kernel settings.
+ *    per-device cache of attributes and kernel settings.  (The host
+ *    pipeline's create and destroy calls create and release CUDA streams
+ *    and events, and nothing else.)
  *  - Execution: each call validates its arguments on the host, then enqueues
  *    one kernel on `stream` and returns; results are ready when the stream
  *    reaches that point.  A NULL stream is the legacy default stream.
@@ -239,6 +241,53 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
  *  codes    out  uint8 [n], 16-byte aligned, not overlapping x
  */
 taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream);
+
+/*
+ * Host pipeline: the two-shot local path between HOST buffers, overlapped.
+ * A run computes, for a pinned bf16 host tensor x_host [P][rows][d] (P
+ * shards), decompress(reduce(compress(shard 0), ..., compress(shard P-1)))
+ * into a pinned host tensor out_host [rows][d] (fp32, or bf16 when
+ * out_is_bf16): the result of taco_compress, taco_reduce_shards and
+ * taco_decompress on the same data ([TACO] 2.B.3, the reducing rank's local
+ * path of the two-shot AllReduce, with the exchange left out).  The rows are
+ * split into chunks; one chunk's host-to-device copy (a single 2-D copy that
+ * gathers the chunk's rows of all P shards), its kernels and its
+ * device-to-host copy run on three streams, overlapping the other chunks.
+ *
+ * taco_host_pipeline_create - creates the pipeline's three CUDA streams and
+ * its events on the current device (the one exception to "the library
+ * never allocates": no device memory, only these CUDA objects and a small
+ * host object) and reports the device workspace a run needs.
+ *  P               1 .. TACO_MAX_SHARDS
+ *  rows, d, block  as for taco_compress; rows >= 1
+ *  chunks          1 .. 64 (capped at rows); chunk sizes differ by at most
+ *                  the last chunk being shorter
+ *  pipe_out        out: the new pipeline (NULL on error)
+ *  workspace_bytes out: bytes of device workspace per run
+ *
+ * taco_host_pipeline_run - enqueues one pass and returns.  workspace is a
+ * device buffer of workspace_bytes, 256-byte aligned, owned by the caller
+ * and reused by every run of this pipeline.  x_host and out_host should be
+ * pinned (page-locked) host memory: pageable memory works but its copies do
+ * not overlap.  The first run is ordered after the work already queued on
+ * `stream`; a later run of the same pipeline overlaps the previous run
+ * chunk by chunk (its copy into a chunk's workspace waits only until the
+ * previous run has compressed that chunk, its decompress only until the
+ * previous run has copied that chunk out).  Every run makes `stream` wait
+ * for its last copy-out, so out_host is complete when `stream` reaches that
+ * point.  Must be called on the device the pipeline was created on.  After
+ * a TACO_ERR_CUDA return the pipeline should be destroyed.
+ *
+ * taco_host_pipeline_destroy - releases the streams and events; work
+ * already enqueued completes.
+ */
+typedef struct taco_host_pipeline taco_host_pipeline;
+taco_status taco_host_pipeline_create(int32_t P, int64_t rows, int64_t d, int32_t block, int32_t chunks,
+                                      int32_t out_is_bf16, taco_host_pipeline **pipe_out,
+                                      uint64_t *workspace_bytes);
+taco_status taco_host_pipeline_run(taco_host_pipeline *pipe, const void *x_host_bf16, void *out_host,
+                                   void *workspace, float e_target, float eps, taco_stream_t stream);
+taco_status taco_host_pipeline_destroy(taco_host_pipeline *pipe);
 
 /*
  * taco_device_error - watchdog flags of the kernels on the current device.

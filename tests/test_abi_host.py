@@ -167,3 +167,20 @@ def test_e4m3_encode_validation(lib):
     assert f(x=A + 4) == MISALIGNED
     assert f(c=A * 8 + 8) == MISALIGNED
     assert f(c=A + 1024) == INVALID  # codes overlap the input
+
+
+def test_host_pipeline_validation(lib):
+    h, ws = ctypes.c_void_p(), ctypes.c_uint64()
+    c = lambda P=4, rows=64, d=1024, block=128, chunks=4: lib.taco_host_pipeline_create(
+        P, rows, d, block, chunks, 0, ctypes.byref(h), ctypes.byref(ws))
+    assert c(P=0) == UNSUPPORTED
+    assert c(P=17) == UNSUPPORTED
+    assert c(block=64) == UNSUPPORTED
+    assert c(d=1000) == INVALID
+    assert c(rows=0) == INVALID
+    assert c(chunks=0) == INVALID
+    assert c(chunks=65) == INVALID
+    assert h.value is None
+    assert lib.taco_host_pipeline_create(4, 64, 1024, 128, 4, 0, None, ctypes.byref(ws)) == INVALID
+    assert lib.taco_host_pipeline_run(None, A, A, A, 1.0, 1e-12, None) == INVALID
+    assert lib.taco_host_pipeline_destroy(None) == INVALID

@@ -430,6 +430,35 @@ def test_host_pipeline_equals_device_path(P, rows, d, block, chunks):
         assert torch.equal(h_out.view(torch.int32), ref.cpu().view(torch.int32))
 
 
+def test_host_pipeline_back_to_back_runs_and_bf16_output():
+    """Runs on two inputs, alternated without synchronising, so that every
+    run reuses the chunk workspace of the previous one while it may still be
+    copying out; and the bf16-output pipeline."""
+    P, rows, d, block = 4, 384, 2048, 128
+    ins, refs = [], []
+    for k in range(2):
+        bits = np.stack([W.tp_activation(450 + 10 * k + p, rows, d, channel_scale=True, block=block)
+                         for p in range(P)])
+        x = to_dev_bf16(bits).reshape(P, rows, d)
+        refs.append(api.TwoShotLocal(P, rows, d, block).run(x).cpu())
+        h = torch.empty((P, rows, d), dtype=torch.bfloat16, pin_memory=True)
+        h.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+        ins.append(h)
+    outs = [torch.empty((rows, d), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    pipe = api.HostPipeline(P, rows, d, block, chunks=5)
+    for _ in range(3):
+        for k in range(2):
+            pipe.run(ins[k], outs[k])
+    torch.cuda.synchronize()
+    for k in range(2):
+        assert torch.equal(outs[k].view(torch.int32), refs[k].view(torch.int32))
+    pb = api.HostPipeline(P, rows, d, block, chunks=3, out_dtype=torch.bfloat16)
+    ob = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
+    pb.run(ins[0], ob)
+    torch.cuda.synchronize()
+    assert torch.equal(ob.view(torch.int16), refs[0].to(torch.bfloat16).view(torch.int16))
+
+
 def test_full_size_agoq_accumulate_and_reduce():
     a = W.AGOQ
     block, n = a["block"], a["n_main"]
