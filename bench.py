@@ -66,6 +66,17 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+def spec_hbm_gbs(torch):
+    """Spec DRAM bandwidth from the device's attributes (memory clock x 2 for
+    double data rate x bus width), or None where torch does not expose them.
+    Context only: fractions are taken of the measured copy peak."""
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    clk_khz, bus_bits = getattr(p, "memory_clock_rate", None), getattr(p, "memory_bus_width", None)
+    if not clk_khz or not bus_bits:
+        return None
+    return clk_khz * 1e3 * 2 * bus_bits / 8 / 1e9
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
@@ -523,6 +534,7 @@ def main():
         e2e_ms = e0.elapsed_time(e1)
         e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     peak, peak_src = hbm_peak()
+    spec = spec_hbm_gbs(torch)
     extra = {}
     if rank == 0 and not args.no_int8:
         extra["int8_" + HEADLINE] = int8_leg(torch, api, x, P, rows, d, block, peak)
@@ -560,7 +572,8 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": f"taco_compress_kernel<{block}>",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": committed_traffic(), "peak_source": peak_src},
+                         "traffic": committed_traffic(), "peak_source": peak_src,
+                         "spec_peak": spec, "frac_of_spec": achieved / spec if spec else None},
             "kernels": kern,
             "step_frac_of_peak": value / world / peak,
             "e2e": None if e2e_ms is None else {
