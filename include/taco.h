@@ -290,6 +290,45 @@ taco_status taco_host_pipeline_run(taco_host_pipeline *pipe, const void *x_host_
 taco_status taco_host_pipeline_destroy(taco_host_pipeline *pipe);
 
 /*
+ * taco_two_shot_host_noalloc - the result of taco_host_pipeline_run (fp32
+ * output), for callers that cannot allocate device memory.  The papers have
+ * no counterpart: this is a way to call the same path, not a step of the
+ * method.
+ *
+ * Some callers cannot call cudaMalloc or any allocator: code that runs
+ * inside an allocator or memory-pool callback, in a section where an
+ * allocation could block or fail (a real-time or signal-handling path), or
+ * a host program whose device memory belongs to another component.  This
+ * call takes no workspace and allocates nothing, and creates no stream or
+ * event.  Its intermediate buffers live in one device array inside the
+ * library, TACO_NOALLOC_SCRATCH_MIB MiB on every GPU that loads the
+ * library, held until the process exits.  The rows are processed in chunks
+ * that fit the array, one after another on `stream`: no overlap between
+ * copies and kernels, so it is slower than the pipeline.
+ *
+ *  P, rows, d, block, e_target, eps   as for taco_host_pipeline_create/run
+ *  x_host_bf16  in   host bf16 [P][rows][d], should be pinned
+ *  out_host     out  host fp32 [rows][d], should be pinned
+ *
+ * Limits and behaviour:
+ *  - One row of all P shards and its intermediates must fit the array:
+ *    P * d * (3 + 8/block) + d * (5 + 8/block) bytes (plus alignment) at most
+ *    TACO_NOALLOC_SCRATCH_MIB MiB; larger rows return TACO_ERR_UNSUPPORTED
+ *    without launching anything.  Any number of rows is accepted.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - Every call on a device uses the same array, which keeps the previous
+ *    call's contents; nothing in it needs to start at zero.  Calls whose
+ *    work overlaps on the GPU (other streams, other threads) race on it:
+ *    serialise them.
+ */
+#define TACO_NOALLOC_SCRATCH_MIB 64
+taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32_t block,
+                                       const void *x_host_bf16, float *out_host, float e_target,
+                                       float eps, taco_stream_t stream);
+
+/*
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
  * (bit 0: compressor, bit 1: decompressor).  Synchronises the device.  With
