@@ -45,6 +45,7 @@ SIGNATURES = {
     "taco_host_pipeline_run": (ctypes.c_int, [_P, _P, _P, _P, _F32, _F32, _P]),
     "taco_host_pipeline_destroy": (ctypes.c_int, [_P]),
     "taco_two_shot_host_noalloc": (ctypes.c_int, [_I32, _I64, _I64, _I32, _P, _P, _F32, _F32, _P]),
+    "taco_watchdog_selftest": (ctypes.c_int, [_P]),
     "taco_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32]),
 }
 

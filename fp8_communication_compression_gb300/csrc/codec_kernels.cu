@@ -346,6 +346,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===================================================================== //
+//                          watchdog self-test                           //
+// ===================================================================== //
+
+constexpr uint32_t kErrSelftest = 16u;
+
+// One warp waits, with the codec kernels' time-limited wait, on an mbarrier
+// that nothing ever arrives on.  The wait must give up (after about a
+// second) and the kernel must record that in the watchdog flags and return,
+// leaving the context usable: the path a stalled TMA copy would take.
+__global__ void __launch_bounds__(32) watchdog_selftest_kernel()
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const bool done = __all_sync(0xFFFFFFFFu, mbar_wait(b, 0));
+    if (!done && threadIdx.x == 0)
+        atomicOr(&g_codec_error, kErrSelftest);
+}
+
+// ===================================================================== //
 //                                 host                                  //
 // ===================================================================== //
 
@@ -485,6 +509,12 @@ cudaError_t launch_decompress(const uint8_t *codes, const float *alpha, const fl
                         : run_decompress<256, false, true>(cm, om, alpha, scale, nrows, grid, stream, dev);
     return out_bf16 ? run_decompress<256, true, false>(cm, om, alpha, scale, nrows, grid, stream, dev)
                     : run_decompress<256, false, false>(cm, om, alpha, scale, nrows, grid, stream, dev);
+}
+
+cudaError_t launch_watchdog_selftest(cudaStream_t stream)
+{
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
 }
 
 cudaError_t read_codec_error(uint32_t *flags, bool clear)

@@ -66,6 +66,7 @@ uint64_t host_pipeline_workspace(const HostPipeline *p);
 cudaError_t host_pipeline_run(HostPipeline *p, const void *x_host, void *out_host, void *workspace, float e_target,
                               float eps, cudaStream_t stream);
 
+cudaError_t launch_watchdog_selftest(cudaStream_t stream);
 cudaError_t read_codec_error(uint32_t *flags, bool clear);
 
 // Launches `kernel` with programmatic stream serialization allowed, so that

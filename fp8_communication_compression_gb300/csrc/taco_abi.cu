@@ -434,6 +434,11 @@ taco_status taco_host_pipeline_destroy(taco_host_pipeline *pipe)
     return TACO_OK;
 }
 
+taco_status taco_watchdog_selftest(taco_stream_t stream)
+{
+    return from_cuda(taco::launch_watchdog_selftest(reinterpret_cast<cudaStream_t>(stream)));
+}
+
 taco_status taco_device_error(uint32_t *flags_out, int32_t clear)
 {
     if (!flags_out)

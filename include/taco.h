@@ -331,10 +331,20 @@ taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32
 /*
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
- * (bit 0: compressor, bit 1: decompressor).  Synchronises the device.  With
- * clear != 0 the flags are reset to 0 after reading.
+ * (bit 0: compressor, bit 1: decompressor, bit 4: taco_watchdog_selftest).
+ * Synchronises the device.  With clear != 0 the flags are reset to 0 after
+ * reading.
  */
 taco_status taco_device_error(uint32_t *flags_out, int32_t clear);
+
+/*
+ * taco_watchdog_selftest - checks the watchdog on this GPU.  Launches one
+ * warp that waits, with the kernels' time-limited wait, on a barrier that
+ * nothing completes.  After about a second the wait gives up, the kernel
+ * sets bit 4 of the flags that taco_device_error reads, and returns; the
+ * context stays usable.  Nothing faults and nothing hangs.
+ */
+taco_status taco_watchdog_selftest(taco_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -459,6 +459,27 @@ def test_host_pipeline_back_to_back_runs_and_bf16_output():
     assert torch.equal(ob.view(torch.int16), refs[0].to(torch.bfloat16).view(torch.int16))
 
 
+def test_two_paths_on_two_streams_at_once_match_sequential_runs():
+    """The kernels keep no state between launches (only the watchdog flags),
+    so two paths running concurrently on two streams give what they give
+    one after the other."""
+    P, rows, d, block = 4, 1024, 2048, 128
+    xs = [to_dev_bf16(np.stack([W.tp_activation(470 + 10 * k + p, rows, d, channel_scale=True, block=block)
+                                for p in range(P)])).reshape(P, rows, d) for k in range(2)]
+    paths = [api.TwoShotLocal(P, rows, d, block) for _ in range(2)]
+    refs = [paths[k].run(xs[k]).clone() for k in range(2)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(4):
+        for k in range(2):
+            paths[k].run(xs[k], stream=streams[k])
+    torch.cuda.synchronize()
+    for k in range(2):
+        assert torch.equal(paths[k].out.view(torch.int32), refs[k].view(torch.int32))
+
+
 def test_full_size_agoq_accumulate_and_reduce():
     a = W.AGOQ
     block, n = a["block"], a["n_main"]
