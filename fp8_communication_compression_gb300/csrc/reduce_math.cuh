@@ -1,9 +1,11 @@
 // Lane-level arithmetic of the shard reductions, shared by the shard-reduce
-// kernels and phase 1 of the fused reduce + decompress kernel so that both
-// produce bit-identical results.  A lane owns 32 consecutive elements of a
-// block (two 16-byte code words per shard) and keeps them as 16 float2
-// registers; products and sums use packed fp32x2 instructions, each product
-// rounded before it is added (no fused multiply-add).
+// kernels, the AGoQ accumulate kernel and phase 1 of the fused reduce +
+// decompress kernel, so that all of them produce bit-identical results.  A
+// lane owns 16 or 32 consecutive elements of a block (one or two 16-byte
+// code words per shard), kept as NF = 8 or 16 float2 registers.  The
+// weighted sums round every product before adding it (scalar __fmul_rn /
+// __fadd_rn, never contracted into a fused multiply-add); the statistics and
+// the re-encoding use packed fp32x2 instructions.
 #pragma once
 
 #include <cfloat>
