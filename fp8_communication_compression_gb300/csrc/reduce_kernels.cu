@@ -217,63 +217,83 @@ __global__ void __launch_bounds__(kBlockThreads)
 
 // ------------------------------------------------- AGoQ accumulate --
 
+// Slots a lane takes per loop trip of the accumulate kernel; the loads of
+// all of them are issued before any is processed.
+constexpr int kAccSlots = 2;
+
 template <int NB>
 __global__ void __launch_bounds__(kBlockThreads)
     agoq_accumulate_kernel(uint8_t *__restrict__ codes, float *__restrict__ scale,
                            const uint16_t *__restrict__ grad, int64_t nblocks)
 {
     constexpr int LPB = NB / kLaneElems;
+    constexpr int U = kAccSlots;
     pdl_wait();
     pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
+    const int part = lane % LPB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
-         base += stride) {
-        const int64_t t = base + lane;
-        const bool valid = t < total;
-        const int64_t blk = valid ? t / LPB : 0;
-        const int part = lane % LPB;
-        const int64_t off = blk * NB + part * kLaneElems;
-        uint4 q[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        uint4 g[4] = {q[0], q[0], q[0], q[0]};
-        float s_old = 1.0f;
-        if (valid) {
-            // codes and scale are rewritten below: coherent loads, not .nc
+         base += U * stride) {
+        uint4 q[U][2], g[U][4];
+        float s_old[U];
+        int64_t blk[U], off[U];
+        bool valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t t = base + u * stride + lane;
+            valid[u] = t < total;
+            blk[u] = valid[u] ? t / LPB : 0;
+            off[u] = blk[u] * NB + part * kLaneElems;
+            s_old[u] = 1.0f;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(q[h].x), "=r"(q[h].y), "=r"(q[h].z), "=r"(q[h].w)
-                             : "l"(codes + off + 16 * h));
+                q[u][h] = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int h = 0; h < 4; ++h)
-                g[h] = ldg128_stream(grad + off + 8 * h);
-            asm volatile("ld.global.f32 %0, [%1];" : "=f"(s_old) : "l"(scale + blk));
-        }
-        // g = dequantise(main) + grad in FP32: one rounded multiply, then one
-        // rounded add (no fused multiply-add), as the stated arithmetic is.
-        float2 d[16];
-        decode32_f2(q, d);
-        const float2 s2 = make_float2(s_old, s_old);
+                g[u][h] = make_uint4(0, 0, 0, 0);
+            if (valid[u]) {
+                // codes and scale are rewritten below: coherent loads, not .nc
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const uint32_t gw[4] = {g[h].x, g[h].y, g[h].z, g[h].w};
+                for (int h = 0; h < 2; ++h)
+                    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(q[u][h].x), "=r"(q[u][h].y), "=r"(q[u][h].z), "=r"(q[u][h].w)
+                                 : "l"(codes + off[u] + 16 * h));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 gr = make_float2(bf16lo_to_f32(gw[j]), bf16hi_to_f32(gw[j]));
-                d[4 * h + j] = add2_rounded(mul2_rounded(d[4 * h + j], s2), gr);
+                for (int h = 0; h < 4; ++h)
+                    g[u][h] = ldg128_stream(grad + off[u] + 8 * h);
+                asm volatile("ld.global.f32 %0, [%1];" : "=f"(s_old[u]) : "l"(scale + blk[u]));
             }
         }
-        const float mx = group_max<LPB>(lane_max_abs(d));
-        float qs, m_new;
-        agoq_scales(mx, qs, m_new);
-        if (valid) {
-            uint4 oq[2];
-            encode32_f2(d, qs, oq);
-            stg128_stream(codes + off, oq[0]);
-            stg128_stream(codes + off + 16, oq[1]);
-            if (part == 0)
-                scale[blk] = m_new;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            // g = dequantise(main) + grad in FP32: one rounded multiply, then
+            // one rounded add (no fused multiply-add), as the stated
+            // arithmetic is.
+            float2 d[16];
+            decode32_f2(q[u], d);
+            const float2 s2 = make_float2(s_old[u], s_old[u]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t gw[4] = {g[u][h].x, g[u][h].y, g[u][h].z, g[u][h].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 gr = make_float2(bf16lo_to_f32(gw[j]), bf16hi_to_f32(gw[j]));
+                    d[4 * h + j] = add2_rounded(mul2_rounded(d[4 * h + j], s2), gr);
+                }
+            }
+            const float mx = group_max<LPB>(lane_max_abs(d));
+            float qs, m_new;
+            agoq_scales(mx, qs, m_new);
+            if (valid[u]) {
+                uint4 oq[2];
+                encode32_f2(d, qs, oq);
+                stg128_stream(codes + off[u], oq[0]);
+                stg128_stream(codes + off[u] + 16, oq[1]);
+                if (part == 0)
+                    scale[blk[u]] = m_new;
+            }
         }
     }
 }
@@ -377,12 +397,12 @@ cudaError_t launch_agoq_accumulate(uint8_t *codes, float *scale, const void *gra
     int grid = 0;
     cudaError_t e;
     if (block == 128) {
-        if ((e = grid_for(agoq_accumulate_kernel<128>, nblocks * (128 / kLaneElems), &grid)) != cudaSuccess)
+        if ((e = grid_for(agoq_accumulate_kernel<128>, (nblocks * (128 / kLaneElems) + kAccSlots - 1) / kAccSlots, &grid)) != cudaSuccess)
             return e;
         return launch_pdl(agoq_accumulate_kernel<128>, grid, kBlockThreads, 0, stream, codes, scale, g,
                           nblocks);
     }
-    if ((e = grid_for(agoq_accumulate_kernel<256>, nblocks * (256 / kLaneElems), &grid)) != cudaSuccess)
+    if ((e = grid_for(agoq_accumulate_kernel<256>, (nblocks * (256 / kLaneElems) + kAccSlots - 1) / kAccSlots, &grid)) != cudaSuccess)
         return e;
     return launch_pdl(agoq_accumulate_kernel<256>, grid, kBlockThreads, 0, stream, codes, scale, g, nblocks);
 }
