@@ -425,6 +425,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--kernel-events-every", type=int, default=10,
+                    help="record per-kernel CUDA events on every N-th timed step")
     ap.add_argument("--e2e-chunks", type=int, default=4, help="row chunks of the host pipeline")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows per shard")
     ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
@@ -478,7 +480,11 @@ def main():
     nbytes = path.bytes_per_step()
     step_bytes = sum(nbytes.values())
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(K)]
+    # per-kernel events on every E-th step of the timed region; the other
+    # steps run without events between their launches
+    E = max(1, args.kernel_events_every)
+    sampled = list(range(0, K, E))
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for k in sampled}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
     time.sleep(0.2 if clocks else 0)
@@ -487,7 +493,11 @@ def main():
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(K):
-        e = ev[k]
+        e = ev.get(k)
+        if e is None:
+            for _, fn in launches:
+                fn(x)
+            continue
         e[0].record(stream)
         for i, (_, fn) in enumerate(launches):
             fn(x)
@@ -510,7 +520,7 @@ def main():
     clk = clocks.stop() if clocks else None
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
-    per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+    per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in sampled)
            for i, name in enumerate(names)}
 
     # end to end through the public API with pinned host buffers
@@ -566,6 +576,7 @@ def main():
             "config": {"workload": HEADLINE if args.rows is None else f"{HEADLINE} (rows={rows})",
                        "P": P, "rows": rows, "d": d, "block": block,
                        "launches": names,
+                       "kernel_events": f"per-launch CUDA events on every {E}th of the {K} timed steps",
                        "bytes_per_step": step_bytes,
                        "input_bf16_bytes_per_step": 2 * P * n,
                        "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
