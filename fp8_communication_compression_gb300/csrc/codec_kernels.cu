@@ -24,6 +24,7 @@
 //  * Every mbarrier wait is time-limited (device_utils.cuh); a wait that
 //    runs out sets a flag readable through taco_device_error().
 
+#include <atomic>
 #include <cfloat>
 #include <mutex>
 
@@ -397,15 +398,18 @@ EncodeTiledFn encode_fn()
 
 constexpr int kMaxDevices = 64;
 
+// Raises a kernel's dynamic shared-memory limit once per device.  The flag
+// is atomic because host threads may make their first launch concurrently;
+// setting the attribute twice is harmless.
 template <typename K>
-cudaError_t ensure_smem(K kernel, uint32_t bytes, int device, bool *done)
+cudaError_t ensure_smem(K kernel, uint32_t bytes, int device, std::atomic<bool> *done)
 {
-    if (done[device])
+    if (done[device].load(std::memory_order_acquire))
         return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
     if (e == cudaSuccess)
-        done[device] = true;
+        done[device].store(true, std::memory_order_release);
     return e;
 }
 
@@ -434,7 +438,7 @@ template <int NB, bool I8>
 cudaError_t run_compress(const CUtensorMap &xm, const CUtensorMap &cm, float *alpha, float *scale,
                          int64_t nrows, float e_target, float eps, int grid, cudaStream_t stream, int device)
 {
-    static bool set[kMaxDevices];
+    static std::atomic<bool> set[kMaxDevices];
     cudaError_t e = ensure_smem(taco_compress_kernel<NB, I8>, kCSmemBytes, device, set);
     if (e != cudaSuccess)
         return e;
@@ -446,7 +450,7 @@ template <int NB, bool BF, bool I8>
 cudaError_t run_decompress(const CUtensorMap &cm, const CUtensorMap &om, const float *alpha,
                            const float *scale, int64_t nrows, int grid, cudaStream_t stream, int device)
 {
-    static bool set[kMaxDevices];
+    static std::atomic<bool> set[kMaxDevices];
     cudaError_t e = ensure_smem(taco_decompress_kernel<NB, BF, I8>, kDSmemBytes, device, set);
     if (e != cudaSuccess)
         return e;

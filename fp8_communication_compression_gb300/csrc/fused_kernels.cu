@@ -15,6 +15,8 @@
 //           decompress kernel (decode, register butterflies, scaling), output
 //           through a swizzled 16 KB staging area and TMA tensor stores.
 
+#include <atomic>
+
 #include "codec_math.cuh"
 #include "device_utils.cuh"
 #include "internal.h"
@@ -249,19 +251,21 @@ __global__ void __launch_bounds__(kFThreads, 1)
         bulk_wait_all();
 }
 
-template <int NB, int PT, bool BF> bool g_smem_set[64];
+// Per device: the kernel's dynamic shared-memory limit has been raised
+// (atomic: host threads may make their first launch concurrently).
+template <int NB, int PT, bool BF> std::atomic<bool> g_smem_set[64];
 
 template <int NB, int PT, bool BF>
 cudaError_t run_fused(const ShardPtrs &in, int P, const CUtensorMap &om, int64_t nrows, float e_target,
                       float eps, uint8_t *oc, float *oa, float *os, cudaStream_t st, const DeviceInfo &di)
 {
     auto kernel = taco_reduce_decompress_kernel<NB, PT, BF>;
-    if (!g_smem_set<NB, PT, BF>[di.device]) {
+    if (!g_smem_set<NB, PT, BF>[di.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kFSmemBytes));
         if (e != cudaSuccess)
             return e;
-        g_smem_set<NB, PT, BF>[di.device] = true;
+        g_smem_set<NB, PT, BF>[di.device].store(true, std::memory_order_release);
     }
     const int64_t ctas = (nrows + kFWarps * 32 - 1) / (kFWarps * 32);
     const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
