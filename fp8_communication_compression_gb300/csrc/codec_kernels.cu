@@ -82,9 +82,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wbase = base + warp * kCWarpBytes;
     const uint32_t outw = wbase + kStages * kCStageBytes;
     const uint32_t bars = base + kWarps * kCWarpBytes + warp * kStages * 8;
-    const int64_t ntiles = (nrows + kWarpRows - 1) / kWarpRows;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-    const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+    // 32-bit row and tile indices (the host rejects nrows >= 2^31): fewer
+    // registers in a kernel that uses all 255
+    const int nrows32 = static_cast<int>(nrows);
+    const int ntiles = (nrows32 + kWarpRows - 1) / kWarpRows;
+    const int gw = blockIdx.x * kWarps + warp;
+    const int W = gridDim.x * kWarps;
 
     pdl_wait();
     pdl_launch_dependents();
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t orow = outw + lane * 128;
     const float c = BlockConst<NB>::c;
     int it = 0;
-    for (int64_t t = gw; t < ntiles; t += W, ++it) {
+    for (int t = gw; t < ntiles; t += W, ++it) {
         const int s = it % kStages;
         // warp-uniform: if any lane's wait runs out, the whole warp stops
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every loaded value has been consumed: refill the stage
         __syncwarp();
         if (lane == 0) {
-            const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
+            const int nt = gw + (it + kStages) * W;
             if (nt < ntiles) {
                 fence_proxy_async_smem();
                 const uint32_t dst = wbase + s * kCStageBytes, full = bars + 8 * s;
@@ -209,13 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int64_t wrow = t * kWarpRows;
+        const int wrow = t * kWarpRows;
         if (lane == 0) {
             tma_store_2d(&c_map, 0, static_cast<int32_t>(wrow), outw);
             bulk_commit();
         }
-        const int64_t grow = wrow + lane;
-        if (grow < nrows && (lane % G) == 0) {
+        const int grow = wrow + lane;
+        if (grow < nrows32 && (lane % G) == 0) {
             alpha_out[grow / G] = alpha;
             scale_out[grow / G] = scale;
         }
@@ -463,6 +466,8 @@ cudaError_t run_decompress(const CUtensorMap &cm, const CUtensorMap &om, const f
 cudaError_t launch_compress(const void *x_bf16, int64_t nrows, int block, float e_target, float eps,
                             uint8_t *codes, float *alpha, float *scale, bool int8_codes, cudaStream_t stream)
 {
+    if (nrows > (int64_t(1) << 31) - 256)  // the kernel's row and tile indices are 32-bit
+        return cudaErrorInvalidValue;
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess)
