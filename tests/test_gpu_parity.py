@@ -175,6 +175,23 @@ def test_reduce_shard_counts(P, block):
     assert_scalars_match(to_host(os_), rs, "reduced scale")
 
 
+@pytest.mark.parametrize("P,block", [(4, 128), (8, 256)])
+def test_reduce_is_invariant_to_shard_order(P, block):
+    """Any order of the shards reduces to the same compressed sum, within
+    the parity bar: the FP32 sum runs in shard order, so a permutation may
+    change the last bit of a sum, hence at most one code step."""
+    rows, d = 128, 1024
+    shards = [api.taco_compress(to_dev_bf16(W.tp_activation(140 + p, rows, d, channel_scale=True,
+                                                           block=block)), block) for p in range(P)]
+    cs, as_, ss = (list(t) for t in zip(*shards))
+    ref = [to_host(t) for t in api.taco_reduce_shards(cs, as_, ss, block)]
+    for perm in (list(range(P))[::-1], [(3 * i + 1) % P for i in range(P)]):
+        got = api.taco_reduce_shards([cs[i] for i in perm], [as_[i] for i in perm], [ss[i] for i in perm], block)
+        assert_codes_match(to_host(got[0]), ref[0], "permuted codes")
+        assert_scalars_match(to_host(got[1]), ref[1], "permuted alpha")
+        assert_scalars_match(to_host(got[2]), ref[2], "permuted scale")
+
+
 def test_reduce_shard_and_negation_gives_zero_blocks():
     block = 128
     c, a, s = api.taco_compress(to_dev_bf16(W.tp_activation(9, 32, 512, block=block)), block)
