@@ -36,6 +36,9 @@
  *    exception crosses the ABI.  Kernels never wait without a time limit;
  *    a wait that runs out records a flag read by taco_device_error().
  *  - Empty input (rows == 0 or n == 0) returns TACO_OK without a launch.
+ *  - Size limit: a TACO call takes at most 2^31 - 256 rows of 128 elements
+ *    (rows * d / 128), more than any GPU memory holds; larger calls return
+ *    TACO_ERR_UNSUPPORTED.
  *  - Inputs must be finite; NaN or Inf input gives unspecified codes
  *    (taco_e4m3_encode states its own handling of them).
  */
