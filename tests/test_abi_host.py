@@ -66,6 +66,9 @@ def test_compress_validation(lib):
     assert compress(lib, e=float("inf")) == INVALID
     assert compress(lib, eps=float("nan")) == INVALID
     assert compress(lib, rows=0) == OK  # empty input: no launch
+    # the size limit: 2^31 - 256 rows of 128 elements; one more is rejected
+    assert compress(lib, rows=(1 << 31) - 255, d=128) == UNSUPPORTED
+    assert compress(lib, rows=1 << 40, d=1 << 30) == INVALID  # rows * d overflows
     assert compress(lib, x=0) == INVALID
     assert compress(lib, codes=0) == INVALID
     assert compress(lib, x=A + 8) == MISALIGNED
