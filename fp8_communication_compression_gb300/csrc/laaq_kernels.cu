@@ -146,28 +146,23 @@ __global__ void __launch_bounds__(kLThreads)
 // The dequantizer's unit is 8 consecutive codes (BITS bytes of the stream);
 // adjacent lanes take adjacent units, so that a warp's code loads and its
 // 16-byte bf16 stores are both contiguous.  A unit's 8 * BITS bits are held
-// as two 32-bit words, code 0 in the lowest bits of lo.  A second word is
-// read only when the unit reaches into it, so no load leaves the stream.
+// as two 32-bit words, code 0 in the lowest bits of lo.  For 4 and 8 bits a
+// unit is one aligned load; for 5 and 6 bits it is not word-aligned, so the
+// warp loads its 32 units' span with 16-byte loads into a shared buffer and
+// each lane takes its two words from there.
 struct UnitBits {
     uint32_t lo, hi;
 };
 
 template <int BITS> __device__ __forceinline__ UnitBits load_unit(const uint8_t *packed, int64_t unit)
 {
+    static_assert(BITS == 4 || BITS == 8, "5- and 6-bit units are loaded through the shared buffer");
     const int64_t byte = unit * BITS;
     if constexpr (BITS == 8) {
         const uint2 v = __ldg(reinterpret_cast<const uint2 *>(packed + byte));
         return {v.x, v.y};
-    } else if constexpr (BITS == 4) {
-        return {__ldg(reinterpret_cast<const uint32_t *>(packed + byte)), 0u};
     } else {
-        const int64_t a = byte & ~static_cast<int64_t>(3);
-        const uint32_t sh = 8u * static_cast<uint32_t>(byte & 3);
-        const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(packed + a));
-        // a unit of 5 or 6 bytes starting at byte offset sh / 8 <= 3 of w0
-        // always reaches into the next word
-        const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(packed + a + 4));
-        return {__funnelshift_r(w0, w1, sh), w1 >> sh};
+        return {__ldg(reinterpret_cast<const uint32_t *>(packed + byte)), 0u};
     }
 }
 
@@ -204,18 +199,70 @@ __global__ void __launch_bounds__(kLThreads)
     pdl_launch_dependents();
     const int64_t units = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < units;
+    // for 5 and 6 bits the loop test is warp-uniform (the warp's first
+    // unit), so that a warp's lanes stay together through the shared-buffer
+    // exchange below
+    constexpr bool kStaged = (BITS == 5 || BITS == 6);
+    const int64_t lane_off = kStaged ? (threadIdx.x & 31) : 0;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base - lane_off < units;
          base += U * stride) {
         UnitBits w[U];
         float m[U];
+        if constexpr (kStaged) {
+            // a warp's 32 consecutive units are one 16-byte-aligned span of
+            // 32 * BITS bytes: 2 * BITS lanes load it with one 16-byte load
+            // each, through the warp's shared buffer to the lanes that need it
+            constexpr int CH = 2 * BITS;             // 16-byte chunks per span
+            constexpr int SPAN = 32 * BITS;          // bytes per span
+            __shared__ __align__(16) uint8_t stage[kLThreads / 32][U * 32 * 6];
+            uint8_t *buf = stage[threadIdx.x >> 5];
+            const int lane = threadIdx.x & 31;
+            const int64_t nbytes = units * BITS;
+            uint4 c[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t j = base + u * stride;
-            w[u] = {0u, 0u};
-            m[u] = 1.0f;
-            if (j < units) {
-                w[u] = load_unit<BITS>(packed, j);
-                m[u] = __ldg(scale + j * 8 / NB);
+            for (int u = 0; u < U; ++u) {
+                const int64_t off = (base - lane + u * stride) * BITS + 16 * lane;
+                c[u] = make_uint4(0, 0, 0, 0);
+                if (lane < CH && off < nbytes) {
+                    if (off + 16 <= nbytes) {
+                        c[u] = ldg128_stream(packed + off);
+                    } else {  // the stream ends inside this chunk: whole words only
+                        uint32_t t[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (off + 4 * k < nbytes)
+                                t[k] = __ldg(reinterpret_cast<const uint32_t *>(packed + off + 4 * k));
+                        c[u] = make_uint4(t[0], t[1], t[2], t[3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane < CH) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    *reinterpret_cast<uint4 *>(buf + u * SPAN + 16 * lane) = c[u];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = base + u * stride;
+                const int byte = BITS * lane, a = byte & ~3;
+                const uint32_t sh = 8u * static_cast<uint32_t>(byte & 3);
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(buf + u * SPAN + a);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(buf + u * SPAN + a + 4);
+                w[u] = {__funnelshift_r(w0, w1, sh), w1 >> sh};
+                m[u] = j < units ? __ldg(scale + j * 8 / NB) : 1.0f;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = base + u * stride;
+                w[u] = {0u, 0u};
+                m[u] = 1.0f;
+                if (j < units) {
+                    w[u] = load_unit<BITS>(packed, j);
+                    m[u] = __ldg(scale + j * 8 / NB);
+                }
             }
         }
 #pragma unroll
