@@ -4,6 +4,11 @@
 // reconstruction.  One pass writes the compressed sum (codes, alpha, s) and
 // decompress(compressed sum) without reading the reduced codes back.
 //
+// Two layouts.  For n=128, taco_reduce_decompress128_kernel (below) takes
+// 16-row tiles with 16 elements per lane in phase 1 and lane pairs in phase
+// 2, at most 128 registers a thread, two CTAs per SM.  For n=256 (where
+// that layout spills and measured slower), taco_reduce_decompress_kernel:
+//
 // Per warp and 32-row tile (32 / (n/128) blocks):
 //  phase 1  the Hadamard-domain reduce of the shard-reduce kernel: 4 (n=128)
 //           or 8 (n=256) lanes per block, 32 elements per lane, coalesced
