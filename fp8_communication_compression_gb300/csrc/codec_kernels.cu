@@ -13,9 +13,10 @@
 //    shuffles.  A 256-element block spans two adjacent lanes and needs one
 //    extra __shfl_xor stage.
 //  * Every warp is an independent pipeline over 32-row tiles: lane 0 keeps
-//    three TMA loads (cp.async.bulk.tensor, 128-byte swizzle) in flight
-//    into the warp's own ring of mbarrier-guarded stages and refills a
-//    stage as soon as the warp has read it.  The swizzle makes each lane's
+//    compress_stages<NB>() (compress) or kDStages (decompress) TMA loads
+//    (cp.async.bulk.tensor, 128-byte swizzle) in flight into the warp's own
+//    ring of mbarrier-guarded stages and refills a stage as soon as the warp
+//    has read it.  The swizzle makes each lane's
 //    row reads bank-conflict free.  No producer warp and no cross-warp
 //    barrier: 8 warps per CTA leave 255 registers per thread.
 //  * Each warp writes its 32 output rows into its own swizzled staging
@@ -39,24 +40,39 @@ __device__ unsigned int g_codec_error;
 constexpr int kWarps = 8;              // warps per CTA, each an independent pipeline
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpRows = 32;          // rows per warp tile, one per lane
-constexpr int kStages = 3;             // TMA ring depth per warp
+// TMA ring depth per warp.  Measured on GB300 in the back-to-back step
+// (where the compressor also writes back the previous decompress output),
+// the n=128 compressor is fastest with one stage: its next tile is loaded
+// while the current one is computed (69.2 us at the headline size, against
+// 76.5 with two stages and 79.0 with three).  At n=256, where a lane pair
+// shares a block and each tile carries more work, two stages are 2% faster.
+// The decompressor keeps three.
+template <int NB> __host__ __device__ constexpr int compress_stages() { return NB == 128 ? 1 : 2; }
+constexpr int kDStages = 3;
 constexpr uint32_t kErrCompress = 1u;
 constexpr uint32_t kErrDecompress = 2u;
 
-// compress, per warp: kStages x (two 128-byte-wide halves of 32 rows of
+// compress, per warp: stages x (two 128-byte-wide halves of 32 rows of
 // bf16) + 32 rows x 128 bytes of codes
 constexpr uint32_t kCHalfBytes = kWarpRows * 128;           // 4 KB
 constexpr uint32_t kCStageBytes = 2 * kCHalfBytes;          // 8 KB
 constexpr uint32_t kCOutBytes = kWarpRows * 128;            // 4 KB
-constexpr uint32_t kCWarpBytes = kStages * kCStageBytes + kCOutBytes;  // 28 KB
-// decompress, per warp: kStages x 32 rows x 128 codes + 32 rows x 512 bytes
+template <int NB> __host__ __device__ constexpr uint32_t compress_warp_bytes()
+{
+    return compress_stages<NB>() * kCStageBytes + kCOutBytes;
+}
+template <int NB> __host__ __device__ constexpr uint32_t compress_smem_bytes()
+{
+    return 1024 + kWarps * compress_warp_bytes<NB>() + kWarps * compress_stages<NB>() * 8;
+}
+// decompress, per warp: kDStages x 32 rows x 128 codes + 32 rows x 512 bytes
 constexpr uint32_t kDStageBytes = kWarpRows * 128;          // 4 KB
 constexpr uint32_t kDOutBytes = kWarpRows * 512;            // 16 KB
-constexpr uint32_t kDWarpBytes = kStages * kDStageBytes + kDOutBytes;  // 28 KB
-static_assert(kCWarpBytes % 1024 == 0 && kDWarpBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-constexpr uint32_t kBarBytes = kWarps * kStages * 8;
-constexpr uint32_t kCSmemBytes = 1024 + kWarps * kCWarpBytes + kBarBytes;
-constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kBarBytes;
+constexpr uint32_t kDWarpBytes = kDStages * kDStageBytes + kDOutBytes;  // 28 KB
+static_assert(compress_warp_bytes<128>() % 1024 == 0 && compress_warp_bytes<256>() % 1024 == 0 &&
+                  kDWarpBytes % 1024 == 0,
+              "swizzle atoms need 1 KB alignment");
+constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kWarps * kDStages * 8;
 
 // ===================================================================== //
 //                              compressor                               //
@@ -64,7 +80,7 @@ constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kBarBytes;
 
 // Each warp streams its own 32-row tiles: warp tile t covers rows
 // 32t .. 32t + 31; the warps of the grid take tiles round-robin.  Lane 0
-// keeps kStages TMA loads in flight and refills a stage as soon as the warp
+// keeps compress_stages<NB>() TMA loads in flight and refills a stage as soon as the warp
 // has read it.
 
 // FMT_INT8: INT8 codes with Q_max = 127 (the fallback format); otherwise
@@ -76,12 +92,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                          float *__restrict__ scale_out, int64_t nrows, float e_target, float eps)
 {
     constexpr int G = NB / 128;  // lanes per block
+    constexpr int kCStages = compress_stages<NB>();
+    constexpr uint32_t kCWarpBytes = compress_warp_bytes<NB>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t wbase = base + warp * kCWarpBytes;
-    const uint32_t outw = wbase + kStages * kCStageBytes;
-    const uint32_t bars = base + kWarps * kCWarpBytes + warp * kStages * 8;
+    const uint32_t outw = wbase + kCStages * kCStageBytes;
+    const uint32_t bars = base + kWarps * kCWarpBytes + warp * kCStages * 8;
     // 32-bit row and tile indices (the host rejects nrows >= 2^31): fewer
     // registers in a kernel that uses all 255
     const int nrows32 = static_cast<int>(nrows);
@@ -94,10 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&x_map);
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < kCStages; ++s)
             mbar_init(bars + 8 * s, 1);
         fence_barrier_init();
-        for (; issued < kStages && gw + issued * W < ntiles; ++issued) {
+        for (; issued < kCStages && gw + issued * W < ntiles; ++issued) {
             const int32_t y = static_cast<int32_t>((gw + issued * W) * kWarpRows);
             const uint32_t dst = wbase + issued * kCStageBytes, full = bars + 8 * issued;
             mbar_arrive_expect_tx(full, kCStageBytes);
@@ -112,9 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = BlockConst<NB>::c;
     int it = 0;
     for (int t = gw; t < ntiles; t += W, ++it) {
-        const int s = it % kStages;
+        const int s = it % kCStages;
         // warp-uniform: if any lane's wait runs out, the whole warp stops
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kCStages) & 1))) {
             if (lane == 0)
                 atomicOr(&g_codec_error, kErrCompress);
             break;
@@ -143,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every loaded value has been consumed: refill the stage
         __syncwarp();
         if (lane == 0) {
-            const int nt = gw + (it + kStages) * W;
+            const int nt = gw + (it + kCStages) * W;
             if (nt < ntiles) {
                 fence_proxy_async_smem();
                 const uint32_t dst = wbase + s * kCStageBytes, full = bars + 8 * s;
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
         // leave no copy in flight into or out of this CTA's shared memory
         for (int k = it; k < issued; ++k)
-            mbar_wait(bars + 8 * (k % kStages), (k / kStages) & 1);
+            mbar_wait(bars + 8 * (k % kCStages), (k / kCStages) & 1);
         bulk_wait_all();
     }
 }
@@ -246,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t wbase = base + warp * kDWarpBytes;
-    const uint32_t outw = wbase + kStages * kDStageBytes;
-    const uint32_t bars = base + kWarps * kDWarpBytes + warp * kStages * 8;
+    const uint32_t outw = wbase + kDStages * kDStageBytes;
+    const uint32_t bars = base + kWarps * kDWarpBytes + warp * kDStages * 8;
     const int64_t ntiles = (nrows + kWarpRows - 1) / kWarpRows;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
@@ -257,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&c_map);
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < kDStages; ++s)
             mbar_init(bars + 8 * s, 1);
         fence_barrier_init();
-        for (; issued < kStages && gw + issued * W < ntiles; ++issued) {
+        for (; issued < kDStages && gw + issued * W < ntiles; ++issued) {
             const uint32_t full = bars + 8 * issued;
             mbar_arrive_expect_tx(full, kDStageBytes);
             tma_load_2d(wbase + issued * kDStageBytes, &c_map, 0,
@@ -282,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int it = 0;
     for (int64_t t = gw; t < ntiles; t += W, ++it) {
-        const int s = it % kStages;
+        const int s = it % kDStages;
         const int64_t wrow = t * kWarpRows;
         const float a = a_next, sc = sc_next;
         if (t + W < ntiles) {
@@ -290,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc_next = __ldg(scale + tile_block(t + W));
         }
         // warp-uniform: if any lane's wait runs out, the whole warp stops
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kStages) & 1))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * s, (it / kDStages) & 1))) {
             if (lane == 0)
                 atomicOr(&g_codec_error, kErrDecompress);
             break;
@@ -311,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fwht128_upper_but_last(v);  // the last stage is fused with the scaling below
         __syncwarp();
         if (lane == 0) {
-            const int64_t nt = gw + static_cast<int64_t>(it + kStages) * W;
+            const int64_t nt = gw + static_cast<int64_t>(it + kDStages) * W;
             if (nt < ntiles) {
                 fence_proxy_async_smem();
                 const uint32_t full = bars + 8 * s;
@@ -344,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
         for (int k = it; k < issued; ++k)
-            mbar_wait(bars + 8 * (k % kStages), (k / kStages) & 1);
+            mbar_wait(bars + 8 * (k % kDStages), (k / kDStages) & 1);
         bulk_wait_all();
     }
 }
@@ -442,11 +460,12 @@ cudaError_t run_compress(const CUtensorMap &xm, const CUtensorMap &cm, float *al
                          int64_t nrows, float e_target, float eps, int grid, cudaStream_t stream, int device)
 {
     static std::atomic<bool> set[kMaxDevices];
-    cudaError_t e = ensure_smem(taco_compress_kernel<NB, I8>, kCSmemBytes, device, set);
+    constexpr uint32_t smem = compress_smem_bytes<NB>();
+    cudaError_t e = ensure_smem(taco_compress_kernel<NB, I8>, smem, device, set);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(taco_compress_kernel<NB, I8>, grid, kThreads, kCSmemBytes, stream, xm, cm, alpha, scale,
-                      nrows, e_target, eps);
+    return launch_pdl(taco_compress_kernel<NB, I8>, grid, kThreads, smem, stream, xm, cm, alpha, scale, nrows,
+                      e_target, eps);
 }
 
 template <int NB, bool BF, bool I8>
