@@ -4,21 +4,12 @@
 // reconstruction.  One pass writes the compressed sum (codes, alpha, s) and
 // decompress(compressed sum) without reading the reduced codes back.
 //
-// Two layouts.  For n=128, taco_reduce_decompress128_kernel (below) takes
-// 16-row tiles with 16 elements per lane in phase 1 and lane pairs in phase
-// 2, at most 128 registers a thread, two CTAs per SM.  For n=256 (where
-// that layout spills and measured slower), taco_reduce_decompress_kernel:
-//
-// Per warp and 32-row tile (32 / (n/128) blocks):
-//  phase 1  the Hadamard-domain reduce of the shard-reduce kernel: 4 (n=128)
-//           or 8 (n=256) lanes per block, 32 elements per lane, coalesced
-//           16-byte loads of the P shards' codes (double-buffered across the
-//           four sub-steps of a tile when P <= 8), FP32 sum, requantisation.
-//           Codes go to global memory and, swizzled, into the warp's 4 KB
-//           shared-memory tile; alpha and s into a shared array.
-//  phase 2  one lane per 128-element row, exactly the arithmetic of the
-//           decompress kernel (decode, register butterflies, scaling), output
-//           through a swizzled 16 KB staging area and TMA tensor stores.
+// The one-pass kernel is for n=128 (taco_reduce_decompress128_kernel
+// below).  For n=256 the call runs the shard-reduce kernel and then the
+// decompress kernel: a one-pass n=256 kernel (32-row tiles, one CTA per SM)
+// took 135.5 us per call at P=8 x [8192, 5120] against 116.4 us for the two
+// launches, because its row-resident phase 2 and the P shards' loads leave
+// room for only one CTA (8 warps) per SM.
 
 #include <atomic>
 #include <cfloat>
@@ -34,233 +25,11 @@ namespace {
 
 constexpr int kFWarps = 8;
 constexpr int kFThreads = kFWarps * 32;
-constexpr int kFEPL = 32;                                   // phase 1: elements per lane
-constexpr uint32_t kFCodeTile = 32 * 128;                   // 4 KB per warp
-constexpr uint32_t kFOutBytes = 32 * 512;                   // 16 KB per warp
-constexpr uint32_t kFWarpBytes = kFCodeTile + kFOutBytes;   // 20 KB
-constexpr uint32_t kFScalarBytes = 2 * 32 * 4;              // alpha', s' of up to 32 blocks
-constexpr uint32_t kFSmemBytes = 1024 + kFWarps * (kFWarpBytes + kFScalarBytes);
-static_assert(kFWarpBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-
-// Per-lane state of phase 1 for one sub-step: which block, where.
-struct Slot {
-    int64_t blk;
-    int64_t off;
-    int lb;  // block index within the tile
-    bool valid;
-};
-
-template <int NB, int LPB, int BPS>
-__device__ __forceinline__ Slot slot_of(int64_t blk0, int si, int lane, int64_t nblocks)
-{
-    Slot s;
-    s.lb = si * BPS + lane / LPB;
-    s.blk = blk0 + s.lb;
-    s.valid = s.blk < nblocks;
-    s.off = (s.valid ? s.blk : 0) * NB + (lane % LPB) * kFEPL;
-    return s;
-}
-
-template <int P>
-__device__ __forceinline__ void load_shards(const ShardPtrs &in, const Slot &sl, uint4 (&q)[P][2])
-{
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-        q[p][0] = sl.valid ? ldg128_stream(in.codes[p] + sl.off) : make_uint4(0, 0, 0, 0);
-        q[p][1] = sl.valid ? ldg128_stream(in.codes[p] + sl.off + 16) : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// Requantises the lane's 32 Hadamard-domain sums T of one block (exactly as
-// the shard-reduce kernel), stores codes and scalars to global memory and
-// to the warp's shared tile.
-template <int NB, int LPB>
-__device__ __forceinline__ void finish_block(float2 (&T)[16], const Slot &sl, int lane, float e_target,
-                                             float eps, uint8_t *out_codes, float *out_alpha,
-                                             float *out_scale, uint32_t ctile, float *sa_s, float *ss_s)
-{
-    constexpr int G = NB / 128;
-    const int part = lane % LPB;
-    uint4 oq[2];
-    float alpha, scale;
-    recompress<NB, LPB, 16>(T, e_target, eps, oq, alpha, scale);
-    if (sl.valid) {
-        stg128_stream(out_codes + sl.off, oq[0]);
-        stg128_stream(out_codes + sl.off + 16, oq[1]);
-        if (part == 0) {
-            out_alpha[sl.blk] = alpha;
-            out_scale[sl.blk] = scale;
-        }
-    }
-    // the lane's 32 codes are 16-byte chunks j0, j0 + 1 of tile row r
-    const int r = sl.lb * G + part / 4;
-    const uint32_t j0 = static_cast<uint32_t>(part % 4) * 2;
-    const uint32_t rsw = static_cast<uint32_t>(r & 7) << 4;
-    sts128(ctile + r * 128 + ((j0 << 4) ^ rsw), oq[0].x, oq[0].y, oq[0].z, oq[0].w);
-    sts128(ctile + r * 128 + (((j0 + 1) << 4) ^ rsw), oq[1].x, oq[1].y, oq[1].z, oq[1].w);
-    if (part == 0) {
-        sa_s[sl.lb] = alpha;
-        ss_s[sl.lb] = scale;
-    }
-}
-
-// Phase 1 for a compile-time shard count (the shard-reduce kernel's math).
-template <int NB, int P>
-__device__ __forceinline__ void accumulate_fixed(const ShardPtrs &in, const Slot &sl, const uint4 (&q)[P][2],
-                                                 int lane, float2 (&T)[16])
-{
-    constexpr int LPB = NB / kFEPL;
-    constexpr int ROUNDS = (P + LPB - 1) / LPB;
-    const int part = lane % LPB;
-    float wr[ROUNDS];
-#pragma unroll
-    for (int r = 0; r < ROUNDS; ++r) {
-        const int p = r * LPB + part;
-        const bool ok = sl.valid && p < P;
-        wr[r] = shard_weight(ok ? __ldg(in.scale[p] + sl.blk) : 1.0f, ok ? __ldg(in.alpha[p] + sl.blk) : 1.0f);
-    }
-    const int gbase = lane & ~(LPB - 1);
-    float w[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p)
-        w[p] = __shfl_sync(0xFFFFFFFFu, wr[p / LPB], gbase + (p % LPB));
-    weighted_sum<P, 16>(q, w, T);
-}
-
-// Phase 1 for a run-time shard count (1 .. 16): shard by shard, same rounding.
-__device__ __forceinline__ void accumulate_any(const ShardPtrs &in, int P, const Slot &sl, float2 (&T)[16])
-{
-#pragma unroll 1
-    for (int p = 0; p < P; ++p) {
-        uint4 q[2];
-        load32_codes(in.codes[p] + sl.off, sl.valid, q);
-        const float w = sl.valid ? shard_weight(__ldg(in.scale[p] + sl.blk), __ldg(in.alpha[p] + sl.blk)) : 1.0f;
-        weighted_sum_step<16>(q, w, p == 0, T);
-    }
-}
-
-// PT > 0: compile-time shard count; PT == 0: run-time P.
-template <int NB, int PT, bool BF16OUT>
-__global__ void __launch_bounds__(kFThreads, 1)
-    taco_reduce_decompress_kernel(const ShardPtrs in, int P, const __grid_constant__ CUtensorMap o_map,
-                                  int64_t nrows, float e_target, float eps, uint8_t *__restrict__ out_codes,
-                                  float *__restrict__ out_alpha, float *__restrict__ out_scale)
-{
-    constexpr int G = NB / 128;       // tile rows per block
-    constexpr int LPB = NB / kFEPL;   // phase-1 lanes per block
-    constexpr int BPS = 32 / LPB;     // blocks per phase-1 sub-step
-    constexpr int BPT = 32 / G;       // blocks per 32-row tile
-    constexpr int SUB = BPT / BPS;    // sub-steps per tile
-    static_assert(SUB == 4, "a 32-row tile is four phase-1 sub-steps");
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ctile = base + warp * kFWarpBytes;
-    const uint32_t outw = ctile + kFCodeTile;
-    float *sa_s = reinterpret_cast<float *>(smem_raw + (base - raw) + kFWarps * kFWarpBytes +
-                                            warp * kFScalarBytes);
-    float *ss_s = sa_s + 32;
-
-    pdl_wait();
-    pdl_launch_dependents();
-    if (lane == 0)
-        tma_prefetch_map(&o_map);
-    const int64_t nblocks = nrows / G;
-    const int64_t ntiles = (nrows + 31) / 32;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kFWarps + warp;
-    const int64_t W = static_cast<int64_t>(gridDim.x) * kFWarps;
-    const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
-
-    for (int64_t t = gw; t < ntiles; t += W) {
-        const int64_t blk0 = t * BPT;
-        // ------------------------------------------------------ phase 1
-        if constexpr (PT > 0 && PT <= 8) {
-            uint4 qa[PT][2], qb[PT][2];
-            Slot sa = slot_of<NB, LPB, BPS>(blk0, 0, lane, nblocks), sb;
-            load_shards<PT>(in, sa, qa);
-#pragma unroll
-            for (int si = 0; si < SUB; si += 2) {
-                sb = slot_of<NB, LPB, BPS>(blk0, si + 1, lane, nblocks);
-                load_shards<PT>(in, sb, qb);
-                float2 T[16];
-                accumulate_fixed<NB, PT>(in, sa, qa, lane, T);
-                finish_block<NB, LPB>(T, sa, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
-                                      sa_s, ss_s);
-                if (si + 2 < SUB) {
-                    sa = slot_of<NB, LPB, BPS>(blk0, si + 2, lane, nblocks);
-                    load_shards<PT>(in, sa, qa);
-                }
-                accumulate_fixed<NB, PT>(in, sb, qb, lane, T);
-                finish_block<NB, LPB>(T, sb, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
-                                      sa_s, ss_s);
-            }
-        } else if constexpr (PT > 8) {
-#pragma unroll 1
-            for (int si = 0; si < SUB; ++si) {
-                const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
-                uint4 q[PT][2];
-                load_shards<PT>(in, sl, q);
-                float2 T[16];
-                accumulate_fixed<NB, PT>(in, sl, q, lane, T);
-                finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
-                                      sa_s, ss_s);
-            }
-        } else {
-#pragma unroll 1
-            for (int si = 0; si < SUB; ++si) {
-                const Slot sl = slot_of<NB, LPB, BPS>(blk0, si, lane, nblocks);
-                float2 T[16];
-                accumulate_any(in, P, sl, T);
-                finish_block<NB, LPB>(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile,
-                                      sa_s, ss_s);
-            }
-        }
-        __syncwarp();
-
-        // ------------------------------------------------------ phase 2
-        const int lb = lane / G;
-        const float a = sa_s[lb], sc = ss_s[lb];
-        float2 v[64];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            decode16_stage1(lds128(ctile + lane * 128 + ((static_cast<uint32_t>(j) << 4) ^ swz)), v, j);
-        // exactly the decompress kernel's arithmetic
-        if constexpr (G == 2) {
-            fwht128_upper(v);
-            fwht_pair_stage(v, lane);
-        } else {
-            fwht128_upper_but_last(v);
-        }
-        const float2 k2 = decompress_multiplier<NB>(v, sc, a);
-        if constexpr (G == 1)
-            last_stage_scaled(v, k2);
-        if (lane == 0)
-            bulk_wait_read_all();
-        __syncwarp();
-        stage_output_row<BF16OUT, G == 1>(v, k2, outw, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int64_t wrow = t * 32;
-        if (lane == 0) {
-            constexpr int nbox = BF16OUT ? 2 : 4;
-            constexpr int box_inner = BF16OUT ? 64 : 32;
-#pragma unroll
-            for (int b = 0; b < nbox; ++b)
-                tma_store_2d(&o_map, b * box_inner, static_cast<int32_t>(wrow), outw + b * 4096);
-            bulk_commit();
-        }
-        __syncwarp();  // the code tile and scalars are rewritten by the next tile's phase 1
-    }
-    if (lane == 0)
-        bulk_wait_all();
-}
 
 // ------------------------------------------------- n = 128, two CTAs/SM --
 //
-// The same pass for 128-element blocks, laid out so that two CTAs fit per
-// SM (at most 128 registers a thread):
+// Each warp takes 16-row tiles (16 blocks), laid out so that two CTAs fit
+// per SM (at most 128 registers a thread):
 //  phase 1  16 elements per lane (8 lanes per block, 4 blocks per sub-step,
 //           4 sub-steps per 16-row tile), the next sub-step's shard loads in
 //           flight for P <= 8; block statistics in the canonical order, so
@@ -539,70 +308,33 @@ cudaError_t dispatch_p128(const ShardPtrs &in, int P, const CUtensorMap &om, int
     }
 }
 
-// Per device: the kernel's dynamic shared-memory limit has been raised
-// (atomic: host threads may make their first launch concurrently).
-template <int NB, int PT, bool BF> std::atomic<bool> g_smem_set[64];
-
-template <int NB, int PT, bool BF>
-cudaError_t run_fused(const ShardPtrs &in, int P, const CUtensorMap &om, int64_t nrows, float e_target,
-                      float eps, uint8_t *oc, float *oa, float *os, cudaStream_t st, const DeviceInfo &di)
-{
-    auto kernel = taco_reduce_decompress_kernel<NB, PT, BF>;
-    if (!g_smem_set<NB, PT, BF>[di.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kFSmemBytes));
-        if (e != cudaSuccess)
-            return e;
-        g_smem_set<NB, PT, BF>[di.device].store(true, std::memory_order_release);
-    }
-    const int64_t ctas = (nrows + kFWarps * 32 - 1) / (kFWarps * 32);
-    const int grid = static_cast<int>(ctas < di.num_sms ? ctas : di.num_sms);
-    return launch_pdl(kernel, grid, kFThreads, kFSmemBytes, st, in, P, om, nrows, e_target, eps, oc, oa,
-                      os);
-}
-
-template <int NB, bool BF>
-cudaError_t dispatch_p(const ShardPtrs &in, int P, const CUtensorMap &om, int64_t nrows, float e_target,
-                       float eps, uint8_t *oc, float *oa, float *os, cudaStream_t st, const DeviceInfo &di)
-{
-    switch (P) {
-    case 2:
-        return run_fused<NB, 2, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
-    case 4:
-        return run_fused<NB, 4, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
-    case 8:
-        return run_fused<NB, 8, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
-    default:
-        return run_fused<NB, 0, BF>(in, P, om, nrows, e_target, eps, oc, oa, os, st, di);
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_reduce_decompress(int P, const ShardPtrs &in, int64_t nrows, int block, float e_target,
                                      float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
                                      void *out, bool out_bf16, cudaStream_t stream)
 {
+    if (block != 128) {
+        const cudaError_t e = launch_taco_reduce(P, in, nrows * 128 / block, block, e_target, eps, out_codes,
+                                                 out_alpha, out_scale, stream);
+        if (e != cudaSuccess)
+            return e;
+        return launch_decompress(out_codes, out_alpha, out_scale, nrows, block, out, out_bf16, false, stream);
+    }
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess)
         return e;
     CUtensorMap om;
-    const uint32_t box_rows = block == 128 ? kPRows : 32;
     const int rc = out_bf16
-                       ? encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 128, nrows, 256, 64, box_rows)
-                       : encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, 128, nrows, 512, 32, box_rows);
+                       ? encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, 128, nrows, 256, 64, kPRows)
+                       : encode_tensor_map_2d(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, 128, nrows, 512, 32, kPRows);
     if (rc != 0)
         return cudaErrorInvalidValue;
-    if (block == 128)
-        return out_bf16 ? dispatch_p128<true>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
-                                              stream, di)
-                        : dispatch_p128<false>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
-                                               stream, di);
-    return out_bf16 ? dispatch_p<256, true>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
-                                            stream, di)
-                    : dispatch_p<256, false>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
-                                             stream, di);
+    return out_bf16 ? dispatch_p128<true>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale, stream,
+                                          di)
+                    : dispatch_p128<false>(in, P, om, nrows, e_target, eps, out_codes, out_alpha, out_scale,
+                                           stream, di);
 }
 
 }  // namespace taco

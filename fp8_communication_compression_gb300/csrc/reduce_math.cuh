@@ -67,8 +67,6 @@ template <int NF> __device__ __forceinline__ void load_codes(const uint8_t *p, b
         q[h] = valid ? ldg128_stream(p + 16 * h) : make_uint4(0, 0, 0, 0);
 }
 
-__device__ __forceinline__ void load32_codes(const uint8_t *p, bool valid, uint4 (&q)[2]) { load_codes<16>(p, valid, q); }
-
 // S = sum_p decode(q_p) * w_p over a compile-time number of shards, in shard
 // order.  Every product is rounded before it is added (__fmul_rn / __fadd_rn
 // are never contracted into a fused multiply-add), so shards that cancel

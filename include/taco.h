@@ -152,11 +152,13 @@ taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes,
 
 /*
  * taco_reduce_decompress - taco_reduce_shards and taco_decompress of its
- * result in one pass.  The rank that reduces in the two-shot AllReduce
- * ([TACO] 2.B.3) both sends the compressed sum (AllGather payload) and needs
- * its reconstruction; this call writes both without reading the compressed
- * sum back.  out_codes / out_alpha / out_scale equal taco_reduce_shards's
- * outputs and `out` equals taco_decompress of them, bit for bit.
+ * result.  The rank that reduces in the two-shot AllReduce ([TACO] 2.B.3)
+ * both sends the compressed sum (AllGather payload) and needs its
+ * reconstruction.  At block 128 this call writes both in one pass, without
+ * reading the compressed sum back; at block 256 it runs the two kernels
+ * back to back on `stream`, which is faster there.  out_codes / out_alpha /
+ * out_scale equal taco_reduce_shards's outputs and `out` equals
+ * taco_decompress of them, bit for bit.
  *
  *  P, codes, alpha, scale,          as taco_reduce_shards
  *  rows, d, block, e_target, eps
