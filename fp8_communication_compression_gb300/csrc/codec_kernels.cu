@@ -83,6 +83,16 @@ constexpr uint32_t kDSmemBytes = 1024 + kWarps * kDWarpBytes + kWarps * kDStages
 // keeps compress_stages<NB>() TMA loads in flight and refills a stage as soon as the warp
 // has read it.
 
+// One 32-row bf16 input tile (two 64-column boxes) into a pipeline stage.
+// The input is read once: evict-first keeps L2 for the codes this kernel
+// writes, which the shard reduce reads next.
+__device__ __forceinline__ void load_input_tile(uint32_t dst, const CUtensorMap *x_map, int32_t y, uint32_t full)
+{
+    const uint64_t pol = policy_evict_first();
+    tma_load_2d_hint(dst, x_map, 0, y, full, pol);
+    tma_load_2d_hint(dst + kCHalfBytes, x_map, 64, y, full, pol);
+}
+
 // FMT_INT8: INT8 codes with Q_max = 127 (the fallback format); otherwise
 // E4M3 codes with Q_max = 448.
 template <int NB, bool FMT_INT8>
@@ -119,8 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t y = static_cast<int32_t>((gw + issued * W) * kWarpRows);
             const uint32_t dst = wbase + issued * kCStageBytes, full = bars + 8 * issued;
             mbar_arrive_expect_tx(full, kCStageBytes);
-            tma_load_2d(dst, &x_map, 0, y, full);
-            tma_load_2d(dst + kCHalfBytes, &x_map, 64, y, full);
+            load_input_tile(dst, &x_map, y, full);
         }
     }
     __syncwarp();
@@ -167,8 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = wbase + s * kCStageBytes, full = bars + 8 * s;
                 const int32_t y = static_cast<int32_t>(nt * kWarpRows);
                 mbar_arrive_expect_tx(full, kCStageBytes);
-                tma_load_2d(dst, &x_map, 0, y, full);
-                tma_load_2d(dst + kCHalfBytes, &x_map, 64, y, full);
+                load_input_tile(dst, &x_map, y, full);
                 ++issued;
             }
         }
@@ -278,11 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kDStages; ++s)
             mbar_init(bars + 8 * s, 1);
         fence_barrier_init();
+        // the codes are read once (evict-first L2 policy)
         for (; issued < kDStages && gw + issued * W < ntiles; ++issued) {
             const uint32_t full = bars + 8 * issued;
             mbar_arrive_expect_tx(full, kDStageBytes);
-            tma_load_2d(wbase + issued * kDStageBytes, &c_map, 0,
-                        static_cast<int32_t>((gw + issued * W) * kWarpRows), full);
+            tma_load_2d_hint(wbase + issued * kDStageBytes, &c_map, 0,
+                             static_cast<int32_t>((gw + issued * W) * kWarpRows), full, policy_evict_first());
         }
     }
     __syncwarp();
@@ -334,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 const uint32_t full = bars + 8 * s;
                 mbar_arrive_expect_tx(full, kDStageBytes);
-                tma_load_2d(wbase + s * kDStageBytes, &c_map, 0, static_cast<int32_t>(nt * kWarpRows), full);
+                tma_load_2d_hint(wbase + s * kDStageBytes, &c_map, 0, static_cast<int32_t>(nt * kWarpRows), full,
+                                 policy_evict_first());
                 ++issued;
             }
         }
@@ -354,9 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr int nbox = BF16OUT ? 2 : 4;
             constexpr int box_inner = BF16OUT ? 64 : 32;
+            // written once and not read again by this path: evict-first
+            // lets L2 write the tile back now instead of leaving it dirty
+            // for the next kernel to flush
+            const uint64_t pol = policy_evict_first();
 #pragma unroll
             for (int b = 0; b < nbox; ++b)
-                tma_store_2d(&o_map, b * box_inner, static_cast<int32_t>(wrow), outw + b * 4096);
+                tma_store_2d_hint(&o_map, b * box_inner, static_cast<int32_t>(wrow), outw + b * 4096, pol);
             bulk_commit();
         }
     }

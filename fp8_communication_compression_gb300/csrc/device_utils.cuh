@@ -107,6 +107,34 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// L2 cache policies (createpolicy) for data read or written exactly once.
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_store_2d / tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, int32_t x, int32_t y, uint32_t src,
+                                                  uint64_t pol)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 // 2-D tiled store shared -> global (rows past the tensor end are clipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t x, int32_t y,
                                              uint32_t src)
@@ -161,6 +189,18 @@ __device__ __forceinline__ uint4 ldg128_stream(const void *p)
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+    return v;
+}
+
+// The same with an L2 cache policy (policy_evict_first() for inputs that
+// nothing reads again, so that they do not displace data the next kernel
+// reads).
+__device__ __forceinline__ uint4 ldg128_stream_hint(const void *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
     return v;
 }
 

@@ -63,11 +63,11 @@ __device__ __forceinline__ Slot16 slot16(int64_t blk0, int si, int lane, int64_t
 }
 
 template <int P>
-__device__ __forceinline__ void load_shards16(const ShardPtrs &in, const Slot16 &sl, uint4 (&q)[P][1])
+__device__ __forceinline__ void load_shards16(const ShardPtrs &in, const Slot16 &sl, uint64_t pol, uint4 (&q)[P][1])
 {
 #pragma unroll
     for (int p = 0; p < P; ++p)
-        q[p][0] = sl.valid ? ldg128_stream(in.codes[p] + sl.off) : make_uint4(0, 0, 0, 0);
+        q[p][0] = sl.valid ? ldg128_stream_hint(in.codes[p] + sl.off, pol) : make_uint4(0, 0, 0, 0);
 }
 
 // T = sum_p decode(q_p) w_p for a compile-time shard count (weights loaded
@@ -93,12 +93,13 @@ __device__ __forceinline__ void accumulate16_fixed(const ShardPtrs &in, const Sl
     weighted_sum<P, 8>(q, w, T);
 }
 
-__device__ __forceinline__ void accumulate16_any(const ShardPtrs &in, int P, const Slot16 &sl, float2 (&T)[8])
+__device__ __forceinline__ void accumulate16_any(const ShardPtrs &in, int P, const Slot16 &sl, uint64_t pol,
+                                                 float2 (&T)[8])
 {
 #pragma unroll 1
     for (int p = 0; p < P; ++p) {
         uint4 q[1];
-        load_codes<8>(in.codes[p] + sl.off, sl.valid, q);
+        load_codes<8, true>(in.codes[p] + sl.off, sl.valid, q, pol);
         const float w = sl.valid ? shard_weight(__ldg(in.scale[p] + sl.blk), __ldg(in.alpha[p] + sl.blk)) : 1.0f;
         weighted_sum_step<8>(q, w, p == 0, T);
     }
@@ -173,6 +174,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
     const int64_t W = static_cast<int64_t>(gridDim.x) * kFWarps;
     const int r = lane >> 1, h = lane & 1;
     const uint32_t swz = static_cast<uint32_t>(r & 7) << 4;
+    // evict-first L2 policy: the shards' codes and the output are touched once
+    const uint64_t pol = policy_evict_first();
 
     for (int64_t t = gw; t < ntiles; t += W) {
         const int64_t blk0 = t * kPRows;
@@ -180,17 +183,17 @@ __global__ void __launch_bounds__(kFThreads, 2)
         if constexpr (PT > 0) {
             uint4 qa[PT][1], qb[PT][1];
             Slot16 sa = slot16(blk0, 0, lane, nblocks), sb;
-            load_shards16<PT>(in, sa, qa);
+            load_shards16<PT>(in, sa, pol, qa);
 #pragma unroll
             for (int si = 0; si < SUB; si += 2) {
                 sb = slot16(blk0, si + 1, lane, nblocks);
-                load_shards16<PT>(in, sb, qb);
+                load_shards16<PT>(in, sb, pol, qb);
                 float2 T[8];
                 accumulate16_fixed<PT>(in, sa, qa, lane, T);
                 finish16(T, sa, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile, sa_s, ss_s);
                 if (si + 2 < SUB) {
                     sa = slot16(blk0, si + 2, lane, nblocks);
-                    load_shards16<PT>(in, sa, qa);
+                    load_shards16<PT>(in, sa, pol, qa);
                 }
                 accumulate16_fixed<PT>(in, sb, qb, lane, T);
                 finish16(T, sb, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile, sa_s, ss_s);
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
             for (int si = 0; si < SUB; ++si) {
                 const Slot16 sl = slot16(blk0, si, lane, nblocks);
                 float2 T[8];
-                accumulate16_any(in, P, sl, T);
+                accumulate16_any(in, P, sl, pol, T);
                 finish16(T, sl, lane, e_target, eps, out_codes, out_alpha, out_scale, ctile, sa_s, ss_s);
             }
         }
@@ -262,9 +265,10 @@ __global__ void __launch_bounds__(kFThreads, 2)
         if (lane == 0) {
             constexpr int nbox = BF16OUT ? 2 : 4;
             constexpr int box_inner = BF16OUT ? 64 : 32;
+            // the output is written once and not read again here: same policy
 #pragma unroll
             for (int b = 0; b < nbox; ++b)
-                tma_store_2d(&o_map, b * box_inner, static_cast<int32_t>(t * kPRows), outw + b * 2048);
+                tma_store_2d_hint(&o_map, b * box_inner, static_cast<int32_t>(t * kPRows), outw + b * 2048, pol);
             bulk_commit();
         }
         __syncwarp();  // the code tile and scalars are rewritten by the next tile's phase 1

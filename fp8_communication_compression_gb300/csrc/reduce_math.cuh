@@ -60,11 +60,20 @@ template <int NF> __device__ __forceinline__ void encode_codes(const float2 (&v)
 
 __device__ __forceinline__ void encode32_f2(const float2 (&v)[16], float k, uint4 (&q)[2]) { encode_codes<16>(v, k, q); }
 
-template <int NF> __device__ __forceinline__ void load_codes(const uint8_t *p, bool valid, uint4 (&q)[NF / 8])
+// EF: load with the L2 cache policy `pol` (evict-first for codes that
+// nothing reads again); without EF, `pol` is ignored.
+template <int NF, bool EF = false>
+__device__ __forceinline__ void load_codes(const uint8_t *p, bool valid, uint4 (&q)[NF / 8], uint64_t pol = 0)
 {
 #pragma unroll
-    for (int h = 0; h < NF / 8; ++h)
-        q[h] = valid ? ldg128_stream(p + 16 * h) : make_uint4(0, 0, 0, 0);
+    for (int h = 0; h < NF / 8; ++h) {
+        if (!valid)
+            q[h] = make_uint4(0, 0, 0, 0);
+        else if constexpr (EF)
+            q[h] = ldg128_stream_hint(p + 16 * h, pol);
+        else
+            q[h] = ldg128_stream(p + 16 * h);
+    }
 }
 
 // S = sum_p decode(q_p) * w_p over a compile-time number of shards, in shard
