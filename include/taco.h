@@ -18,8 +18,11 @@
  *    pipeline's create and destroy calls create and release CUDA streams
  *    and events, and nothing else.)
  *  - Execution: each call validates its arguments on the host, then enqueues
- *    one kernel on `stream` and returns; results are ready when the stream
- *    reaches that point.  A NULL stream is the legacy default stream.
+ *    its work on `stream` and returns; results are ready when the stream
+ *    reaches that point.  Device-buffer calls enqueue one kernel, except
+ *    taco_reduce_decompress at block 256 (two); the host-buffer calls
+ *    enqueue copies and kernels per row chunk.  A NULL stream is the legacy
+ *    default stream.
  *  - Layout: tensors are row-major and contiguous.  A "block" is a run of
  *    `block` consecutive elements of a row; `d % block == 0`, so a tensor
  *    of rows x d elements holds nb = rows * d / block blocks, stored one after
