@@ -1,13 +1,13 @@
 // Shard reduce (TACO two-shot local step) and AGoQ FP8 gradient kernels for
 // sm_103a.  None of these needs a Hadamard rotation on its path, so they
-// use plain coalesced 16-byte loads: a lane owns 32 (or 16) consecutive
-// elements of a block, adjacent lanes own one block, per-block statistics (sum
+// use plain coalesced 16-byte loads: a lane owns 16 (shard reduces) or 32
+// (AGoQ accumulate) consecutive elements of a block, adjacent lanes own one
+// block, per-block statistics (sum
 // of squares, absolute maximum) are combined with __shfl_xor_sync, and the
 // per-shard scalars of a block are fetched once per lane group and
-// broadcast with __shfl_sync.  The shard reduces use 16 elements per lane
-// when there are more than four shards, and for up to four shards keep the
-// next grid-stride slot's loads in flight while they compute the current
-// one.
+// broadcast with __shfl_sync.  The shard reduces use 16 elements per lane,
+// and for up to four shards keep the next grid-stride slot's loads in
+// flight while they compute the current one.
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -48,11 +48,11 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
     }
 }
 
-// Elements per lane of the two reduces: 32 for up to four shards; with more
-// shards 16, so that a lane's codes in flight (16 or 32 bytes per shard)
-// leave room for occupancy.  Block statistics are bit-identical in both
-// layouts (reduce_math.cuh).
-template <int P> __host__ __device__ constexpr int elems_per_lane() { return P <= 4 ? 32 : 16; }
+// Elements per lane of the two reduces: 16 (one 16-byte code word per
+// shard).  A 32-element layout (two words per shard) is supported by the
+// lane arithmetic, with bit-identical block statistics (reduce_math.cuh),
+// but measured slower in the back-to-back step (see taco_reduce_kernel).
+template <int P> __host__ __device__ constexpr int elems_per_lane() { return 16; }
 
 // Whether a lane keeps its next grid-stride slot's loads in flight while it
 // processes the current one (two slots of registers).
@@ -149,10 +149,9 @@ __device__ __forceinline__ void for_each_slot(const ShardPtrs &in, int64_t nbloc
 // ------------------------------------------------------ TACO reduce --
 
 template <int NB, int P>
-__global__ void __launch_bounds__(kBlockThreads)
-    taco_reduce_kernel(const ShardPtrs in, int64_t nblocks, float e_target, float eps,
-                       uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
-                       float *__restrict__ out_scale)
+__device__ __forceinline__ void taco_reduce_body(const ShardPtrs &in, int64_t nblocks, float e_target, float eps,
+                                                 uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
+                                                 float *__restrict__ out_scale)
 {
     constexpr int LPB = lanes_per_block<NB, P>();
     constexpr int NF = elems_per_lane<P>() / 2;
@@ -184,6 +183,32 @@ __global__ void __launch_bounds__(kBlockThreads)
             }
         }
     });
+}
+
+// Up to four shards: at most 128 registers a thread, two CTAs per SM.  In
+// the back-to-back step (compress, reduce, decompress launched with
+// programmatic dependent launch) this layout took 122.5 us per step against
+// 136.7 us for 32 elements per lane, although launched alone it is slower
+// (30.1 against 27.1 us); with an event after the compress the 32-element
+// step took 124.6 us.  Three CTAs per SM (80 registers) measured 2 % slower.
+template <int NB, int P>
+__global__ void __launch_bounds__(kBlockThreads, 2)
+    taco_reduce_kernel(const ShardPtrs in, int64_t nblocks, float e_target, float eps,
+                       uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
+                       float *__restrict__ out_scale)
+{
+    taco_reduce_body<NB, P>(in, nblocks, e_target, eps, out_codes, out_alpha, out_scale);
+}
+
+// Five or more shards: the compiler's register choice (a two-CTA bound
+// measured 22 % slower at P = 8).
+template <int NB, int P>
+__global__ void __launch_bounds__(kBlockThreads)
+    taco_reduce_many_kernel(const ShardPtrs in, int64_t nblocks, float e_target, float eps,
+                            uint8_t *__restrict__ out_codes, float *__restrict__ out_alpha,
+                            float *__restrict__ out_scale)
+{
+    taco_reduce_body<NB, P>(in, nblocks, e_target, eps, out_codes, out_alpha, out_scale);
 }
 
 // ----------------------------------------------------- AGoQ reduce --
@@ -321,16 +346,24 @@ template <typename K> cudaError_t grid_for(K kernel, int64_t lanes_total, int *g
     return cudaSuccess;
 }
 
+template <int NB, int P> constexpr auto taco_reduce_kernel_for()
+{
+    if constexpr (P <= 4)
+        return taco_reduce_kernel<NB, P>;
+    else
+        return taco_reduce_many_kernel<NB, P>;
+}
+
 template <int NB, int P>
 cudaError_t run_taco_reduce(const ShardPtrs &in, int64_t nblocks, float e_target, float eps,
                             uint8_t *oc, float *oa, float *os, cudaStream_t st)
 {
+    constexpr auto kernel = taco_reduce_kernel_for<NB, P>();
     int grid = 0;
-    cudaError_t e = grid_for(taco_reduce_kernel<NB, P>, nblocks * lanes_per_block<NB, P>(), &grid);
+    cudaError_t e = grid_for(kernel, nblocks * lanes_per_block<NB, P>(), &grid);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(taco_reduce_kernel<NB, P>, grid, kBlockThreads, 0, st, in, nblocks, e_target, eps, oc,
-                      oa, os);
+    return launch_pdl(kernel, grid, kBlockThreads, 0, st, in, nblocks, e_target, eps, oc, oa, os);
 }
 
 template <int NB, int P>
