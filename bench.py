@@ -384,7 +384,7 @@ def laaq_leg(torch, api, peak: float) -> dict:
 
 def gpt13b_leg(torch, api, peak: float) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
-    device times (graph replays) of compress, the fused reduce + decompress,
+    device times (graph replays) of compress, reduce + decompress in one call,
     and the separate reduce and decompress."""
     from fp8_communication_compression_gb300 import workloads as W
 
@@ -437,7 +437,7 @@ def main():
     ap.add_argument("--no-int8", action="store_true", help="skip the INT8-codec leg")
     ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
     ap.add_argument("--fused", action="store_true",
-                    help="run reduce and decompress as one fused launch instead of two")
+                    help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
     ap.add_argument("--gpt13b", action="store_true",
                     help="also time the GPT-13B-shaped path (P=8, n=256; slow input generation)")
     ap.add_argument("--rows", type=int, default=None,
@@ -601,7 +601,8 @@ def main():
                 "block_values": [round(whole_job_gbs(step_bytes, args.e2e_steps, world, t), 1) for t in e2e_blocks],
                 "api": f"taco_host_pipeline_run via HostPipeline.run (pinned host in/out, {pipe.C} row chunks on 3 streams)"},
             "other_workloads": extra,
-            "gpu_launches": len(launches) * K,
+            # kernels per call: taco_reduce_decompress runs two
+            "gpu_launches": sum(2 if nm == "reduce_decompress" else 1 for nm in names) * K,
             "clocks": clk,
             "watchdog_flags": flags,
         }

@@ -165,7 +165,8 @@ def taco_reduce_decompress(codes: Sequence[torch.Tensor], alpha: Sequence[torch.
                            out_alpha: torch.Tensor | None = None, out_scale: torch.Tensor | None = None,
                            out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
                            stream=None):
-    """Compressed sum of P compressed shards and its reconstruction, in one pass."""
+    """Compressed sum of P compressed shards and its reconstruction, in one call
+    (the shard-reduce and decompress kernels back to back)."""
     P = len(codes)
     if not (len(alpha) == P and len(scale) == P) or P == 0:
         raise ValueError("codes, alpha and scale must be non-empty lists of equal length")
@@ -283,8 +284,8 @@ def taco_device_error(clear: bool = True) -> int:
 class TwoShotLocal:
     """The two-shot AllReduce's on-GPU path for P shards of [rows, d]:
     compress all shards in one call, reduce them, decompress the result
-    (two launches, or one fused reduce + decompress launch with
-    ``fused=True``).  Buffers are allocated once; ``run`` only launches."""
+    (two launches, or one ``taco_reduce_decompress`` call with ``fused=True``,
+    which runs the same two kernels).  Buffers are allocated once; ``run`` only launches."""
 
     def __init__(self, P: int, rows: int, d: int, block: int = 128, device="cuda",
                  e_target: float = E_TARGET, eps: float = EPS, out_dtype=torch.float32,

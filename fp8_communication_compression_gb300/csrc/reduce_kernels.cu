@@ -418,6 +418,28 @@ cudaError_t launch_taco_reduce(int P, const ShardPtrs &in, int64_t nblocks, int 
     return AllP<256>::taco(P, in, nblocks, e_target, eps, out_codes, out_alpha, out_scale, stream);
 }
 
+// TACO 2.B.3: the rank that reduces both sends the compressed sum (the
+// AllGather payload) and uses its reconstruction.  The two kernels run back
+// to back on the stream, so the outputs are those of the two separate calls.
+// One-pass kernels were built for both block sizes and measured slower in
+// the back-to-back step: at n=128 (16-row tiles, two CTAs per SM) the step
+// took 127.8 us against 122.5 us, at n=256 (32-row tiles, one CTA per SM)
+// the call took 135.5 us against 116.4 us.  A one-pass kernel saves the
+// re-read of the compressed sum, but its warps alternate between the
+// reduce's load-bound phase and the decompress's store-bound phase, and the
+// decompress phase holds registers and staging memory that cap it at 16
+// warps per SM.
+cudaError_t launch_reduce_decompress(int P, const ShardPtrs &in, int64_t nrows, int block, float e_target,
+                                     float eps, uint8_t *out_codes, float *out_alpha, float *out_scale,
+                                     void *out, bool out_bf16, cudaStream_t stream)
+{
+    const cudaError_t e = launch_taco_reduce(P, in, nrows * 128 / block, block, e_target, eps, out_codes,
+                                             out_alpha, out_scale, stream);
+    if (e != cudaSuccess)
+        return e;
+    return launch_decompress(out_codes, out_alpha, out_scale, nrows, block, out, out_bf16, false, stream);
+}
+
 cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block, uint8_t *out_codes,
                                float *out_scale, cudaStream_t stream)
 {

@@ -1,8 +1,8 @@
 // Lane-level arithmetic of the shard reductions, shared by the shard-reduce
-// kernels, the AGoQ accumulate kernel and phase 1 of the fused reduce +
-// decompress kernel, so that all of them produce bit-identical results.  A
-// lane owns 16 or 32 consecutive elements of a block (one or two 16-byte
-// code words per shard), kept as NF = 8 or 16 float2 registers.  The
+// kernels and the AGoQ accumulate kernel.  A lane owns 16 or 32 consecutive
+// elements of a block (one or two 16-byte code words per shard), kept as
+// NF = 8 or 16 float2 registers; the block statistics are bit-identical in
+// either layout.  The
 // weighted sums round every product before adding it (scalar __fmul_rn /
 // __fadd_rn, never contracted into a fused multiply-add); the statistics and
 // the re-encoding use packed fp32x2 instructions.

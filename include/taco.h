@@ -20,8 +20,8 @@
  *  - Execution: each call validates its arguments on the host, then enqueues
  *    its work on `stream` and returns; results are ready when the stream
  *    reaches that point.  Device-buffer calls enqueue one kernel, except
- *    taco_reduce_decompress at block 256 (two); the host-buffer calls
- *    enqueue copies and kernels per row chunk.  A NULL stream is the legacy
+ *    taco_reduce_decompress (two); the host-buffer calls enqueue copies and
+ *    kernels per row chunk.  A NULL stream is the legacy
  *    default stream.
  *  - Layout: tensors are row-major and contiguous.  A "block" is a run of
  *    `block` consecutive elements of a row; `d % block == 0`, so a tensor
@@ -155,13 +155,13 @@ taco_status taco_reduce_shards(int32_t P, const uint8_t *const *codes,
 
 /*
  * taco_reduce_decompress - taco_reduce_shards and taco_decompress of its
- * result.  The rank that reduces in the two-shot AllReduce ([TACO] 2.B.3)
- * both sends the compressed sum (AllGather payload) and needs its
- * reconstruction.  At block 128 this call writes both in one pass, without
- * reading the compressed sum back; at block 256 it runs the two kernels
- * back to back on `stream`, which is faster there.  out_codes / out_alpha /
- * out_scale equal taco_reduce_shards's outputs and `out` equals
- * taco_decompress of them, bit for bit.
+ * result in one call.  The rank that reduces in the two-shot AllReduce
+ * ([TACO] 2.B.3) both sends the compressed sum (AllGather payload) and
+ * needs its reconstruction.  The call runs the shard-reduce kernel and the
+ * decompress kernel back to back on `stream` (one-pass kernels measured
+ * slower on this GPU), so out_codes / out_alpha / out_scale equal
+ * taco_reduce_shards's outputs and `out` equals taco_decompress of them,
+ * bit for bit.
  *
  *  P, codes, alpha, scale,          as taco_reduce_shards
  *  rows, d, block, e_target, eps

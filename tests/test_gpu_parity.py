@@ -395,7 +395,7 @@ def test_full_size_two_shot_local_path(name):
     nb = rows * d // block
     path = api.TwoShotLocal(P, rows, d, block)  # the benchmark's path
     out = path.run(x)
-    if P > 1:  # the fused launch gives the same bits
+    if P > 1:  # the one-call reduce + decompress gives the same bits
         fpath = api.TwoShotLocal(P, rows, d, block, fused=True)
         fpath.codes.copy_(path.codes)
         fpath.alpha.copy_(path.alpha)
