@@ -99,25 +99,6 @@ __device__ __forceinline__ void weighted_sum(const uint4 (&q)[P][NF / 8], const 
     }
 }
 
-// Adds shard p (p > 0) or starts the sum (p == 0): the run-time-P form of
-// weighted_sum, with the same rounding.
-template <int NF>
-__device__ __forceinline__ void weighted_sum_step(const uint4 (&q)[NF / 8], float w, bool first, float2 (&S)[NF])
-{
-    float2 d[NF];
-    decode_codes<NF>(q, d);
-    const float2 w2 = make_float2(w, w);
-    if (first) {
-#pragma unroll
-        for (int i = 0; i < NF; ++i)
-            S[i] = mul2_rounded(d[i], w2);
-    } else {
-#pragma unroll
-        for (int i = 0; i < NF; ++i)
-            S[i] = add2_rounded(S[i], mul2_rounded(d[i], w2));
-    }
-}
-
 // Sum over the LPB lanes of a group.  The xor butterfly runs in ascending
 // order (1, 2, 4, ...), which adds aligned neighbours first: with partial
 // sums p_0, p_1, ... in element order the result is the balanced tree
