@@ -8,8 +8,6 @@ import os
 import subprocess
 import sys
 
-
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
