@@ -86,7 +86,7 @@ __device__ __forceinline__ void load_slot(const ShardPtrs &in, int64_t base, int
     const int part = lane % LPB;
     const int64_t t = base + lane;
     s.valid = t < total;
-    s.blk = s.valid ? t / LPB : 0;
+    s.blk = s.valid ? static_cast<int64_t>(static_cast<uint64_t>(t) / LPB) : 0;  // t >= 0: a shift
     s.off = s.blk * NB + part * elems_per_lane<P>();
 #pragma unroll
     for (int p = 0; p < P; ++p)

@@ -22,14 +22,27 @@ constexpr int kLaneElems = 32;  // elements per lane in the default layout
 // bit-identical in either layout.
 
 // 16 E4M3 codes -> 8 float2 (element order), exact.
+// 4 E4M3 codes (bytes 0..3 of w) -> 2 float2, exact: the word's two halves
+// go to the FP8-pair conversion as register halves, with no shift.
+__device__ __forceinline__ void decode4_f2(uint32_t w, float2 &a, float2 &b)
+{
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    asm("{\n\t.reg .f16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\tcvt.f32.f16 %2, c;\n\tcvt.f32.f16 %3, d;\n\t}"
+        : "=f"(a.x), "=f"(a.y), "=f"(b.x), "=f"(b.y)
+        : "r"(h0), "r"(h1));
+}
+
 __device__ __forceinline__ void decode16_f2(const uint4 q, float2 *d)
 {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        e4m3x2_to_f32x2(w[t], d[2 * t].x, d[2 * t].y);
-        e4m3x2_to_f32x2(w[t] >> 16, d[2 * t + 1].x, d[2 * t + 1].y);
-    }
+    for (int t = 0; t < 4; ++t)
+        decode4_f2(w[t], d[2 * t], d[2 * t + 1]);
 }
 
 template <int NF> __device__ __forceinline__ void decode_codes(const uint4 (&q)[NF / 8], float2 (&d)[NF])
