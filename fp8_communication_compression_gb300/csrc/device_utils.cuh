@@ -96,17 +96,6 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled load global -> shared, completing `bytes` on mbarrier `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x,
-                                            int32_t y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // L2 cache policies (createpolicy) for data read or written exactly once.
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
@@ -115,7 +104,9 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return pol;
 }
 
-// tma_store_2d / tma_load_2d with an L2 cache policy.
+// 2-D tiled TMA copies with an L2 cache policy: a store shared -> global
+// (as tma_store_2d), and a load global -> shared whose bytes complete on the
+// mbarrier `bar`.
 __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, int32_t x, int32_t y, uint32_t src,
                                                   uint64_t pol)
 {
