@@ -12,16 +12,27 @@ L2 (268 MB of bf16 per step), so no L2 flush is needed between steps.
 
 Prints one JSON line (rank 0).  ``value`` is algorithmic HBM bytes moved per
 step (reads + writes of the three kernels) x steps x ranks / max-over-ranks
-time, in GB/s.  Under torchrun each rank runs its own replica on its own
-shards (weak scaling, no data-path collective).
+time, in GB/s.  Under torchrun (N > 1) each rank holds one activation of
+the same shape and a step is the two-shot AllReduce across the ranks:
+compress, All-to-All of codes and scalars (NCCL), shard reduce of the
+received chunks, AllGather, decompress; ``--replicas`` runs independent
+replicas of the one-GPU path instead (no data-path collective).
+
+After the timed region, a sampling phase of a fixed number of steps (60 by
+default, whatever K is) records a CUDA event after every launch; the first
+sampled step is dropped.  The per-kernel figures and the roofline come from
+these samples, so they do not depend on K.  Side legs (GPT-2.7B and GPT-13B
+shapes, INT8 codec, AGoQ, LAAQ) time single kernels from CUDA-graph replays.
 
 ``--impl reference`` times the CPU oracle (the plain reference
-implementation of the method) on a bounded sample of the same workload.
+implementation of the method) on bounded samples of the same workload, on
+all host cores.
 """
 
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -37,7 +48,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ASH+DS FP8 compress/decompress/reduce GB/s and % of GB300 HBM roofline"
 HEADLINE = "gpt6.7b_p4x8192x4096_n128"
+GPT27B = "gpt2.7b_4096x2560_n128"
+GPT13B = "gpt13b_p8x8192x5120_n256"
 FALLBACK_HBM_GBS = 6800.0
+# GB300 HBM3e, nominal: 8 stacks, 7.9 TB/s (NVIDIA's published figure).  Used
+# only when the device attributes cannot be read.
+SPEC_NOMINAL_GBS = 7900.0
+L2_BYTES = 129 * 2**20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csrc", f)
                   for f in ("codec_kernels.cu", "codec_math.cuh", "device_utils.cuh")]
@@ -45,7 +62,11 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp8_communication_compression_gb300", "csr
 
 def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: bool = False) -> dict:
     """Bytes each launch must move at minimum (reads + writes), per step of
-    the two-shot local path over P shards of n elements."""
+    the two-shot local path over P shards of n elements each: the bf16
+    input, one code byte per element and two fp32 scalars (alpha, s) per
+    block, and the decompressed output of ``out_bytes`` per element.  The
+    one-call reduce + decompress (``fused``) does not re-read the compressed
+    sum."""
     nb = n // block
     comp = P * (2 * n + n + 8 * nb)             # bf16 in; codes + alpha + s out
     red_in = P * (n + 8 * nb)                   # P compressed shards in
@@ -54,6 +75,12 @@ def algorithmic_bytes(P: int, n: int, block: int, out_bytes: int = 4, fused: boo
     if fused:
         return {"compress": comp, "reduce_decompress": red_in + red_out + dec_out}
     return {"compress": comp, "reduce": red_in + red_out, "decompress": red_out + dec_out}
+
+
+def codec_bytes(n: int, block: int, out_bytes: int = 4) -> dict:
+    """Algorithmic bytes of one compress and one decompress of n elements."""
+    nb = n // block
+    return {"compress": 2 * n + n + 8 * nb, "decompress": n + 8 * nb + out_bytes * n}
 
 
 def hbm_peak():
@@ -66,15 +93,30 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-def spec_hbm_gbs(torch):
-    """Spec DRAM bandwidth from the device's attributes (memory clock x 2 for
-    double data rate x bus width), or None where torch does not expose them.
-    Context only: fractions are taken of the measured copy peak."""
-    p = torch.cuda.get_device_properties(torch.cuda.current_device())
-    clk_khz, bus_bits = getattr(p, "memory_clock_rate", None), getattr(p, "memory_bus_width", None)
-    if not clk_khz or not bus_bits:
-        return None
-    return clk_khz * 1e3 * 2 * bus_bits / 8 / 1e9
+def spec_hbm_gbs(device_index: int = 0):
+    """Spec DRAM bandwidth: peak memory clock x 2 (double data rate) x bus
+    width, read from the device attributes through the CUDA driver API
+    (torch does not expose the memory clock).  Falls back to the nominal
+    figure when the attributes cannot be read.  Returns (GB/s, source)."""
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        if cu.cuInit(0) != 0:
+            raise OSError("cuInit failed")
+        dev = ctypes.c_int()
+        if cu.cuDeviceGet(ctypes.byref(dev), int(device_index)) != 0:
+            raise OSError("cuDeviceGet failed")
+        clk, bus = ctypes.c_int(), ctypes.c_int()
+        # CU_DEVICE_ATTRIBUTE_MEMORY_CLOCK_RATE (kHz), ..._GLOBAL_MEMORY_BUS_WIDTH (bits)
+        if cu.cuDeviceGetAttribute(ctypes.byref(clk), 36, dev) != 0 or \
+                cu.cuDeviceGetAttribute(ctypes.byref(bus), 37, dev) != 0:
+            raise OSError("cuDeviceGetAttribute failed")
+        if clk.value > 0 and bus.value > 0:
+            gbs = clk.value * 1e3 * 2 * bus.value / 8 / 1e9
+            return gbs, (f"device attributes: memory clock {clk.value / 1e3:.0f} MHz x 2 (DDR) x "
+                         f"{bus.value}-bit bus")
+    except (OSError, AttributeError):
+        pass
+    return SPEC_NOMINAL_GBS, "nominal 7.9 TB/s (device attributes unavailable)"
 
 
 def kernel_source_digest() -> str:
@@ -169,42 +211,140 @@ def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) ->
     return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
 
 
-def make_inputs(rank: int, rows: int | None = None):
+def summarize(ms: list) -> dict:
+    """Mean, median, spread and count of per-launch times (ms -> us)."""
+    us = [m * 1e3 for m in ms]
+    return {"us_mean": statistics.mean(us), "us_median": statistics.median(us), "us_min": min(us),
+            "us_max": max(us), "samples": len(us)}
+
+
+# ------------------------------------------------------------ host workers --
+# Input generation and the oracle baseline run in worker processes started
+# with "spawn" (safe whatever the parent's CUDA state).
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def worker_pool(n: int):
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    return cf.ProcessPoolExecutor(max_workers=max(1, n), mp_context=mp.get_context("spawn"))
+
+
+def _tp_shard(args):
+    from fp8_communication_compression_gb300 import workloads as W
+
+    seed, rows, d, channel_scale, spikes, block = args
+    return W.tp_activation(seed, rows, d, channel_scale=channel_scale, spikes=spikes, block=block)
+
+
+def _named_shard(args):
+    from fp8_communication_compression_gb300 import workloads as W
+
+    name, p = args
+    return W.shard_input(name, p)
+
+
+def make_inputs(rank: int, rows: int | None = None, pool=None):
     from fp8_communication_compression_gb300 import workloads as W
 
     w = dict(W.WORKLOADS[HEADLINE])
     if rows is not None:
         w["rows"] = rows
-    shards = []
-    for p in range(w["shards"]):
-        seed = replica_seed(w["seeds"][p], rank)
-        shards.append(W.tp_activation(seed, w["rows"], w["d"], channel_scale=w["channel_scale"],
-                                      spikes=w["spikes"], block=w["block"]))
+    jobs = [(replica_seed(w["seeds"][p], rank), w["rows"], w["d"], w["channel_scale"], w["spikes"],
+             w["block"]) for p in range(w["shards"])]
+    shards = list(pool.map(_tp_shard, jobs)) if pool else [_tp_shard(j) for j in jobs]
     return w, np.stack(shards)
 
 
-def cpu_baseline(bits: np.ndarray, w: dict, sample_rows: int) -> dict:
-    """The oracle, as it stands, on the first ``sample_rows`` rows of every
-    shard: compress each shard, reduce, decompress.  Single-threaded."""
+def _oracle_path_rows(task):
+    """Worker: the oracle's two-shot local path (compress every shard,
+    reduce, decompress) on rows r0..r1 of the shards held in shared memory.
+    Returns the decompressed rows' sum, so that the work is not dead."""
+    from multiprocessing import shared_memory
+
     import oracle
 
-    P, block = bits.shape[0], w["block"]
+    shm_name, shape, r0, r1, block = task
+    shm = shared_memory.SharedMemory(name=shm_name)
+    view = np.ndarray(shape, dtype=np.uint16, buffer=shm.buf)
+    sub = [view[p, r0:r1].copy() for p in range(shape[0])]  # copies: the segment is closed next
+    del view
+    shm.close()
+    comp = [oracle.compress(s, block) for s in sub]
+    rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
+    return float(oracle.decompress(rc, ra, rs, block).sum())
+
+
+class SharedShards:
+    """bf16 shard bits [P, rows, d] in a shared-memory segment for the pool."""
+
+    def __init__(self, bits: np.ndarray):
+        from multiprocessing import shared_memory
+
+        self.shm = shared_memory.SharedMemory(create=True, size=bits.nbytes)
+        np.ndarray(bits.shape, dtype=np.uint16, buffer=self.shm.buf)[...] = bits
+        self.shape = tuple(bits.shape)
+
+    def tasks(self, rows: int, pieces: int, block: int):
+        step = max(1, -(-rows // pieces))
+        return [(self.shm.name, self.shape, r, min(rows, r + step), block) for r in range(0, rows, step)]
+
+    def close(self):
+        self.shm.close()
+        self.shm.unlink()
+
+
+def oracle_wall_seconds(pool, shards: SharedShards, rows: int, cores: int, block: int) -> float:
+    """Wall time of the oracle path over the first ``rows`` rows of every
+    shard, split over ``cores`` workers (a few row ranges each)."""
+    tasks = shards.tasks(rows, 4 * cores, block)
+    t0 = time.perf_counter()
+    list(pool.map(_oracle_path_rows, tasks))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(bits: np.ndarray, w: dict, sample_rows: int, pool, cores: int) -> dict:
+    """The oracle, as it stands, timed twice: single-threaded on the first
+    ``sample_rows`` rows of every shard, and on all host cores (one worker
+    process per core, row ranges handed out in turn) over the whole
+    workload.  Both run compress of each shard, reduce and decompress."""
+    import oracle
+
+    P, block, rows = bits.shape[0], w["block"], bits.shape[1]
     sub = [np.ascontiguousarray(bits[p, :sample_rows]) for p in range(P)]
-    n = sample_rows * w["d"]
+    n1 = sample_rows * w["d"]
     t0 = time.perf_counter()
     comp = [oracle.compress(s, block) for s in sub]
     rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
     oracle.decompress(rc, ra, rs, block)
-    dt = time.perf_counter() - t0
-    total = sum(algorithmic_bytes(P, n, block).values())
-    return {"value": total / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {sample_rows} of {w['rows']} rows of each of the {P} shards "
-                      f"({P * n} elements compressed, {n} reduced and decompressed), "
-                      f"{dt:.1f} s single-threaded"}
+    dt1 = time.perf_counter() - t0
+    single = sum(algorithmic_bytes(P, n1, block).values()) / dt1 / 1e9
+    shards = SharedShards(bits)
+    try:
+        oracle_wall_seconds(pool, shards, min(rows, 4 * cores), cores, block)  # workers load the oracle
+        dtn = oracle_wall_seconds(pool, shards, rows, cores, block)
+    finally:
+        shards.close()
+    n = rows * w["d"]
+    allc = sum(algorithmic_bytes(P, n, block).values()) / dtn / 1e9
+    return {"value": allc, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {rows} rows of each of the {P} shards ({P * n} elements compressed, {n} reduced "
+                      f"and decompressed) on {cores} worker processes, {dtn:.1f} s wall",
+            "single_thread": {"value": single, "unit": "GB/s", "cores": 1,
+                              "sample": f"first {sample_rows} of {rows} rows of each of the {P} shards "
+                                        f"({P * n1} elements compressed, {n1} reduced and decompressed), "
+                                        f"{dt1:.1f} s"}}
 
 
 def run_reference(args, rank: int, world: int) -> None:
-    """The reference arm: the CPU oracle timed on bounded samples."""
+    """The reference arm: the CPU oracle timed on bounded samples, on all
+    host cores."""
     if rank != 0:
         return
     from fp8_communication_compression_gb300 import workloads as W
@@ -213,25 +353,22 @@ def run_reference(args, rank: int, world: int) -> None:
     oracle.build()
     w = W.WORKLOADS[HEADLINE]
     P, block, rows_s = w["shards"], w["block"], args.ref_rows
-    bits = np.stack([W.tp_activation(w["seeds"][p], rows_s, w["d"], channel_scale=True, block=block)
-                     for p in range(P)])
+    cores = host_cores()
     n = rows_s * w["d"]
     step_bytes = sum(algorithmic_bytes(P, n, block).values())
-
-    def step():
-        comp = [oracle.compress(bits[p], block) for p in range(P)]
-        rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
-        oracle.decompress(rc, ra, rs, block)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+    with worker_pool(cores) as pool:
+        jobs = [(w["seeds"][p], rows_s, w["d"], True, False, block) for p in range(P)]
+        bits = np.stack(list(pool.map(_tp_shard, jobs)))
+        shards = SharedShards(bits)
+        try:
+            for _ in range(args.warmup):
+                oracle_wall_seconds(pool, shards, rows_s, cores, block)
+            dt = sum(oracle_wall_seconds(pool, shards, rows_s, cores, block) for _ in range(args.steps))
+        finally:
+            shards.close()
     value = step_bytes * args.steps / dt / 1e9
     sample = (f"each step: {rows_s} of {w['rows']} rows of each of the {P} shards "
-              f"(compress {P * n}, reduce and decompress {n} elements), single-threaded")
+              f"(compress {P * n}, reduce and decompress {n} elements), split over {cores} worker processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
@@ -239,11 +376,13 @@ def run_reference(args, rank: int, world: int) -> None:
         "data": "synthetic",
         "config": {"workload": HEADLINE, "P": P, "rows": w["rows"], "d": w["d"], "block": block,
                    "sample_rows": rows_s},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
+
+# ------------------------------------------------------------- GPU timing --
 
 def time_launches(torch, fn, reps: int, stream, replays: int = 3) -> float:
     """Mean device time (ms) per launch of ``fn``: ``reps`` calls captured in
@@ -274,6 +413,31 @@ def time_launches(torch, fn, reps: int, stream, replays: int = 3) -> float:
     return ms
 
 
+def sample_kernel_times(torch, launches, x, stream, samples: int) -> dict:
+    """Per-launch device times of the step's launches: ``samples`` + 1 steps,
+    each with a CUDA event before the first launch and after every launch;
+    the first step is dropped (it follows the host's preceding work).  The
+    events separate the launches, so each sample includes the launch's own
+    start-up, which programmatic dependent launch hides in the unsampled
+    step."""
+    nl = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(samples + 1)]
+    for e in ev:
+        e[0].record(stream)
+        for i, (_, fn) in enumerate(launches):
+            fn(x)
+            e[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return {name: [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(1, samples + 1)]
+            for i, (name, _) in enumerate(launches)}
+
+
+def kernel_entry(ms: float, nbytes: int, peak: float, **extra) -> dict:
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"us_per_launch": ms * 1e3, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak,
+            **extra}
+
+
 def agoq_leg(torch, api, peak: float) -> dict:
     """AGoQ accumulate over the 2^28-element buffer and the P=8 reduce of
     2^25-element shards; inputs larger than L2, timed per launch from graph
@@ -299,13 +463,8 @@ def agoq_leg(torch, api, peak: float) -> dict:
     api.agoq_reduce_shards(sc, ss, block, oc, os_)
     red_ms = time_launches(torch, lambda: api.agoq_reduce_shards(sc, ss, block, oc, os_), 5, stream)
     red_bytes = (P + 1) * (ns + 4 * (ns // block))
-    out = {}
-    for name, ms, b, units in (("accumulate", acc_ms, acc_bytes, f"2^28 elements, n={block}"),
-                               ("reduce", red_ms, red_bytes, f"P={P} x 2^25 elements, n={block}")):
-        gbs = b / (ms / 1e3) / 1e9
-        out[name] = {"us_per_launch": ms * 1e3, "algorithmic_bytes": b, "gbs": gbs,
-                     "frac_of_peak": gbs / peak, "workload": units}
-    return out
+    return {"accumulate": kernel_entry(acc_ms, acc_bytes, peak, workload=f"2^28 elements, n={block}"),
+            "reduce": kernel_entry(red_ms, red_bytes, peak, workload=f"P={P} x 2^25 elements, n={block}")}
 
 
 def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) -> dict:
@@ -334,9 +493,7 @@ def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) 
     ms = {"compress_int8": time_launches(torch, comp, 10, stream),
           "decompress_int8": time_launches(torch, dec, 10, stream)}
     nbytes = {"compress_int8": P * (2 * n + n + 8 * nb), "decompress_int8": n + 8 * nb + 4 * n}
-    return {k: {"us_per_launch": ms[k] * 1e3, "algorithmic_bytes": nbytes[k],
-                "gbs": nbytes[k] / (ms[k] / 1e3) / 1e9, "frac_of_peak": nbytes[k] / (ms[k] / 1e3) / 1e9 / peak}
-            for k in ms}
+    return {k: kernel_entry(ms[k], nbytes[k], peak) for k in ms}
 
 
 def laaq_leg(torch, api, peak: float) -> dict:
@@ -375,25 +532,77 @@ def laaq_leg(torch, api, peak: float) -> dict:
             dequant()
         for name, fn, b in (("quantize", quant, 2 * n + n * bits // 8 + 4 * (n // block)),
                             ("dequantize", dequant, n * bits // 8 + 4 * (n // block) + 2 * n)):
-            ms = time_launches(torch, fn, 12, stream)
-            gbs = b / (ms / 1e3) / 1e9
-            res[f"{name}_{bits}bit"] = {"us_per_launch": ms * 1e3, "algorithmic_bytes": b, "gbs": gbs,
-                                        "frac_of_peak": gbs / peak}
+            res[f"{name}_{bits}bit"] = kernel_entry(time_launches(torch, fn, 12, stream), b, peak)
     return res
 
 
-def gpt13b_leg(torch, api, peak: float) -> dict:
+def gpt27b_leg(torch, api, peak: float) -> dict:
+    """The GPT-2.7B-shaped round trip (one bf16 [4096, 2560] activation,
+    n=128): compress, decompress to fp32, and the two back to back, timed per
+    launch from graph replays, L2-flushed and warm.  The tensor and its
+    outputs (74 MB) fit in the 129 MB L2, so the flushed figures rotate over
+    12 copies in distinct buffers (888 MB): between two launches on the same
+    copy, the launches on the other eleven move more than twice the L2.  The
+    warm figures repeat the launch on one copy, whose data then stays in
+    L2."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    w = W.WORKLOADS[GPT27B]
+    rows, d, block = w["rows"], w["d"], w["block"]
+    n, nb, R = rows * d, rows * d // block, 12
+    bits = torch.from_numpy(W.shard_input(GPT27B, 0).view(np.int16)).cuda().view(torch.bfloat16)
+    x = bits.unsqueeze(0).repeat(R, 1, 1).contiguous()
+    codes = torch.empty((R, rows, d), dtype=torch.uint8, device="cuda")
+    alpha = torch.empty((R, nb), dtype=torch.float32, device="cuda")
+    scale = torch.empty((R, nb), dtype=torch.float32, device="cuda")
+    out = torch.empty((R, rows, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    it = [0]
+
+    def comp(i):
+        api.taco_compress(x[i], block, codes=codes[i], alpha=alpha[i], scale=scale[i])
+
+    def dec(i):
+        api.taco_decompress(codes[i], alpha[i], scale[i], block, out=out[i])
+
+    def rotating(fn):
+        def call():
+            i = it[0] % R
+            it[0] += 1
+            fn(i)
+        return call
+
+    for i in range(R):
+        comp(i)
+        dec(i)
+    b = codec_bytes(n, block)
+    b["round_trip"] = b["compress"] + b["decompress"]
+    fns = {"compress": comp, "decompress": dec, "round_trip": lambda i: (comp(i), dec(i))}
+    res = {}
+    for name, fn in fns.items():
+        it[0] = 0
+        flushed = time_launches(torch, rotating(fn), 2 * R, stream)
+        warm = time_launches(torch, lambda: fn(0), 2 * R, stream)
+        res[name] = kernel_entry(flushed, b[name], peak, l2="flushed (12-copy rotation)",
+                                 warm=kernel_entry(warm, b[name], peak, l2="warm (one copy)"))
+    res["round_trip"]["launches"] = "compress then decompress of the same copy (2 launches)"
+    return res
+
+
+def gpt13b_leg(torch, api, peak: float, pool=None) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     device times (graph replays) of compress, reduce + decompress in one call,
     and the separate reduce and decompress."""
     from fp8_communication_compression_gb300 import workloads as W
 
-    name = "gpt13b_p8x8192x5120_n256"
-    w = W.WORKLOADS[name]
+    w = W.WORKLOADS[GPT13B]
     P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
-    bits = np.stack([W.shard_input(name, p) for p in range(P)])
-    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-    del bits
+    jobs = [(GPT13B, p) for p in range(P)]
+    shards = list(pool.map(_named_shard, jobs)) if pool else [_named_shard(j) for j in jobs]
+    x = torch.empty((P, rows, d), dtype=torch.bfloat16, device="cuda")
+    for p in range(P):
+        x[p].view(torch.int16).copy_(torch.from_numpy(shards[p].view(np.int16)))
+    del shards
     path = api.TwoShotLocal(P, rows, d, block, fused=True)
     for _ in range(3):
         path.run(x)
@@ -413,9 +622,127 @@ def gpt13b_leg(torch, api, peak: float) -> dict:
           "decompress": time_launches(torch, dec, 16, stream)}
     nb = dict(algorithmic_bytes(P, rows * d, block, fused=True))
     nb.update(algorithmic_bytes(P, rows * d, block, fused=False))
-    return {k: {"us_per_launch": ms[k] * 1e3, "algorithmic_bytes": nb[k],
-                "gbs": nb[k] / (ms[k] / 1e3) / 1e9, "frac_of_peak": nb[k] / (ms[k] / 1e3) / 1e9 / peak}
-            for k in ms}
+    return {k: kernel_entry(ms[k], nb[k], peak) for k in ms}
+
+
+def exchange_bytes(world: int, rows: int, d: int, block: int, out_bytes: int = 4) -> dict:
+    """Algorithmic bytes of one rank's kernels in one two-shot AllReduce over
+    ``world`` ranks of a [rows, d] tensor: compress of the whole tensor, the
+    reduce of ``world`` received chunks of R = ceil(rows / world) rows into
+    one, and the decompress of the ``world`` gathered chunks."""
+    R = -(-rows // world)
+    n, c = rows * d, R * d
+    return {"compress": 3 * n + 8 * (n // block),
+            "reduce": (world + 1) * (c + 8 * (c // block)),
+            "decompress": world * (c + 8 * (c // block) + out_bytes * c)}
+
+
+def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
+    """The two-shot AllReduce across the ranks (NCCL): each rank holds one
+    bf16 [8192, 4096] activation of the GPT-6.7B shape (seeded by rank; with
+    four ranks these are the headline's four shards) and every step runs
+    compress, All-to-All, shard reduce, AllGather and decompress."""
+    import torch
+    import torch.distributed as dist
+
+    from fp8_communication_compression_gb300 import api, exchange
+    from fp8_communication_compression_gb300 import workloads as W
+
+    w = W.WORKLOADS[HEADLINE]
+    rows = args.rows or w["rows"]
+    d, block = w["d"], w["block"]
+    bits = pool.submit(_tp_shard, (rank, rows, d, w["channel_scale"], w["spikes"], block)).result()
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    ar = exchange.TwoShotAllReduce(rows, d, block)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ar.run(x)
+    torch.cuda.synchronize()
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
+    time.sleep(0.2 if clocks else 0)
+    dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(K):
+        ar.run(x)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
+    # per-kernel samples: events around the three local launches
+    names = ("compress", "reduce", "decompress")
+    ns = max(2, args.kernel_samples)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(ns + 1)]
+    for e in ev:
+        e[0].record(stream)
+        ar.compress(x)
+        e[1].record(stream)
+        ar.exchange()
+        e[2].record(stream)
+        ar.reduce()
+        e[3].record(stream)
+        ar.gather()
+        e[4].record(stream)
+        ar.decompress()
+        e[5].record(stream)
+    torch.cuda.synchronize()
+    pairs = {"compress": (0, 1), "reduce": (2, 3), "decompress": (4, 5)}
+    samples = {k: [ev[j][a].elapsed_time(ev[j][b]) for j in range(1, ns + 1)] for k, (a, b) in pairs.items()}
+    # end to end: pinned host input in, result out, every step
+    h_in = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
+    h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
+    h_out = torch.empty((rows, d), dtype=torch.float32, pin_memory=True)
+    E = max(1, args.e2e_steps)
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        x.copy_(h_in, non_blocking=True)
+        h_out.copy_(ar.run(x), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+    flags = api.taco_device_error(clear=True)
+    if rank == 0:
+        peak, peak_src = hbm_peak()
+        spec, spec_src = spec_hbm_gbs(local)
+        nbytes = exchange_bytes(world, rows, d, block)
+        step_bytes = sum(nbytes.values())
+        kern = {}
+        for k in names:
+            st = summarize(samples[k])
+            kern[k] = kernel_entry(st["us_mean"] / 1e3, nbytes[k], peak, **st)
+        achieved = kern["compress"]["gbs"]
+        line = {
+            "metric": METRIC, "value": whole_job_gbs(step_bytes, K, world, elapsed_ms), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": elapsed_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"two-shot AllReduce of one bf16 [{rows}, {d}] activation per rank "
+                                   f"(GPT-6.7B shape, block {block}) across {world} ranks",
+                       "rows": rows, "d": d, "block": block, "parallelism": f"tp{world} two-shot exchange (NCCL)",
+                       "bytes_per_step_per_rank": step_bytes,
+                       "exchange_bytes_sent_per_rank": ar.bytes_exchanged(),
+                       "l2": "inputs larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "kernel": f"taco_compress_kernel<{block}>", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": peak_src, "samples": ns, "spec_peak": spec, "spec_peak_source": spec_src,
+                         "frac_of_spec": achieved / spec},
+            "kernels": kern,
+            "e2e": {"value": whole_job_gbs(step_bytes, E, world, e2e_ms), "unit": "GB/s",
+                    "h2d_bytes_per_step": 2 * rows * d, "d2h_bytes_per_step": 4 * rows * d,
+                    "api": "TwoShotAllReduce.run with pinned host copies in and out"},
+            "gpu_launches": 3 * K,
+            "clocks": clk,
+            "watchdog_flags": flags,
+        }
+        print(json.dumps(line), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
 
 
 def main():
@@ -425,21 +752,23 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--kernel-events-every", type=int, default=10,
-                    help="record per-kernel CUDA events on every N-th timed step")
+    ap.add_argument("--kernel-samples", type=int, default=60,
+                    help="steps of the per-kernel sampling phase after the timed region")
     ap.add_argument("--e2e-chunks", type=int, default=4, help="row chunks of the host pipeline")
     ap.add_argument("--e2e-blocks", type=int, default=5, help="timed blocks of the end-to-end leg (median reported)")
-    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows per shard")
-    ap.add_argument("--ref-rows", type=int, default=128, help="reference arm rows per shard per step")
+    ap.add_argument("--cpu-rows", type=int, default=2048, help="single-thread oracle sample rows per shard")
+    ap.add_argument("--ref-rows", type=int, default=1024, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi clock sampling")
     ap.add_argument("--no-agoq", action="store_true", help="skip the AGoQ accumulate/reduce leg")
     ap.add_argument("--no-int8", action="store_true", help="skip the INT8-codec leg")
     ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
+    ap.add_argument("--no-gpt27b", action="store_true", help="skip the GPT-2.7B-shaped round-trip leg")
+    ap.add_argument("--no-gpt13b", action="store_true", help="skip the GPT-13B-shaped leg")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
-    ap.add_argument("--gpt13b", action="store_true",
-                    help="also time the GPT-13B-shaped path (P=8, n=256; slow input generation)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="under torchrun: independent replicas of the one-GPU path instead of the exchange")
     ap.add_argument("--rows", type=int, default=None,
                     help="rows per shard (a smaller case of the same workload, e.g. for profiling)")
     args = ap.parse_args()
@@ -453,10 +782,18 @@ def main():
         run_reference(args, rank, world)
         return
 
+    cores = max(1, host_cores() // max(1, int(os.environ.get("LOCAL_WORLD_SIZE", world))))
+    pool = worker_pool(cores)
+
     import torch
 
     from fp8_communication_compression_gb300 import api
 
+    if world > 1 and not args.replicas:
+        run_exchange(args, rank, world, local, pool)
+        pool.shutdown()
+        return
+    w, bits = make_inputs(rank, args.rows, pool)
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
@@ -464,7 +801,6 @@ def main():
 
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    w, bits = make_inputs(rank, args.rows)
     P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
     n = rows * d
 
@@ -481,11 +817,6 @@ def main():
     nbytes = path.bytes_per_step()
     step_bytes = sum(nbytes.values())
     K = args.steps
-    # per-kernel events on every E-th step of the timed region; the other
-    # steps run without events between their launches
-    E = max(1, args.kernel_events_every)
-    sampled = list(range(0, K, E))
-    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for k in sampled}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
     time.sleep(0.2 if clocks else 0)
@@ -493,16 +824,9 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for k in range(K):
-        e = ev.get(k)
-        if e is None:
-            for _, fn in launches:
-                fn(x)
-            continue
-        e[0].record(stream)
-        for i, (_, fn) in enumerate(launches):
+    for _ in range(K):
+        for _, fn in launches:
             fn(x)
-            e[i + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -519,10 +843,10 @@ def main():
             t_region += 200 * elapsed_ms / K / 1e3
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
-
     elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
-    per = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in sampled)
-           for i, name in enumerate(names)}
+
+    # per-kernel figures: a sampling phase of a fixed number of steps
+    samples = sample_kernel_times(torch, launches, x, stream, max(2, args.kernel_samples))
 
     # end to end through the public API with pinned host buffers
     e2e_ms = None
@@ -551,20 +875,24 @@ def main():
             e2e_blocks.append(max_over_ranks(e0.elapsed_time(e1), dist, "cuda"))
         e2e_ms = statistics.median(e2e_blocks)
     peak, peak_src = hbm_peak()
-    spec = spec_hbm_gbs(torch)
+    spec, spec_src = spec_hbm_gbs(local)
     extra = {}
     if rank == 0 and not args.no_int8:
         extra["int8_" + HEADLINE] = int8_leg(torch, api, x, P, rows, d, block, peak)
-    if rank == 0 and not args.no_agoq:
+    if rank == 0:
         del path, x
         torch.cuda.empty_cache()
+    if rank == 0 and not args.no_gpt27b:
+        extra[GPT27B] = gpt27b_leg(torch, api, peak)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_gpt13b:
+        extra[GPT13B] = gpt13b_leg(torch, api, peak, pool)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_agoq:
         extra["agoq"] = agoq_leg(torch, api, peak)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_laaq:
         extra["laaq_8192x4096_n128"] = laaq_leg(torch, api, peak)
-        torch.cuda.empty_cache()
-    if rank == 0 and args.gpt13b:
-        extra["gpt13b_p8x8192x5120_n256"] = gpt13b_leg(torch, api, peak)
         torch.cuda.empty_cache()
     flags = api.taco_device_error(clear=True)
 
@@ -572,10 +900,10 @@ def main():
         value = whole_job_gbs(step_bytes, K, world, elapsed_ms)
         kern = {}
         for name in names:
-            gbs = nbytes[name] / (per[name] / 1e3) / 1e9
-            kern[name] = {"us_per_launch": per[name] * 1e3, "algorithmic_bytes": nbytes[name],
-                          "gbs": gbs, "frac_of_peak": gbs / peak}
+            st = summarize(samples[name])
+            kern[name] = kernel_entry(st["us_mean"] / 1e3, nbytes[name], peak, **st)
         achieved = kern["compress"]["gbs"]
+        ns = len(samples[names[0]])
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
@@ -583,7 +911,8 @@ def main():
             "config": {"workload": HEADLINE if args.rows is None else f"{HEADLINE} (rows={rows})",
                        "P": P, "rows": rows, "d": d, "block": block,
                        "launches": names,
-                       "kernel_events": f"per-launch CUDA events on every {E}th of the {K} timed steps",
+                       "kernel_events": (f"per-launch CUDA events in a sampling phase of {ns + 1} steps after "
+                                         f"the timed region, first step dropped ({ns} samples per kernel)"),
                        "bytes_per_step": step_bytes,
                        "input_bf16_bytes_per_step": 2 * P * n,
                        "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
@@ -591,9 +920,11 @@ def main():
             "roofline": {"bound": "hbm", "kernel": f"taco_compress_kernel<{block}>",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": committed_traffic(), "peak_source": peak_src,
-                         "spec_peak": spec, "frac_of_spec": achieved / spec if spec else None},
+                         "samples": ns,
+                         "spec_peak": spec, "spec_peak_source": spec_src, "frac_of_spec": achieved / spec},
             "kernels": kern,
             "step_frac_of_peak": value / world / peak,
+            "step_frac_of_spec": value / world / spec,
             "e2e": None if e2e_ms is None else {
                 "value": whole_job_gbs(step_bytes, args.e2e_steps, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * P * n, "d2h_bytes_per_step": 4 * n,
@@ -610,8 +941,9 @@ def main():
             line["clocks"]["window"] = (f"timed region plus {soak} further identical steps"
                                         if soak else "timed region")
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(bits, w, args.cpu_rows)
+            line["cpu_baseline"] = cpu_baseline(bits, w, args.cpu_rows, pool, cores)
         print(json.dumps(line), flush=True)
+    pool.shutdown()
     if dist:
         dist.barrier()
         dist.destroy_process_group()

@@ -44,3 +44,49 @@ def test_traffic_record_is_dropped_when_the_sources_change(tmp_path, monkeypatch
     assert bench.committed_traffic() is None
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
     assert bench.committed_traffic() is None
+
+
+def test_codec_bytes_of_the_round_trip_leg():
+    n = 4096 * 2560  # the GPT-2.7B-shaped activation
+    b = bench.codec_bytes(n, 128)
+    assert b["compress"] == n * (2 + 1 + 8 / 128)
+    assert b["decompress"] == n * (1 + 8 / 128 + 4)
+    assert bench.codec_bytes(n, 256, out_bytes=2)["decompress"] == n * (1 + 8 / 256 + 2)
+
+
+def test_kernel_sample_summary_reports_count_and_spread():
+    st = bench.summarize([0.070, 0.069, 0.071, 0.090])
+    assert st["samples"] == 4
+    assert st["us_min"] == pytest.approx(69.0) and st["us_max"] == pytest.approx(90.0)
+    assert st["us_mean"] == pytest.approx(75.0) and st["us_median"] == pytest.approx(70.5)
+    e = bench.kernel_entry(0.075, 411_041_792, 6780.0, **st)
+    assert e["gbs"] == pytest.approx(411_041_792 / 75e-6 / 1e9)
+    assert e["frac_of_peak"] == pytest.approx(e["gbs"] / 6780.0) and e["samples"] == 4
+
+
+def test_spec_peak_is_always_reported():
+    gbs, src = bench.spec_hbm_gbs(0)
+    assert gbs > 0 and src
+    # without a GPU (this host) the nominal GB300 figure stands in
+    import torch
+
+    if not torch.cuda.is_available():
+        assert gbs == bench.SPEC_NOMINAL_GBS and "nominal" in src
+
+
+@pytest.mark.parametrize("world", [2, 4, 8])
+def test_exchange_bytes_split_the_local_path_across_ranks(world):
+    # W ranks of one [8192, 4096] activation each: together they compress
+    # what the one-GPU path compresses for P = W shards, each reduces 1/W of
+    # the rows over W shards, and each decompresses the whole sum
+    rows, d, block = 8192, 4096, 128
+    e = bench.exchange_bytes(world, rows, d, block)
+    local = bench.algorithmic_bytes(world, rows * d, block)
+    assert world * e["compress"] == local["compress"]
+    assert world * e["reduce"] == local["reduce"]
+    assert e["decompress"] == local["decompress"]
+    # a ragged split pads the last chunk: the padded rows are reduced and
+    # decompressed too
+    r = bench.exchange_bytes(3, 100, 256, 128)
+    assert r["reduce"] == 4 * (34 * 256 + 8 * 34 * 2)
+    assert r["decompress"] == 3 * (34 * 256 * 5 + 8 * 34 * 2)
