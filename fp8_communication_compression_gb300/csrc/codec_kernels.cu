@@ -118,7 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int W = gridDim.x * kWarps;
 
     pdl_wait();
-    pdl_launch_dependents();
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&x_map);
@@ -279,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
 
     pdl_wait();
-    pdl_launch_dependents();
     int issued = 0;
     if (lane == 0) {
         tma_prefetch_map(&c_map);

@@ -20,7 +20,6 @@ __global__ void __launch_bounds__(kEThreads)
     e4m3_encode_kernel(const float *__restrict__ x, int64_t n, uint8_t *__restrict__ codes)
 {
     pdl_wait();
-    pdl_launch_dependents();
     const int64_t groups = n / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += stride) {

@@ -1,13 +1,13 @@
 // Shard reduce (TACO two-shot local step) and AGoQ FP8 gradient kernels for
 // sm_103a.  None of these needs a Hadamard rotation on its path, so they
-// use plain coalesced 16-byte loads: a lane owns 16 (shard reduces) or 32
-// (AGoQ accumulate) consecutive elements of a block, adjacent lanes own one
-// block, per-block statistics (sum
-// of squares, absolute maximum) are combined with __shfl_xor_sync, and the
-// per-shard scalars of a block are fetched once per lane group and
-// broadcast with __shfl_sync.  The shard reduces use 16 elements per lane,
-// and for up to four shards keep the next grid-stride slot's loads in
-// flight while they compute the current one.
+// use plain coalesced 16-byte loads: a lane owns 32 (AGoQ accumulate, shard
+// reduces of up to four shards) or 16 (shard reduces of more shards)
+// consecutive elements of a block, adjacent lanes own one block, per-block
+// statistics (sum of squares, absolute maximum) are combined with
+// __shfl_xor_sync, and the per-shard scalars of a block are fetched once per
+// lane group and broadcast with __shfl_sync.  For up to four shards the
+// shard reduces keep the next grid-stride slot's loads in flight while they
+// compute the current one.
 //
 // TACO shard reduce, computed in the Hadamard domain.  With c = 1/sqrt(n)
 // and H the Sylvester matrix (c H c H = I), shard p decompresses to
@@ -48,11 +48,11 @@ __device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
     }
 }
 
-// Elements per lane of the two reduces: 16 (one 16-byte code word per
-// shard).  A 32-element layout (two words per shard) is supported by the
-// lane arithmetic, with bit-identical block statistics (reduce_math.cuh),
-// but measured slower in the back-to-back step (see taco_reduce_kernel).
-template <int P> __host__ __device__ constexpr int elems_per_lane() { return 16; }
+// Elements per lane of the two reduces: 32 (two 16-byte code words per
+// shard) for up to four shards, 16 (one word) above that, where the P words
+// in flight per slot would otherwise cost occupancy.  The block statistics
+// are bit-identical in either layout (reduce_math.cuh).
+template <int P> __host__ __device__ constexpr int elems_per_lane() { return P <= 4 ? 32 : 16; }
 
 // Whether a lane keeps its next grid-stride slot's loads in flight while it
 // processes the current one (two slots of registers).
@@ -157,7 +157,6 @@ __device__ __forceinline__ void taco_reduce_body(const ShardPtrs &in, int64_t nb
     constexpr int NF = elems_per_lane<P>() / 2;
     constexpr int ROUNDS = rounds_of<NB, P>();
     pdl_wait();
-    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     // the shards' codes are read once: evict-first keeps L2 for the reduced
     // codes, which the decompress reads next
@@ -185,12 +184,14 @@ __device__ __forceinline__ void taco_reduce_body(const ShardPtrs &in, int64_t nb
     });
 }
 
-// Up to four shards: at most 128 registers a thread, two CTAs per SM.  In
-// the back-to-back step (compress, reduce, decompress launched with
-// programmatic dependent launch) this layout took 122.5 us per step against
-// 136.7 us for 32 elements per lane, although launched alone it is slower
-// (30.1 against 27.1 us); with an event after the compress the 32-element
-// step took 124.6 us.  Three CTAs per SM (80 registers) measured 2 % slower.
+// Up to four shards: 32 elements per lane, at most 128 registers a thread,
+// two CTAs per SM.  Launched alone at the GPT-6.7B size it takes 27.1 us
+// against 30.1 us with 16 elements per lane.  In the back-to-back step
+// (compress, reduce, decompress launched with programmatic dependent launch)
+// the step took 118.9 us against 120.3 us with 16 elements.  (While every
+// kernel triggered its dependents at its start, the 32-element step took
+// 132.7 us: device_utils.cuh.)  Three CTAs per SM (80 registers) measured
+// 2 % slower with 16 elements.
 template <int NB, int P>
 __global__ void __launch_bounds__(kBlockThreads, 2)
     taco_reduce_kernel(const ShardPtrs in, int64_t nblocks, float e_target, float eps,
@@ -221,7 +222,6 @@ __global__ void __launch_bounds__(kBlockThreads)
     constexpr int LPB = lanes_per_block<NB, P>();
     constexpr int NF = elems_per_lane<P>() / 2;
     pdl_wait();
-    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     // default L2 policy: evict-first loads measured 5% slower here
     for_each_slot<NB, P, false, false>(in, nblocks, [&](const SlotOf<NB, P> &s) {
@@ -259,7 +259,6 @@ __global__ void __launch_bounds__(kBlockThreads)
     constexpr int LPB = NB / kLaneElems;
     constexpr int U = kAccSlots;
     pdl_wait();
-    pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
     const int part = lane % LPB;
