@@ -13,10 +13,11 @@
 // The clamp never binds (|x q| <= qmax up to one rounding); the kernels
 // round with a magic-number addition instead of conversion instructions.
 //
-// A lane owns 32 consecutive elements of a block; its 32 codes are exactly
-// b 32-bit words of the stream, packed with compile-time shifts.  Each lane
-// takes several grid-stride slots per loop trip and issues all of their
-// loads before it processes the first.
+// In the quantizer a lane owns 32 consecutive elements of a block; their 32
+// codes are exactly b 32-bit words of the stream, packed with compile-time
+// shifts.  Each lane takes several grid-stride slots per loop trip and
+// issues all of their loads before it processes the first.  The
+// dequantizer's layout is described above its kernel.
 
 #include <cfloat>
 
@@ -87,7 +88,6 @@ __global__ void __launch_bounds__(kLThreads)
     constexpr int U = kQuantSlots;
     constexpr float kQmax = static_cast<float>((1 << (BITS - 1)) - 1);
     pdl_wait();
-    pdl_launch_dependents();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
     const int part = lane % LPB;
@@ -143,34 +143,28 @@ __global__ void __launch_bounds__(kLThreads)
     }
 }
 
-// The dequantizer's unit is 8 consecutive codes (BITS bytes of the stream);
-// adjacent lanes take adjacent units, so that a warp's code loads and its
-// 16-byte bf16 stores are both contiguous.  A unit's 8 * BITS bits are held
-// as two 32-bit words, code 0 in the lowest bits of lo.  For 4 and 8 bits a
-// unit is one aligned load; for 5 and 6 bits it is not word-aligned, so the
-// warp loads its 32 units' span with 16-byte loads into a shared buffer and
-// each lane takes its two words from there.
+// The dequantizer works on warp tiles of 1024 codes (128 units of 8 codes;
+// 128 * BITS bytes of the stream, 16-byte aligned).  Lane l decodes units
+// l, 32 + l, 64 + l and 96 + l of its tile, so each of its four 16-byte
+// bf16 stores (two fp32 ones) joins the warp's into one contiguous 512-byte
+// (1 KB) run.  A unit's 8 * BITS bits are held as two 32-bit words, code 0
+// in the lowest bits of lo.  At 4 and 8 bits a unit is one aligned 4- or
+// 8-byte load, and a warp's loads of one unit index are contiguous.  At 5
+// and 6 bits a unit is not word-aligned, so the warp loads the tile with
+// 16-byte loads into its shared buffer and each lane takes its two words
+// from there.  Codes become floats with the magic-number trick (one logic
+// operation after the shift) and are scaled two at a time with packed
+// fp32x2 instructions.
 struct UnitBits {
     uint32_t lo, hi;
 };
 
-template <int BITS> __device__ __forceinline__ UnitBits load_unit(const uint8_t *packed, int64_t unit)
-{
-    static_assert(BITS == 4 || BITS == 8, "5- and 6-bit units are loaded through the shared buffer");
-    const int64_t byte = unit * BITS;
-    if constexpr (BITS == 8) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(packed + byte));
-        return {v.x, v.y};
-    } else {
-        return {__ldg(reinterpret_cast<const uint32_t *>(packed + byte)), 0u};
-    }
-}
-
-// Code i (0..7) of a unit as an exact float: the BITS-bit field with its
-// sign bit flipped is code + 2^(BITS-1) in [0, 2^BITS); placed in the low
-// mantissa bits of 1.5 * 2^23 it gives the float 1.5 * 2^23 + code +
-// 2^(BITS-1), from which one exact subtraction leaves the code.
-template <int BITS> __device__ __forceinline__ float unit_code(const UnitBits &u, int i)
+// Code i (0..7) of a unit as a float 1.5 * 2^23 + code + 2^(BITS-1): the
+// BITS-bit field with its sign bit flipped is code + 2^(BITS-1) in
+// [0, 2^BITS), and placed in the low mantissa bits of 1.5 * 2^23 (with
+// which it shares no bit) it gives that float.  One exact subtraction of
+// 1.5 * 2^23 + 2^(BITS-1) leaves the code.
+template <int BITS> __device__ __forceinline__ float biased_code(const UnitBits &u, int i)
 {
     constexpr uint32_t kMask = (1u << BITS) - 1u, kSign = 1u << (BITS - 1);
     const int bit = BITS * i;
@@ -181,110 +175,119 @@ template <int BITS> __device__ __forceinline__ float unit_code(const UnitBits &u
         raw = u.hi >> (bit - 32);
     else
         raw = __funnelshift_r(u.lo, u.hi, bit);
-    // (raw & mask) has no bit in common with 1.5 * 2^23, so the sign flip and
-    // the exponent bits go in with one exclusive or
-    const float biased = __uint_as_float((raw & kMask) ^ (kSign | 0x4B400000u));
-    return __fsub_rn(biased, kRoundMagic + static_cast<float>(kSign));
+    return __uint_as_float((raw & kMask) ^ (kSign | 0x4B400000u));
 }
 
-constexpr int kDequantUnits = 8;  // units per lane per loop trip, loads issued together
+constexpr int kTileUnits = 128;                  // units of 8 codes per warp tile
+constexpr int kTileCodes = 8 * kTileUnits;       // 1024
+
+template <int BITS, bool BF16OUT>
+__device__ __forceinline__ void decode_store_unit(const UnitBits &u, float m, void *out, int64_t unit)
+{
+    constexpr float kBias = kRoundMagic + static_cast<float>(1 << (BITS - 1));
+    const float2 nb2 = make_float2(-kBias, -kBias), m2 = make_float2(m, m);
+    float2 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)  // x_hat = code * m: an exact subtraction, then one rounded multiply
+        v[i] = __fmul2_rn(__fadd2_rn(make_float2(biased_code<BITS>(u, 2 * i), biased_code<BITS>(u, 2 * i + 1)),
+                                     nb2),
+                          m2);
+    if constexpr (BF16OUT) {
+        stg128_stream(static_cast<uint16_t *>(out) + 8 * unit,
+                      make_uint4(f32x2_to_bf16x2(v[0].x, v[0].y), f32x2_to_bf16x2(v[1].x, v[1].y),
+                                 f32x2_to_bf16x2(v[2].x, v[2].y), f32x2_to_bf16x2(v[3].x, v[3].y)));
+    } else {
+        float *o = static_cast<float *>(out) + 8 * unit;
+        stg128_stream(o, make_uint4(__float_as_uint(v[0].x), __float_as_uint(v[0].y), __float_as_uint(v[1].x),
+                                    __float_as_uint(v[1].y)));
+        stg128_stream(o + 4, make_uint4(__float_as_uint(v[2].x), __float_as_uint(v[2].y),
+                                        __float_as_uint(v[3].x), __float_as_uint(v[3].y)));
+    }
+}
 
 template <int BITS, int NB, bool BF16OUT>
 __global__ void __launch_bounds__(kLThreads)
     laaq_dequantize_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale, int64_t n,
                            void *__restrict__ out)
 {
-    constexpr int U = kDequantUnits;
-    pdl_wait();
-    pdl_launch_dependents();
-    const int64_t units = n / 8;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // for 5 and 6 bits the loop test is warp-uniform (the warp's first
-    // unit), so that a warp's lanes stay together through the shared-buffer
-    // exchange below
     constexpr bool kStaged = (BITS == 5 || BITS == 6);
-    const int64_t lane_off = kStaged ? (threadIdx.x & 31) : 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base - lane_off < units;
-         base += U * stride) {
-        UnitBits w[U];
-        float m[U];
+    constexpr int kTileBytes = kTileUnits * BITS;   // 640 or 768 at 5 / 6 bits
+    constexpr int kChunks = kTileBytes / 16;        // 16-byte chunks per tile: 40 or 48
+    __shared__ __align__(16) uint8_t stage[kLThreads / 32][kStaged ? kTileBytes : 16];
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    uint8_t *buf = stage[threadIdx.x >> 5];
+    const int64_t units = n / 8;
+    const int64_t nbytes = units * BITS;
+    const int64_t ntiles = (units + kTileUnits - 1) / kTileUnits;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kLThreads / 32);
+    for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (kLThreads / 32) + (threadIdx.x >> 5); tile < ntiles;
+         tile += nwarps) {
+        const int64_t u0 = tile * kTileUnits;                  // first unit of the tile
+        const bool full = u0 + kTileUnits <= units;            // warp-uniform
+        UnitBits w[4];
+        float m[4];
         if constexpr (kStaged) {
-            // a warp's 32 consecutive units are one 16-byte-aligned span of
-            // 32 * BITS bytes: 2 * BITS lanes load it with one 16-byte load
-            // each, through the warp's shared buffer to the lanes that need it
-            constexpr int CH = 2 * BITS;             // 16-byte chunks per span
-            constexpr int SPAN = 32 * BITS;          // bytes per span
-            __shared__ __align__(16) uint8_t stage[kLThreads / 32][U * 32 * 6];
-            uint8_t *buf = stage[threadIdx.x >> 5];
-            const int lane = threadIdx.x & 31;
-            const int64_t nbytes = units * BITS;
-            uint4 c[U];
+            // the tile's bytes: chunks lane and 32 + lane (the second only for
+            // lanes below kChunks - 32), whole words at the stream's ragged end
+            const uint8_t *src = packed + u0 * BITS;
+            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+            if (full) {
+                c0 = ldg128_stream(src + 16 * lane);
+                if (lane < kChunks - 32)
+                    c1 = ldg128_stream(src + 16 * (32 + lane));
+            } else {
+                const int64_t left = nbytes - u0 * BITS;           // bytes of the tile in the stream
+                uint32_t t[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t off = (base - lane + u * stride) * BITS + 16 * lane;
-                c[u] = make_uint4(0, 0, 0, 0);
-                if (lane < CH && off < nbytes) {
-                    if (off + 16 <= nbytes) {
-                        c[u] = ldg128_stream(packed + off);
-                    } else {  // the stream ends inside this chunk: whole words only
-                        uint32_t t[4] = {0u, 0u, 0u, 0u};
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if (off + 4 * k < nbytes)
-                                t[k] = __ldg(reinterpret_cast<const uint32_t *>(packed + off + 4 * k));
-                        c[u] = make_uint4(t[0], t[1], t[2], t[3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const int64_t off = 16 * (32 * h + lane) + 4 * k;
+                        if ((h == 0 || lane < kChunks - 32) && off < left)
+                            t[4 * h + k] = __ldg(reinterpret_cast<const uint32_t *>(src + off));
                     }
-                }
+                c0 = make_uint4(t[0], t[1], t[2], t[3]);
+                c1 = make_uint4(t[4], t[5], t[6], t[7]);
             }
-            __syncwarp();
-            if (lane < CH) {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    *reinterpret_cast<uint4 *>(buf + u * SPAN + 16 * lane) = c[u];
-            }
+            __syncwarp();  // the previous tile's words have been read
+            *reinterpret_cast<uint4 *>(buf + 16 * lane) = c0;
+            if (lane < kChunks - 32)
+                *reinterpret_cast<uint4 *>(buf + 16 * (32 + lane)) = c1;
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t j = base + u * stride;
-                const int byte = BITS * lane, a = byte & ~3;
+            for (int k = 0; k < 4; ++k) {
+                const int byte = BITS * (32 * k + lane), a = byte & ~3;
                 const uint32_t sh = 8u * static_cast<uint32_t>(byte & 3);
-                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(buf + u * SPAN + a);
-                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(buf + u * SPAN + a + 4);
-                w[u] = {__funnelshift_r(w0, w1, sh), w1 >> sh};
-                m[u] = j < units ? __ldg(scale + j * 8 / NB) : 1.0f;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(buf + a);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(buf + a + 4);
+                w[k] = {__funnelshift_r(w0, w1, sh), w1 >> sh};
             }
         } else {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t j = base + u * stride;
-                w[u] = {0u, 0u};
-                m[u] = 1.0f;
-                if (j < units) {
-                    w[u] = load_unit<BITS>(packed, j);
-                    m[u] = __ldg(scale + j * 8 / NB);
+            for (int k = 0; k < 4; ++k) {
+                const int64_t u = u0 + 32 * k + lane;
+                w[k] = {0u, 0u};
+                if (full || u < units) {
+                    if constexpr (BITS == 8) {
+                        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(packed) + u);
+                        w[k] = {v.x, v.y};
+                    } else {
+                        w[k] = {__ldg(reinterpret_cast<const uint32_t *>(packed) + u), 0u};
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t j = base + u * stride;
-            if (j >= units)
-                break;
-            float v[8];
+        for (int k = 0; k < 4; ++k) {
+            const int64_t u = u0 + 32 * k + lane;
+            m[k] = (full || u < units) ? __ldg(scale + u / (NB / 8)) : 1.0f;
+        }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = __fmul_rn(unit_code<BITS>(w[u], i), m[u]);
-            if constexpr (BF16OUT) {
-                stg128_stream(static_cast<uint16_t *>(out) + 8 * j,
-                              make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]),
-                                         f32x2_to_bf16x2(v[4], v[5]), f32x2_to_bf16x2(v[6], v[7])));
-            } else {
-                float *o = static_cast<float *>(out) + 8 * j;
-                stg128_stream(o, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                                            __float_as_uint(v[3])));
-                stg128_stream(o + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]),
-                                                __float_as_uint(v[6]), __float_as_uint(v[7])));
-            }
+        for (int k = 0; k < 4; ++k) {
+            const int64_t u = u0 + 32 * k + lane;
+            if (full || u < units)
+                decode_store_unit<BITS, BF16OUT>(w[k], m[k], out, u);
         }
     }
 }
@@ -321,7 +324,7 @@ cudaError_t run_dequantize(const uint8_t *packed, const float *scale, int64_t n,
                            cudaStream_t st)
 {
     int grid = 0;
-    const int64_t lanes = (n / 8 + kDequantUnits - 1) / kDequantUnits;
+    const int64_t lanes = (n / 8 + kTileUnits - 1) / kTileUnits * 32;  // one warp per tile
     if (bf16) {
         cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, true>, lanes, &grid);
         if (e != cudaSuccess)
