@@ -1,10 +1,10 @@
 """GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
 oracle on the same seeded inputs.
 
-Small and ragged cases are compared element by element; the full-size
-GPT-shaped and AGoQ workloads (launched exactly as the benchmark launches
-them) are compared on sampled blocks, which the oracle computes one by one,
-plus properties checked on every block.
+Small and ragged cases are compared element by element.  The full-size
+GPT-shaped workloads (launched exactly as the benchmark launches them) are
+and the full-size AGoQ buffers are compared on every block, with the oracle
+run over all host cores.
 """
 
 import math
@@ -18,6 +18,7 @@ import oracle
 from fp8_communication_compression_gb300 import api
 from fp8_communication_compression_gb300 import workloads as W
 
+import oracle_pool
 from parity import (assert_codes_match, assert_recon_match, assert_scalars_match, gather_blocks,
                     gather_scalars, sample_blocks, to_dev_bf16, to_host)
 
@@ -378,21 +379,16 @@ def assert_code_properties(codes: torch.Tensor, x_bits_dev: torch.Tensor | None,
         assert torch.all(mag.amax(dim=1)[nonzero] == 0x7E), "a non-zero block misses +-448"
 
 
-def sampled_compress_check(x_dev, bits_host_blocks, c, a, s, blocks, block):
-    rc, ra, rs = oracle.compress(bits_host_blocks, block)
-    assert_codes_match(gather_blocks(c, blocks, block), rc)
-    assert_scalars_match(gather_scalars(a, blocks), ra, "alpha")
-    assert_scalars_match(gather_scalars(s, blocks), rs, "scale")
-
-
 @pytest.mark.parametrize("name", ["gpt2.7b_4096x2560_n128", "gpt6.7b_p4x8192x4096_n128",
                                   "gpt13b_p8x8192x5120_n256"])
 def test_full_size_two_shot_local_path(name):
+    """Every block of every shard, at full size, against the oracle run over
+    all host cores: the compress of each shard, the reduce of the GPU's own
+    compressed shards, and the decompress of the GPU's reduced codes."""
     w = W.WORKLOADS[name]
     P, rows, d, block = w["shards"], w["rows"], w["d"], w["block"]
     bits = np.stack([W.shard_input(name, p) for p in range(P)])
     x = to_dev_bf16(bits).reshape(P, rows, d)
-    nb = rows * d // block
     path = api.TwoShotLocal(P, rows, d, block)  # the benchmark's path
     out = path.run(x)
     if P > 1:  # the one-call reduce + decompress gives the same bits
@@ -407,28 +403,28 @@ def test_full_size_two_shot_local_path(name):
     torch.cuda.synchronize()
     assert_code_properties(path.codes, x, block)
     assert_code_properties(path.r_codes, None, block)
-    blocks = sample_blocks(nb, 1024, seed=P)
-    # compress: every shard on the sampled blocks
-    for p in range(P):
-        hb = bits[p].reshape(-1, block)[blocks]
-        sampled_compress_check(x[p], hb, path.codes[p], path.alpha[p], path.scale[p], blocks, block)
+    del x
+    codes, alpha, scale = to_host(path.codes), to_host(path.alpha), to_host(path.scale)
+    # compress: every block of every shard
+    rc, ra, rs = oracle_pool.compress(bits, block)
+    del bits
+    assert_codes_match(codes, rc, f"codes of all {P} shards")
+    assert_scalars_match(alpha, ra, "alpha")
+    assert_scalars_match(scale, rs, "scale")
+    del rc, ra, rs
     if P > 1:
-        # reduce on the GPU's own compressed shards
-        rc, ra, rs = oracle.reduce_shards([gather_blocks(path.codes[p], blocks, block) for p in range(P)],
-                                          [gather_scalars(path.alpha[p], blocks) for p in range(P)],
-                                          [gather_scalars(path.scale[p], blocks) for p in range(P)], block)
-        assert_codes_match(gather_blocks(path.r_codes, blocks, block), rc, "reduced codes")
-        assert_scalars_match(gather_scalars(path.r_alpha, blocks), ra, "reduced alpha")
-        assert_scalars_match(gather_scalars(path.r_scale, blocks), rs, "reduced scale")
-    # decompress of the (reduced) codes
-    src_c = path.r_codes if P > 1 else path.codes[0]
-    src_a = path.r_alpha if P > 1 else path.alpha[0]
-    src_s = path.r_scale if P > 1 else path.scale[0]
-    if P == 1:
+        # reduce of the GPU's own compressed shards, every block
+        rc, ra, rs = oracle_pool.reduce_shards(codes, alpha, scale, block)
+        assert_codes_match(to_host(path.r_codes), rc, "reduced codes")
+        assert_scalars_match(to_host(path.r_alpha), ra, "reduced alpha")
+        assert_scalars_match(to_host(path.r_scale), rs, "reduced scale")
+        src = (to_host(path.r_codes), to_host(path.r_alpha), to_host(path.r_scale))
+    else:
+        src = (codes[0], alpha[0], scale[0])
         out = api.taco_decompress(path.codes[0], path.alpha[0], path.scale[0], block)
-    ref = oracle.decompress(gather_blocks(src_c, blocks, block), gather_scalars(src_a, blocks),
-                            gather_scalars(src_s, blocks), block)
-    assert_recon_match(gather_blocks(out, blocks, block), ref, block)
+    # decompress of the (reduced) codes, every block
+    ref = oracle_pool.decompress(*src, block)
+    assert_recon_match(to_host(out), ref, block)
 
 
 @pytest.mark.parametrize("P,rows,d,block,chunks", [(4, 512, 1024, 128, 8), (2, 96, 512, 256, 3),
@@ -498,21 +494,22 @@ def test_two_paths_on_two_streams_at_once_match_sequential_runs():
 
 
 def test_full_size_agoq_accumulate_and_reduce():
+    """Every block of the 2^28-element buffer after each of the four
+    accumulation steps, and every block of the P = 8 reduce of 2^25-element
+    shards, against the oracle run over all host cores (bit-exact)."""
     a = W.AGOQ
     block, n = a["block"], a["n_main"]
     nb = n // block
-    blocks = sample_blocks(nb, 2048, seed=5)
     codes = torch.zeros(n, dtype=torch.uint8, device="cuda")
     scale = torch.ones(nb, dtype=torch.float32, device="cuda")
     for k, seed in enumerate(a["grad_seeds"]):
         g = W.agoq_grad(seed, n)
-        prev_c = gather_blocks(codes, blocks, block)
-        prev_s = gather_scalars(scale, blocks)
+        prev_c, prev_s = to_host(codes), to_host(scale)
         api.agoq_fp8_accumulate(codes, scale, to_dev_bf16(g), block)
-        rc, rs = oracle.agoq_accumulate(prev_c, prev_s, g.reshape(-1, block)[blocks], block)
-        assert_codes_match(gather_blocks(codes, blocks, block), rc, f"step {k}", exact=True)
-        assert_scalars_match(gather_scalars(scale, blocks), rs, f"step {k} scale", exact=True)
-        del g
+        rc, rs = oracle_pool.agoq_accumulate(prev_c, prev_s, g, block)
+        assert_codes_match(to_host(codes), rc, f"step {k}", exact=True)
+        assert_scalars_match(to_host(scale), rs, f"step {k} scale", exact=True)
+        del g, prev_c, prev_s, rc, rs
     assert_code_properties(codes, None, block)
     del codes, scale
     ns = a["n_shard"]
@@ -525,8 +522,7 @@ def test_full_size_agoq_accumulate_and_reduce():
         shards.append((c, s))
     cs, ss = zip(*shards)
     oc, os_ = api.agoq_reduce_shards(list(cs), list(ss), block)
-    blocks = sample_blocks(ns // block, 2048, seed=6)
-    rc, rs = oracle.agoq_reduce([gather_blocks(c, blocks, block) for c in cs],
-                                [gather_scalars(s, blocks) for s in ss], block)
-    assert_codes_match(gather_blocks(oc, blocks, block), rc, "agoq reduce", exact=True)
-    assert_scalars_match(gather_scalars(os_, blocks), rs, "agoq reduce scale", exact=True)
+    rc, rs = oracle_pool.agoq_reduce(np.stack([to_host(c) for c in cs]), np.stack([to_host(s) for s in ss]),
+                                     block)
+    assert_codes_match(to_host(oc), rc, "agoq reduce", exact=True)
+    assert_scalars_match(to_host(os_), rs, "agoq reduce scale", exact=True)
