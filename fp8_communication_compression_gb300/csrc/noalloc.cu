@@ -39,16 +39,13 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 uint64_t round_up(uint64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-// Device address of the scratch array on the current device (looked up once
-// per device).
-cudaError_t scratch_address(uint8_t **out)
+// Device address of the scratch array on device `dev`, which must be the
+// current device (looked up once per device).
+cudaError_t scratch_address(int dev, uint8_t **out)
 {
     static uint8_t *addr[kMaxDevices];
     static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
+    cudaError_t e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
@@ -121,10 +118,17 @@ taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32
     if (R < 1)
         return TACO_ERR_UNSUPPORTED;  // one row of all P shards does not fit the array
 
-    uint8_t *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess)
-        return TACO_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the array's address is the current device's: the stream must belong
+    // to that device
+    int dev = 0, stream_dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(st, &stream_dev) != cudaSuccess)
+        return TACO_ERR_CUDA;
+    if (stream_dev != dev)
+        return TACO_ERR_INVALID_ARG;
+    uint8_t *scratch = nullptr;
+    if (scratch_address(dev, &scratch) != cudaSuccess)
+        return TACO_ERR_CUDA;
     for (int64_t r0 = 0; r0 < rows; r0 += R) {
         const int64_t Rc = (rows - r0 < R) ? rows - r0 : R;
         const int64_t e = Rc * d, nb = e / block;

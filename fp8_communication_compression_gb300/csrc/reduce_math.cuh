@@ -21,7 +21,6 @@ constexpr int kLaneElems = 32;  // elements per lane in the default layout
 // Everything below is written so that a block's statistics come out
 // bit-identical in either layout.
 
-// 16 E4M3 codes -> 8 float2 (element order), exact.
 // 4 E4M3 codes (bytes 0..3 of w) -> 2 float2, exact: the word's two halves
 // go to the FP8-pair conversion as register halves, with no shift.
 __device__ __forceinline__ void decode4_f2(uint32_t w, float2 &a, float2 &b)
@@ -37,6 +36,7 @@ __device__ __forceinline__ void decode4_f2(uint32_t w, float2 &a, float2 &b)
         : "r"(h0), "r"(h1));
 }
 
+// 16 E4M3 codes -> 8 float2 (element order), exact.
 __device__ __forceinline__ void decode16_f2(const uint4 q, float2 *d)
 {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};

@@ -330,6 +330,13 @@ taco_status taco_host_pipeline_destroy(taco_host_pipeline *pipe);
  *    call's contents; nothing in it needs to start at zero.  Calls whose
  *    work overlaps on the GPU (other streams, other threads) race on it:
  *    serialise them.
+ *  - `stream` must belong to the current device (the array used is the
+ *    current device's); a stream of another device returns
+ *    TACO_ERR_INVALID_ARG with nothing enqueued.
+ *  - On TACO_ERR_CUDA, the copies and kernels of the chunks before the
+ *    failing one may already be enqueued on `stream`: out_host is then
+ *    partly written and its contents are undefined until the stream has
+ *    drained.
  */
 #define TACO_NOALLOC_SCRATCH_MIB 64
 taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32_t block,
