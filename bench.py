@@ -657,13 +657,13 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     ar = exchange.TwoShotAllReduce(rows, d, block)
     stream = torch.cuda.current_stream()
+    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
+    time.sleep(0.2 if clocks else 0)
     for _ in range(args.warmup):
         ar.run(x)
     torch.cuda.synchronize()
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
-    time.sleep(0.2 if clocks else 0)
     dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
@@ -808,6 +808,10 @@ def main():
     path = api.TwoShotLocal(P, rows, d, block, fused=args.fused)
     stream = torch.cuda.current_stream()
 
+    # the clock sampler starts before the warm-up steps, so that no idle gap
+    # separates the warm-up from the timed region
+    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
+    time.sleep(0.2 if clocks else 0)
     for _ in range(args.warmup):
         path.run(x)
     torch.cuda.synchronize()
@@ -818,16 +822,16 @@ def main():
     step_bytes = sum(nbytes.values())
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
-    time.sleep(0.2 if clocks else 0)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    t_host = time.perf_counter()
     start.record(stream)
     for _ in range(K):
         for _, fn in launches:
             fn(x)
     end.record(stream)
+    host_us = (time.perf_counter() - t_host) / K * 1e6
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -914,6 +918,7 @@ def main():
                        "kernel_events": (f"per-launch CUDA events in a sampling phase of {ns + 1} steps after "
                                          f"the timed region, first step dropped ({ns} samples per kernel)"),
                        "bytes_per_step": step_bytes,
+                       "host_enqueue_us_per_step": host_us,
                        "input_bf16_bytes_per_step": 2 * P * n,
                        "l2": "inputs larger than L2 (268 MB bf16 read per step), no flush",
                        "parallelism": f"replicas x{world}"},
