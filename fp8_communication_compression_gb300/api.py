@@ -275,6 +275,37 @@ def taco_e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=No
     return out
 
 
+def taco_gemm_compress(a: torch.Tensor, b: torch.Tensor, block: int = 128, e_target: float = E_TARGET,
+                       eps: float = EPS, codes: torch.Tensor | None = None, alpha: torch.Tensor | None = None,
+                       scale: torch.Tensor | None = None, y_out: torch.Tensor | None = None, stream=None):
+    """Y = a @ b.T on the tensor cores (a bf16 [M, K], b bf16 [N, K]), leaving
+    the kernel compressed: (codes uint8 [M, N], alpha, scale fp32 [M * N / 128]).
+    ``y_out`` (fp32 [M, N]), if given, also receives the uncompressed Y."""
+    _need(a, "a", _BF16)
+    _need(b, "b", _BF16)
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("a must be [M, K] and b [N, K]")
+    M, K = a.shape
+    N = b.shape[0]
+    nb = M * N // block if block else 0
+    if codes is None:
+        codes = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+    if alpha is None:
+        alpha = torch.empty(nb, dtype=torch.float32, device=a.device)
+    if scale is None:
+        scale = torch.empty(nb, dtype=torch.float32, device=a.device)
+    _need(codes, "codes", _U8, M * N)
+    _need(alpha, "alpha", (torch.float32,), nb)
+    _need(scale, "scale", (torch.float32,), nb)
+    if y_out is not None:
+        _need(y_out, "y_out", (torch.float32,), M * N)
+    st = _lib.load().taco_gemm_compress(a.data_ptr(), b.data_ptr(), M, N, K, block, e_target, eps,
+                                        codes.data_ptr(), alpha.data_ptr(), scale.data_ptr(),
+                                        y_out.data_ptr() if y_out is not None else None, _stream_handle(stream))
+    _lib.check("taco_gemm_compress", st)
+    return codes, alpha, scale
+
+
 def taco_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))

@@ -1,0 +1,277 @@
+// The tensor-core GEMM that produces a tensor-parallel partial sum, with the
+// TACO compressor fused into its epilogue.
+//
+// AGoQ (gist.science summary of arXiv 2605.00539), 2.C: the quantisation
+// runs inside the adjacent GEMM kernel, the tensor cores doing the matrix
+// product and the CUDA cores the quantisation.  Applied here to TACO's
+// compressor (gist.science summary of arXiv 2604.24088, 2.B.1-2.B.3): the
+// partial sum Y = A B^T of a row-parallel layer leaves the kernel already as
+// ASH + DS E4M3 codes with their two scalars per block, ready for the
+// two-shot exchange, instead of being written in bf16 and read back by the
+// compressor.
+//
+// Design (sm_103a):
+//  * One CTA computes a 128 x 256 tile of Y in tensor memory (fp32, 256
+//    columns).  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A
+//    and 256 x 64 tiles of B (bf16, 128-byte swizzle) through a 4-stage
+//    mbarrier ring.  Warp 1 allocates the tensor memory and one of its
+//    threads issues the tcgen05.mma steps (128 x 256 x 16 each, four per
+//    64-wide stage) and commits each stage back to the producer.  Warps 2-5
+//    are the epilogue.
+//  * The accumulator's lane is the tile row, so after tcgen05.ld each
+//    epilogue thread holds 128 consecutive fp32 values of one row: exactly
+//    one compression block, the layout the compress kernel gives a thread.
+//    The 128-point Walsh-Hadamard transform, the block energy, alpha, s and
+//    the E4M3 conversion run in that thread's registers; the codes go
+//    through a swizzled staging tile (the emptied stage buffers) and TMA
+//    stores.
+//  * Every mbarrier wait is time-limited; a wait that runs out sets a flag
+//    readable through taco_device_error() and the CTA winds down.
+
+#include <atomic>
+#include <cfloat>
+
+#include "codec_math.cuh"
+#include "device_utils.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace taco {
+
+// Watchdog flags of this file's kernel (bit 5), read with the codec
+// kernels' flags by taco_device_error().
+__device__ unsigned int g_gemm_error;
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kGStages = 4;
+constexpr int kGThreads = 192;                       // warps: 0 producer, 1 MMA, 2-5 epilogue
+constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr uint32_t kGStageBytes = kABytes + kBBytes; // 48 KB
+constexpr uint32_t kTmemCols = kBN;                  // fp32 accumulator, one column per tile column
+constexpr uint32_t kGemmSmem = 1024 + kGStages * kGStageBytes + 8 * (2 * kGStages + 1) + 16;
+constexpr uint32_t kErrGemm = 32u;
+static_assert(kGStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kGemmSmem <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_compress_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
+                         const __grid_constant__ CUtensorMap c_map, float *__restrict__ alpha_out,
+                         float *__restrict__ scale_out, float *__restrict__ y_out, int64_t N, int K, float e_target,
+                         float eps)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bars = base + kGStages * kGStageBytes;
+    const uint32_t accum_bar = bars + 16 * kGStages;
+    const uint32_t tmem_slot = accum_bar + 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+    const int KB = K / kBK;
+    auto full = [&](int s) { return bars + 8 * s; };
+    auto empty = [&](int s) { return bars + 8 * (kGStages + s); };
+    auto stage_a = [&](int s) { return base + s * kGStageBytes; };
+    auto stage_b = [&](int s) { return base + s * kGStageBytes + kABytes; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(accum_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    pdl_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = lds32(tmem_slot);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_map(&a_map);
+            tma_prefetch_map(&b_map);
+            int issued = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % kGStages;
+                if (!mbar_wait(empty(s), ((kb / kGStages) & 1) ^ 1)) {
+                    atomicOr(&g_gemm_error, kErrGemm);
+                    break;
+                }
+                mbar_arrive_expect_tx(full(s), kGStageBytes);
+                tma_load_2d(stage_a(s), &a_map, kb * kBK, m0, full(s));
+                tma_load_2d(stage_b(s), &b_map, kb * kBK, n0, full(s));
+                ++issued;
+            }
+            // leave no load in flight into this CTA's shared memory
+            for (int kb = issued > kGStages ? issued - kGStages : 0; kb < issued; ++kb)
+                mbar_wait(full(kb % kGStages), (kb / kGStages) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32<kBM, kBN>();
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % kGStages;
+                if (!mbar_wait(full(s), (kb / kGStages) & 1)) {
+                    atomicOr(&g_gemm_error, kErrGemm);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t ad = smem_desc_k_sw128(stage_a(s)), bd = smem_desc_k_sw128(stage_b(s));
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
+                    mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                mma_commit(empty(s));  // the stage is free once these MMAs have read it
+            }
+            mma_commit(accum_bar);  // the accumulator is complete once every MMA has
+        }
+    } else {
+        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accum_bar, 0));
+        if (!ok) {
+            if (lane == 0)
+                atomicOr(&g_gemm_error, kErrGemm);
+        } else {
+            tc_fence_after_sync();
+            const uint32_t outw = base + q * 2 * 4096;  // this warp's staging rows (the stages are free)
+            const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+            const float c = BlockConst<128>::c;
+            const int64_t nblk_row = N / 128;
+#pragma unroll 1
+            for (int blk = 0; blk < kBN / 128; ++blk) {
+                float2 v[64];
+                float2 acc[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x[32];
+                    tmem_load_32(tmem + (static_cast<uint32_t>(32 * q) << 16) + blk * 128 + 32 * j, x);
+                    if (y_out) {
+                        float4 *yo = reinterpret_cast<float4 *>(y_out + (m0 + row) * N + n0 + blk * 128 + 32 * j);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            yo[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                    }
+                    // step 1 (energy) and the bit-0 butterfly stage of step 3
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int kk = 16 * j + t;
+                        const float2 xx = make_float2(x[2 * t], x[2 * t + 1]);
+                        acc[kk & 7] = (kk < 8) ? __fmul2_rn(xx, xx) : __ffma2_rn(xx, xx, acc[kk & 7]);
+                        v[kk] = make_float2(xx.x + xx.y, xx.x - xx.y);
+                    }
+                }
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w; ++i)
+                        acc[i] = __fadd2_rn(acc[i], acc[i + w]);
+                const float ss = acc[0].x + acc[0].y;
+                // step 3: remaining butterflies; the last is fused with the scaling
+                fwht128_upper_but_last(v);
+                const float mh = max_abs_last_stage(v);
+                // step 2: alpha = sqrt(E / (m + eps));  step 4: s = 448 / max|y|
+                const float alpha = sqrtf(e_target / (ss * BlockConst<128>::inv_n + eps));
+                const float ac = alpha * c;
+                const float M = ac * mh;
+                const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+                float k = ac * scale;
+                if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
+                    const float2 ac2 = make_float2(ac, ac);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        v[i] = __fmul2_rn(v[i], ac2);
+                    k = scale;
+                }
+                last_stage_scaled(v, make_float2(k, k));
+                // step 5: E4M3 codes into the swizzled staging rows, then a TMA store
+                const uint32_t stg = outw + blk * 4096, orow = stg + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    encode8_prescaled(&v[8 * j], w0, w1);
+                    encode8_prescaled(&v[8 * j + 4], w2, w3);
+                    sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&c_map, n0 + blk * 128, m0 + 32 * q, stg);
+                    bulk_commit();
+                }
+                const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128 + blk;
+                alpha_out[bi] = alpha;
+                scale_out[bi] = scale;
+            }
+            if (lane == 0)
+                bulk_wait_all();
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+cudaError_t read_gemm_error(uint32_t *flags, bool clear)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof v);
+    if (e != cudaSuccess)
+        return e;
+    *flags = v;
+    if (clear) {
+        v = 0;
+        e = cudaMemcpyToSymbol(g_gemm_error, &v, sizeof v);
+    }
+    return e;
+}
+
+cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                 float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
+                                 float *y_out, cudaStream_t stream)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap am, bm, cm;
+    if (encode_tensor_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(a_bf16), K, M, K * 2, kBK,
+                             kBM) != 0 ||
+        encode_tensor_map_2d(&bm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(b_bf16), K, N, K * 2, kBK,
+                             kBN) != 0 ||
+        encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, N, M, N, 128, 32) != 0)
+        return cudaErrorInvalidValue;
+    static std::atomic<bool> set[kMaxDevices];
+    if (!set[di.device].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(gemm_compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemmSmem));
+        if (e != cudaSuccess)
+            return e;
+        set[di.device].store(true, std::memory_order_release);
+    }
+    const dim3 grid(static_cast<unsigned>(N / kBN), static_cast<unsigned>(M / kBM));
+    return launch_pdl(gemm_compress_kernel, grid, kGThreads, kGemmSmem, stream, am, bm, cm, alpha, scale, y_out, N,
+                      static_cast<int>(K), e_target, eps);
+}
+
+}  // namespace taco

@@ -361,6 +361,41 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                               int32_t block, float e_target, float eps, uint8_t *codes, float *alpha,
+                               float *scale, float *y_out, taco_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0 || !positive_finite(e_target) || !positive_finite(eps))
+        return TACO_ERR_INVALID_ARG;
+    if (block != 128)
+        return TACO_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return TACO_OK;
+    if (K == 0 || M % 128 != 0 || N % 256 != 0 || K % 64 != 0 || M / 128 > 65535 || N > (int64_t(1) << 30) ||
+        K > (int64_t(1) << 30))
+        return TACO_ERR_UNSUPPORTED;
+    if (!a_bf16 || !b_bf16 || !codes || !alpha || !scale)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(a_bf16, 16) || !aligned(b_bf16, 16) || !aligned(codes, 16) || !aligned(alpha, 4) ||
+        !aligned(scale, 4) || (y_out && !aligned(y_out, 16)))
+        return TACO_ERR_MISALIGNED;
+    const uint64_t mn = static_cast<uint64_t>(M) * N, nb = mn / 128;
+    const void *outs[4] = {codes, alpha, scale, y_out};
+    const uint64_t olen[4] = {mn, 4 * nb, 4 * nb, y_out ? 4 * mn : 0};
+    const void *ins[2] = {a_bf16, b_bf16};
+    const uint64_t ilen[2] = {2 * static_cast<uint64_t>(M) * K, 2 * static_cast<uint64_t>(N) * K};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], olen[i], outs[j], olen[j]))
+                return TACO_ERR_INVALID_ARG;
+        for (int j = 0; j < 2; ++j)
+            if (overlap(outs[i], olen[i], ins[j], ilen[j]))
+                return TACO_ERR_INVALID_ARG;
+    }
+    return from_cuda(taco::launch_gemm_compress(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream)
 {
     if (n < 0)
@@ -446,7 +481,12 @@ taco_status taco_device_error(uint32_t *flags_out, int32_t clear)
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return TACO_ERR_CUDA;
-    return from_cuda(taco::read_codec_error(flags_out, clear != 0));
+    uint32_t codec = 0, gemm = 0;
+    if ((e = taco::read_codec_error(&codec, clear != 0)) != cudaSuccess ||
+        (e = taco::read_gemm_error(&gemm, clear != 0)) != cudaSuccess)
+        return from_cuda(e);
+    *flags_out = codec | gemm;
+    return TACO_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,134 @@
+// Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) of
+// sm_100-family GPUs: tensor-memory allocation, the single-thread MMA issue
+// with shared-memory matrix descriptors, completion tracking on an mbarrier,
+// and the warp-wide tensor-memory loads of the epilogue.
+#pragma once
+
+#include <cstdint>
+
+#include "device_utils.cuh"
+
+namespace taco {
+
+// ------------------------------------------------------ tensor memory --
+
+// Allocates `ncols` columns (a power of two, 32..512) of tensor memory for
+// this CTA; the whole warp executes it.  The TMEM address is written to the
+// shared-memory word at `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_alloc_permit()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Orders tcgen05 operations around a thread synchronisation (barrier or
+// mbarrier wait).
+__device__ __forceinline__ void tc_fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ MMA --
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the
+// 128-byte swizzle: rows of 64 bf16 (128 bytes), eight-row groups 1024 bytes
+// apart.  Fields: start address >> 4 (bits 0-13), leading byte offset >> 4
+// (bits 16-29; unused for this layout, set to 1), stride byte offset >> 4
+// (bits 32-45: 1024 bytes between eight-row groups), descriptor version 1
+// (bits 46-47), base offset 0 (the tile is 1024-byte aligned), layout type
+// 2 = 128-byte swizzle (bits 61-63).  Advancing the start address by 32
+// bytes selects the next 16 elements of K inside the swizzle atom.
+__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr)
+{
+    uint64_t d = static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
+// both operands K-major: accumulator format (bits 4-5) = F32, A and B
+// formats (bits 7-9, 10-12) = BF16, N >> 3 (bits 17-22), M >> 4 (bits
+// 24-28).
+template <int M, int N> __host__ __device__ constexpr uint32_t idesc_bf16_f32()
+{
+    static_assert(M == 64 || M == 128, "one-CTA MMA shapes");
+    static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N: multiple of 16 up to 256");
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for one M x N x 16 step; issued by one
+// thread.  accumulate = false overwrites D.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+// The mbarrier at `bar` receives one arrival once every MMA this thread has
+// issued so far has completed (and has finished reading shared memory).
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// ----------------------------------------------------- epilogue loads --
+
+// 32 consecutive fp32 columns of tensor memory: thread t of the warp gets
+// lane (taddr lane + t), columns col .. col + 31.  The warp's lane quarter
+// is fixed by its warp index modulo 4.  The load and the wait for it are one
+// asm statement, so that no use of the registers can be scheduled before
+// they have landed.
+__device__ __forceinline__ void tmem_load_32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// 2-D tiled TMA load global -> shared with the default L2 policy.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+}  // namespace taco

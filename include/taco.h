@@ -251,6 +251,33 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
 taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream);
 
 /*
+ * taco_gemm_compress - the GEMM that produces a tensor-parallel partial sum,
+ * with the compressor fused into its epilogue ([AGoQ] 2.C: quantisation
+ * fused into the adjacent GEMM kernel, the tensor cores doing the product
+ * and the CUDA cores the quantisation; applied to the [TACO] 2.B.1-2.B.2
+ * compressor).  Y = A B^T is accumulated in fp32 on the tensor cores
+ * (tcgen05, bf16 operands), and each 128-element block of each row of Y is
+ * compressed exactly as taco_compress compresses a block, from the fp32
+ * accumulator values (no bf16 rounding of Y).  The codes and scalars have
+ * taco_compress's layout for a [M][N] tensor.
+ *
+ *  a_bf16   in   bf16 [M][K] (the layer input), 16-byte aligned
+ *  b_bf16   in   bf16 [N][K] (the weight as [out][in]), 16-byte aligned
+ *  M, N, K       M % 128 == 0, N % 256 == 0, K % 64 == 0, K > 0,
+ *                M / 128 <= 65535; other shapes return TACO_ERR_UNSUPPORTED
+ *  block         128 (others return TACO_ERR_UNSUPPORTED)
+ *  e_target, eps as for taco_compress
+ *  codes    out  uint8 [M][N]
+ *  alpha    out  fp32 [M][N / 128]
+ *  scale    out  fp32 [M][N / 128]
+ *  y_out    out  optional fp32 [M][N]: the uncompressed Y, as accumulated
+ *                (NULL: not written)
+ */
+taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                               int32_t block, float e_target, float eps, uint8_t *codes, float *alpha,
+                               float *scale, float *y_out, taco_stream_t stream);
+
+/*
  * Host pipeline: the two-shot local path between HOST buffers, overlapped.
  * A run computes, for a pinned bf16 host tensor x_host [P][rows][d] (P
  * shards), decompress(reduce(compress(shard 0), ..., compress(shard P-1)))
@@ -346,7 +373,8 @@ taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32
 /*
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
- * (bit 0: compressor, bit 1: decompressor, bit 4: taco_watchdog_selftest).
+ * (bit 0: compressor, bit 1: decompressor, bit 4: taco_watchdog_selftest,
+ * bit 5: taco_gemm_compress).
  * Synchronises the device.  With clear != 0 the flags are reset to 0 after
  * reading.
  */

@@ -170,6 +170,26 @@ def reduce_shards(codes, alphas, scales, block: int, e_target: float = 1.0, eps:
     return out_c, out_a, out_s
 
 
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gemm_bt(a_bf16: np.ndarray, b_bf16: np.ndarray) -> np.ndarray:
+    """Y = A B^T in float64 for bf16 A [M, K] and B [N, K] (the GEMM whose
+    output the fused kernel compresses; AGoQ 2.C).  Every product of two
+    bf16 values is exact in float64; the sums are numpy's float64 matrix
+    product (a library primitive)."""
+    return bf16_to_f64(a_bf16) @ bf16_to_f64(b_bf16).T
+
+
+def gemm_compress(a_bf16: np.ndarray, b_bf16: np.ndarray, block: int = 128, e_target: float = 1.0,
+                  eps: float = 1e-12):
+    """The fused GEMM + compress, as two plain steps: Y = A B^T in float64,
+    then the TACO compressor on Y's blocks (compress_f64)."""
+    return compress_f64(gemm_bt(a_bf16, b_bf16), block, e_target, eps)
+
+
 # ------------------------------------------------------------------ AGoQ --
 
 def agoq_accumulate(codes: np.ndarray, scale: np.ndarray, grad_bf16: np.ndarray, block: int = 128):

@@ -86,6 +86,11 @@ def _task(args):
                 A["codes"][p, r0:r1] = c
                 A["alpha"][p, r0:r1] = a
                 A["scale"][p, r0:r1] = s
+        elif kind == "compress_f64":  # y float64 [rows, d] -> codes [rows, d], alpha / scale [rows, d / block]
+            c, a, s = oracle.compress_f64(A["y"][r0:r1].copy(), block)
+            A["rcodes"][r0:r1] = c
+            A["ralpha"][r0:r1] = a
+            A["rscale"][r0:r1] = s
         elif kind == "reduce":  # shards [P, rows, d] + scalars -> one compressed [rows, d]
             P = A["codes"].shape[0]
             c, a, s = oracle.reduce_shards([A["codes"][p, r0:r1].copy() for p in range(P)],
@@ -152,6 +157,25 @@ def compress(bits: np.ndarray, block: int):
             finally:
                 sh.close()
     return codes, alpha, scale
+
+
+def compress_f64(y: np.ndarray, block: int):
+    """float64 [rows, d] -> the oracle's (codes [rows, d], alpha, scale [rows, d / block])."""
+    rows, d = y.shape
+    nbr = d // block
+    out = (np.empty((rows, d), np.uint8), np.empty((rows, nbr), np.float32), np.empty((rows, nbr), np.float32))
+    for r0, r1 in _pieces(rows, 9 * d + 8 * nbr):
+        sh = Shared()
+        try:
+            sh.put("y", y[r0:r1])
+            c = sh.empty("rcodes", (r1 - r0, d), np.uint8)
+            a = sh.empty("ralpha", (r1 - r0, nbr), np.float32)
+            s = sh.empty("rscale", (r1 - r0, nbr), np.float32)
+            _run("compress_f64", sh, r1 - r0, block)
+            out[0][r0:r1], out[1][r0:r1], out[2][r0:r1] = c, a, s
+        finally:
+            sh.close()
+    return out
 
 
 def reduce_shards(codes: np.ndarray, alpha: np.ndarray, scale: np.ndarray, block: int):

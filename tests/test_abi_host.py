@@ -187,3 +187,32 @@ def test_host_pipeline_validation(lib):
     assert lib.taco_host_pipeline_create(4, 64, 1024, 128, 4, 0, None, ctypes.byref(ws)) == INVALID
     assert lib.taco_host_pipeline_run(None, A, A, A, 1.0, 1e-12, None) == INVALID
     assert lib.taco_host_pipeline_destroy(None) == INVALID
+
+
+def gemm_compress(lib, a=A, b=A * 64, M=256, N=512, K=128, block=128, e=1.0, eps=1e-12, codes=A * 128,
+                  alpha=A * 192, scale=A * 200, y=None):
+    return lib.taco_gemm_compress(a, b, M, N, K, block, e, eps, codes, alpha, scale, y, None)
+
+
+def test_gemm_compress_validation(lib):
+    # shapes the tile grid does not cover, and block sizes other than 128
+    assert gemm_compress(lib, block=256) == UNSUPPORTED
+    assert gemm_compress(lib, M=100) == UNSUPPORTED
+    assert gemm_compress(lib, N=384) == UNSUPPORTED
+    assert gemm_compress(lib, K=96) == UNSUPPORTED
+    assert gemm_compress(lib, M=128 * 65536) == UNSUPPORTED
+    assert gemm_compress(lib, M=-1) == INVALID
+    assert gemm_compress(lib, e=0.0) == INVALID
+    assert gemm_compress(lib, eps=float("nan")) == INVALID
+    # nothing to do
+    assert gemm_compress(lib, M=0) == OK and gemm_compress(lib, N=0) == OK
+    # pointers
+    assert gemm_compress(lib, a=None) == INVALID
+    assert gemm_compress(lib, scale=None) == INVALID
+    assert gemm_compress(lib, a=A + 8) == MISALIGNED
+    assert gemm_compress(lib, y=A * 300 + 4) == MISALIGNED
+    assert gemm_compress(lib, alpha=A * 192 + 2) == MISALIGNED
+    # outputs overlapping each other or the operands
+    assert gemm_compress(lib, codes=A) == INVALID
+    assert gemm_compress(lib, alpha=A * 128 + 16) == INVALID
+    assert gemm_compress(lib, y=A * 64) == INVALID

@@ -1,0 +1,118 @@
+"""GPU parity of taco_gemm_compress: the tensor-core GEMM with the compressor
+fused into its epilogue (AGoQ 2.C applied to the TACO compressor).
+
+Two separate checks, so that the GEMM's rounding and the compressor's do
+not blur each other:
+  * the uncompressed Y the kernel accumulated (its optional fp32 output)
+    against the oracle's float64 product, within an fp32-accumulation bound
+    of (K/16 + 2) * 2^-22 * sum_k |a_k b_k| per element (each 16-deep MMA
+    step and each accumulation rounds at most a few units in the last place
+    of fp32, truncation allowed), and against cuBLAS (torch.matmul) within
+    twice that;
+  * the codes and scalars against the oracle's compressor run on that same
+    fp32 Y: the codec's parity bar (codes >= 99.99 % bit-identical and never
+    more than 1 E4M3 ULP apart, alpha and s within 1e-6 relative), since
+    both sides take the code decisions from the same fp32 values.
+The call without the optional output gives the same codes bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pool
+from fp8_communication_compression_gb300 import api
+from fp8_communication_compression_gb300 import workloads as W
+
+from parity import assert_codes_match, assert_recon_match, assert_scalars_match, to_dev_bf16, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def no_watchdog_flags():
+    api.taco_device_error(clear=True)
+    yield
+    assert api.taco_device_error(clear=True) == 0
+
+
+def operands(M, N, K, seed):
+    """A: a TP activation (near-zero mixture, per-channel scales); B: weights
+    N(0, 0.02^2), both rounded to bf16."""
+    a = W.tp_activation(700 + seed, M, K, channel_scale=True)
+    b = W.f32_to_bf16_bits(np.random.default_rng(800 + seed).normal(0.0, 0.02, (N, K)).astype(np.float32))
+    return a, b
+
+
+def check_gemm_compress(M, N, K, seed=0):
+    a, b = operands(M, N, K, seed)
+    ad, bd = to_dev_bf16(a), to_dev_bf16(b)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    c, al, sc = api.taco_gemm_compress(ad, bd, y_out=y)
+    c2, al2, sc2 = api.taco_gemm_compress(ad, bd)
+    torch.cuda.synchronize()
+    # the optional output changes nothing
+    assert torch.equal(c, c2) and torch.equal(al, al2) and torch.equal(sc, sc2)
+    # GEMM: against the float64 product, within the accumulation bound
+    yg = to_host(y).astype(np.float64)
+    ref = oracle.gemm_bt(a, b)
+    mag = np.abs(oracle.bf16_to_f64(a)) @ np.abs(oracle.bf16_to_f64(b)).T
+    bound = (K / 16 + 2) * 2.0 ** -22 * mag
+    err = np.abs(yg - ref)
+    assert np.all(err <= bound), f"GEMM error {float((err / np.maximum(bound, 1e-300)).max()):.2f} x the bound"
+    cub = to_host(torch.matmul(ad.float(), bd.float().T)).astype(np.float64)
+    assert np.all(np.abs(yg - cub) <= 2 * bound)
+    # compressor: against the oracle on the same fp32 values
+    rc, ra, rs = oracle.compress_f64(yg, 128)
+    assert_codes_match(to_host(c), rc, "gemm codes")
+    assert_scalars_match(to_host(al), ra, "gemm alpha")
+    assert_scalars_match(to_host(sc), rs, "gemm scale")
+    # and the codes decompress to the oracle's reconstruction of them
+    out = api.taco_decompress(c, al, sc, 128)
+    assert_recon_match(to_host(out), oracle.decompress(to_host(c), to_host(al), to_host(sc), 128), 128)
+    return yg, ref
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (384, 768, 1024), (128, 256, 4096)])
+def test_gemm_compress_small_shapes(M, N, K):
+    check_gemm_compress(M, N, K)
+
+
+def test_gemm_compress_many_tiles_per_sm():
+    # more tiles than SMs (1024 x 2048: 8 x 8 = 64 tiles; 2048 x 4096: 256 tiles)
+    check_gemm_compress(2048, 4096, 512, seed=3)
+
+
+def test_gemm_compress_zero_rows_give_zero_blocks():
+    """Rows of A that are all zero make rows of Y that are all zero: their
+    blocks take the zero-block rule (codes +0, s = 1, alpha = sqrt(E/eps))."""
+    M, N, K = 256, 256, 128
+    a, b = operands(M, N, K, 5)
+    a[7] = 0
+    a[200] = 0
+    c, al, sc = api.taco_gemm_compress(to_dev_bf16(a), to_dev_bf16(b))
+    c, al, sc = to_host(c), to_host(al).reshape(M, -1), to_host(sc).reshape(M, -1)
+    for r in (7, 200):
+        assert np.all(c[r] == 0) and np.all(sc[r] == 1.0)
+        assert np.allclose(al[r], np.float32(np.sqrt(1.0 / 1e-12)), rtol=1e-6)
+
+
+def test_gemm_compress_full_size_gpt67b_down_projection():
+    """The GPT-6.7B row-parallel MLP down-projection at TP = 4: [8192 tokens,
+    4096] x [4096, 4096]^T, every block; the codes against the oracle's
+    compressor on the kernel's own fp32 Y, Y against cuBLAS."""
+    M, N, K = 8192, 4096, 4096
+    a, b = operands(M, N, K, 9)
+    ad, bd = to_dev_bf16(a), to_dev_bf16(b)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    c, al, sc = api.taco_gemm_compress(ad, bd, y_out=y)
+    cub = torch.matmul(ad.float(), bd.float().T)
+    mag = torch.matmul(ad.float().abs(), bd.float().abs().T)
+    bound = 2 * (K / 16 + 2) * 2.0 ** -22 * mag
+    assert bool(torch.all((y - cub).abs() <= bound))
+    del cub, mag, bound
+    rc, ra, rs = oracle_pool.compress_f64(to_host(y).astype(np.float64), 128)
+    assert_codes_match(to_host(c), rc, "gemm codes, full size")
+    assert_scalars_match(to_host(al), ra, "gemm alpha, full size")
+    assert_scalars_match(to_host(sc), rs, "gemm scale, full size")

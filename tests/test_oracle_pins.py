@@ -600,3 +600,45 @@ def test_laaq_error_within_half_a_step_and_uses_the_full_range(bits):
     qmax = 2 ** (bits - 1) - 1
     nz = np.any(xf != 0, axis=1)
     assert np.all(np.abs(np.rint(out / step)).max(axis=1)[nz] == qmax)
+
+
+# ------------------------------------------- GEMM feeding the compressor --
+
+def test_gemm_bt_matches_exactly_rounded_dot_products():
+    """AGoQ 2.C fuses the compressor into the GEMM that produces the tensor:
+    the oracle's GEMM is numpy's float64 product of the exact bf16 values.
+    Pinned against dot products summed with math.fsum (exactly rounded) on a
+    small case, including a K that is not a power of two."""
+    import math
+
+    from fp8_communication_compression_gb300 import workloads as W
+
+    a = W.tp_activation(11, 5, 37)
+    b = W.f32_to_bf16_bits(np.random.default_rng(3).normal(0, 0.02, (7, 37)).astype(np.float32))
+    y = oracle.gemm_bt(a, b)
+    af, bf = oracle.bf16_to_f64(a), oracle.bf16_to_f64(b)
+    for i in range(5):
+        for j in range(7):
+            terms = [af[i, k] * bf[j, k] for k in range(37)]
+            exact = math.fsum(terms)
+            assert abs(y[i, j] - exact) <= 1e-15 * math.fsum(abs(t) for t in terms)
+    # a transposed operand would not even have the right shape; a swapped
+    # pair of operands would give Y^T
+    assert y.shape == (5, 7)
+
+
+def test_gemm_compress_is_compress_of_the_product():
+    """The fused path's oracle on a case where Y is known in closed form: with
+    A = I (the first N columns of an identity, in bf16) Y = B exactly, so
+    the codes equal those of compressing B itself."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    n = 128
+
+    b = W.tp_activation(12, 256, n)          # [N = 256, K = 128]
+    a = np.zeros((n, n), dtype=np.uint16)    # [M = 128, K = 128] identity in bf16 (1.0 = 0x3F80)
+    a[np.arange(n), np.arange(n)] = 0x3F80
+    c, al, sc = oracle.gemm_compress(a, b, n)
+    # Y = A B^T = B^T [128, 256]: compress the transpose of B directly
+    rc, ra, rs = oracle.compress_f64(oracle.bf16_to_f64(b).T.copy(), n)
+    assert np.array_equal(c, rc) and np.array_equal(al, ra) and np.array_equal(sc, rs)

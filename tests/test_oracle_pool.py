@@ -28,6 +28,9 @@ def test_pool_matches_the_oracle_called_directly(piece_bytes, monkeypatch):
     assert np.array_equal(pc, rc) and np.array_equal(pa, ra) and np.array_equal(ps, rs)
     out = oracle_pool.decompress(pc, pa, ps, block)
     assert np.array_equal(out, oracle.decompress(rc, ra, rs, block))
+    fc, fa, fs = oracle_pool.compress_f64(out, block)
+    gc, ga, gs = oracle.compress_f64(out, block)
+    assert np.array_equal(fc, gc) and np.array_equal(fa, ga) and np.array_equal(fs, gs)
 
 
 @pytest.mark.parametrize("piece_bytes", [None, 5_000])
