@@ -73,19 +73,40 @@ template <int NF> __device__ __forceinline__ void encode_codes(const float2 (&v)
 
 __device__ __forceinline__ void encode32_f2(const float2 (&v)[16], float k, uint4 (&q)[2]) { encode_codes<16>(v, k, q); }
 
+// 32 codes with one 32-byte load (p 32-byte aligned) and an L2 cache
+// policy: a warp's request then covers 32 whole sectors, where two 16-byte
+// loads 32 bytes apart each touch 32 sectors half.
+__device__ __forceinline__ void ldg256_stream_hint(const void *p, uint64_t pol, uint4 &lo, uint4 &hi)
+{
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p), "l"(pol));
+}
+
 // EF: load with the L2 cache policy `pol` (evict-first for codes that
-// nothing reads again); without EF, `pol` is ignored.
-template <int NF, bool EF = false>
+// nothing reads again); without EF, `pol` is ignored.  WIDE (32 codes, EF,
+// p 32-byte aligned): one 32-byte load instead of two 16-byte ones.
+template <int NF, bool EF = false, bool WIDE = false>
 __device__ __forceinline__ void load_codes(const uint8_t *p, bool valid, uint4 (&q)[NF / 8], uint64_t pol = 0)
 {
+    if constexpr (WIDE) {
+        static_assert(NF == 16 && EF, "the 32-byte load covers 32 codes, with a cache policy");
+        if (valid) {
+            ldg256_stream_hint(p, pol, q[0], q[1]);
+        } else {
+            q[0] = make_uint4(0, 0, 0, 0);
+            q[1] = make_uint4(0, 0, 0, 0);
+        }
+    } else {
 #pragma unroll
-    for (int h = 0; h < NF / 8; ++h) {
-        if (!valid)
-            q[h] = make_uint4(0, 0, 0, 0);
-        else if constexpr (EF)
-            q[h] = ldg128_stream_hint(p + 16 * h, pol);
-        else
-            q[h] = ldg128_stream(p + 16 * h);
+        for (int h = 0; h < NF / 8; ++h) {
+            if (!valid)
+                q[h] = make_uint4(0, 0, 0, 0);
+            else if constexpr (EF)
+                q[h] = ldg128_stream_hint(p + 16 * h, pol);
+            else
+                q[h] = ldg128_stream(p + 16 * h);
+        }
     }
 }
 

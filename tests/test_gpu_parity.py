@@ -193,6 +193,35 @@ def test_reduce_is_invariant_to_shard_order(P, block):
         assert_scalars_match(to_host(got[2]), ref[2], "permuted scale")
 
 
+@pytest.mark.parametrize("P,block", [(1, 128), (3, 128), (4, 256)])
+def test_reduce_with_16_byte_aligned_shards_equals_32_byte_aligned(P, block):
+    """The reduce loads each shard's codes with one 32-byte load when every
+    shard is 32-byte aligned, with two 16-byte loads otherwise: the same
+    arithmetic on the same values, so the results are bit-identical.  The
+    shards are copied to 16-byte (not 32-byte) aligned views, and against
+    the oracle the reduce is checked on the misaligned path too."""
+    rows, d = 96, 1024
+    shards = [api.taco_compress(to_dev_bf16(W.tp_activation(160 + p, rows, d, channel_scale=True, block=block)),
+                                block) for p in range(P)]
+    cs, as_, ss = (list(t) for t in zip(*shards))
+    ref = api.taco_reduce_shards(cs, as_, ss, block)
+    n = rows * d
+    buf = torch.empty(P * n + 64, dtype=torch.uint8, device="cuda")
+    base = (32 - buf.data_ptr() % 32) % 32 + 16  # 16 bytes past a 32-byte boundary
+    mis = [buf[base + p * n: base + (p + 1) * n].view(rows, d) for p in range(P)]
+    for p in range(P):
+        assert mis[p].data_ptr() % 32 == 16
+        mis[p].copy_(cs[p])
+    got = api.taco_reduce_shards(mis, as_, ss, block)
+    for g, r in zip(got, ref):
+        assert torch.equal(g.view(torch.uint8) if g.dtype == torch.uint8 else g.view(torch.int32),
+                           r.view(torch.uint8) if r.dtype == torch.uint8 else r.view(torch.int32))
+    rc, ra, rs = oracle.reduce_shards([to_host(c) for c in cs], [to_host(a) for a in as_],
+                                      [to_host(s) for s in ss], block)
+    assert_codes_match(to_host(got[0]), rc, "reduced codes, 16-byte aligned shards")
+    assert_scalars_match(to_host(got[1]), ra, "reduced alpha, 16-byte aligned shards")
+
+
 def test_reduce_shard_and_negation_gives_zero_blocks():
     block = 128
     c, a, s = api.taco_compress(to_dev_bf16(W.tp_activation(9, 32, 512, block=block)), block)
