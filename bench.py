@@ -589,6 +589,66 @@ def gpt27b_leg(torch, api, peak: float) -> dict:
     return res
 
 
+def bf16_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s, burst) from
+    MEASURED_PEAKS.json, else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst (no MEASURED_PEAKS.json)"
+
+
+def gemm_leg(torch, api, pool=None) -> dict:
+    """The GEMM that produces a GPT-6.7B TP partial sum, with the compressor
+    in its epilogue: the row-parallel MLP down-projection at TP = 4, A =
+    [8192 tokens, 4096] activations, B = [4096, 4096] weights, Y = A B^T
+    compressed per 128-element block (taco_gemm_compress).  Timed from graph
+    replays beside the unfused path it replaces: cuBLAS (torch.matmul, bf16
+    out) then taco_compress, and beside each of those two alone.  The
+    operands (96 MB) stay in L2 across replays, as they would between the
+    layer's tiles; the fused call's and cuBLAS's outputs are written every
+    replay."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    M, N, K = 8192, 4096, 4096
+    a_bits = pool.submit(_tp_shard, (900, M, K, True, False, 128)).result() if pool else \
+        _tp_shard((900, M, K, True, False, 128))
+    b_bits = W.f32_to_bf16_bits(np.random.default_rng(901).normal(0.0, 0.02, (N, K)).astype(np.float32))
+    a = torch.from_numpy(a_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    b = torch.from_numpy(b_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    nb = M * N // 128
+    codes = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    alpha = torch.empty(nb, dtype=torch.float32, device="cuda")
+    scale = torch.empty(nb, dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    fused = lambda: api.taco_gemm_compress(a, b, codes=codes, alpha=alpha, scale=scale)
+    gemm = lambda: torch.matmul(a, b.t(), out=y)
+    comp = lambda: api.taco_compress(y, 128, codes=codes, alpha=alpha, scale=scale)
+
+    def unfused():
+        gemm()
+        comp()
+
+    for fn in (fused, unfused):
+        fn()
+    ms = {"fused": time_launches(torch, fused, 10, stream), "cublas_gemm": time_launches(torch, gemm, 10, stream),
+          "compress": time_launches(torch, comp, 10, stream), "unfused": time_launches(torch, unfused, 10, stream)}
+    flops = 2.0 * M * N * K
+    peak, src = bf16_peak()
+    out = {k: {"us_per_launch": v * 1e3, "tflops": flops / (v / 1e3) / 1e12 if k != "compress" else None}
+           for k, v in ms.items()}
+    for k in ("fused", "cublas_gemm", "unfused"):
+        out[k]["frac_of_bf16_peak"] = out[k]["tflops"] / peak
+    out["shape"] = {"M": M, "N": N, "K": K, "block": 128}
+    out["bf16_peak_tflops"] = peak
+    out["bf16_peak_source"] = src
+    out["fused_vs_unfused_speedup"] = ms["unfused"] / ms["fused"]
+    out["hbm_bytes_saved_per_call"] = 2 * 2 * M * N  # the bf16 Y written and read back
+    return out
+
+
 def gpt13b_leg(torch, api, peak: float, pool=None) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     device times (graph replays) of compress, reduce + decompress in one call,
@@ -765,6 +825,7 @@ def main():
     ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
     ap.add_argument("--no-gpt27b", action="store_true", help="skip the GPT-2.7B-shaped round-trip leg")
     ap.add_argument("--no-gpt13b", action="store_true", help="skip the GPT-13B-shaped leg")
+    ap.add_argument("--no-gemm", action="store_true", help="skip the fused GEMM + compress leg")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
     ap.add_argument("--replicas", action="store_true",
@@ -891,6 +952,9 @@ def main():
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_gpt13b:
         extra[GPT13B] = gpt13b_leg(torch, api, peak, pool)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_gemm:
+        extra["gemm_compress_gpt6.7b_down_proj_8192x4096x4096"] = gemm_leg(torch, api, pool)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_agoq:
         extra["agoq"] = agoq_leg(torch, api, peak)
