@@ -11,20 +11,22 @@
 // compressor.
 //
 // Design (sm_103a):
-//  * One CTA computes a 128 x 256 tile of Y in tensor memory (fp32, 256
-//    columns).  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A
-//    and 256 x 64 tiles of B (bf16, 128-byte swizzle) through a 4-stage
-//    mbarrier ring.  Warp 1 allocates the tensor memory and one of its
-//    threads issues the tcgen05.mma steps (128 x 256 x 16 each, four per
-//    64-wide stage) and commits each stage back to the producer.  Warps 2-5
-//    are the epilogue.
+//  * A persistent grid, one CTA per SM, walks the 128 x 256 tiles of Y in
+//    turn.  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A and
+//    256 x 64 tiles of B (bf16, 128-byte swizzle) through a 4-stage mbarrier
+//    ring, from one output tile into the next without a gap.  Warp 1
+//    allocates 512 columns of tensor memory (two fp32 accumulators of 256
+//    columns) and one of its threads issues the tcgen05.mma steps (128 x 256
+//    x 16 each, four per 64-wide stage), frees each stage with
+//    tcgen05.commit, and signals a finished accumulator the same way.  Warps
+//    2-5 are the epilogue: while they compress tile i from one accumulator,
+//    the MMAs of tile i + 1 fill the other.
 //  * The accumulator's lane is the tile row, so after tcgen05.ld each
 //    epilogue thread holds 128 consecutive fp32 values of one row: exactly
 //    one compression block, the layout the compress kernel gives a thread.
 //    The 128-point Walsh-Hadamard transform, the block energy, alpha, s and
 //    the E4M3 conversion run in that thread's registers; the codes go
-//    through a swizzled staging tile (the emptied stage buffers) and TMA
-//    stores.
+//    through the warp's swizzled staging rows and TMA stores.
 //  * Every mbarrier wait is time-limited; a wait that runs out sets a flag
 //    readable through taco_device_error() and the CTA winds down.
 
@@ -49,8 +51,11 @@ constexpr int kGThreads = 192;                       // warps: 0 producer, 1 MMA
 constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr uint32_t kGStageBytes = kABytes + kBBytes; // 48 KB
-constexpr uint32_t kTmemCols = kBN;                  // fp32 accumulator, one column per tile column
-constexpr uint32_t kGemmSmem = 1024 + kGStages * kGStageBytes + 8 * (2 * kGStages + 1) + 16;
+constexpr uint32_t kAccCols = kBN;                   // fp32 accumulator, one column per tile column
+constexpr uint32_t kTmemCols = 2 * kAccCols;         // two accumulators
+constexpr uint32_t kStageOut = 4 * 2 * 4096;         // epilogue staging: 4 warps x 2 blocks x 32 rows x 128 B
+constexpr uint32_t kBars = 8 * (2 * kGStages + 4);   // full / empty per stage, full / empty per accumulator
+constexpr uint32_t kGemmSmem = 1024 + kGStages * kGStageBytes + kStageOut + kBars + 16;
 constexpr uint32_t kErrGemm = 32u;
 static_assert(kGStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kGemmSmem <= 232448, "shared memory per CTA");
@@ -62,22 +67,90 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Compresses one 128-element block of the thread's row from tensor memory
+// (columns col .. col + 127 of lane quarter q) into the staging row at
+// `orow` (swizzled), and returns its alpha and s.  y_row (optional) gets the
+// raw accumulator values.
+__device__ __forceinline__ void compress_block_from_tmem(uint32_t taddr, float *y_row, uint32_t orow, uint32_t swz,
+                                                         float e_target, float eps, float &alpha, float &scale)
+{
+    float2 v[64];
+    float2 acc[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x[32];
+        tmem_load_32(taddr + 32 * j, x);
+        if (y_row) {
+            float4 *yo = reinterpret_cast<float4 *>(y_row + 32 * j);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                yo[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+        // step 1 (energy) and the bit-0 butterfly stage of step 3
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const int kk = 16 * j + t;
+            const float2 xx = make_float2(x[2 * t], x[2 * t + 1]);
+            acc[kk & 7] = (kk < 8) ? __fmul2_rn(xx, xx) : __ffma2_rn(xx, xx, acc[kk & 7]);
+            v[kk] = make_float2(xx.x + xx.y, xx.x - xx.y);
+        }
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            acc[i] = __fadd2_rn(acc[i], acc[i + w]);
+    const float ss = acc[0].x + acc[0].y;
+    // step 3: remaining butterflies; the last is fused with the scaling
+    fwht128_upper_but_last(v);
+    const float mh = max_abs_last_stage(v);
+    // step 2: alpha = sqrt(E / (m + eps));  step 4: s = 448 / max|y|
+    alpha = sqrtf(e_target / (ss * BlockConst<128>::inv_n + eps));
+    const float ac = alpha * BlockConst<128>::c;
+    const float M = ac * mh;
+    scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
+    float k = ac * scale;
+    if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
+        const float2 ac2 = make_float2(ac, ac);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            v[i] = __fmul2_rn(v[i], ac2);
+        k = scale;
+    }
+    last_stage_scaled(v, make_float2(k, k));
+    // step 5: E4M3 codes into the swizzled staging row
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        encode8_prescaled(&v[8 * j], w0, w1);
+        encode8_prescaled(&v[8 * j + 4], w2, w3);
+        sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
+    }
+}
+
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_compress_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                          const __grid_constant__ CUtensorMap c_map, float *__restrict__ alpha_out,
-                         float *__restrict__ scale_out, float *__restrict__ y_out, int64_t N, int K, float e_target,
-                         float eps)
+                         float *__restrict__ scale_out, float *__restrict__ y_out, int64_t N, int K, int ntiles,
+                         float e_target, float eps)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t bars = base + kGStages * kGStageBytes;
-    const uint32_t accum_bar = bars + 16 * kGStages;
-    const uint32_t tmem_slot = accum_bar + 8;
+    const uint32_t stage_out = base + kGStages * kGStageBytes;
+    const uint32_t bars = stage_out + kStageOut;
+    const uint32_t tmem_slot = bars + kBars;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
     const int KB = K / kBK;
+    const int ntn = static_cast<int>(N / kBN);  // tiles along N
     auto full = [&](int s) { return bars + 8 * s; };
     auto empty = [&](int s) { return bars + 8 * (kGStages + s); };
+    auto acc_full = [&](int a) { return bars + 8 * (2 * kGStages + a); };
+    auto acc_empty = [&](int a) { return bars + 8 * (2 * kGStages + 2 + a); };
     auto stage_a = [&](int s) { return base + s * kGStageBytes; };
     auto stage_b = [&](int s) { return base + s * kGStageBytes + kABytes; };
 
@@ -86,7 +159,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);   // one tcgen05.commit
+            mbar_init(acc_empty(a), 4);  // one arrival per epilogue warp
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -103,122 +179,103 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&a_map);
             tma_prefetch_map(&b_map);
-            int issued = 0;
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % kGStages;
-                if (!mbar_wait(empty(s), ((kb / kGStages) & 1) ^ 1)) {
-                    atomicOr(&g_gemm_error, kErrGemm);
-                    break;
+            int g = 0;  // k-blocks issued so far (all tiles): stage g % S, phase (g / S) & 1
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % kGStages;
+                    if (!mbar_wait(empty(s), ((g / kGStages) & 1) ^ 1)) {
+                        atomicOr(&g_gemm_error, kErrGemm);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), kGStageBytes);
+                    tma_load_2d(stage_a(s), &a_map, kb * kBK, m0, full(s));
+                    tma_load_2d(stage_b(s), &b_map, kb * kBK, n0, full(s));
                 }
-                mbar_arrive_expect_tx(full(s), kGStageBytes);
-                tma_load_2d(stage_a(s), &a_map, kb * kBK, m0, full(s));
-                tma_load_2d(stage_b(s), &b_map, kb * kBK, n0, full(s));
-                ++issued;
             }
             // leave no load in flight into this CTA's shared memory
-            for (int kb = issued > kGStages ? issued - kGStages : 0; kb < issued; ++kb)
-                mbar_wait(full(kb % kGStages), (kb / kGStages) & 1);
+            for (int i = g > kGStages ? g - kGStages : 0; i < g; ++i)
+                mbar_wait(full(i % kGStages), (i / kGStages) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32<kBM, kBN>();
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % kGStages;
-                if (!mbar_wait(full(s), (kb / kGStages) & 1)) {
+            int g = 0, i = 0;  // k-blocks consumed, tiles done
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++i) {
+                const int a = i & 1;
+                // the epilogue has emptied this accumulator (tile i - 2)
+                if (!mbar_wait(acc_empty(a), ((i >> 1) & 1) ^ 1)) {
                     atomicOr(&g_gemm_error, kErrGemm);
                     break;
                 }
                 tc_fence_after_sync();
-                const uint64_t ad = smem_desc_k_sw128(stage_a(s)), bd = smem_desc_k_sw128(stage_b(s));
+                const uint32_t d = tmem + a * kAccCols;
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % kGStages;
+                    if (!mbar_wait(full(s), (g / kGStages) & 1)) {
+                        atomicOr(&g_gemm_error, kErrGemm);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = smem_desc_k_sw128(stage_a(s)), bd = smem_desc_k_sw128(stage_b(s));
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
-                    mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-                mma_commit(empty(s));  // the stage is free once these MMAs have read it
+                    for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
+                        mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    mma_commit(empty(s));  // the stage is free once these MMAs have read it
+                }
+                mma_commit(acc_full(a));  // the accumulator is complete once every MMA has
             }
-            mma_commit(accum_bar);  // the accumulator is complete once every MMA has
         }
     } else {
         // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
         const int q = warp & 3;
         const int row = 32 * q + lane;
-        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accum_bar, 0));
-        if (!ok) {
-            if (lane == 0)
-                atomicOr(&g_gemm_error, kErrGemm);
-        } else {
-            tc_fence_after_sync();
-            const uint32_t outw = base + q * 2 * 4096;  // this warp's staging rows (the stages are free)
-            const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
-            const float c = BlockConst<128>::c;
-            const int64_t nblk_row = N / 128;
-#pragma unroll 1
-            for (int blk = 0; blk < kBN / 128; ++blk) {
-                float2 v[64];
-                float2 acc[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float x[32];
-                    tmem_load_32(tmem + (static_cast<uint32_t>(32 * q) << 16) + blk * 128 + 32 * j, x);
-                    if (y_out) {
-                        float4 *yo = reinterpret_cast<float4 *>(y_out + (m0 + row) * N + n0 + blk * 128 + 32 * j);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            yo[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-                    }
-                    // step 1 (energy) and the bit-0 butterfly stage of step 3
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int kk = 16 * j + t;
-                        const float2 xx = make_float2(x[2 * t], x[2 * t + 1]);
-                        acc[kk & 7] = (kk < 8) ? __fmul2_rn(xx, xx) : __ffma2_rn(xx, xx, acc[kk & 7]);
-                        v[kk] = make_float2(xx.x + xx.y, xx.x - xx.y);
-                    }
-                }
-#pragma unroll
-                for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int i = 0; i < w; ++i)
-                        acc[i] = __fadd2_rn(acc[i], acc[i + w]);
-                const float ss = acc[0].x + acc[0].y;
-                // step 3: remaining butterflies; the last is fused with the scaling
-                fwht128_upper_but_last(v);
-                const float mh = max_abs_last_stage(v);
-                // step 2: alpha = sqrt(E / (m + eps));  step 4: s = 448 / max|y|
-                const float alpha = sqrtf(e_target / (ss * BlockConst<128>::inv_n + eps));
-                const float ac = alpha * c;
-                const float M = ac * mh;
-                const float scale = (M > 0.0f) ? fminf(448.0f / M, FLT_MAX) : 1.0f;
-                float k = ac * scale;
-                if (!(k <= FLT_MAX)) {  // block of tiny values: apply the two factors separately
-                    const float2 ac2 = make_float2(ac, ac);
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        v[i] = __fmul2_rn(v[i], ac2);
-                    k = scale;
-                }
-                last_stage_scaled(v, make_float2(k, k));
-                // step 5: E4M3 codes into the swizzled staging rows, then a TMA store
-                const uint32_t stg = outw + blk * 4096, orow = stg + lane * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w0, w1, w2, w3;
-                    encode8_prescaled(&v[8 * j], w0, w1);
-                    encode8_prescaled(&v[8 * j + 4], w2, w3);
-                    sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), w0, w1, w2, w3);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&c_map, n0 + blk * 128, m0 + 32 * q, stg);
-                    bulk_commit();
-                }
-                const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128 + blk;
-                alpha_out[bi] = alpha;
-                scale_out[bi] = scale;
+        const uint32_t outw = stage_out + q * 2 * 4096;  // this warp's two staging tiles
+        const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
+        const int64_t nblk_row = N / 128;
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(a), (i >> 1) & 1))) {
+                if (lane == 0)
+                    atomicOr(&g_gemm_error, kErrGemm);
+                break;
             }
+            tc_fence_after_sync();
             if (lane == 0)
-                bulk_wait_all();
+                bulk_wait_read_all();  // the previous tile's stores have read the staging tiles
+            __syncwarp();
+            const uint32_t tq = tmem + a * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
+            float *yrow = y_out ? y_out + (m0 + row) * N + n0 : nullptr;
+            float al0, sc0, al1, sc1;
+            compress_block_from_tmem(tq, yrow, outw + lane * 128, swz, e_target, eps, al0, sc0);
+            compress_block_from_tmem(tq + 128, yrow ? yrow + 128 : nullptr, outw + 4096 + lane * 128, swz, e_target,
+                                     eps, al1, sc1);
+            // every tensor-memory read of this accumulator is done: hand it back
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acc_empty(a));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                for (int blk = 0; blk < kBN / 128; ++blk)
+                    tma_store_2d(&c_map, n0 + blk * 128, m0 + 32 * q, outw + blk * 4096);
+                bulk_commit();
+            }
+            const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128;
+            alpha_out[bi] = al0;
+            alpha_out[bi + 1] = al1;
+            scale_out[bi] = sc0;
+            scale_out[bi + 1] = sc1;
         }
+        if (lane == 0)
+            bulk_wait_all();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -269,9 +326,10 @@ cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t
             return e;
         set[di.device].store(true, std::memory_order_release);
     }
-    const dim3 grid(static_cast<unsigned>(N / kBN), static_cast<unsigned>(M / kBM));
+    const int64_t ntiles = (M / kBM) * (N / kBN);
+    const int grid = static_cast<int>(ntiles < di.num_sms ? ntiles : di.num_sms);
     return launch_pdl(gemm_compress_kernel, grid, kGThreads, kGemmSmem, stream, am, bm, cm, alpha, scale, y_out, N,
-                      static_cast<int>(K), e_target, eps);
+                      static_cast<int>(K), static_cast<int>(ntiles), e_target, eps);
 }
 
 }  // namespace taco

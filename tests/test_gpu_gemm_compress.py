@@ -79,9 +79,12 @@ def test_gemm_compress_small_shapes(M, N, K):
     check_gemm_compress(M, N, K)
 
 
-def test_gemm_compress_many_tiles_per_sm():
-    # more tiles than SMs (1024 x 2048: 8 x 8 = 64 tiles; 2048 x 4096: 256 tiles)
-    check_gemm_compress(2048, 4096, 512, seed=3)
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 512), (4096, 4096, 128), (8192, 2048, 64)])
+def test_gemm_compress_many_tiles_per_sm(M, N, K):
+    """More tiles than SMs: the persistent CTAs take several tiles each
+    (256, 512 and 512 tiles), so both tensor-memory accumulators are used and
+    reused, and a tile's epilogue runs while the next tile's MMAs do."""
+    check_gemm_compress(M, N, K, seed=3)
 
 
 def test_gemm_compress_zero_rows_give_zero_blocks():
