@@ -11,12 +11,16 @@ FP32 and requantises, and an All-Gather returns the reduced shards.
 With W ranks, the rows (or, for a flat gradient buffer, the blocks) are cut
 into W contiguous chunks of equal size; rank j owns chunk j.  One call:
 
-  1. compress the whole local tensor (one launch);
-  2. All-to-All of codes, alpha and s: chunk j of every rank lands on rank j,
+  1. compress the local tensor (one launch per chunk, into a packed send
+     buffer: each chunk's codes, alphas and scales as one byte run);
+  2. All-to-All of the packed chunks: chunk j of every rank lands on rank j,
      in the rank's own memory, in rank order;
   3. the shard reduce over the W received chunks (one launch);
-  4. AllGather of the reduced chunk's codes and scalars;
-  5. decompress the gathered tensor (one launch).
+  4. AllGather of the reduced chunk, packed the same way;
+  5. decompress the gathered chunks (one launch per chunk).
+
+With ``stages`` > 1 the chunks travel in pieces and the kernels of one
+piece overlap the collectives of another (TwoShotAllReduce).
 
 Rows that do not divide evenly are padded: the last chunk is filled up with
 rows whose codes are 0 and whose scalars are 1, written once when the
@@ -70,72 +74,113 @@ class TwoShotAllReduce:
     """Sum of a bf16 [rows, d] tensor over the ranks of ``group``, exchanged
     as ASH+DS FP8 codes (TACO 2.B.3).  Buffers are allocated once; ``run``
     only launches and communicates.  Every rank returns the same
-    reconstruction [rows, d]."""
+    reconstruction [rows, d].
+
+    ``stages`` > 1 overlaps the kernels with the collectives (TACO 2.B.3:
+    the compression and decompression kernels run while communication is in
+    flight).  Each rank's chunk is cut into ``stages`` pieces of Rs rows;
+    piece k of every chunk travels in stage k.  The compress of stage k + 1
+    runs while stage k's All-to-All is in flight, the reduce of stage k + 1
+    while stage k's AllGather is, and the decompress of stage k while later
+    AllGathers are.  The collectives are issued asynchronously; on GPUs each
+    one waits for the kernels queued before it on the current stream, and
+    the kernels that read its result wait for it.  Stage k's pieces are not
+    contiguous rows of the tensor, so its compress and decompress are one
+    launch per chunk."""
 
     def __init__(self, rows: int, d: int, block: int = 128, group=None, device="cuda",
-                 e_target: float = api.E_TARGET, eps: float = api.EPS, out_dtype=torch.float32, ops=None):
+                 e_target: float = api.E_TARGET, eps: float = api.EPS, out_dtype=torch.float32, ops=None,
+                 stages: int = 1):
         if d % block:
             raise ValueError("d must be a multiple of the block size")
+        if stages < 1:
+            raise ValueError("stages must be at least 1")
         self.group = group
         self.W = dist.get_world_size(group)
         self.rank = dist.get_rank(group)
         self.rows, self.d, self.block = rows, d, block
         self.e_target, self.eps = e_target, eps
         self.ops = ops if ops is not None else CudaOps
-        self.R = chunk_rows(rows, self.W)
-        self.Rb = self.R * d // block  # blocks per chunk
-        W, R, Rb = self.W, self.R, self.Rb
-        u8, f32 = torch.uint8, torch.float32
-        # send side: the local tensor's codes and scalars, chunk j at [j]
-        self.codes = torch.zeros((W * R, d), dtype=u8, device=device)
-        self.alpha = torch.ones(W * Rb, dtype=f32, device=device)
-        self.scale = torch.ones(W * Rb, dtype=f32, device=device)
-        # receive side: this rank's chunk of every rank, in rank order
-        self.recv_codes = torch.empty((W, R, d), dtype=u8, device=device)
-        self.recv_alpha = torch.empty((W, Rb), dtype=f32, device=device)
-        self.recv_scale = torch.empty((W, Rb), dtype=f32, device=device)
-        # the reduced chunk, then every rank's reduced chunk
-        self.red_codes = torch.empty((R, d), dtype=u8, device=device)
-        self.red_alpha = torch.empty(Rb, dtype=f32, device=device)
-        self.red_scale = torch.empty(Rb, dtype=f32, device=device)
-        self.gat_codes = torch.empty((W * R, d), dtype=u8, device=device)
-        self.gat_alpha = torch.empty(W * Rb, dtype=f32, device=device)
-        self.gat_scale = torch.empty(W * Rb, dtype=f32, device=device)
-        self.out = torch.empty((W * R, d), dtype=out_dtype, device=device)
-        nb = rows * d // block
-        self._codes_live = self.codes[:rows]
-        self._alpha_live = self.alpha[:nb]
-        self._scale_live = self.scale[:nb]
+        self.S = stages
+        self.R = -(-chunk_rows(rows, self.W) // stages) * stages  # rows per chunk, a multiple of S
+        self.Rs = self.R // stages                                # rows per piece
+        self.Rb = self.R * d // block                             # blocks per chunk
+        W, S, Rs = self.W, self.S, self.Rs
+        self.Rsb = Rs * d // block
+        # One piece travels as one packed byte run: Rs * d codes, then Rsb
+        # fp32 alphas, then Rsb fp32 scales, padded to a multiple of 256
+        # bytes so that every piece's codes start 256-byte aligned (the
+        # scalars follow at 4-byte aligned offsets: Rs * d is a multiple of
+        # 128).  Each stage is then one All-to-All and one AllGather.
+        self.piece_bytes = -(-(Rs * d + 8 * self.Rsb) // 256) * 256
+        u8 = torch.uint8
+        # per stage k: the send side holds piece k of every chunk of the
+        # local tensor (chunk j at [j]; rows past the tensor stay code 0 and
+        # scalars 1); the receive side this rank's piece k from every rank,
+        # in rank order; then its reduced piece, and every rank's reduced piece
+        self.send = torch.zeros((S, W, self.piece_bytes), dtype=u8, device=device)
+        self._alpha_of(self.send).fill_(1.0)
+        self._scale_of(self.send).fill_(1.0)
+        self.recv = torch.empty((S, W, self.piece_bytes), dtype=u8, device=device)
+        self.red = torch.empty((S, self.piece_bytes), dtype=u8, device=device)
+        self.gat = torch.empty((S, W, self.piece_bytes), dtype=u8, device=device)
+        self.out = torch.empty((W * self.R, d), dtype=out_dtype, device=device)
+
+    # views of packed pieces (last dimension = one piece's bytes)
+    def _codes_of(self, t):
+        return t[..., :self.Rs * self.d].unflatten(-1, (self.Rs, self.d))
+
+    def _alpha_of(self, t):
+        o = self.Rs * self.d
+        return t[..., o:o + 4 * self.Rsb].view(torch.float32)
+
+    def _scale_of(self, t):
+        o = self.Rs * self.d + 4 * self.Rsb
+        return t[..., o:o + 4 * self.Rsb].view(torch.float32)
 
     def bytes_exchanged(self) -> dict:
         """Bytes each rank sends per call in the two collectives (codes and
         both scalars of the W - 1 chunks that leave the rank)."""
-        chunk = self.R * self.d + 8 * self.Rb
+        chunk = self.S * self.piece_bytes
         return {"all_to_all": (self.W - 1) * chunk, "all_gather": (self.W - 1) * chunk}
 
-    def compress(self, x: torch.Tensor):
-        self.ops.compress(x, self._codes_live, self._alpha_live, self._scale_live, self.block, self.e_target,
-                          self.eps)
+    def _piece(self, j: int, k: int):
+        """Rows of the tensor in piece k of chunk j (possibly fewer than Rs,
+        or none, at the padded end)."""
+        r0 = j * self.R + k * self.Rs
+        return r0, max(r0, min(r0 + self.Rs, self.rows))
 
-    def exchange(self):
-        """ReduceScatter in compressed form: chunk j of every rank to rank j."""
-        g = self.group
-        dist.all_to_all_single(self.recv_codes.view(-1), self.codes.view(-1), group=g)
-        dist.all_to_all_single(self.recv_alpha.view(-1), self.alpha, group=g)
-        dist.all_to_all_single(self.recv_scale.view(-1), self.scale, group=g)
+    def compress(self, x: torch.Tensor, k: int = 0):
+        """Stage k's pieces of the local tensor into the send buffer."""
+        nbr = self.d // self.block
+        for j in range(self.W):
+            r0, r1 = self._piece(j, k)
+            if r1 > r0:
+                n = r1 - r0
+                piece = self.send[k, j]
+                self.ops.compress(x[r0:r1], self._codes_of(piece)[:n], self._alpha_of(piece)[:n * nbr],
+                                  self._scale_of(piece)[:n * nbr], self.block, self.e_target, self.eps)
 
-    def reduce(self):
-        self.ops.reduce(list(self.recv_codes), list(self.recv_alpha), list(self.recv_scale), self.block,
-                        self.e_target, self.eps, self.red_codes, self.red_alpha, self.red_scale)
+    def exchange(self, k: int = 0, async_op: bool = False):
+        """ReduceScatter in compressed form: piece k of chunk j of every rank
+        to rank j (codes and both scalars in one collective)."""
+        return dist.all_to_all_single(self.recv[k].view(-1), self.send[k].view(-1), group=self.group,
+                                      async_op=async_op)
 
-    def gather(self):
-        g = self.group
-        dist.all_gather_into_tensor(self.gat_codes.view(-1), self.red_codes.view(-1), group=g)
-        dist.all_gather_into_tensor(self.gat_alpha, self.red_alpha, group=g)
-        dist.all_gather_into_tensor(self.gat_scale, self.red_scale, group=g)
+    def reduce(self, k: int = 0):
+        r, out = self.recv[k], self.red[k]
+        self.ops.reduce(list(self._codes_of(r)), list(self._alpha_of(r)), list(self._scale_of(r)), self.block,
+                        self.e_target, self.eps, self._codes_of(out), self._alpha_of(out), self._scale_of(out))
 
-    def decompress(self) -> torch.Tensor:
-        self.ops.decompress(self.gat_codes, self.gat_alpha, self.gat_scale, self.block, self.out)
+    def gather(self, k: int = 0, async_op: bool = False):
+        return dist.all_gather_into_tensor(self.gat[k].view(-1), self.red[k], group=self.group, async_op=async_op)
+
+    def decompress(self, k: int = 0) -> torch.Tensor:
+        g = self.gat[k]
+        for j in range(self.W):
+            r0 = j * self.R + k * self.Rs
+            self.ops.decompress(self._codes_of(g[j]), self._alpha_of(g[j]), self._scale_of(g[j]), self.block,
+                                self.out[r0:r0 + self.Rs])
         return self.out[:self.rows]
 
     def run(self, x: torch.Tensor) -> torch.Tensor:
@@ -143,11 +188,25 @@ class TwoShotAllReduce:
         ([rows, d] view of the output buffer)."""
         if tuple(x.shape) != (self.rows, self.d):
             raise ValueError(f"x must be [{self.rows}, {self.d}]")
-        self.compress(x)
-        self.exchange()
-        self.reduce()
-        self.gather()
-        return self.decompress()
+        if self.S == 1:
+            self.compress(x)
+            self.exchange()
+            self.reduce()
+            self.gather()
+            return self.decompress()
+        a2a = []
+        for k in range(self.S):  # compress k + 1 is queued while exchange k is in flight
+            self.compress(x, k)
+            a2a.append(self.exchange(k, async_op=True))
+        ag = []
+        for k in range(self.S):
+            a2a[k].wait()
+            self.reduce(k)
+            ag.append(self.gather(k, async_op=True))
+        for k in range(self.S):
+            ag[k].wait()
+            self.decompress(k)
+        return self.out[:self.rows]
 
 
 class AgoqAllReduce:

@@ -90,3 +90,6 @@ def test_exchange_bytes_split_the_local_path_across_ranks(world):
     r = bench.exchange_bytes(3, 100, 256, 128)
     assert r["reduce"] == 4 * (34 * 256 + 8 * 34 * 2)
     assert r["decompress"] == 3 * (34 * 256 * 5 + 8 * 34 * 2)
+    # pieces of a chunk: its rows are rounded up to a multiple of the stages
+    assert bench.exchange_bytes(3, 100, 256, 128, stages=4)["reduce"] == 4 * (36 * 256 + 8 * 36 * 2)
+    assert bench.exchange_bytes(4, 8192, 4096, 128, stages=4) == bench.exchange_bytes(4, 8192, 4096, 128)

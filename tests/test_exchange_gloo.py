@@ -78,11 +78,11 @@ def _worker(rank, world, port, case, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        kind, a, b, block = case
+        kind, a, b, block, stages = case
         if kind == "taco":
             rows, d = a, b
             x = torch.from_numpy(_taco_input(rank, rows, d, block).view(np.int16)).view(torch.bfloat16)
-            ar = exchange.TwoShotAllReduce(rows, d, block, device="cpu", ops=OracleOps)
+            ar = exchange.TwoShotAllReduce(rows, d, block, device="cpu", ops=OracleOps, stages=stages)
             out = ar.run(x).clone().numpy()
             sent = ar.bytes_exchanged()
             q.put((rank, out, ar.R, sent))
@@ -113,14 +113,19 @@ def _run(world, case):
     return sorted(out, key=lambda o: o[0])
 
 
-@pytest.mark.parametrize("world,rows,d,block", [(2, 64, 512, 128), (3, 50, 512, 256)])
-def test_two_shot_exchange_equals_the_reduce_of_all_ranks(world, rows, d, block):
-    res = _run(world, ("taco", rows, d, block))
+@pytest.mark.parametrize("world,rows,d,block,stages", [(2, 64, 512, 128, 1), (3, 50, 512, 256, 1),
+                                                       (2, 64, 512, 128, 4), (3, 50, 256, 128, 3)])
+def test_two_shot_exchange_equals_the_reduce_of_all_ranks(world, rows, d, block, stages):
+    """stages > 1 is the overlapped exchange: pieces of every chunk travel
+    in turn with asynchronous collectives (the 3-rank, 3-stage case has
+    pieces that are partly and wholly padding)."""
+    res = _run(world, ("taco", rows, d, block, stages))
     comp = [oracle.compress(_taco_input(r, rows, d, block), block) for r in range(world)]
     rc, ra, rs = oracle.reduce_shards(*zip(*comp), block)
     ref = oracle.decompress(rc, ra, rs, block).astype(np.float32)
-    R = -(-rows // world)
-    chunk_bytes = R * d + 8 * (R * d // block)
+    R = -(-(-(-rows // world)) // stages) * stages
+    Rs = R // stages
+    chunk_bytes = stages * (-(-(Rs * d + 8 * (Rs * d // block)) // 256) * 256)
     for rank, out, r_chunk, sent in res:
         assert r_chunk == R
         assert out.shape == (rows, d)
@@ -130,7 +135,7 @@ def test_two_shot_exchange_equals_the_reduce_of_all_ranks(world, rows, d, block)
 
 def test_agoq_exchange_equals_the_reduce_of_all_ranks():
     world, n, block = 2, 37 * 128, 128  # 37 blocks: a padded last chunk
-    res = _run(world, ("agoq", n, None, block))
+    res = _run(world, ("agoq", n, None, block, 1))
     bufs = [_agoq_buffer(r, n, block) for r in range(world)]
     rc, rs = oracle.agoq_reduce([b[0] for b in bufs], [b[1] for b in bufs], block)
     for rank, (c, s), cb, _ in res:
