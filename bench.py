@@ -685,12 +685,13 @@ def gpt13b_leg(torch, api, peak: float, pool=None) -> dict:
     return {k: kernel_entry(ms[k], nb[k], peak) for k in ms}
 
 
-def exchange_bytes(world: int, rows: int, d: int, block: int, out_bytes: int = 4) -> dict:
+def exchange_bytes(world: int, rows: int, d: int, block: int, out_bytes: int = 4, stages: int = 1) -> dict:
     """Algorithmic bytes of one rank's kernels in one two-shot AllReduce over
     ``world`` ranks of a [rows, d] tensor: compress of the whole tensor, the
-    reduce of ``world`` received chunks of R = ceil(rows / world) rows into
-    one, and the decompress of the ``world`` gathered chunks."""
-    R = -(-rows // world)
+    reduce of ``world`` received chunks of R rows into one (R =
+    ceil(rows / world), rounded up to a multiple of ``stages``), and the
+    decompress of the ``world`` gathered chunks."""
+    R = -(-(-(-rows // world)) // stages) * stages
     n, c = rows * d, R * d
     return {"compress": 3 * n + 8 * (n // block),
             "reduce": (world + 1) * (c + 8 * (c // block)),
@@ -713,45 +714,71 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
     d, block = w["d"], w["block"]
     bits = pool.submit(_tp_shard, (rank, rows, d, w["channel_scale"], w["spikes"], block)).result()
     torch.cuda.set_device(local)
-    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if world == 1 and "MASTER_ADDR" not in os.environ:  # a group of one, without torchrun
+        import socket
+
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                device_id=torch.device("cuda", local))
+    else:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-    ar = exchange.TwoShotAllReduce(rows, d, block)
+    ar = exchange.TwoShotAllReduce(rows, d, block, stages=args.exchange_stages)
     stream = torch.cuda.current_stream()
     clocks = ClockSampler().start() if rank == 0 and not args.no_clocks else None
     time.sleep(0.2 if clocks else 0)
     for _ in range(args.warmup):
         ar.run(x)
     torch.cuda.synchronize()
+    # one step as a CUDA graph (kernels and NCCL collectives), so that the
+    # host's per-call cost (Python, the binding, torch.distributed) is not
+    # timed; eager steps if the capture is refused
+    graph, capture = None, "CUDA graph of one step (kernels and NCCL collectives), replayed"
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            ar.run(x)
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            ar.run(x)
+    except Exception as exc:  # noqa: BLE001 - report and time eagerly
+        graph = None
+        capture = f"eager steps (graph capture failed: {type(exc).__name__})"
+    torch.cuda.synchronize()
+    step = graph.replay if graph is not None else (lambda: ar.run(x))
+    for _ in range(3):
+        step()
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
+    t_host = time.perf_counter()
     start.record(stream)
     for _ in range(K):
-        ar.run(x)
+        step()
     end.record(stream)
+    host_us = (time.perf_counter() - t_host) / K * 1e6
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     elapsed_ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
-    # per-kernel samples: events around the three local launches
-    names = ("compress", "reduce", "decompress")
-    ns = max(2, args.kernel_samples)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(ns + 1)]
-    for e in ev:
-        e[0].record(stream)
-        ar.compress(x)
-        e[1].record(stream)
-        ar.exchange()
-        e[2].record(stream)
-        ar.reduce()
-        e[3].record(stream)
-        ar.gather()
-        e[4].record(stream)
-        ar.decompress()
-        e[5].record(stream)
+    # the captured graph holds the communicator's collectives: release it
+    # (after the device has finished with it) before the process group goes
+    step = None
+    del graph
     torch.cuda.synchronize()
-    pairs = {"compress": (0, 1), "reduce": (2, 3), "decompress": (4, 5)}
-    samples = {k: [ev[j][a].elapsed_time(ev[j][b]) for j in range(1, ns + 1)] for k, (a, b) in pairs.items()}
+    # per-kernel figures: each local phase of a step (its launches for every
+    # stage, no collective) captured in a CUDA graph and replayed, so that the
+    # host's per-call cost is not timed
+    names = ("compress", "reduce", "decompress")
+    phases = {"compress": lambda: [ar.compress(x, k) for k in range(ar.S)],
+              "reduce": lambda: [ar.reduce(k) for k in range(ar.S)],
+              "decompress": lambda: [ar.decompress(k) for k in range(ar.S)]}
+    ns = max(2, args.kernel_samples)
+    per_phase_ms = {k: time_launches(torch, fn, 10, stream, replays=max(1, ns // 10)) for k, fn in phases.items()}
     # end to end: pinned host input in, result out, every step
     h_in = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
     h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
@@ -770,12 +797,11 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
     if rank == 0:
         peak, peak_src = hbm_peak()
         spec, spec_src = spec_hbm_gbs(local)
-        nbytes = exchange_bytes(world, rows, d, block)
+        nbytes = exchange_bytes(world, rows, d, block, stages=ar.S)
         step_bytes = sum(nbytes.values())
-        kern = {}
-        for k in names:
-            st = summarize(samples[k])
-            kern[k] = kernel_entry(st["us_mean"] / 1e3, nbytes[k], peak, **st)
+        kern = {k: kernel_entry(per_phase_ms[k], nbytes[k], peak, launches=(ar.S if k == "reduce" else ar.W * ar.S),
+                                timed_as="graph replays of the phase's launches")
+                for k in names}
         achieved = kern["compress"]["gbs"]
         line = {
             "metric": METRIC, "value": whole_job_gbs(step_bytes, K, world, elapsed_ms), "unit": "GB/s",
@@ -785,23 +811,25 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
             "config": {"workload": f"two-shot AllReduce of one bf16 [{rows}, {d}] activation per rank "
                                    f"(GPT-6.7B shape, block {block}) across {world} ranks",
                        "rows": rows, "d": d, "block": block, "parallelism": f"tp{world} two-shot exchange (NCCL)",
+                       "exchange_stages": ar.S, "timed_as": capture, "host_enqueue_us_per_step": host_us,
                        "bytes_per_step_per_rank": step_bytes,
                        "exchange_bytes_sent_per_rank": ar.bytes_exchanged(),
                        "l2": "inputs larger than L2, no flush"},
             "roofline": {"bound": "hbm", "kernel": f"taco_compress_kernel<{block}>", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                         "peak_source": peak_src, "samples": ns, "spec_peak": spec, "spec_peak_source": spec_src,
+                         "peak_source": peak_src, "spec_peak": spec, "spec_peak_source": spec_src,
                          "frac_of_spec": achieved / spec},
             "kernels": kern,
             "e2e": {"value": whole_job_gbs(step_bytes, E, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": 2 * rows * d, "d2h_bytes_per_step": 4 * rows * d,
                     "api": "TwoShotAllReduce.run with pinned host copies in and out"},
-            "gpu_launches": 3 * K,
+            "gpu_launches": (2 * ar.W * ar.S + ar.S) * K,  # compress and decompress per piece, reduce per stage
             "clocks": clk,
             "watchdog_flags": flags,
         }
         print(json.dumps(line), flush=True)
     dist.barrier()
+    torch.cuda.synchronize()
     dist.destroy_process_group()
 
 
@@ -830,6 +858,10 @@ def main():
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
     ap.add_argument("--replicas", action="store_true",
                     help="under torchrun: independent replicas of the one-GPU path instead of the exchange")
+    ap.add_argument("--exchange", action="store_true",
+                    help="run the exchange path even on one rank (an NCCL group of one)")
+    ap.add_argument("--exchange-stages", type=int, default=4,
+                    help="pieces per chunk in the exchange (compress and decompress overlap the collectives)")
     ap.add_argument("--rows", type=int, default=None,
                     help="rows per shard (a smaller case of the same workload, e.g. for profiling)")
     args = ap.parse_args()
@@ -850,7 +882,7 @@ def main():
 
     from fp8_communication_compression_gb300 import api
 
-    if world > 1 and not args.replicas:
+    if (world > 1 and not args.replicas) or args.exchange:
         run_exchange(args, rank, world, local, pool)
         pool.shutdown()
         return

@@ -73,9 +73,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 }
 
 // Compresses one 128-element block of the thread's row from tensor memory
-// (columns col .. col + 127 of lane quarter q) into the staging row at
-// `orow` (swizzled), and returns its alpha and s.  y_row (optional) gets the
-// raw accumulator values.
+// (`taddr`: the block's first column, in the warp's lane quarter) into the
+// staging row at `orow` (swizzled), and returns its alpha and s.  y_row
+// (optional) gets the raw accumulator values.
 __device__ __forceinline__ void compress_block_from_tmem(uint32_t taddr, float *y_row, uint32_t orow, uint32_t swz,
                                                          float e_target, float eps, float &alpha, float &scale)
 {
