@@ -57,6 +57,7 @@ def _load():
             lib.oracle_reduce_shards.argtypes = [i32, P, P, P, i64, i64, i32, f32, f32, P, P, P]
             lib.oracle_agoq_accumulate.argtypes = [P, P, P, i64, i32]
             lib.oracle_agoq_reduce.argtypes = [i32, P, P, i64, i32, P, P]
+            lib.oracle_agoq_accumulate_f32.argtypes = [P, P, P, i64, i32]
             lib.oracle_int8_roundtrip.argtypes = [P, i64, i64, i32, P]
             lib.oracle_compress_int8.argtypes = [P, i64, i64, i32, f32, f32, P, P, P]
             lib.oracle_decompress_int8.argtypes = [P, P, P, i64, i64, i32, P]
@@ -64,6 +65,7 @@ def _load():
             lib.oracle_laaq_dequantize.argtypes = [P, P, i64, i32, i32, P]
             for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
                       "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
+                      "oracle_agoq_accumulate_f32",
                       "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8",
                       "oracle_laaq_quantize", "oracle_laaq_dequantize"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -200,6 +202,24 @@ def agoq_accumulate(codes: np.ndarray, scale: np.ndarray, grad_bf16: np.ndarray,
     assert g.size == c.size and s.size == c.size // block
     _check(_load().oracle_agoq_accumulate(_ptr(c), _ptr(s), _ptr(g), c.size, block))
     return c, s
+
+
+def agoq_accumulate_f32(codes: np.ndarray, scale: np.ndarray, grad_f32: np.ndarray, block: int = 128):
+    """The accumulation step with an fp32 gradient (the GEMM-fused form,
+    AGoQ 2.C); returns the new (codes, scale), the inputs unmodified."""
+    c = np.array(codes, dtype=np.uint8, copy=True).reshape(-1)
+    s = np.array(scale, dtype=np.float32, copy=True).reshape(-1)
+    g = np.ascontiguousarray(grad_f32, dtype=np.float32).reshape(-1)
+    assert g.size == c.size and s.size == c.size // block
+    _check(_load().oracle_agoq_accumulate_f32(_ptr(c), _ptr(s), _ptr(g), c.size, block))
+    return c, s
+
+
+def gemm_agoq_accumulate(a_bf16: np.ndarray, b_bf16: np.ndarray, codes: np.ndarray, scale: np.ndarray,
+                         block: int = 128):
+    """The fused weight-gradient GEMM + FP8 accumulation, as two plain steps:
+    Y = A B^T in float64, rounded to fp32, then the FP32 accumulation step."""
+    return agoq_accumulate_f32(codes, scale, gemm_bt(a_bf16, b_bf16).astype(np.float32), block)
 
 
 def agoq_reduce(codes, scales, block: int = 128):

@@ -343,6 +343,29 @@ int oracle_agoq_accumulate(uint8_t *main_codes, float *main_scale, const uint16_
     return 0;
 }
 
+/* The same accumulation step with an FP32 gradient, the form it takes when
+ * it is fused into the GEMM that produces the gradient ([AGoQ] 2.C): the
+ * GEMM's FP32 result is the value added, with no bf16 rounding. */
+int oracle_agoq_accumulate_f32(uint8_t *main_codes, float *main_scale, const float *grad, int64_t n, int block)
+{
+    int64_t nb, k;
+    int i;
+    float *g;
+    if (n < 0 || !valid_block(block) || n % block != 0)
+        return -1;
+    nb = n / block;
+    g = (float *)malloc(sizeof(float) * block);
+    for (k = 0; k < nb; ++k) {
+        for (i = 0; i < block; ++i) {
+            const float deq = agoq_dequantise(main_codes[k * block + i], main_scale[k]);
+            g[i] = deq + grad[k * block + i];
+        }
+        agoq_requantise(g, block, main_codes + k * block, main_scale + k);
+    }
+    free(g);
+    return 0;
+}
+
 /* [AGoQ] 2.B precision-preserving all-reduce, step 2: dequantise the P
  * received FP8 shards to FP32, sum them in FP32 in shard order, requantise. */
 int oracle_agoq_reduce(int P, const uint8_t *const *codes, const float *const *scale, int64_t n,

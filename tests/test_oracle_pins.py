@@ -642,3 +642,36 @@ def test_gemm_compress_is_compress_of_the_product():
     # Y = A B^T = B^T [128, 256]: compress the transpose of B directly
     rc, ra, rs = oracle.compress_f64(oracle.bf16_to_f64(b).T.copy(), n)
     assert np.array_equal(c, rc) and np.array_equal(al, ra) and np.array_equal(sc, rs)
+
+
+def test_agoq_accumulate_f32_equals_the_bf16_step_on_bf16_representable_gradients():
+    """The fp32-gradient accumulation (the GEMM-fused form, AGoQ 2.C) runs the
+    same FP32 sequence as the bf16 one: on gradients that are bf16 values it
+    gives the same codes and scales, step after step."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    n = 128 * 40
+    c, s = np.zeros(n, np.uint8), np.ones(n // 128, np.float32)
+    cf, sf = c.copy(), s.copy()
+    for step in range(3):
+        g = W.agoq_grad(500 + step, n)
+        c, s = oracle.agoq_accumulate(c, s, g, 128)
+        cf, sf = oracle.agoq_accumulate_f32(cf, sf, oracle.bf16_to_f64(g).astype(np.float32), 128)
+        assert np.array_equal(c, cf) and np.array_equal(s, sf)
+
+
+def test_agoq_accumulate_f32_first_step_is_absmax_quantisation():
+    """From the zero buffer (codes 0, multiplier 1) one step is plain
+    per-block absmax FP8 quantisation of the gradient: the multiplier is
+    max|g| / 448 and the codes are E4M3(g * 448 / max|g|)."""
+    rng = np.random.default_rng(4)
+    g = (rng.standard_normal(256) * 1e-3).astype(np.float32)
+    g[:128] *= 1000.0
+    c, s = oracle.agoq_accumulate_f32(np.zeros(256, np.uint8), np.ones(2, np.float32), g, 128)
+    for b in range(2):
+        blk = g[128 * b:128 * (b + 1)]
+        amax = np.float32(np.abs(blk).max())
+        assert s[b] == np.float32(amax / np.float32(448.0))
+        q = np.float32(448.0) / amax
+        want = oracle.e4m3_encode_array((blk * q).astype(np.float32))
+        assert np.array_equal(c[128 * b:128 * (b + 1)], want)
