@@ -649,6 +649,47 @@ def gemm_leg(torch, api, pool=None) -> dict:
     return out
 
 
+def agoq_gemm_leg(torch, api) -> dict:
+    """The weight-gradient GEMM with the FP8 main-gradient accumulation in its
+    epilogue (agoq_gemm_accumulate): a GPT-6.7B-shaped dW [4096, 4096] =
+    dY^T X over 8192 tokens, added into an FP8 main gradient per 128-element
+    block.  Timed from graph replays beside the path it replaces: cuBLAS
+    (torch.matmul, bf16 out) then agoq_fp8_accumulate."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    M, N, K = 4096, 4096, 8192
+    a_bits = W.agoq_grad(960, M * K).reshape(M, K)
+    b_bits = W.f32_to_bf16_bits(np.random.default_rng(961).normal(0.0, 0.05, (N, K)).astype(np.float32))
+    a = torch.from_numpy(a_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    b = torch.from_numpy(b_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    codes = torch.zeros((M, N), dtype=torch.uint8, device="cuda")
+    scale = torch.ones(M * N // 128, dtype=torch.float32, device="cuda")
+    g = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    fused = lambda: api.agoq_gemm_accumulate(a, b, codes, scale)
+    gemm = lambda: torch.matmul(a, b.t(), out=g)
+    acc = lambda: api.agoq_fp8_accumulate(codes.view(-1), scale, g.view(-1))
+
+    def unfused():
+        gemm()
+        acc()
+
+    for fn in (fused, unfused):
+        fn()
+    ms = {"fused": time_launches(torch, fused, 10, stream), "cublas_gemm": time_launches(torch, gemm, 10, stream),
+          "accumulate": time_launches(torch, acc, 10, stream), "unfused": time_launches(torch, unfused, 10, stream)}
+    flops = 2.0 * M * N * K
+    peak, src = bf16_peak()
+    out = {k: {"us_per_launch": v * 1e3, "tflops": flops / (v / 1e3) / 1e12 if k != "accumulate" else None}
+           for k, v in ms.items()}
+    for k in ("fused", "cublas_gemm", "unfused"):
+        out[k]["frac_of_bf16_peak"] = out[k]["tflops"] / peak
+    out["shape"] = {"M": M, "N": N, "K": K, "block": 128}
+    out["fused_vs_unfused_speedup"] = ms["unfused"] / ms["fused"]
+    out["hbm_bytes_saved_per_call"] = 2 * 2 * M * N  # the bf16 gradient written and read back
+    return out
+
+
 def gpt13b_leg(torch, api, peak: float, pool=None) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     device times (graph replays) of compress, reduce + decompress in one call,
@@ -853,7 +894,7 @@ def main():
     ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
     ap.add_argument("--no-gpt27b", action="store_true", help="skip the GPT-2.7B-shaped round-trip leg")
     ap.add_argument("--no-gpt13b", action="store_true", help="skip the GPT-13B-shaped leg")
-    ap.add_argument("--no-gemm", action="store_true", help="skip the fused GEMM + compress leg")
+    ap.add_argument("--no-gemm", action="store_true", help="skip the fused GEMM legs (compress, AGoQ accumulate)")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
     ap.add_argument("--replicas", action="store_true",
@@ -987,6 +1028,7 @@ def main():
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_gemm:
         extra["gemm_compress_gpt6.7b_down_proj_8192x4096x4096"] = gemm_leg(torch, api, pool)
+        extra["agoq_gemm_accumulate_gpt6.7b_dw_4096x4096x8192"] = agoq_gemm_leg(torch, api)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_agoq:
         extra["agoq"] = agoq_leg(torch, api, peak)

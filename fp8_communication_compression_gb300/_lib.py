@@ -40,6 +40,7 @@ SIGNATURES = {
     "agoq_laaq_dequantize": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _I32, _P]),
     "taco_e4m3_encode": (ctypes.c_int, [_P, _I64, _P, _P]),
     "taco_gemm_compress": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P, _P]),
+    "agoq_gemm_accumulate": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
     "taco_host_pipeline_create": (ctypes.c_int, [_I32, _I64, _I64, _I32, _I32, _I32,
                                                  ctypes.POINTER(ctypes.c_void_p),
                                                  ctypes.POINTER(ctypes.c_uint64)]),

@@ -306,6 +306,29 @@ def taco_gemm_compress(a: torch.Tensor, b: torch.Tensor, block: int = 128, e_tar
     return codes, alpha, scale
 
 
+def agoq_gemm_accumulate(a: torch.Tensor, b: torch.Tensor, main_codes: torch.Tensor, main_scale: torch.Tensor,
+                         block: int = 128, y_out: torch.Tensor | None = None, stream=None):
+    """In place: main <- requantise(dequantise(main) + a @ b.T), the GEMM
+    (a bf16 [M, K], b bf16 [N, K]) on the tensor cores and the FP8
+    accumulation in its epilogue.  main_codes uint8 [M, N], main_scale fp32
+    [M * N / 128].  ``y_out`` (fp32 [M, N]), if given, also receives a @ b.T."""
+    _need(a, "a", _BF16)
+    _need(b, "b", _BF16)
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("a must be [M, K] and b [N, K]")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(main_codes, "main_codes", _U8, M * N)
+    _need(main_scale, "main_scale", (torch.float32,), M * N // block if block else 0)
+    if y_out is not None:
+        _need(y_out, "y_out", (torch.float32,), M * N)
+    st = _lib.load().agoq_gemm_accumulate(a.data_ptr(), b.data_ptr(), M, N, K, block, main_codes.data_ptr(),
+                                          main_scale.data_ptr(), y_out.data_ptr() if y_out is not None else None,
+                                          _stream_handle(stream))
+    _lib.check("agoq_gemm_accumulate", st)
+    return main_codes, main_scale
+
+
 def taco_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))

@@ -36,6 +36,7 @@
 #include "codec_math.cuh"
 #include "device_utils.cuh"
 #include "internal.h"
+#include "reduce_math.cuh"
 #include "tcgen05.cuh"
 
 namespace taco {
@@ -46,19 +47,26 @@ __device__ unsigned int g_gemm_error;
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kGStages = 4;
-constexpr int kGThreads = 192;                       // warps: 0 producer, 1 MMA, 2-5 epilogue
-constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr uint32_t kGStageBytes = kABytes + kBBytes; // 48 KB
-constexpr uint32_t kAccCols = kBN;                   // fp32 accumulator, one column per tile column
-constexpr uint32_t kTmemCols = 2 * kAccCols;         // two accumulators
-constexpr uint32_t kStageOut = 4 * 2 * 4096;         // epilogue staging: 4 warps x 2 blocks x 32 rows x 128 B
-constexpr uint32_t kBars = 8 * (2 * kGStages + 4);   // full / empty per stage, full / empty per accumulator
-constexpr uint32_t kGemmSmem = 1024 + kGStages * kGStageBytes + kStageOut + kBars + 16;
+constexpr int kBM = 128, kBK = 64;
+constexpr int kGThreads = 192;                  // warps: 0 producer, 1 MMA, 2-5 epilogue
+constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kErrGemm = 32u;
-static_assert(kGStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-static_assert(kGemmSmem <= 232448, "shared memory per CTA");
+
+// Tile width BN (256, or 128 where 256-wide tiles would leave more SMs idle
+// in the last round): stage and tensor-memory sizes follow from it.
+template <int BN> struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr uint32_t kBBytes = BN * kBK * 2;            // 32 or 16 KB
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;    // 48 or 32 KB
+    static constexpr uint32_t kAccCols = BN;                      // fp32 accumulator, a column per tile column
+    static constexpr uint32_t kTmemCols = 2 * BN;                 // two accumulators
+    static constexpr int kBlocks = BN / 128;                      // compression blocks per tile row
+    static constexpr uint32_t kStageOut = 4 * kBlocks * 4096;     // staging: 4 warps x blocks x 32 rows x 128 B
+    static constexpr uint32_t kBars = 8 * (2 * kStages + 4);      // full / empty per stage and per accumulator
+    static constexpr uint32_t kSmem = 1024 + kStages * kStageBytes + kStageOut + kBars + 16;
+    static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {
@@ -133,20 +141,73 @@ __device__ __forceinline__ void compress_block_from_tmem(uint32_t taddr, float *
     }
 }
 
-__global__ void __launch_bounds__(kGThreads, 1)
-    gemm_compress_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
-                         const __grid_constant__ CUtensorMap c_map, float *__restrict__ alpha_out,
-                         float *__restrict__ scale_out, float *__restrict__ y_out, int64_t N, int K, int ntiles,
-                         float e_target, float eps)
+// AGoQ 2.B local accumulation of one 128-element block of the thread's row
+// into the FP8 main gradient: g = decode(code) * m_old + y (FP32: one
+// rounded multiply, then one rounded add), then the block is requantised
+// (m_new = max|g| / 448, codes E4M3(g * 448 / max|g|)).  `old` holds the
+// block's 128 current codes; the new codes go to the staging row at `orow`
+// (swizzled).  y_row (optional) gets the raw accumulator values.
+__device__ __forceinline__ void agoq_block_from_tmem(uint32_t taddr, float *y_row, const uint8_t *old, float m_old,
+                                                     uint32_t orow, uint32_t swz, float &m_new)
 {
+    float2 g[64];
+    const float2 m2 = make_float2(m_old, m_old);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+        uint4 q;
+        asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                     : "l"(old + 16 * h));
+        decode16_f2(q, g + 8 * h);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            g[8 * h + i] = mul2_rounded(g[8 * h + i], m2);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x[32];
+        tmem_load_32(taddr + 32 * j, x);
+        if (y_row) {
+            float4 *yo = reinterpret_cast<float4 *>(y_row + 32 * j);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                yo[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            g[16 * j + t] = add2_rounded(g[16 * j + t], make_float2(x[2 * t], x[2 * t + 1]));
+    }
+    float q;
+    agoq_scales(lane_max_abs<64>(g), q, m_new);
+    uint4 oq[8];
+    encode_codes<64>(g, q, oq);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), oq[j].x, oq[j].y, oq[j].z, oq[j].w);
+}
+
+// AGOQ selects the epilogue: false, the TACO compressor (codes, alpha and s
+// out); true, the AGoQ accumulation into the FP8 main gradient (codes and
+// the multipliers in `scale_out` read and rewritten in place; alpha_out
+// unused).
+template <int BN, bool AGOQ>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_epilogue_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
+                         const __grid_constant__ CUtensorMap c_map, const uint8_t *__restrict__ old_codes,
+                         float *__restrict__ alpha_out, float *__restrict__ scale_out, float *__restrict__ y_out,
+                         int64_t N, int K, int ntiles, float e_target, float eps)
+{
+    using C = GemmCfg<BN>;
+    constexpr int kGStages = C::kStages;
+    constexpr uint32_t kGStageBytes = C::kStageBytes, kAccCols = C::kAccCols, kTmemCols = C::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t stage_out = base + kGStages * kGStageBytes;
-    const uint32_t bars = stage_out + kStageOut;
-    const uint32_t tmem_slot = bars + kBars;
+    const uint32_t bars = stage_out + C::kStageOut;
+    const uint32_t tmem_slot = bars + C::kBars;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = K / kBK;
-    const int ntn = static_cast<int>(N / kBN);  // tiles along N
+    const int ntn = static_cast<int>(N / BN);  // tiles along N
     auto full = [&](int s) { return bars + 8 * s; };
     auto empty = [&](int s) { return bars + 8 * (kGStages + s); };
     auto acc_full = [&](int a) { return bars + 8 * (2 * kGStages + a); };
@@ -182,7 +243,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             int g = 0;  // k-blocks issued so far (all tiles): stage g % S, phase (g / S) & 1
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+                const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * BN;
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int s = g % kGStages;
                     if (!mbar_wait(empty(s), ((g / kGStages) & 1) ^ 1)) {
@@ -201,7 +262,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32<kBM, kBN>();
+            constexpr uint32_t idesc = idesc_bf16_f32<kBM, BN>();
             int g = 0, i = 0;  // k-blocks consumed, tiles done
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++i) {
@@ -234,13 +295,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
         // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
         const int q = warp & 3;
         const int row = 32 * q + lane;
-        const uint32_t outw = stage_out + q * 2 * 4096;  // this warp's two staging tiles
+        const uint32_t outw = stage_out + q * C::kBlocks * 4096;  // this warp's staging tiles
         const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
         const int64_t nblk_row = N / 128;
         int i = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int a = i & 1;
-            const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+            const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * BN;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(a), (i >> 1) & 1))) {
                 if (lane == 0)
                     atomicOr(&g_gemm_error, kErrGemm);
@@ -252,10 +313,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
             __syncwarp();
             const uint32_t tq = tmem + a * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
             float *yrow = y_out ? y_out + (m0 + row) * N + n0 : nullptr;
-            float al0, sc0, al1, sc1;
-            compress_block_from_tmem(tq, yrow, outw + lane * 128, swz, e_target, eps, al0, sc0);
-            compress_block_from_tmem(tq + 128, yrow ? yrow + 128 : nullptr, outw + 4096 + lane * 128, swz, e_target,
-                                     eps, al1, sc1);
+            const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128;
+            float al[C::kBlocks], sc[C::kBlocks];
+#pragma unroll
+            for (int blk = 0; blk < C::kBlocks; ++blk) {
+                float *yb = yrow ? yrow + 128 * blk : nullptr;
+                const uint32_t orow = outw + blk * 4096 + lane * 128;
+                if constexpr (AGOQ)
+                    agoq_block_from_tmem(tq + 128 * blk, yb, old_codes + (m0 + row) * N + n0 + 128 * blk,
+                                         scale_out[bi + blk], orow, swz, sc[blk]);
+                else
+                    compress_block_from_tmem(tq + 128 * blk, yb, orow, swz, e_target, eps, al[blk], sc[blk]);
+            }
             // every tensor-memory read of this accumulator is done: hand it back
             tc_fence_before_sync();
             __syncwarp();
@@ -264,15 +333,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                for (int blk = 0; blk < kBN / 128; ++blk)
+                for (int blk = 0; blk < C::kBlocks; ++blk)
                     tma_store_2d(&c_map, n0 + blk * 128, m0 + 32 * q, outw + blk * 4096);
                 bulk_commit();
             }
-            const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128;
-            alpha_out[bi] = al0;
-            alpha_out[bi + 1] = al1;
-            scale_out[bi] = sc0;
-            scale_out[bi + 1] = sc1;
+#pragma unroll
+            for (int blk = 0; blk < C::kBlocks; ++blk) {
+                if constexpr (!AGOQ)
+                    alpha_out[bi + blk] = al[blk];
+                scale_out[bi + blk] = sc[blk];
+            }
         }
         if (lane == 0)
             bulk_wait_all();
@@ -303,33 +373,72 @@ cudaError_t read_gemm_error(uint32_t *flags, bool clear)
     return e;
 }
 
-cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
-                                 float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
-                                 float *y_out, cudaStream_t stream)
+namespace {
+
+template <int BN, bool AGOQ>
+cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64_t N, int64_t K, float e_target,
+                     float eps, uint8_t *codes, const CUtensorMap &cm, float *alpha, float *scale, float *y_out,
+                     const DeviceInfo &di, cudaStream_t stream)
+{
+    using C = GemmCfg<BN>;
+    CUtensorMap bm;
+    if (encode_tensor_map_2d(&bm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(b_bf16), K, N, K * 2, kBK,
+                             BN) != 0)
+        return cudaErrorInvalidValue;
+    static std::atomic<bool> set[kMaxDevices];
+    if (!set[di.device].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_epilogue_kernel<BN, AGOQ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+        if (e != cudaSuccess)
+            return e;
+        set[di.device].store(true, std::memory_order_release);
+    }
+    const int64_t ntiles = (M / kBM) * (N / BN);
+    const int grid = static_cast<int>(ntiles < di.num_sms ? ntiles : di.num_sms);
+    return launch_pdl(gemm_epilogue_kernel<BN, AGOQ>, grid, kGThreads, C::kSmem, stream, am, bm, cm,
+                      static_cast<const uint8_t *>(codes), alpha, scale, y_out, N, static_cast<int>(K),
+                      static_cast<int>(ntiles), e_target, eps);
+}
+
+// 256-wide tiles whenever N allows, 128-wide otherwise.  With a one-CTA MMA
+// a 128-wide tile does half the arithmetic per byte of A it reads from shared
+// memory: measured on the GPT-6.7B shapes, 128-wide tiles took 226 us where
+// 256-wide ones took 152 us (down-projection, 8192 x 4096 x 4096) and 181 us
+// (weight gradient, 4096 x 4096 x 8192), though the latter's 1024 narrow
+// tiles fill the last round of SMs better than its 512 wide ones.
+template <bool AGOQ>
+cudaError_t launch_gemm_epilogue(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                 float e_target, float eps, uint8_t *codes, float *alpha, float *scale, float *y_out,
+                                 cudaStream_t stream)
 {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
     if (e != cudaSuccess)
         return e;
-    CUtensorMap am, bm, cm;
+    CUtensorMap am, cm;
     if (encode_tensor_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(a_bf16), K, M, K * 2, kBK,
                              kBM) != 0 ||
-        encode_tensor_map_2d(&bm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(b_bf16), K, N, K * 2, kBK,
-                             kBN) != 0 ||
         encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, N, M, N, 128, 32) != 0)
         return cudaErrorInvalidValue;
-    static std::atomic<bool> set[kMaxDevices];
-    if (!set[di.device].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(gemm_compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kGemmSmem));
-        if (e != cudaSuccess)
-            return e;
-        set[di.device].store(true, std::memory_order_release);
-    }
-    const int64_t ntiles = (M / kBM) * (N / kBN);
-    const int grid = static_cast<int>(ntiles < di.num_sms ? ntiles : di.num_sms);
-    return launch_pdl(gemm_compress_kernel, grid, kGThreads, kGemmSmem, stream, am, bm, cm, alpha, scale, y_out, N,
-                      static_cast<int>(K), static_cast<int>(ntiles), e_target, eps);
+    if (N % 256 == 0)
+        return run_gemm<256, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, di, stream);
+    return run_gemm<128, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, di, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                 float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
+                                 float *y_out, cudaStream_t stream)
+{
+    return launch_gemm_epilogue<false>(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out, stream);
+}
+
+cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                        uint8_t *main_codes, float *main_scale, float *y_out, cudaStream_t stream)
+{
+    return launch_gemm_epilogue<true>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, main_codes, nullptr, main_scale, y_out,
+                                      stream);
 }
 
 }  // namespace taco

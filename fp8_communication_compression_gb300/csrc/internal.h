@@ -68,10 +68,14 @@ cudaError_t host_pipeline_run(HostPipeline *p, const void *x_host, void *out_hos
 
 // Tensor-core GEMM Y = A B^T (bf16, fp32 accumulate) with the ASH + DS
 // compressor in its epilogue (gemm_compress.cu): M % 128 == 0,
-// N % 256 == 0, K % 64 == 0, block 128.  y_out (fp32 [M][N]) may be null.
+// N % 128 == 0, K % 64 == 0, block 128.  y_out (fp32 [M][N]) may be null.
 cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
                                  float *y_out, cudaStream_t stream);
+// The same GEMM with the AGoQ accumulation into an FP8 main gradient
+// ([M][N] codes and [M][N / 128] multipliers, in place) in its epilogue.
+cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                        uint8_t *main_codes, float *main_scale, float *y_out, cudaStream_t stream);
 
 cudaError_t launch_watchdog_selftest(cudaStream_t stream);
 cudaError_t read_codec_error(uint32_t *flags, bool clear);

@@ -34,20 +34,6 @@ namespace {
 
 constexpr int kBlockThreads = 256;
 
-// AGoQ per-block requantisation scalars from the block's absolute maximum:
-// codes use q = 448 / amax; the stored scale is the dequantisation
-// multiplier m = amax / 448 (both 1 for an all-zero block).
-__device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
-{
-    if (amax > 0.0f) {
-        q = fminf(448.0f / amax, FLT_MAX);
-        m = amax / 448.0f;
-    } else {
-        q = 1.0f;
-        m = 1.0f;
-    }
-}
-
 // Elements per lane of the two reduces: 32 (two 16-byte code words per
 // shard) for up to four shards, 16 (one word) above that, where the P words
 // in flight per slot would otherwise cost occupancy.  The block statistics

@@ -1,5 +1,5 @@
 // Lane-level arithmetic of the shard reductions, shared by the shard-reduce
-// kernels and the AGoQ accumulate kernel.  A lane owns 16 or 32 consecutive
+// kernels, the AGoQ accumulate kernel and the AGoQ epilogue of the GEMM.  A lane owns 16 or 32 consecutive
 // elements of a block (one or two 16-byte code words per shard), kept as
 // NF = 8 or 16 float2 registers; the block statistics are bit-identical in
 // either layout.  The
@@ -206,6 +206,20 @@ __device__ __forceinline__ void recompress(float2 (&T)[NF], float e_target, floa
         k = scale;
     }
     encode_codes<NF>(T, k, codes);
+}
+
+// AGoQ per-block requantisation scalars from the block's absolute maximum:
+// codes use q = 448 / amax; the stored scale is the dequantisation
+// multiplier m = amax / 448 (both 1 for an all-zero block).
+__device__ __forceinline__ void agoq_scales(float amax, float &q, float &m)
+{
+    if (amax > 0.0f) {
+        q = fminf(448.0f / amax, FLT_MAX);
+        m = amax / 448.0f;
+    } else {
+        q = 1.0f;
+        m = 1.0f;
+    }
 }
 
 // 1 / (s alpha) of shard p's block, the weight of its decoded codes in the

@@ -263,7 +263,7 @@ taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_str
  *
  *  a_bf16   in   bf16 [M][K] (the layer input), 16-byte aligned
  *  b_bf16   in   bf16 [N][K] (the weight as [out][in]), 16-byte aligned
- *  M, N, K       M % 128 == 0, N % 256 == 0, K % 64 == 0, K > 0,
+ *  M, N, K       M % 128 == 0, N % 128 == 0, K % 64 == 0, K > 0,
  *                M / 128 <= 65535; other shapes return TACO_ERR_UNSUPPORTED
  *  block         128 (others return TACO_ERR_UNSUPPORTED)
  *  e_target, eps as for taco_compress
@@ -276,6 +276,34 @@ taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_str
 taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                int32_t block, float e_target, float eps, uint8_t *codes, float *alpha,
                                float *scale, float *y_out, taco_stream_t stream);
+
+/*
+ * agoq_gemm_accumulate - the GEMM that produces a weight gradient, with the
+ * FP8 accumulation into the main gradient fused into its epilogue ([AGoQ]
+ * 2.C: quantisation fused into the adjacent GEMM kernel; 2.B: the main
+ * gradient is kept in FP8 and each micro-batch's gradient is added by
+ * dequantising, adding in FP32 and requantising).  G = A B^T is accumulated
+ * in fp32 on the tensor cores (bf16 operands), and for each 128-element block
+ * of each row of G, in place:
+ *     g = decode(main_codes) * main_scale + G       (FP32: one rounded
+ *                                                    multiply, one rounded add)
+ *     main_scale = max|g| / 448 (1 for an all-zero block),
+ *     main_codes = E4M3(g * (448 / max|g|))
+ * -- agoq_fp8_accumulate's arithmetic, with the fp32 GEMM result in place of
+ * the bf16 gradient.  For a weight gradient dW = dY^T X, pass A = dY^T and
+ * B = X^T, both K-major (K = the tokens).
+ *
+ *  a_bf16      in      bf16 [M][K], 16-byte aligned
+ *  b_bf16      in      bf16 [N][K], 16-byte aligned
+ *  M, N, K, block      as for taco_gemm_compress
+ *  main_codes  in/out  uint8 [M][N] (E4M3; all zero with main_scale 1 is
+ *                      the zero gradient)
+ *  main_scale  in/out  fp32 [M][N / 128], dequantisation multipliers
+ *  y_out       out     optional fp32 [M][N]: G as accumulated (NULL: not written)
+ */
+taco_status agoq_gemm_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                 int32_t block, uint8_t *main_codes, float *main_scale, float *y_out,
+                                 taco_stream_t stream);
 
 /*
  * Host pipeline: the two-shot local path between HOST buffers, overlapped.
@@ -374,7 +402,7 @@ taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
  * (bit 0: compressor, bit 1: decompressor, bit 4: taco_watchdog_selftest,
- * bit 5: taco_gemm_compress).
+ * bit 5: taco_gemm_compress and agoq_gemm_accumulate).
  * Synchronises the device.  With clear != 0 the flags are reset to 0 after
  * reading.
  */

@@ -198,7 +198,7 @@ def test_gemm_compress_validation(lib):
     # shapes the tile grid does not cover, and block sizes other than 128
     assert gemm_compress(lib, block=256) == UNSUPPORTED
     assert gemm_compress(lib, M=100) == UNSUPPORTED
-    assert gemm_compress(lib, N=384) == UNSUPPORTED
+    assert gemm_compress(lib, N=320) == UNSUPPORTED
     assert gemm_compress(lib, K=96) == UNSUPPORTED
     assert gemm_compress(lib, M=128 * 65536) == UNSUPPORTED
     assert gemm_compress(lib, M=-1) == INVALID
@@ -216,3 +216,17 @@ def test_gemm_compress_validation(lib):
     assert gemm_compress(lib, codes=A) == INVALID
     assert gemm_compress(lib, alpha=A * 128 + 16) == INVALID
     assert gemm_compress(lib, y=A * 64) == INVALID
+
+
+def test_agoq_gemm_accumulate_validation(lib):
+    f = lambda **k: lib.agoq_gemm_accumulate(k.get("a", A), k.get("b", A * 64), k.get("M", 256), k.get("N", 512),
+                                             k.get("K", 128), k.get("block", 128), k.get("codes", A * 128),
+                                             k.get("scale", A * 200), k.get("y", None), None)
+    assert f(block=256) == UNSUPPORTED
+    assert f(M=100) == UNSUPPORTED and f(N=192) == UNSUPPORTED and f(K=32) == UNSUPPORTED
+    assert f(M=-1) == INVALID
+    assert f(M=0) == OK
+    assert f(codes=None) == INVALID and f(scale=None) == INVALID
+    assert f(codes=A * 128 + 8) == MISALIGNED
+    assert f(scale=A * 128 + 64) == INVALID  # multipliers inside the codes
+    assert f(y=A * 64) == INVALID            # output over an operand
