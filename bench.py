@@ -624,6 +624,7 @@ def gemm_leg(torch, api, pool=None) -> dict:
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     fused = lambda: api.taco_gemm_compress(a, b, codes=codes, alpha=alpha, scale=scale)
+    fused_ns = lambda: api.taco_gemm_compress(a, b, codes=codes, alpha=alpha, scale=scale, split_tail=False)
     gemm = lambda: torch.matmul(a, b.t(), out=y)
     comp = lambda: api.taco_compress(y, 128, codes=codes, alpha=alpha, scale=scale)
 
@@ -631,17 +632,20 @@ def gemm_leg(torch, api, pool=None) -> dict:
         gemm()
         comp()
 
-    for fn in (fused, unfused):
+    for fn in (fused, fused_ns, unfused):
         fn()
-    ms = {"fused": time_launches(torch, fused, 10, stream), "cublas_gemm": time_launches(torch, gemm, 10, stream),
+    ms = {"fused": time_launches(torch, fused, 10, stream),
+          "fused_no_split_tail": time_launches(torch, fused_ns, 10, stream),
+          "cublas_gemm": time_launches(torch, gemm, 10, stream),
           "compress": time_launches(torch, comp, 10, stream), "unfused": time_launches(torch, unfused, 10, stream)}
     flops = 2.0 * M * N * K
     peak, src = bf16_peak()
     out = {k: {"us_per_launch": v * 1e3, "tflops": flops / (v / 1e3) / 1e12 if k != "compress" else None}
            for k, v in ms.items()}
-    for k in ("fused", "cublas_gemm", "unfused"):
+    for k in ("fused", "fused_no_split_tail", "cublas_gemm", "unfused"):
         out[k]["frac_of_bf16_peak"] = out[k]["tflops"] / peak
     out["shape"] = {"M": M, "N": N, "K": K, "block": 128}
+    out["split_tail_workspace_bytes"] = api.gemm_workspace_bytes(M, N, K)
     out["bf16_peak_tflops"] = peak
     out["bf16_peak_source"] = src
     out["fused_vs_unfused_speedup"] = ms["unfused"] / ms["fused"]
@@ -667,6 +671,7 @@ def agoq_gemm_leg(torch, api) -> dict:
     g = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     fused = lambda: api.agoq_gemm_accumulate(a, b, codes, scale)
+    fused_ns = lambda: api.agoq_gemm_accumulate(a, b, codes, scale, split_tail=False)
     gemm = lambda: torch.matmul(a, b.t(), out=g)
     acc = lambda: api.agoq_fp8_accumulate(codes.view(-1), scale, g.view(-1))
 
@@ -674,17 +679,20 @@ def agoq_gemm_leg(torch, api) -> dict:
         gemm()
         acc()
 
-    for fn in (fused, unfused):
+    for fn in (fused, fused_ns, unfused):
         fn()
-    ms = {"fused": time_launches(torch, fused, 10, stream), "cublas_gemm": time_launches(torch, gemm, 10, stream),
+    ms = {"fused": time_launches(torch, fused, 10, stream),
+          "fused_no_split_tail": time_launches(torch, fused_ns, 10, stream),
+          "cublas_gemm": time_launches(torch, gemm, 10, stream),
           "accumulate": time_launches(torch, acc, 10, stream), "unfused": time_launches(torch, unfused, 10, stream)}
     flops = 2.0 * M * N * K
     peak, src = bf16_peak()
     out = {k: {"us_per_launch": v * 1e3, "tflops": flops / (v / 1e3) / 1e12 if k != "accumulate" else None}
            for k, v in ms.items()}
-    for k in ("fused", "cublas_gemm", "unfused"):
+    for k in ("fused", "fused_no_split_tail", "cublas_gemm", "unfused"):
         out[k]["frac_of_bf16_peak"] = out[k]["tflops"] / peak
     out["shape"] = {"M": M, "N": N, "K": K, "block": 128}
+    out["split_tail_workspace_bytes"] = api.gemm_workspace_bytes(M, N, K)
     out["fused_vs_unfused_speedup"] = ms["unfused"] / ms["fused"]
     out["hbm_bytes_saved_per_call"] = 2 * 2 * M * N  # the bf16 gradient written and read back
     return out

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "TACO_OK", 1: "TACO_ERR_INVALID_ARG", 2: "TACO_ERR_UNSUPPORTE
 
 # name -> (restype, argtypes); mirrors include/taco.h
 _P = ctypes.c_void_p
-_I64, _I32, _F32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+_I64, _I32, _F32, _U64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64
 _PP = ctypes.POINTER(ctypes.c_void_p)
 SIGNATURES = {
     "taco_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -39,8 +39,10 @@ SIGNATURES = {
     "agoq_laaq_quantize": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
     "agoq_laaq_dequantize": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _I32, _P]),
     "taco_e4m3_encode": (ctypes.c_int, [_P, _I64, _P, _P]),
-    "taco_gemm_compress": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P, _P]),
-    "agoq_gemm_accumulate": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P]),
+    "taco_gemm_compress": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P, _P, _U64,
+                                          _P]),
+    "agoq_gemm_accumulate": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _U64, _P]),
+    "taco_gemm_workspace_bytes": (ctypes.c_int, [_I64, _I64, _I64, _P]),
     "taco_host_pipeline_create": (ctypes.c_int, [_I32, _I64, _I64, _I32, _I32, _I32,
                                                  ctypes.POINTER(ctypes.c_void_p),
                                                  ctypes.POINTER(ctypes.c_uint64)]),

@@ -275,18 +275,61 @@ def taco_e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=No
     return out
 
 
-def taco_gemm_compress(a: torch.Tensor, b: torch.Tensor, block: int = 128, e_target: float = E_TARGET,
-                       eps: float = EPS, codes: torch.Tensor | None = None, alpha: torch.Tensor | None = None,
-                       scale: torch.Tensor | None = None, y_out: torch.Tensor | None = None, stream=None):
-    """Y = a @ b.T on the tensor cores (a bf16 [M, K], b bf16 [N, K]), leaving
-    the kernel compressed: (codes uint8 [M, N], alpha, scale fp32 [M * N / 128]).
-    ``y_out`` (fp32 [M, N]), if given, also receives the uncompressed Y."""
+_gemm_workspaces: dict = {}
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of workspace the GEMM's split tail takes for an M x N x K
+    product on the current device (0: no split for this shape)."""
+    v = ctypes.c_uint64(0)
+    _lib.check("taco_gemm_workspace_bytes", _lib.load().taco_gemm_workspace_bytes(M, N, K, ctypes.byref(v)))
+    return int(v.value)
+
+
+def _gemm_workspace(device: torch.device, M: int, N: int, K: int, workspace: torch.Tensor | None):
+    """(pointer, bytes) of the split tail's workspace: the caller's, or the
+    one kept per device, grown when a shape needs more.  A new one is zeroed
+    and synchronised, so it cannot be made during a CUDA graph capture (call
+    once outside the capture first).  The kept one is shared by every stream
+    of the device: GEMM calls that may run at the same time on different
+    streams pass their own ``workspace``."""
+    if workspace is not None:
+        _need(workspace, "workspace", _U8)
+        return workspace.data_ptr(), workspace.numel()
+    need = gemm_workspace_bytes(M, N, K)
+    if need == 0:
+        return None, 0
+    ws = _gemm_workspaces.get(device.index)
+    if ws is None or ws.numel() < need:
+        if torch.cuda.is_current_stream_capturing():
+            raise RuntimeError("the GEMM's split-tail workspace must be made outside a CUDA graph capture: "
+                               "call once with this shape before capturing, or pass workspace=")
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize(device)
+        _gemm_workspaces[device.index] = ws
+    return ws.data_ptr(), ws.numel()
+
+
+def _gemm_operands(a, b):
     _need(a, "a", _BF16)
     _need(b, "b", _BF16)
     if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
         raise ValueError("a must be [M, K] and b [N, K]")
-    M, K = a.shape
-    N = b.shape[0]
+    return a.shape[0], b.shape[0], a.shape[1]
+
+
+def taco_gemm_compress(a: torch.Tensor, b: torch.Tensor, block: int = 128, e_target: float = E_TARGET,
+                       eps: float = EPS, codes: torch.Tensor | None = None, alpha: torch.Tensor | None = None,
+                       scale: torch.Tensor | None = None, y_out: torch.Tensor | None = None, stream=None,
+                       split_tail: bool = True, workspace: torch.Tensor | None = None):
+    """Y = a @ b.T on the tensor cores (a bf16 [M, K], b bf16 [N, K]), leaving
+    the kernel compressed: (codes uint8 [M, N], alpha, scale fp32 [M * N / 128]).
+    ``y_out`` (fp32 [M, N]), if given, also receives the uncompressed Y.
+    ``split_tail`` lets the tiles of a partial last round of SMs be split
+    along K, through ``workspace`` (uint8, zeroed before its first use, at
+    least gemm_workspace_bytes(M, N, K) bytes) or, if that is None, a
+    workspace kept per device."""
+    M, N, K = _gemm_operands(a, b)
     nb = M * N // block if block else 0
     if codes is None:
         codes = torch.empty((M, N), dtype=torch.uint8, device=a.device)
@@ -299,32 +342,32 @@ def taco_gemm_compress(a: torch.Tensor, b: torch.Tensor, block: int = 128, e_tar
     _need(scale, "scale", (torch.float32,), nb)
     if y_out is not None:
         _need(y_out, "y_out", (torch.float32,), M * N)
+    ws, ws_bytes = _gemm_workspace(a.device, M, N, K, workspace) if split_tail and M and N else (None, 0)
     st = _lib.load().taco_gemm_compress(a.data_ptr(), b.data_ptr(), M, N, K, block, e_target, eps,
                                         codes.data_ptr(), alpha.data_ptr(), scale.data_ptr(),
-                                        y_out.data_ptr() if y_out is not None else None, _stream_handle(stream))
+                                        y_out.data_ptr() if y_out is not None else None, ws, ws_bytes,
+                                        _stream_handle(stream))
     _lib.check("taco_gemm_compress", st)
     return codes, alpha, scale
 
 
 def agoq_gemm_accumulate(a: torch.Tensor, b: torch.Tensor, main_codes: torch.Tensor, main_scale: torch.Tensor,
-                         block: int = 128, y_out: torch.Tensor | None = None, stream=None):
+                         block: int = 128, y_out: torch.Tensor | None = None, stream=None, split_tail: bool = True,
+                         workspace: torch.Tensor | None = None):
     """In place: main <- requantise(dequantise(main) + a @ b.T), the GEMM
     (a bf16 [M, K], b bf16 [N, K]) on the tensor cores and the FP8
     accumulation in its epilogue.  main_codes uint8 [M, N], main_scale fp32
-    [M * N / 128].  ``y_out`` (fp32 [M, N]), if given, also receives a @ b.T."""
-    _need(a, "a", _BF16)
-    _need(b, "b", _BF16)
-    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
-        raise ValueError("a must be [M, K] and b [N, K]")
-    M, K = a.shape
-    N = b.shape[0]
+    [M * N / 128].  ``y_out`` (fp32 [M, N]), if given, also receives a @ b.T.
+    ``split_tail`` and ``workspace`` as for taco_gemm_compress."""
+    M, N, K = _gemm_operands(a, b)
     _need(main_codes, "main_codes", _U8, M * N)
     _need(main_scale, "main_scale", (torch.float32,), M * N // block if block else 0)
     if y_out is not None:
         _need(y_out, "y_out", (torch.float32,), M * N)
+    ws, ws_bytes = _gemm_workspace(a.device, M, N, K, workspace) if split_tail and M and N else (None, 0)
     st = _lib.load().agoq_gemm_accumulate(a.data_ptr(), b.data_ptr(), M, N, K, block, main_codes.data_ptr(),
                                           main_scale.data_ptr(), y_out.data_ptr() if y_out is not None else None,
-                                          _stream_handle(stream))
+                                          ws, ws_bytes, _stream_handle(stream))
     _lib.check("agoq_gemm_accumulate", st)
     return main_codes, main_scale
 

@@ -80,19 +80,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Compresses one 128-element block of the thread's row from tensor memory
-// (`taddr`: the block's first column, in the warp's lane quarter) into the
-// staging row at `orow` (swizzled), and returns its alpha and s.  y_row
-// (optional) gets the raw accumulator values.
-__device__ __forceinline__ void compress_block_from_tmem(uint32_t taddr, float *y_row, uint32_t orow, uint32_t swz,
-                                                         float e_target, float eps, float &alpha, float &scale)
+// Compresses one 128-element block of the thread's row into the staging row
+// at `orow` (swizzled), and returns its alpha and s.  load32(j, x) gives
+// the block's values 32 j .. 32 j + 31 (from tensor memory, or the summed
+// partials of a split tile).  y_row (optional) gets those values.
+template <class Load>
+__device__ __forceinline__ void compress_block(Load &&load32, float *y_row, uint32_t orow, uint32_t swz,
+                                               float e_target, float eps, float &alpha, float &scale)
 {
     float2 v[64];
     float2 acc[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float x[32];
-        tmem_load_32(taddr + 32 * j, x);
+        load32(j, x);
         if (y_row) {
             float4 *yo = reinterpret_cast<float4 *>(y_row + 32 * j);
 #pragma unroll
@@ -146,9 +147,10 @@ __device__ __forceinline__ void compress_block_from_tmem(uint32_t taddr, float *
 // rounded multiply, then one rounded add), then the block is requantised
 // (m_new = max|g| / 448, codes E4M3(g * 448 / max|g|)).  `old` holds the
 // block's 128 current codes; the new codes go to the staging row at `orow`
-// (swizzled).  y_row (optional) gets the raw accumulator values.
-__device__ __forceinline__ void agoq_block_from_tmem(uint32_t taddr, float *y_row, const uint8_t *old, float m_old,
-                                                     uint32_t orow, uint32_t swz, float &m_new)
+// (swizzled).  load32 and y_row as for compress_block.
+template <class Load>
+__device__ __forceinline__ void agoq_block(Load &&load32, float *y_row, const uint8_t *old, float m_old, uint32_t orow,
+                                           uint32_t swz, float &m_new)
 {
     float2 g[64];
     const float2 m2 = make_float2(m_old, m_old);
@@ -166,7 +168,7 @@ __device__ __forceinline__ void agoq_block_from_tmem(uint32_t taddr, float *y_ro
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float x[32];
-        tmem_load_32(taddr + 32 * j, x);
+        load32(j, x);
         if (y_row) {
             float4 *yo = reinterpret_cast<float4 *>(y_row + 32 * j);
 #pragma unroll
@@ -186,16 +188,114 @@ __device__ __forceinline__ void agoq_block_from_tmem(uint32_t taddr, float *y_ro
         sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), oq[j].x, oq[j].y, oq[j].z, oq[j].w);
 }
 
+// The last piece's warp of a split tile: for its row, the sum over the
+// pieces p = 0 .. S-1 of the partials, added in that order, its own piece
+// (`own`) taken from the accumulator at `tq` and the others from the
+// workspace (`parts`: piece 0's [column / 4][row][4] array, offset to the
+// row); the sum goes back into the accumulator.  CH chunks of 32 columns
+// at a time, the other pieces' loads for them all issued before the first
+// add (the loop is bound by the latency of L2).
+template <int S, int BN, int CH>
+__device__ __forceinline__ void sum_pieces(const float4 *parts, int own, uint32_t tq)
+{
+#pragma unroll 1
+    for (int j0 = 0; j0 < BN / 32; j0 += CH) {
+        float4 o[S - 1][CH][8];
+#pragma unroll
+        for (int p = 0; p < S - 1; ++p) {
+            const float4 *src = parts + static_cast<int64_t>(p < own ? p : p + 1) * (kBM * BN / 4) + 8 * j0 * kBM;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    o[p][c][k] = __ldcg(src + (8 * c + k) * kBM);
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            float x[32];
+            tmem_load_32(tq + 32 * (j0 + c), x);
+            float acc[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                // piece 0
+                const float4 v0 = own == 0 ? make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]) : o[0][c][k];
+                acc[4 * k] = v0.x;
+                acc[4 * k + 1] = v0.y;
+                acc[4 * k + 2] = v0.z;
+                acc[4 * k + 3] = v0.w;
+            }
+#pragma unroll
+            for (int p = 1; p < S; ++p) {
+                const int lo = p < S - 1 ? p : S - 2;  // (a constant once unrolled)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    // piece p is o[p] below the own piece, o[p - 1] above it
+                    const float4 v = p == own ? make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3])
+                                              : (p < own ? o[lo][c][k] : o[p - 1][c][k]);
+                    acc[4 * k] = __fadd_rn(acc[4 * k], v.x);
+                    acc[4 * k + 1] = __fadd_rn(acc[4 * k + 1], v.y);
+                    acc[4 * k + 2] = __fadd_rn(acc[4 * k + 2], v.z);
+                    acc[4 * k + 3] = __fadd_rn(acc[4 * k + 3], v.w);
+                }
+            }
+            tmem_store_32(tq + 32 * (j0 + c), acc);
+        }
+    }
+}
+
+// The CTA's work: item i is global index blockIdx.x + i * gridDim.x.  The
+// first `full_tiles` indices are whole tiles; the rest are pieces of the
+// remaining tiles, each split along K into `split` pieces of equal length
+// (the split tail: it spreads the partial last round of tiles over every
+// SM).  Returns false past the end.
+struct WorkItem {
+    int m0, n0, kb0, kb1;
+    int tail;  // the split tile's index among the tail tiles, or -1 for a whole tile
+    int part;
+};
+
+__device__ __forceinline__ bool work_item(int idx, int full_tiles, int ntiles, int split, int ntn, int BN, int KB,
+                                          WorkItem &w)
+{
+    int t;
+    if (idx < full_tiles) {
+        t = idx;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.tail = -1;
+        w.part = 0;
+    } else {
+        const int u = idx - full_tiles;
+        if (u >= (ntiles - full_tiles) * split)
+            return false;
+        w.tail = u / split;
+        w.part = u - w.tail * split;
+        t = full_tiles + w.tail;
+        const int per = KB / split;
+        w.kb0 = w.part * per;
+        w.kb1 = w.kb0 + per;
+    }
+    w.m0 = (t / ntn) * kBM;
+    w.n0 = (t % ntn) * BN;
+    return true;
+}
+
 // AGOQ selects the epilogue: false, the TACO compressor (codes, alpha and s
 // out); true, the AGoQ accumulation into the FP8 main gradient (codes and
 // the multipliers in `scale_out` read and rewritten in place; alpha_out
-// unused).
+// unused).  Split-tail pieces write their fp32 partial tile to
+// `ws_partial`; for each quarter of a split tile's rows, the epilogue warp
+// that completes the last piece (counted in `ws_count`, 4 counters per tail
+// tile, which it resets to 0) sums the pieces in piece order and runs the
+// epilogue on the sum, so the result does not depend on which piece ends
+// last.  No warp waits for another CTA.
 template <int BN, bool AGOQ>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                          const __grid_constant__ CUtensorMap c_map, const uint8_t *__restrict__ old_codes,
                          float *__restrict__ alpha_out, float *__restrict__ scale_out, float *__restrict__ y_out,
-                         int64_t N, int K, int ntiles, float e_target, float eps)
+                         float *__restrict__ ws_partial, unsigned int *__restrict__ ws_count, int64_t N, int K,
+                         int ntiles, int full_tiles, int split, float e_target, float eps)
 {
     using C = GemmCfg<BN>;
     constexpr int kGStages = C::kStages;
@@ -208,6 +308,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = K / kBK;
     const int ntn = static_cast<int>(N / BN);  // tiles along N
+    const int G = gridDim.x;
     auto full = [&](int s) { return bars + 8 * s; };
     auto empty = [&](int s) { return bars + 8 * (kGStages + s); };
     auto acc_full = [&](int a) { return bars + 8 * (2 * kGStages + a); };
@@ -240,11 +341,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&a_map);
             tma_prefetch_map(&b_map);
-            int g = 0;  // k-blocks issued so far (all tiles): stage g % S, phase (g / S) & 1
+            int g = 0;  // k-blocks issued so far (all items): stage g % S, phase (g / S) & 1
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * BN;
-                for (int kb = 0; kb < KB; ++kb, ++g) {
+            WorkItem w;
+            for (int idx = blockIdx.x; ok && work_item(idx, full_tiles, ntiles, split, ntn, BN, KB, w); idx += G) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % kGStages;
                     if (!mbar_wait(empty(s), ((g / kGStages) & 1) ^ 1)) {
                         atomicOr(&g_gemm_error, kErrGemm);
@@ -252,8 +353,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full(s), kGStageBytes);
-                    tma_load_2d(stage_a(s), &a_map, kb * kBK, m0, full(s));
-                    tma_load_2d(stage_b(s), &b_map, kb * kBK, n0, full(s));
+                    tma_load_2d(stage_a(s), &a_map, kb * kBK, w.m0, full(s));
+                    tma_load_2d(stage_b(s), &b_map, kb * kBK, w.n0, full(s));
                 }
             }
             // leave no load in flight into this CTA's shared memory
@@ -263,18 +364,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32<kBM, BN>();
-            int g = 0, i = 0;  // k-blocks consumed, tiles done
+            int g = 0, i = 0;  // k-blocks consumed, items done
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++i) {
+            WorkItem w;
+            for (int idx = blockIdx.x; ok && work_item(idx, full_tiles, ntiles, split, ntn, BN, KB, w);
+                 idx += G, ++i) {
                 const int a = i & 1;
-                // the epilogue has emptied this accumulator (tile i - 2)
+                // the epilogue has emptied this accumulator (item i - 2)
                 if (!mbar_wait(acc_empty(a), ((i >> 1) & 1) ^ 1)) {
                     atomicOr(&g_gemm_error, kErrGemm);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d = tmem + a * kAccCols;
-                for (int kb = 0; kb < KB; ++kb, ++g) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
                     const int s = g % kGStages;
                     if (!mbar_wait(full(s), (g / kGStages) & 1)) {
                         atomicOr(&g_gemm_error, kErrGemm);
@@ -285,7 +388,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const uint64_t ad = smem_desc_k_sw128(stage_a(s)), bd = smem_desc_k_sw128(stage_b(s));
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes = 2 descriptor units
-                        mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb > w.kb0) || k != 0);
                     mma_commit(empty(s));  // the stage is free once these MMAs have read it
                 }
                 mma_commit(acc_full(a));  // the accumulator is complete once every MMA has
@@ -299,19 +402,63 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const uint32_t swz = static_cast<uint32_t>(lane & 7) << 4;
         const int64_t nblk_row = N / 128;
         int i = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        WorkItem w;
+        for (int idx = blockIdx.x; work_item(idx, full_tiles, ntiles, split, ntn, BN, KB, w); idx += G, ++i) {
             const int a = i & 1;
-            const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * BN;
+            const int m0 = w.m0, n0 = w.n0;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(a), (i >> 1) & 1))) {
                 if (lane == 0)
                     atomicOr(&g_gemm_error, kErrGemm);
                 break;
             }
             tc_fence_after_sync();
+            const uint32_t tq = tmem + a * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
+            if (w.tail >= 0) {
+                // a piece of a split tile: this warp's 32 rows of fp32
+                // partials to the workspace, laid out [column / 4][row][4]
+                // so that a warp's 16-byte stores form one 512-byte run
+                float4 *part = reinterpret_cast<float4 *>(ws_partial) +
+                               (static_cast<int64_t>(w.tail) * split + w.part) * (kBM * BN / 4) + row;
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j) {
+                    float x[32];
+                    tmem_load_32(tq + 32 * j, x);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        __stcg(part + (8 * j + k) * kBM, make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]));
+                }
+                // count this warp's rows in; the warp that brings the count
+                // of rows 32 q .. 32 q + 31 to `split` finishes them
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0) {
+                    unsigned int *cnt = ws_count + 4 * w.tail + q;
+                    last = atomicAdd(cnt, 1u) == static_cast<unsigned int>(split - 1);
+                    if (last)
+                        *cnt = 0;  // ready for the next call
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(acc_empty(a));
+                    continue;
+                }
+                __threadfence();
+                // the sum of the pieces, in piece order, into this
+                // accumulator (which holds this CTA's own piece)
+                const float4 *parts = reinterpret_cast<const float4 *>(ws_partial) +
+                                      static_cast<int64_t>(w.tail) * split * (kBM * BN / 4) + row;
+                switch (split) {
+                case 2: sum_pieces<2, BN, 2>(parts, w.part, tq); break;
+                case 3: sum_pieces<3, BN, 1>(parts, w.part, tq); break;
+                default: sum_pieces<4, BN, 1>(parts, w.part, tq); break;
+                }
+            }
             if (lane == 0)
                 bulk_wait_read_all();  // the previous tile's stores have read the staging tiles
             __syncwarp();
-            const uint32_t tq = tmem + a * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
             float *yrow = y_out ? y_out + (m0 + row) * N + n0 : nullptr;
             const int64_t bi = static_cast<int64_t>(m0 + row) * nblk_row + n0 / 128;
             float al[C::kBlocks], sc[C::kBlocks];
@@ -319,11 +466,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int blk = 0; blk < C::kBlocks; ++blk) {
                 float *yb = yrow ? yrow + 128 * blk : nullptr;
                 const uint32_t orow = outw + blk * 4096 + lane * 128;
+                const uint32_t tb = tq + 128 * blk;
+                auto load32 = [&](int j, float (&x)[32]) { tmem_load_32(tb + 32 * j, x); };
                 if constexpr (AGOQ)
-                    agoq_block_from_tmem(tq + 128 * blk, yb, old_codes + (m0 + row) * N + n0 + 128 * blk,
-                                         scale_out[bi + blk], orow, swz, sc[blk]);
+                    agoq_block(load32, yb, old_codes + (m0 + row) * N + n0 + 128 * blk, scale_out[bi + blk], orow,
+                               swz, sc[blk]);
                 else
-                    compress_block_from_tmem(tq + 128 * blk, yb, orow, swz, e_target, eps, al[blk], sc[blk]);
+                    compress_block(load32, yb, orow, swz, e_target, eps, al[blk], sc[blk]);
             }
             // every tensor-memory read of this accumulator is done: hand it back
             tc_fence_before_sync();
@@ -375,10 +524,68 @@ cudaError_t read_gemm_error(uint32_t *flags, bool clear)
 
 namespace {
 
+// The split tail.  A persistent grid of G CTAs (one per SM) takes the
+// tiles in rounds of G; when the tile count T is not a multiple of G, the
+// last round leaves SMs idle.  Instead, the rem = T mod G tiles of that round
+// (all T tiles when T < G) are each cut along K into S pieces, and the
+// rem * S pieces are dealt out like tiles; a piece costs 1/S of a tile, so
+// the tail costs ceil(rem S / G) / S rounds instead of one.  S is the
+// smallest of 1..4 dividing the k-block count that brings the tail's cost
+// down the most, and a split is taken only if it saves at least 1/8 of a
+// round (the pieces' partial sums go through L2), if each piece spans at
+// least kMinPieceKB k-blocks, and if the workspace holds it.  The piece
+// length bound keeps the MMAs ahead of the epilogue warps: a piece's MMAs
+// must outlast the epilogue of the item before it (a tile's compression,
+// or a piece's partial store and, for the last piece, the sum and the
+// compression), else the MMA warp waits for a free accumulator.  Measured
+// on the GPT-6.7B down-projection (8192 x 4096 x 4096, 1024 tiles): the
+// split of its last 112 tiles into pieces of 16 k-blocks took 175-179 us
+// against 150-157 us unsplit, the tensor pipe active 77 % of the time
+// against 84 %; the weight gradient (4096 x 4096 x 8192, 512 tiles), split
+// into pieces of 64 k-blocks, went from 181-185 us to 168-173 us.
+constexpr int kMinPieceKB = 32;
+struct TailPlan {
+    int grid = 0, full_tiles = 0, split = 1, tail_tiles = 0;
+    uint64_t ws_bytes = 0;  // workspace the split needs (0: no split)
+};
+
+// The workspace starts with the arrival counters, 4 per tail tile, at a
+// place and of a size that do not depend on the shape (fewer tail tiles than
+// SMs): every call leaves the counters it used at zero, and no call writes
+// partial sums over them, so one workspace serves calls of any shape.
+uint64_t count_bytes(int sms) { return (16 * static_cast<uint64_t>(sms) + 255) & ~uint64_t(255); }
+
+TailPlan plan_tail(int64_t ntiles, int64_t KB, int BN, int sms, uint64_t ws_avail)
+{
+    TailPlan p;
+    const int64_t rem = ntiles >= sms ? ntiles % sms : ntiles;
+    double best = rem > 0 ? 1.0 : 0.0;
+    for (int S = 2; S <= 4; ++S) {
+        if (KB % S != 0 || KB / S < kMinPieceKB)
+            continue;
+        const double cost = static_cast<double>((rem * S + sms - 1) / sms) / S;
+        const uint64_t ws = count_bytes(sms) + static_cast<uint64_t>(rem) * S * kBM * BN * 4;
+        if (cost <= best - 0.125) {
+            best = cost;
+            p.split = S;
+            p.ws_bytes = ws;
+        }
+    }
+    if (p.ws_bytes > ws_avail) {  // no room for the best split: none
+        p.split = 1;
+        p.ws_bytes = 0;
+    }
+    p.tail_tiles = p.split > 1 ? static_cast<int>(rem) : 0;
+    p.full_tiles = static_cast<int>(ntiles - p.tail_tiles);
+    const int64_t units = p.full_tiles + static_cast<int64_t>(p.tail_tiles) * p.split;
+    p.grid = static_cast<int>(units < sms ? units : sms);
+    return p;
+}
+
 template <int BN, bool AGOQ>
 cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64_t N, int64_t K, float e_target,
                      float eps, uint8_t *codes, const CUtensorMap &cm, float *alpha, float *scale, float *y_out,
-                     const DeviceInfo &di, cudaStream_t stream)
+                     void *workspace, uint64_t workspace_bytes, const DeviceInfo &di, cudaStream_t stream)
 {
     using C = GemmCfg<BN>;
     CUtensorMap bm;
@@ -394,10 +601,13 @@ cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64
         set[di.device].store(true, std::memory_order_release);
     }
     const int64_t ntiles = (M / kBM) * (N / BN);
-    const int grid = static_cast<int>(ntiles < di.num_sms ? ntiles : di.num_sms);
-    return launch_pdl(gemm_epilogue_kernel<BN, AGOQ>, grid, kGThreads, C::kSmem, stream, am, bm, cm,
-                      static_cast<const uint8_t *>(codes), alpha, scale, y_out, N, static_cast<int>(K),
-                      static_cast<int>(ntiles), e_target, eps);
+    const TailPlan p = plan_tail(ntiles, K / kBK, BN, di.num_sms, workspace ? workspace_bytes : 0);
+    unsigned int *count = p.split > 1 ? static_cast<unsigned int *>(workspace) : nullptr;
+    float *partial =
+        p.split > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + count_bytes(di.num_sms)) : nullptr;
+    return launch_pdl(gemm_epilogue_kernel<BN, AGOQ>, p.grid, kGThreads, C::kSmem, stream, am, bm, cm,
+                      static_cast<const uint8_t *>(codes), alpha, scale, y_out, partial, count, N,
+                      static_cast<int>(K), static_cast<int>(ntiles), p.full_tiles, p.split, e_target, eps);
 }
 
 // 256-wide tiles whenever N allows, 128-wide otherwise.  With a one-CTA MMA
@@ -406,10 +616,12 @@ cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64
 // 256-wide ones took 152 us (down-projection, 8192 x 4096 x 4096) and 181 us
 // (weight gradient, 4096 x 4096 x 8192), though the latter's 1024 narrow
 // tiles fill the last round of SMs better than its 512 wide ones.
+int tile_width(int64_t N) { return N % 256 == 0 ? 256 : 128; }
+
 template <bool AGOQ>
 cudaError_t launch_gemm_epilogue(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale, float *y_out,
-                                 cudaStream_t stream)
+                                 void *workspace, uint64_t workspace_bytes, cudaStream_t stream)
 {
     DeviceInfo di;
     cudaError_t e = current_device_info(&di);
@@ -420,25 +632,40 @@ cudaError_t launch_gemm_epilogue(const void *a_bf16, const void *b_bf16, int64_t
                              kBM) != 0 ||
         encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, N, M, N, 128, 32) != 0)
         return cudaErrorInvalidValue;
-    if (N % 256 == 0)
-        return run_gemm<256, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, di, stream);
-    return run_gemm<128, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, di, stream);
+    if (tile_width(N) == 256)
+        return run_gemm<256, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
+                                   workspace_bytes, di, stream);
+    return run_gemm<128, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
+                               workspace_bytes, di, stream);
 }
 
 }  // namespace
 
+cudaError_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, uint64_t *bytes)
+{
+    DeviceInfo di;
+    cudaError_t e = current_device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    const int BN = tile_width(N);
+    *bytes = plan_tail((M / kBM) * (N / BN), K / kBK, BN, di.num_sms, ~uint64_t(0)).ws_bytes;
+    return cudaSuccess;
+}
+
 cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
-                                 float *y_out, cudaStream_t stream)
+                                 float *y_out, void *workspace, uint64_t workspace_bytes, cudaStream_t stream)
 {
-    return launch_gemm_epilogue<false>(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out, stream);
+    return launch_gemm_epilogue<false>(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out, workspace,
+                                       workspace_bytes, stream);
 }
 
 cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
-                                        uint8_t *main_codes, float *main_scale, float *y_out, cudaStream_t stream)
+                                        uint8_t *main_codes, float *main_scale, float *y_out, void *workspace,
+                                        uint64_t workspace_bytes, cudaStream_t stream)
 {
     return launch_gemm_epilogue<true>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, main_codes, nullptr, main_scale, y_out,
-                                      stream);
+                                      workspace, workspace_bytes, stream);
 }
 
 }  // namespace taco

@@ -69,13 +69,19 @@ cudaError_t host_pipeline_run(HostPipeline *p, const void *x_host, void *out_hos
 // Tensor-core GEMM Y = A B^T (bf16, fp32 accumulate) with the ASH + DS
 // compressor in its epilogue (gemm_compress.cu): M % 128 == 0,
 // N % 128 == 0, K % 64 == 0, block 128.  y_out (fp32 [M][N]) may be null.
+// workspace (workspace_bytes, 256-byte aligned, zeroed before its first
+// use) holds the split tail's partial sums; null or too small: no split.
 cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
-                                 float *y_out, cudaStream_t stream);
+                                 float *y_out, void *workspace, uint64_t workspace_bytes, cudaStream_t stream);
 // The same GEMM with the AGoQ accumulation into an FP8 main gradient
 // ([M][N] codes and [M][N / 128] multipliers, in place) in its epilogue.
 cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
-                                        uint8_t *main_codes, float *main_scale, float *y_out, cudaStream_t stream);
+                                        uint8_t *main_codes, float *main_scale, float *y_out, void *workspace,
+                                        uint64_t workspace_bytes, cudaStream_t stream);
+// Workspace the split tail of an M x N x K GEMM takes on the current device
+// (0 when it takes none).
+cudaError_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, uint64_t *bytes);
 
 cudaError_t launch_watchdog_selftest(cudaStream_t stream);
 cudaError_t read_codec_error(uint32_t *flags, bool clear);

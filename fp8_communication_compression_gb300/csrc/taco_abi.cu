@@ -361,11 +361,20 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// The GEMM shapes the tensor-core kernel takes (M, N > 0).
+static bool gemm_shape_supported(int64_t M, int64_t N, int64_t K)
+{
+    return K > 0 && M % 128 == 0 && N % 128 == 0 && K % 64 == 0 && M / 128 <= 65535 && N <= (int64_t(1) << 30) &&
+           K <= (int64_t(1) << 30) && (M / 128) * (N / 128) <= (int64_t(1) << 30);
+}
+
 // Shared checks of the two GEMM entry points.  alpha may be null (the AGoQ
-// epilogue has none); y_out may be null.
-static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K, int32_t block,
-                            const uint8_t *codes, const float *alpha, bool need_alpha, const float *scale,
-                            const float *y_out)
+// epilogue has none); y_out may be null; a null workspace or one of 0 bytes
+// is none.
+static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                   int32_t block, const uint8_t *codes, const float *alpha, bool need_alpha,
+                                   const float *scale, const float *y_out, const void *workspace,
+                                   uint64_t workspace_bytes)
 {
     if (M < 0 || N < 0 || K < 0)
         return TACO_ERR_INVALID_ARG;
@@ -373,21 +382,21 @@ static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64
         return TACO_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return TACO_OK;
-    if (K == 0 || M % 128 != 0 || N % 128 != 0 || K % 64 != 0 || M / 128 > 65535 || N > (int64_t(1) << 30) ||
-        K > (int64_t(1) << 30))
+    if (!gemm_shape_supported(M, N, K))
         return TACO_ERR_UNSUPPORTED;
     if (!a_bf16 || !b_bf16 || !codes || (need_alpha && !alpha) || !scale)
         return TACO_ERR_INVALID_ARG;
+    const bool ws = workspace && workspace_bytes > 0;
     if (!aligned(a_bf16, 16) || !aligned(b_bf16, 16) || !aligned(codes, 16) || (alpha && !aligned(alpha, 4)) ||
-        !aligned(scale, 4) || (y_out && !aligned(y_out, 16)))
+        !aligned(scale, 4) || (y_out && !aligned(y_out, 16)) || (ws && !aligned(workspace, 256)))
         return TACO_ERR_MISALIGNED;
     const uint64_t mn = static_cast<uint64_t>(M) * N, nb = mn / 128;
-    const void *outs[4] = {codes, alpha, scale, y_out};
-    const uint64_t olen[4] = {mn, alpha ? 4 * nb : 0, 4 * nb, y_out ? 4 * mn : 0};
+    const void *outs[5] = {codes, alpha, scale, y_out, ws ? workspace : nullptr};
+    const uint64_t olen[5] = {mn, alpha ? 4 * nb : 0, 4 * nb, y_out ? 4 * mn : 0, ws ? workspace_bytes : 0};
     const void *ins[2] = {a_bf16, b_bf16};
     const uint64_t ilen[2] = {2 * static_cast<uint64_t>(M) * K, 2 * static_cast<uint64_t>(N) * K};
-    for (int i = 0; i < 4; ++i) {
-        for (int j = i + 1; j < 4; ++j)
+    for (int i = 0; i < 5; ++i) {
+        for (int j = i + 1; j < 5; ++j)
             if (overlap(outs[i], olen[i], outs[j], olen[j]))
                 return TACO_ERR_INVALID_ARG;
         for (int j = 0; j < 2; ++j)
@@ -397,27 +406,43 @@ static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64
     return TACO_OK;
 }
 
+taco_status taco_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, uint64_t *bytes)
+{
+    if (!bytes || M < 0 || N < 0 || K < 0)
+        return TACO_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (M == 0 || N == 0)
+        return TACO_OK;
+    if (!gemm_shape_supported(M, N, K))
+        return TACO_ERR_UNSUPPORTED;
+    return from_cuda(taco::gemm_workspace_bytes(M, N, K, bytes));
+}
+
 taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                int32_t block, float e_target, float eps, uint8_t *codes, float *alpha,
-                               float *scale, float *y_out, taco_stream_t stream)
+                               float *scale, float *y_out, void *workspace, uint64_t workspace_bytes,
+                               taco_stream_t stream)
 {
     if (!positive_finite(e_target) || !positive_finite(eps))
         return TACO_ERR_INVALID_ARG;
-    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, codes, alpha, true, scale, y_out);
+    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, codes, alpha, true, scale, y_out, workspace,
+                                     workspace_bytes);
     if (st != TACO_OK || M == 0 || N == 0)
         return st;
     return from_cuda(taco::launch_gemm_compress(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+                                                workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 taco_status agoq_gemm_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  int32_t block, uint8_t *main_codes, float *main_scale, float *y_out,
-                                 taco_stream_t stream)
+                                 void *workspace, uint64_t workspace_bytes, taco_stream_t stream)
 {
-    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, main_codes, nullptr, false, main_scale, y_out);
+    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, main_codes, nullptr, false, main_scale, y_out,
+                                     workspace, workspace_bytes);
     if (st != TACO_OK || M == 0 || N == 0)
         return st;
     return from_cuda(taco::launch_gemm_agoq_accumulate(a_bf16, b_bf16, M, N, K, main_codes, main_scale, y_out,
+                                                       workspace, workspace_bytes,
                                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 

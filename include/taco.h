@@ -272,10 +272,26 @@ taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_str
  *  scale    out  fp32 [M][N / 128]
  *  y_out    out  optional fp32 [M][N]: the uncompressed Y, as accumulated
  *                (NULL: not written)
+ *  workspace     optional device scratch for the split tail (below), 256-byte
+ *                aligned, not overlapping any other argument, all zero before
+ *                its first use; of workspace_bytes bytes.  NULL, 0 bytes or
+ *                fewer than taco_gemm_workspace_bytes() gives: no split.
+ *
+ * Split tail: the kernel runs one CTA per SM over 128 x 256 tiles of Y (128
+ * x 128 when N % 256 != 0).  When the tiles do not fill whole rounds of SMs,
+ * the tiles of the last, partial round are each cut along K into 2-4
+ * pieces spread over all SMs; the pieces' fp32 partial sums meet in the
+ * workspace and are added in piece order (so the result is the same on
+ * every run), then compressed.  A call leaves the workspace's counters at
+ * zero again, except after a watchdog error (taco_device_error bit 5),
+ * after which the caller zeroes it before reusing it.  One call at a time
+ * per workspace: calls on different streams need their own.  The split
+ * changes the order of the fp32 additions of Y, not the bound on its error.
  */
 taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                int32_t block, float e_target, float eps, uint8_t *codes, float *alpha,
-                               float *scale, float *y_out, taco_stream_t stream);
+                               float *scale, float *y_out, void *workspace, uint64_t workspace_bytes,
+                               taco_stream_t stream);
 
 /*
  * agoq_gemm_accumulate - the GEMM that produces a weight gradient, with the
@@ -300,10 +316,21 @@ taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M
  *                      the zero gradient)
  *  main_scale  in/out  fp32 [M][N / 128], dequantisation multipliers
  *  y_out       out     optional fp32 [M][N]: G as accumulated (NULL: not written)
+ *  workspace, workspace_bytes  as for taco_gemm_compress (the split tail)
  */
 taco_status agoq_gemm_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  int32_t block, uint8_t *main_codes, float *main_scale, float *y_out,
-                                 taco_stream_t stream);
+                                 void *workspace, uint64_t workspace_bytes, taco_stream_t stream);
+
+/*
+ * taco_gemm_workspace_bytes - the workspace that taco_gemm_compress and
+ * agoq_gemm_accumulate take for their split tail on an M x N x K product on
+ * the current device (it depends on the SM count); 0 when the shape gets no
+ * split.  No counterpart in the pages: a property of this implementation.
+ *
+ *  bytes  out  the size; shapes as for taco_gemm_compress (M or N = 0: 0)
+ */
+taco_status taco_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, uint64_t *bytes);
 
 /*
  * Host pipeline: the two-shot local path between HOST buffers, overlapped.

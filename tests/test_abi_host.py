@@ -190,8 +190,8 @@ def test_host_pipeline_validation(lib):
 
 
 def gemm_compress(lib, a=A, b=A * 64, M=256, N=512, K=128, block=128, e=1.0, eps=1e-12, codes=A * 128,
-                  alpha=A * 192, scale=A * 200, y=None):
-    return lib.taco_gemm_compress(a, b, M, N, K, block, e, eps, codes, alpha, scale, y, None)
+                  alpha=A * 192, scale=A * 200, y=None, ws=None, ws_bytes=0):
+    return lib.taco_gemm_compress(a, b, M, N, K, block, e, eps, codes, alpha, scale, y, ws, ws_bytes, None)
 
 
 def test_gemm_compress_validation(lib):
@@ -216,12 +216,26 @@ def test_gemm_compress_validation(lib):
     assert gemm_compress(lib, codes=A) == INVALID
     assert gemm_compress(lib, alpha=A * 128 + 16) == INVALID
     assert gemm_compress(lib, y=A * 64) == INVALID
+    # the split tail's workspace: 256-byte aligned, apart from every other buffer
+    assert gemm_compress(lib, ws=A * 400 + 128, ws_bytes=1 << 20) == MISALIGNED
+    assert gemm_compress(lib, ws=A * 128 + 256, ws_bytes=1 << 20) == INVALID  # over the codes
+    assert gemm_compress(lib, ws=A * 63, ws_bytes=2 << 20) == INVALID         # over both operands
+
+
+def test_gemm_workspace_bytes_validation(lib):
+    v = ctypes.c_uint64(7)
+    assert lib.taco_gemm_workspace_bytes(256, 512, 128, None) == INVALID
+    assert lib.taco_gemm_workspace_bytes(-1, 512, 128, ctypes.byref(v)) == INVALID
+    assert lib.taco_gemm_workspace_bytes(100, 512, 128, ctypes.byref(v)) == UNSUPPORTED
+    assert lib.taco_gemm_workspace_bytes(256, 512, 96, ctypes.byref(v)) == UNSUPPORTED
+    assert lib.taco_gemm_workspace_bytes(0, 512, 128, ctypes.byref(v)) == OK and v.value == 0
 
 
 def test_agoq_gemm_accumulate_validation(lib):
     f = lambda **k: lib.agoq_gemm_accumulate(k.get("a", A), k.get("b", A * 64), k.get("M", 256), k.get("N", 512),
                                              k.get("K", 128), k.get("block", 128), k.get("codes", A * 128),
-                                             k.get("scale", A * 200), k.get("y", None), None)
+                                             k.get("scale", A * 200), k.get("y", None), k.get("ws", None),
+                                             k.get("ws_bytes", 0), None)
     assert f(block=256) == UNSUPPORTED
     assert f(M=100) == UNSUPPORTED and f(N=192) == UNSUPPORTED and f(K=32) == UNSUPPORTED
     assert f(M=-1) == INVALID
@@ -230,3 +244,5 @@ def test_agoq_gemm_accumulate_validation(lib):
     assert f(codes=A * 128 + 8) == MISALIGNED
     assert f(scale=A * 128 + 64) == INVALID  # multipliers inside the codes
     assert f(y=A * 64) == INVALID            # output over an operand
+    assert f(ws=A * 400 + 16, ws_bytes=4096) == MISALIGNED
+    assert f(ws=A * 200 - 256, ws_bytes=4096) == INVALID  # workspace over the multipliers

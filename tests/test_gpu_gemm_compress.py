@@ -14,7 +14,16 @@ not blur each other:
     more than 1 E4M3 ULP apart, alpha and s within 1e-6 relative), since
     both sides take the code decisions from the same fp32 values.
 The call without the optional output gives the same codes bit for bit.
+
+Shapes whose tiles do not fill whole rounds of SMs, with K long enough for
+pieces of 2048 or more, take the split tail (the last round's tiles cut
+along K, their fp32 partial sums added in piece order through a workspace);
+they are checked with and without it.  The split
+changes the order of Y's fp32 additions, so the two Y differ in the last
+places, each within the bound.
 """
+
+import ctypes
 
 import numpy as np
 import pytest
@@ -22,7 +31,7 @@ import torch
 
 import oracle
 import oracle_pool
-from fp8_communication_compression_gb300 import api
+from fp8_communication_compression_gb300 import _lib, api
 from fp8_communication_compression_gb300 import workloads as W
 
 from parity import assert_codes_match, assert_recon_match, assert_scalars_match, to_dev_bf16, to_host
@@ -45,12 +54,22 @@ def operands(M, N, K, seed):
     return a, b
 
 
-def check_gemm_compress(M, N, K, seed=0):
+def sentinel_outputs(M, N):
+    """Outputs filled with values the kernel never writes (code 0x7F, NaN
+    scalars and Y), so that a block left unwritten fails the checks."""
+    nb = M * N // 128
+    return (torch.full((M, N), 0x7F, dtype=torch.uint8, device="cuda"),
+            torch.full((nb,), float("nan"), device="cuda"), torch.full((nb,), float("nan"), device="cuda"))
+
+
+def check_gemm_compress(M, N, K, seed=0, split_tail=True):
     a, b = operands(M, N, K, seed)
     ad, bd = to_dev_bf16(a), to_dev_bf16(b)
-    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    c, al, sc = api.taco_gemm_compress(ad, bd, y_out=y)
-    c2, al2, sc2 = api.taco_gemm_compress(ad, bd)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    c, al, sc = sentinel_outputs(M, N)
+    c2, al2, sc2 = sentinel_outputs(M, N)
+    api.taco_gemm_compress(ad, bd, codes=c, alpha=al, scale=sc, y_out=y, split_tail=split_tail)
+    api.taco_gemm_compress(ad, bd, codes=c2, alpha=al2, scale=sc2, split_tail=split_tail)
     torch.cuda.synchronize()
     # the optional output changes nothing
     assert torch.equal(c, c2) and torch.equal(al, al2) and torch.equal(sc, sc2)
@@ -88,6 +107,78 @@ def test_gemm_compress_many_tiles_per_sm(M, N, K):
     (256, 512 and 512 tiles), so both tensor-memory accumulators are used and
     reused, and a tile's epilogue runs while the next tile's MMAs do."""
     check_gemm_compress(M, N, K, seed=3)
+
+
+def expected_workspace(M, N, K, sms):
+    """The split-tail rule of taco_gemm_workspace_bytes, restated: the tiles
+    of the partial last round (all tiles when fewer than the SMs) split into
+    the S in 2..4 dividing K / 64, into pieces of at least 32 k-blocks, that
+    lowers ceil(rem S / sms) / S by at least 1/8 of a round the most."""
+    bn = 256 if N % 256 == 0 else 128
+    t, kb = (M // 128) * (N // bn), K // 64
+    rem = t % sms if t >= sms else t
+    best, split = (1.0 if rem else 0.0), 1
+    for s in (2, 3, 4):
+        if kb % s == 0 and kb // s >= 32:
+            cost = -(-rem * s // sms) / s
+            if cost <= best - 0.125:
+                best, split = cost, s
+    if split == 1:
+        return 0
+    return -(-16 * sms // 256) * 256 + rem * split * 128 * bn * 4
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 768, 1024), (128, 256, 4096), (256, 384, 128), (128, 128, 6144),
+                                   (384, 768, 4096), (2048, 4096, 8192), (2048, 4096, 512), (4096, 4096, 128),
+                                   (8192, 4096, 4096), (4096, 4096, 8192), (256, 512, 8192), (384, 640, 4096)])
+def test_gemm_workspace_bytes_follows_the_split_rule(M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert api.gemm_workspace_bytes(M, N, K) == expected_workspace(M, N, K, sms)
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 768, 4096), (128, 128, 6144), (2048, 4096, 8192)])
+def test_gemm_compress_with_and_without_the_split_tail(M, N, K):
+    """Shapes that take a split tail (S = 2, 3 and 4; 9, 1 and 104 tail
+    tiles), computed without it and with it: both pass the same checks."""
+    assert api.gemm_workspace_bytes(M, N, K) > 0
+    check_gemm_compress(M, N, K, seed=4, split_tail=False)
+    check_gemm_compress(M, N, K, seed=4, split_tail=True)
+
+
+def test_gemm_compress_with_a_workspace_too_small_takes_no_split():
+    """A workspace smaller than taco_gemm_workspace_bytes() is not used: the
+    result is the unsplit kernel's, bit for bit."""
+    M, N, K = 384, 768, 4096
+    a, b = operands(M, N, K, 6)
+    ad, bd = to_dev_bf16(a), to_dev_bf16(b)
+    ref = api.taco_gemm_compress(ad, bd, split_tail=False)
+    need = api.gemm_workspace_bytes(M, N, K)
+    ws = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    c, al, sc = sentinel_outputs(M, N)
+    st = _lib.load().taco_gemm_compress(ad.data_ptr(), bd.data_ptr(), M, N, K, 128, api.E_TARGET, api.EPS,
+                                        c.data_ptr(), al.data_ptr(), sc.data_ptr(), None, ws.data_ptr(), need - 256,
+                                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(c, ref[0]) and torch.equal(al, ref[1]) and torch.equal(sc, ref[2])
+    assert bool(torch.all(ws == 0))  # untouched
+
+
+def test_one_workspace_serves_shapes_in_any_order():
+    """Calls of different shapes, one after another on the workspace kept per
+    device, give the same bits as each shape on a fresh zeroed workspace of
+    its own: a call leaves nothing behind that another shape would read."""
+    shapes = [(2048, 4096, 8192), (384, 768, 4096), (128, 128, 6144), (2048, 4096, 8192), (384, 768, 4096)]
+    ops = {s: tuple(to_dev_bf16(x) for x in operands(*s, 11)) for s in set(shapes)}
+    fresh = {}
+    for s in set(shapes):
+        ws = torch.zeros(api.gemm_workspace_bytes(*s), dtype=torch.uint8, device="cuda")
+        fresh[s] = api.taco_gemm_compress(*ops[s], workspace=ws)
+    for s in shapes:
+        c, al, sc = sentinel_outputs(s[0], s[1])
+        api.taco_gemm_compress(*ops[s], codes=c, alpha=al, scale=sc)
+        torch.cuda.synchronize()
+        assert torch.equal(c, fresh[s][0]) and torch.equal(al, fresh[s][1]) and torch.equal(sc, fresh[s][2]), s
 
 
 def test_gemm_compress_zero_rows_give_zero_blocks():
@@ -135,7 +226,7 @@ def grad_operands(M, N, K, seed):
     return a, b
 
 
-def check_agoq_gemm(M, N, K, steps=2, seed=0):
+def check_agoq_gemm(M, N, K, steps=2, seed=0, split_tail=True):
     """agoq_gemm_accumulate over several micro-batches from the zero gradient:
     after every step the main gradient's codes and multipliers equal, bit for
     bit, the oracle's FP32 accumulation of the kernel's own fp32 G (the AGoQ
@@ -149,9 +240,9 @@ def check_agoq_gemm(M, N, K, steps=2, seed=0):
         a, b = grad_operands(M, N, K, seed + 7 * step)
         ad, bd = to_dev_bf16(a), to_dev_bf16(b)
         c2, s2 = codes.clone(), scale.clone()
-        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        api.agoq_gemm_accumulate(ad, bd, codes, scale, y_out=y)
-        api.agoq_gemm_accumulate(ad, bd, c2, s2)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        api.agoq_gemm_accumulate(ad, bd, codes, scale, y_out=y, split_tail=split_tail)
+        api.agoq_gemm_accumulate(ad, bd, c2, s2, split_tail=split_tail)
         torch.cuda.synchronize()
         assert torch.equal(codes, c2) and torch.equal(scale, s2)
         yg = to_host(y)
@@ -166,6 +257,15 @@ def check_agoq_gemm(M, N, K, steps=2, seed=0):
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (2048, 4096, 512), (384, 640, 128)])
 def test_agoq_gemm_accumulate_small_shapes(M, N, K):
     check_agoq_gemm(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 640, 4096), (256, 512, 8192)])
+def test_agoq_gemm_accumulate_with_and_without_the_split_tail(M, N, K):
+    """Shapes that take a split tail (S = 2 with 128-wide tiles, S = 4 with
+    256-wide ones), without it and with it."""
+    assert api.gemm_workspace_bytes(M, N, K) > 0
+    check_agoq_gemm(M, N, K, seed=2, split_tail=False)
+    check_agoq_gemm(M, N, K, seed=2, split_tail=True)
 
 
 def test_agoq_gemm_accumulate_full_size_weight_gradient():
