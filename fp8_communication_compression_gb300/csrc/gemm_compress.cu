@@ -11,8 +11,8 @@
 // compressor.
 //
 // Design (sm_103a):
-//  * A persistent grid, one CTA per SM, walks the 128 x 256 tiles of Y in
-//    turn.  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A and
+//  * A persistent grid, one CTA per SM, walks the 128 x 256 tiles of Y
+//    (128 x 128 where N % 256 != 0) in turn.  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A and
 //    256 x 64 tiles of B (bf16, 128-byte swizzle) through a 4-stage mbarrier
 //    ring, from one output tile into the next without a gap.  Warp 1
 //    allocates 512 columns of tensor memory (two fp32 accumulators of 256
@@ -27,6 +27,11 @@
 //    The 128-point Walsh-Hadamard transform, the block energy, alpha, s and
 //    the E4M3 conversion run in that thread's registers; the codes go
 //    through the warp's swizzled staging rows and TMA stores.
+//  * Split tail: when the tiles do not fill whole rounds of SMs and K is
+//    long enough, the tiles of the last round are cut along K into 2-4
+//    pieces dealt out like tiles; their fp32 partial sums meet in a
+//    caller's workspace and the warp that stores a tile quarter's last
+//    piece adds them up in piece order, then compresses (no spin waits).
 //  * Every mbarrier wait is time-limited; a wait that runs out sets a flag
 //    readable through taco_device_error() and the CTA winds down.
 

@@ -280,7 +280,8 @@ taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_str
  * Split tail: the kernel runs one CTA per SM over 128 x 256 tiles of Y (128
  * x 128 when N % 256 != 0).  When the tiles do not fill whole rounds of SMs,
  * the tiles of the last, partial round are each cut along K into 2-4
- * pieces spread over all SMs; the pieces' fp32 partial sums meet in the
+ * pieces of at least 2048 (if K allows and it saves at least an eighth of
+ * a round) spread over all SMs; the pieces' fp32 partial sums meet in the
  * workspace and are added in piece order (so the result is the same on
  * every run), then compressed.  A call leaves the workspace's counters at
  * zero again, except after a watchdog error (taco_device_error bit 5),
