@@ -276,6 +276,7 @@ def taco_e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=No
 
 
 _gemm_workspaces: dict = {}
+_gemm_workspaces_replaced: list = []  # kept alive: a captured CUDA graph may still use them
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
@@ -290,9 +291,10 @@ def _gemm_workspace(device: torch.device, M: int, N: int, K: int, workspace: tor
     """(pointer, bytes) of the split tail's workspace: the caller's, or the
     one kept per device, grown when a shape needs more.  A new one is zeroed
     and synchronised, so it cannot be made during a CUDA graph capture (call
-    once outside the capture first).  The kept one is shared by every stream
-    of the device: GEMM calls that may run at the same time on different
-    streams pass their own ``workspace``."""
+    once outside the capture first); one it replaces stays allocated, since
+    a captured graph may still use it.  The kept one is shared by every
+    stream of the device: GEMM calls that may run at the same time on
+    different streams pass their own ``workspace``."""
     if workspace is not None:
         _need(workspace, "workspace", _U8)
         return workspace.data_ptr(), workspace.numel()
@@ -304,6 +306,8 @@ def _gemm_workspace(device: torch.device, M: int, N: int, K: int, workspace: tor
         if torch.cuda.is_current_stream_capturing():
             raise RuntimeError("the GEMM's split-tail workspace must be made outside a CUDA graph capture: "
                                "call once with this shape before capturing, or pass workspace=")
+        if ws is not None:
+            _gemm_workspaces_replaced.append(ws)
         ws = torch.zeros(need, dtype=torch.uint8, device=device)
         torch.cuda.synchronize(device)
         _gemm_workspaces[device.index] = ws
