@@ -79,7 +79,12 @@ template <int BITS> __device__ __forceinline__ void store_words(uint8_t *dst, co
 // slots (128 bytes of bf16 per lane) are in flight together.
 constexpr int kQuantSlots = 2;
 
-template <int BITS, int NB>
+// A lane's 32 bf16 values are 64 contiguous bytes, and lane l's follow lane
+// l - 1's.  WIDE (x 32-byte aligned): two 32-byte loads, each filling whole
+// 32-byte sectors (lane l reads sector 2l, then 2l + 1), so every sector is
+// requested once.  Otherwise four 16-byte loads, each of which touches 32
+// sectors half (a sector is requested twice, from L2 the second time).
+template <int BITS, int NB, bool WIDE>
 __global__ void __launch_bounds__(kLThreads)
     laaq_quantize_kernel(const uint16_t *__restrict__ x, int64_t nblocks, uint8_t *__restrict__ packed,
                          float *__restrict__ scale)
@@ -87,6 +92,7 @@ __global__ void __launch_bounds__(kLThreads)
     constexpr int LPB = NB / 32;
     constexpr int U = kQuantSlots;
     constexpr float kQmax = static_cast<float>((1 << (BITS - 1)) - 1);
+    const uint64_t pol = WIDE ? policy_evict_first() : 0;  // the input is read once
     pdl_wait();
     const int64_t total = nblocks * LPB;
     const int lane = threadIdx.x & 31;
@@ -102,9 +108,20 @@ __global__ void __launch_bounds__(kLThreads)
             const int64_t t = base + u * stride + lane;
             valid[u] = t < total;
             off[u] = (valid[u] ? t / LPB : 0) * NB + part * 32;
+            if constexpr (WIDE) {
+                if (valid[u]) {
+                    ldg256_stream_hint(x + off[u], pol, g[u][0], g[u][1]);
+                    ldg256_stream_hint(x + off[u] + 16, pol, g[u][2], g[u][3]);
+                } else {
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
-                g[u][h] = valid[u] ? ldg128_stream(x + off[u] + 8 * h) : make_uint4(0, 0, 0, 0);
+                    for (int h = 0; h < 4; ++h)
+                        g[u][h] = make_uint4(0, 0, 0, 0);
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    g[u][h] = valid[u] ? ldg128_stream(x + off[u] + 8 * h) : make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -307,16 +324,24 @@ template <typename K> cudaError_t laaq_grid(K kernel, int64_t lanes, int *grid)
     return cudaSuccess;
 }
 
-template <int BITS, int NB>
-cudaError_t run_quantize(const void *x, int64_t n, uint8_t *packed, float *scale, cudaStream_t st)
+template <int BITS, int NB, bool WIDE>
+cudaError_t run_quantize_w(const void *x, int64_t n, uint8_t *packed, float *scale, cudaStream_t st)
 {
     int grid = 0;
     const int64_t nb = n / NB;
-    cudaError_t e = laaq_grid(laaq_quantize_kernel<BITS, NB>, nb * (NB / 32), &grid);
+    cudaError_t e = laaq_grid(laaq_quantize_kernel<BITS, NB, WIDE>, nb * (NB / 32), &grid);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(laaq_quantize_kernel<BITS, NB>, grid, kLThreads, 0, st, static_cast<const uint16_t *>(x),
-                      nb, packed, scale);
+    return launch_pdl(laaq_quantize_kernel<BITS, NB, WIDE>, grid, kLThreads, 0, st,
+                      static_cast<const uint16_t *>(x), nb, packed, scale);
+}
+
+template <int BITS, int NB>
+cudaError_t run_quantize(const void *x, int64_t n, uint8_t *packed, float *scale, cudaStream_t st)
+{
+    if (reinterpret_cast<uintptr_t>(x) % 32 == 0)
+        return run_quantize_w<BITS, NB, true>(x, n, packed, scale, st);
+    return run_quantize_w<BITS, NB, false>(x, n, packed, scale, st);
 }
 
 template <int BITS, int NB>

@@ -323,6 +323,23 @@ def test_laaq_codec_is_bit_identical_to_the_oracle(bits, block):
     assert np.array_equal(to_host(out16.view(torch.int16)).view(np.uint16), W.f32_to_bf16_bits(ref))
 
 
+@pytest.mark.parametrize("bits,block", [(4, 128), (5, 64), (6, 32), (8, 256)])
+def test_laaq_quantize_of_an_input_16_but_not_32_byte_aligned(bits, block):
+    """The quantizer takes 32-byte loads when the input is 32-byte aligned
+    and 16-byte loads otherwise: an input 16 bytes past a 32-byte boundary
+    gives the same codes as the oracle too."""
+    n = 40 * 1024 + 256
+    x = W.tp_activation(540 + bits, n // 256, 256, channel_scale=True, zero_blocks=(1,), block=block)
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    xs = buf[8:]
+    assert xs.data_ptr() % 32 == 16
+    xs.copy_(to_dev_bf16(x).reshape(-1))
+    packed, scale = api.agoq_laaq_quantize(xs, block, bits)
+    rp, rs = oracle.laaq_quantize(x, block, bits)
+    assert np.array_equal(to_host(packed), rp)
+    assert np.array_equal(to_host(scale), rs)
+
+
 @pytest.mark.parametrize("bits,block", [(4, 128), (5, 32), (6, 256), (8, 64)])
 def test_laaq_codec_many_slots_per_lane(bits, block):
     """8.4 M elements: more lanes than one grid holds, so each lane takes
