@@ -63,11 +63,12 @@ def _load():
             lib.oracle_decompress_int8.argtypes = [P, P, P, i64, i64, i32, P]
             lib.oracle_laaq_quantize.argtypes = [P, i64, i32, i32, P, P]
             lib.oracle_laaq_dequantize.argtypes = [P, P, i64, i32, i32, P]
+            lib.oracle_laaq_quantize_f32.argtypes = [P, i64, i32, i32, P, P]
             for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
                       "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
                       "oracle_agoq_accumulate_f32",
                       "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8",
-                      "oracle_laaq_quantize", "oracle_laaq_dequantize"):
+                      "oracle_laaq_quantize", "oracle_laaq_dequantize", "oracle_laaq_quantize_f32"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -284,6 +285,22 @@ def laaq_quantize(x_bf16: np.ndarray, block: int = 128, bits: int = 4):
     scale = np.empty(x.size // block, dtype=np.float32)
     _check(_load().oracle_laaq_quantize(_ptr(x), x.size, block, bits, _ptr(packed), _ptr(scale)))
     return packed, scale
+
+
+def laaq_quantize_f32(x_f32: np.ndarray, block: int = 128, bits: int = 4):
+    """The quantisation of fp32 values (the GEMM-fused form, AGoQ 2.C):
+    fp32 [n] -> (packed uint8 [n * bits / 8], scale fp32 [n / block])."""
+    x = np.ascontiguousarray(x_f32, dtype=np.float32).reshape(-1)
+    packed = np.zeros(x.size * bits // 8, dtype=np.uint8)
+    scale = np.empty(x.size // block, dtype=np.float32)
+    _check(_load().oracle_laaq_quantize_f32(_ptr(x), x.size, block, bits, _ptr(packed), _ptr(scale)))
+    return packed, scale
+
+
+def gemm_laaq_quantize(a_bf16: np.ndarray, b_bf16: np.ndarray, block: int = 128, bits: int = 4):
+    """The GEMM with LAAQ quantisation of its output, as two plain steps:
+    Y = A B^T in float64, rounded to fp32, then the fp32 quantisation."""
+    return laaq_quantize_f32(gemm_bt(a_bf16, b_bf16).astype(np.float32), block, bits)
 
 
 def laaq_dequantize(packed: np.ndarray, scale: np.ndarray, n: int, block: int = 128, bits: int = 4):

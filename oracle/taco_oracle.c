@@ -550,40 +550,66 @@ static int32_t get_bits_signed(const uint8_t *stream, int64_t bitpos, int bits)
     return (int32_t)v;
 }
 
+/* One block of fp32 values x[0 .. block) -> its codes at element offset
+ * `first` of the stream, and its multiplier. */
+static void laaq_quantize_block(const float *x, int block, int bits, uint8_t *packed, int64_t first,
+                                float *scale)
+{
+    int i;
+    const float qmax = (float)((1 << (bits - 1)) - 1);
+    float amax = 0.0f, q = 1.0f, m = 1.0f;
+    for (i = 0; i < block; ++i) {
+        const float v = fabsf(x[i]);
+        if (v > amax)
+            amax = v;
+    }
+    if (amax > 0.0f) {
+        q = qmax / amax;
+        if (!(q <= FLT_MAX))
+            q = FLT_MAX;
+        m = amax / qmax;
+    }
+    for (i = 0; i < block; ++i) {
+        const float v = x[i] * q;
+        float r = rintf(v);
+        if (r > qmax)
+            r = qmax;
+        if (r < -qmax)
+            r = -qmax;
+        put_bits(packed, (first + i) * (int64_t)bits, (uint32_t)(int32_t)r & ((1u << bits) - 1u), bits);
+    }
+    *scale = m;
+}
+
 int oracle_laaq_quantize(const uint16_t *x_bf16, int64_t n, int block, int bits, uint8_t *packed,
                          float *scale)
 {
     int64_t nb, k;
     int i;
-    const float qmax = (float)((1 << (bits - 1)) - 1);
+    float x[256];
     if (!laaq_args_ok(n, block, bits))
         return -1;
     nb = n / block;
     for (k = 0; k < nb; ++k) {
-        float amax = 0.0f, q = 1.0f, m = 1.0f;
-        for (i = 0; i < block; ++i) {
-            const float v = fabsf((float)bf16_to_double(x_bf16[k * block + i]));
-            if (v > amax)
-                amax = v;
-        }
-        if (amax > 0.0f) {
-            q = qmax / amax;
-            if (!(q <= FLT_MAX))
-                q = FLT_MAX;
-            m = amax / qmax;
-        }
-        for (i = 0; i < block; ++i) {
-            const float v = (float)bf16_to_double(x_bf16[k * block + i]) * q;
-            float r = rintf(v);
-            if (r > qmax)
-                r = qmax;
-            if (r < -qmax)
-                r = -qmax;
-            put_bits(packed, (k * block + i) * (int64_t)bits, (uint32_t)(int32_t)r & ((1u << bits) - 1u),
-                     bits);
-        }
-        scale[k] = m;
+        for (i = 0; i < block; ++i)
+            x[i] = (float)bf16_to_double(x_bf16[k * block + i]);  /* exact */
+        laaq_quantize_block(x, block, bits, packed, k * block, scale + k);
     }
+    return 0;
+}
+
+/* The same quantisation of fp32 values: the form it takes when it is fused
+ * into the GEMM that produces the activation ([AGoQ] 2.C: quantisation in
+ * the adjacent GEMM kernel), which quantises its fp32 result with no bf16
+ * rounding in between. */
+int oracle_laaq_quantize_f32(const float *x, int64_t n, int block, int bits, uint8_t *packed, float *scale)
+{
+    int64_t nb, k;
+    if (!laaq_args_ok(n, block, bits))
+        return -1;
+    nb = n / block;
+    for (k = 0; k < nb; ++k)
+        laaq_quantize_block(x + k * block, block, bits, packed, k * block, scale + k);
     return 0;
 }
 

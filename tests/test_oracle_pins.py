@@ -675,3 +675,50 @@ def test_agoq_accumulate_f32_first_step_is_absmax_quantisation():
         q = np.float32(448.0) / amax
         want = oracle.e4m3_encode_array((blk * q).astype(np.float32))
         assert np.array_equal(c[128 * b:128 * (b + 1)], want)
+
+
+# ------------------------------- LAAQ quantisation fused into the GEMM --
+# AGoQ 2.C: the activation quantisation runs in the epilogue of the GEMM that
+# produces the activation, on its fp32 result.
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+def test_laaq_quantize_f32_equals_the_bf16_quantize_on_bf16_values(bits):
+    """The fp32-input quantisation runs the same FP32 sequence as the bf16
+    one: on values that are bf16 values it gives the same stream and
+    multipliers."""
+    for block in (32, 128, 256):
+        x = W.tp_activation(60 + bits, 8, 1024, channel_scale=True, zero_blocks=(3,), block=block)
+        p16, s16 = oracle.laaq_quantize(x, block, bits)
+        p32, s32 = oracle.laaq_quantize_f32(W.bf16_bits_to_f32(x), block, bits)
+        assert np.array_equal(p16, p32) and np.array_equal(s16, s32)
+
+
+def test_laaq_quantize_f32_hand_worked_ties_and_non_bf16_values():
+    """One 32-element block at 4 bits with max|x| = 7, so q = 7 / 7 = 1 and
+    the multiplier is 1: the codes are the values rounded to the nearest
+    integer, ties to even.  2.4999998 and 2.5000002 (the fp32 neighbours of
+    2.5, no bf16 value) go to 2 and 3; -3.5 and 4.5 to -4 and 4; -0.5 to 0;
+    1.5 to 2.  Element i takes bits 4i .. 4i + 3 (two's complement), so byte
+    j holds element 2j in its low nibble and 2j + 1 in its high one."""
+    f = lambda bits: np.array([bits], np.uint32).view(np.float32)[0]
+    x = np.zeros(32, np.float32)
+    x[:9] = [7.0, -7.0, f(0x401FFFFF), f(0x40200001), -3.5, 4.5, 0.5, -0.5, 1.5]
+    assert x[2] == np.float32(2.4999998) and x[3] == np.float32(2.5000002)
+    packed, scale = oracle.laaq_quantize_f32(x, 32, 4)
+    # codes 7, -7, 2, 3, -4, 4, 0, 0, 2, 0 ... -> nibbles 7, 9, 2, 3, C, 4, 0, 0, 2, 0 ...
+    assert packed.tolist() == [0x97, 0x32, 0x4C, 0x00, 0x02] + [0] * 11
+    assert scale.tolist() == [1.0]
+
+
+def test_gemm_laaq_quantize_is_quantize_of_the_product():
+    """The fused path's oracle on a case where Y is known in closed form: with
+    A = I in bf16, Y = B^T exactly, so the stream and multipliers equal
+    those of quantising B^T's bf16 values."""
+    n = 128
+    b = W.tp_activation(13, 256, n)           # [N = 256, K = 128]
+    a = np.zeros((n, n), dtype=np.uint16)     # [M = 128, K = 128] identity (1.0 = 0x3F80)
+    a[np.arange(n), np.arange(n)] = 0x3F80
+    for bits in (4, 5, 6, 8):
+        p, s = oracle.gemm_laaq_quantize(a, b, 128, bits)
+        rp, rs = oracle.laaq_quantize(np.ascontiguousarray(b.T), 128, bits)
+        assert np.array_equal(p, rp) and np.array_equal(s, rs)
