@@ -698,6 +698,49 @@ def agoq_gemm_leg(torch, api) -> dict:
     return out
 
 
+def laaq_gemm_leg(torch, api, pool=None, bits: int = 4) -> dict:
+    """The GEMM that produces an activation with AGoQ's 4-bit LAAQ
+    quantisation in its epilogue (agoq_gemm_laaq_quantize): a GPT-6.7B-sized
+    [8192 tokens, 4096] = X W^T with W [4096, 4096], stored as packed codes
+    and a multiplier per 128-element block.  Timed from graph replays beside
+    the path it replaces: cuBLAS (torch.matmul, bf16 out) then
+    agoq_laaq_quantize."""
+    from fp8_communication_compression_gb300 import workloads as W
+
+    M, N, K = 8192, 4096, 4096
+    a_bits = pool.submit(_tp_shard, (902, M, K, True, False, 128)).result() if pool else \
+        _tp_shard((902, M, K, True, False, 128))
+    b_bits = W.f32_to_bf16_bits(np.random.default_rng(903).normal(0.0, 0.02, (N, K)).astype(np.float32))
+    a = torch.from_numpy(a_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    b = torch.from_numpy(b_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    packed = torch.empty(M * N * bits // 8, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(M * N // 128, dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    fused = lambda: api.agoq_gemm_laaq_quantize(a, b, bits, packed=packed, scale=scale)
+    gemm = lambda: torch.matmul(a, b.t(), out=y)
+    quant = lambda: api.agoq_laaq_quantize(y.view(-1), 128, bits, packed, scale)
+
+    def unfused():
+        gemm()
+        quant()
+
+    for fn in (fused, unfused):
+        fn()
+    ms = {"fused": time_launches(torch, fused, 10, stream), "cublas_gemm": time_launches(torch, gemm, 10, stream),
+          "quantize": time_launches(torch, quant, 10, stream), "unfused": time_launches(torch, unfused, 10, stream)}
+    flops = 2.0 * M * N * K
+    peak, _ = bf16_peak()
+    out = {k: {"us_per_launch": v * 1e3, "tflops": flops / (v / 1e3) / 1e12 if k != "quantize" else None}
+           for k, v in ms.items()}
+    for k in ("fused", "cublas_gemm", "unfused"):
+        out[k]["frac_of_bf16_peak"] = out[k]["tflops"] / peak
+    out["shape"] = {"M": M, "N": N, "K": K, "block": 128, "bits": bits}
+    out["fused_vs_unfused_speedup"] = ms["unfused"] / ms["fused"]
+    out["hbm_bytes_saved_per_call"] = 2 * 2 * M * N  # the bf16 activation written and read back
+    return out
+
+
 def gpt13b_leg(torch, api, peak: float, pool=None) -> dict:
     """The GPT-13B-shaped path (8 shards of [8192, 5120], n=256): per-launch
     device times (graph replays) of compress, reduce + decompress in one call,
@@ -1037,6 +1080,7 @@ def main():
     if rank == 0 and not args.no_gemm:
         extra["gemm_compress_gpt6.7b_down_proj_8192x4096x4096"] = gemm_leg(torch, api, pool)
         extra["agoq_gemm_accumulate_gpt6.7b_dw_4096x4096x8192"] = agoq_gemm_leg(torch, api)
+        extra["laaq_gemm_quantize_4bit_gpt6.7b_8192x4096x4096"] = laaq_gemm_leg(torch, api, pool)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_agoq:
         extra["agoq"] = agoq_leg(torch, api, peak)

@@ -42,6 +42,7 @@ SIGNATURES = {
     "taco_gemm_compress": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P, _P, _U64,
                                           _P]),
     "agoq_gemm_accumulate": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _U64, _P]),
+    "agoq_gemm_laaq_quantize": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _U64, _P]),
     "taco_gemm_workspace_bytes": (ctypes.c_int, [_I64, _I64, _I64, _P]),
     "taco_host_pipeline_create": (ctypes.c_int, [_I32, _I64, _I64, _I32, _I32, _I32,
                                                  ctypes.POINTER(ctypes.c_void_p),

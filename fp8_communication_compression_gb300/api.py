@@ -376,6 +376,33 @@ def agoq_gemm_accumulate(a: torch.Tensor, b: torch.Tensor, main_codes: torch.Ten
     return main_codes, main_scale
 
 
+def agoq_gemm_laaq_quantize(a: torch.Tensor, b: torch.Tensor, bits: int = 4, block: int = 128,
+                            packed: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                            y_out: torch.Tensor | None = None, stream=None, split_tail: bool = True,
+                            workspace: torch.Tensor | None = None):
+    """Y = a @ b.T on the tensor cores (a bf16 [M, K], b bf16 [N, K]),
+    leaving the kernel as LAAQ codes: (packed uint8 [M * N * bits / 8],
+    scale fp32 [M * N / 128]), readable by agoq_laaq_dequantize.  ``y_out``
+    (fp32 [M, N]), if given, also receives Y; ``split_tail`` and
+    ``workspace`` as for taco_gemm_compress."""
+    M, N, K = _gemm_operands(a, b)
+    nb = M * N // block if block else 0
+    if packed is None:
+        packed = torch.empty(M * N * bits // 8, dtype=torch.uint8, device=a.device)
+    if scale is None:
+        scale = torch.empty(nb, dtype=torch.float32, device=a.device)
+    _need(packed, "packed", _U8, M * N * bits // 8)
+    _need(scale, "scale", (torch.float32,), nb)
+    if y_out is not None:
+        _need(y_out, "y_out", (torch.float32,), M * N)
+    ws, ws_bytes = _gemm_workspace(a.device, M, N, K, workspace) if split_tail and M and N else (None, 0)
+    st = _lib.load().agoq_gemm_laaq_quantize(a.data_ptr(), b.data_ptr(), M, N, K, block, bits, packed.data_ptr(),
+                                             scale.data_ptr(), y_out.data_ptr() if y_out is not None else None,
+                                             ws, ws_bytes, _stream_handle(stream))
+    _lib.check("agoq_gemm_laaq_quantize", st)
+    return packed, scale
+
+
 def taco_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _lib.check("taco_device_error", _lib.load().taco_device_error(ctypes.byref(v), int(clear)))

@@ -450,7 +450,7 @@ cudaError_t ensure_smem(K kernel, uint32_t bytes, int device, std::atomic<bool> 
 
 int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t inner,
                          uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
-                         uint32_t box_rows)
+                         uint32_t box_rows, CUtensorMapSwizzle swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -459,9 +459,8 @@ int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : -2;
 }
 

@@ -41,6 +41,7 @@
 #include "codec_math.cuh"
 #include "device_utils.cuh"
 #include "internal.h"
+#include "laaq_math.cuh"
 #include "reduce_math.cuh"
 #include "tcgen05.cuh"
 
@@ -193,6 +194,71 @@ __device__ __forceinline__ void agoq_block(Load &&load32, float *y_row, const ui
         sts128(orow + ((static_cast<uint32_t>(j) << 4) ^ swz), oq[j].x, oq[j].y, oq[j].z, oq[j].w);
 }
 
+// The epilogues.  kEpiCompress: the TACO compressor (codes, alpha and s
+// out).  kEpiAgoq: the AGoQ accumulation into the FP8 main gradient (codes
+// and the multipliers in `scale_out` read and rewritten in place).  4, 5, 6
+// or 8: AGoQ's LAAQ activation quantisation at that many bits (packed codes
+// and multipliers out).
+constexpr int kEpiCompress = 0, kEpiAgoq = 1;
+__host__ __device__ constexpr bool epi_is_laaq(int epi) { return epi >= 4; }
+// Bytes of one 128-element block's output in a row of the staging tile.
+__host__ __device__ constexpr int epi_block_bytes(int epi) { return epi_is_laaq(epi) ? 16 * epi : 128; }
+
+// AGoQ 2.A quantisation (the GEMM-fused form of 2.C) of one 128-element
+// block of the thread's row: amax = max|y|, q = qmax / amax, codes
+// rint(y q) (the clamp to +-qmax never binds), m = amax / qmax, all in fp32
+// as the stand-alone quantizer computes them.  The 128 codes, BITS bits
+// each in a little-endian stream, go to the staging row at `orow` (16 BITS
+// bytes, unswizzled); load32 and y_row as for compress_block.
+template <int BITS, class Load>
+__device__ __forceinline__ void laaq_block(Load &&load32, float *y_row, uint32_t orow, float &m)
+{
+    float v[128];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x[32];
+        load32(j, x);
+        if (y_row) {
+            float4 *yo = reinterpret_cast<float4 *>(y_row + 32 * j);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                yo[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[32 * j + i] = x[i];
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+    }
+    float q;
+    laaq_factors<BITS>(amax, q, m);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t c[32], w[BITS];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            c[i] = __float_as_uint(__fadd_rn(__fmul_rn(v[32 * j + i], q), kRoundMagic));
+        pack32<BITS>(c, w);
+        // 32 codes = BITS words at byte 4 BITS j of the row: 16-byte aligned
+        // at 4 and 8 bits, 8-byte at 6, 4-byte at 5
+        const uint32_t at = orow + 4 * BITS * j;
+        if constexpr (BITS % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < BITS; k += 4)
+                sts128(at + 4 * k, w[k], w[k + 1], w[k + 2], w[k + 3]);
+        } else if constexpr (BITS % 2 == 0) {
+#pragma unroll
+            for (int k = 0; k < BITS; k += 2)
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(at + 4 * k), "r"(w[k]), "r"(w[k + 1]) : "memory");
+        } else {
+#pragma unroll
+            for (int k = 0; k < BITS; ++k)
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(at + 4 * k), "r"(w[k]) : "memory");
+        }
+    }
+}
+
 // The last piece's warp of a split tile: for its row, the sum over the
 // pieces p = 0 .. S-1 of the partials, added in that order, its own piece
 // (`own`) taken from the accumulator at `tq` and the others from the
@@ -285,16 +351,16 @@ __device__ __forceinline__ bool work_item(int idx, int full_tiles, int ntiles, i
     return true;
 }
 
-// AGOQ selects the epilogue: false, the TACO compressor (codes, alpha and s
-// out); true, the AGoQ accumulation into the FP8 main gradient (codes and
-// the multipliers in `scale_out` read and rewritten in place; alpha_out
-// unused).  Split-tail pieces write their fp32 partial tile to
+// EPI selects the epilogue (kEpiCompress, kEpiAgoq, or LAAQ bits; alpha_out
+// is written by the compressor only, old_codes read by the AGoQ
+// accumulation only; c_map is the codes' or packed codes' tensor map).
+// Split-tail pieces write their fp32 partial tile to
 // `ws_partial`; for each quarter of a split tile's rows, the epilogue warp
 // that completes the last piece (counted in `ws_count`, 4 counters per tail
 // tile, which it resets to 0) sums the pieces in piece order and runs the
 // epilogue on the sum, so the result does not depend on which piece ends
 // last.  No warp waits for another CTA.
-template <int BN, bool AGOQ>
+template <int BN, int EPI>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                          const __grid_constant__ CUtensorMap c_map, const uint8_t *__restrict__ old_codes,
@@ -470,14 +536,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
             for (int blk = 0; blk < C::kBlocks; ++blk) {
                 float *yb = yrow ? yrow + 128 * blk : nullptr;
-                const uint32_t orow = outw + blk * 4096 + lane * 128;
+                const uint32_t orow = outw + blk * 4096 + lane * epi_block_bytes(EPI);
                 const uint32_t tb = tq + 128 * blk;
                 auto load32 = [&](int j, float (&x)[32]) { tmem_load_32(tb + 32 * j, x); };
-                if constexpr (AGOQ)
+                if constexpr (EPI == kEpiAgoq)
                     agoq_block(load32, yb, old_codes + (m0 + row) * N + n0 + 128 * blk, scale_out[bi + blk], orow,
                                swz, sc[blk]);
-                else
+                else if constexpr (EPI == kEpiCompress)
                     compress_block(load32, yb, orow, swz, e_target, eps, al[blk], sc[blk]);
+                else
+                    laaq_block<EPI>(load32, yb, orow, sc[blk]);
             }
             // every tensor-memory read of this accumulator is done: hand it back
             tc_fence_before_sync();
@@ -487,13 +555,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                for (int blk = 0; blk < C::kBlocks; ++blk)
-                    tma_store_2d(&c_map, n0 + blk * 128, m0 + 32 * q, outw + blk * 4096);
+                for (int blk = 0; blk < C::kBlocks; ++blk)  // x in bytes: a multiple of 16
+                    tma_store_2d(&c_map, (n0 + blk * 128) / 128 * epi_block_bytes(EPI), m0 + 32 * q,
+                                 outw + blk * 4096);
                 bulk_commit();
             }
 #pragma unroll
             for (int blk = 0; blk < C::kBlocks; ++blk) {
-                if constexpr (!AGOQ)
+                if constexpr (EPI == kEpiCompress)
                     alpha_out[bi + blk] = al[blk];
                 scale_out[bi + blk] = sc[blk];
             }
@@ -587,7 +656,7 @@ TailPlan plan_tail(int64_t ntiles, int64_t KB, int BN, int sms, uint64_t ws_avai
     return p;
 }
 
-template <int BN, bool AGOQ>
+template <int BN, int EPI>
 cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64_t N, int64_t K, float e_target,
                      float eps, uint8_t *codes, const CUtensorMap &cm, float *alpha, float *scale, float *y_out,
                      void *workspace, uint64_t workspace_bytes, const DeviceInfo &di, cudaStream_t stream)
@@ -599,7 +668,7 @@ cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64
         return cudaErrorInvalidValue;
     static std::atomic<bool> set[kMaxDevices];
     if (!set[di.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_epilogue_kernel<BN, AGOQ>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_epilogue_kernel<BN, EPI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
         if (e != cudaSuccess)
             return e;
@@ -610,7 +679,7 @@ cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64
     unsigned int *count = p.split > 1 ? static_cast<unsigned int *>(workspace) : nullptr;
     float *partial =
         p.split > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + count_bytes(di.num_sms)) : nullptr;
-    return launch_pdl(gemm_epilogue_kernel<BN, AGOQ>, p.grid, kGThreads, C::kSmem, stream, am, bm, cm,
+    return launch_pdl(gemm_epilogue_kernel<BN, EPI>, p.grid, kGThreads, C::kSmem, stream, am, bm, cm,
                       static_cast<const uint8_t *>(codes), alpha, scale, y_out, partial, count, N,
                       static_cast<int>(K), static_cast<int>(ntiles), p.full_tiles, p.split, e_target, eps);
 }
@@ -623,7 +692,10 @@ cudaError_t run_gemm(const CUtensorMap &am, const void *b_bf16, int64_t M, int64
 // tiles fill the last round of SMs better than its 512 wide ones.
 int tile_width(int64_t N) { return N % 256 == 0 ? 256 : 128; }
 
-template <bool AGOQ>
+// The codes' tensor map: one byte a code ([M][N], 128-byte rows of a
+// block, swizzled like the staging rows), or LAAQ's packed stream ([M][N
+// bits / 8], 16 bits bytes a block, unswizzled staging rows).
+template <int EPI>
 cudaError_t launch_gemm_epilogue(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale, float *y_out,
                                  void *workspace, uint64_t workspace_bytes, cudaStream_t stream)
@@ -633,15 +705,18 @@ cudaError_t launch_gemm_epilogue(const void *a_bf16, const void *b_bf16, int64_t
     if (e != cudaSuccess)
         return e;
     CUtensorMap am, cm;
+    const uint64_t row_bytes = static_cast<uint64_t>(N) / 128 * epi_block_bytes(EPI);
     if (encode_tensor_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(a_bf16), K, M, K * 2, kBK,
                              kBM) != 0 ||
-        encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, N, M, N, 128, 32) != 0)
+        encode_tensor_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, row_bytes, M, row_bytes,
+                             epi_block_bytes(EPI), 32,
+                             epi_is_laaq(EPI) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) != 0)
         return cudaErrorInvalidValue;
     if (tile_width(N) == 256)
-        return run_gemm<256, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
-                                   workspace_bytes, di, stream);
-    return run_gemm<128, AGOQ>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
-                               workspace_bytes, di, stream);
+        return run_gemm<256, EPI>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
+                                  workspace_bytes, di, stream);
+    return run_gemm<128, EPI>(am, b_bf16, M, N, K, e_target, eps, codes, cm, alpha, scale, y_out, workspace,
+                              workspace_bytes, di, stream);
 }
 
 }  // namespace
@@ -661,16 +736,38 @@ cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t
                                  float e_target, float eps, uint8_t *codes, float *alpha, float *scale,
                                  float *y_out, void *workspace, uint64_t workspace_bytes, cudaStream_t stream)
 {
-    return launch_gemm_epilogue<false>(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out, workspace,
-                                       workspace_bytes, stream);
+    return launch_gemm_epilogue<kEpiCompress>(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out,
+                                              workspace, workspace_bytes, stream);
 }
 
 cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                         uint8_t *main_codes, float *main_scale, float *y_out, void *workspace,
                                         uint64_t workspace_bytes, cudaStream_t stream)
 {
-    return launch_gemm_epilogue<true>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, main_codes, nullptr, main_scale, y_out,
-                                      workspace, workspace_bytes, stream);
+    return launch_gemm_epilogue<kEpiAgoq>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, main_codes, nullptr, main_scale,
+                                          y_out, workspace, workspace_bytes, stream);
+}
+
+cudaError_t launch_gemm_laaq_quantize(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                      int bits, uint8_t *packed, float *scale, float *y_out, void *workspace,
+                                      uint64_t workspace_bytes, cudaStream_t stream)
+{
+    switch (bits) {
+    case 4:
+        return launch_gemm_epilogue<4>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, packed, nullptr, scale, y_out, workspace,
+                                       workspace_bytes, stream);
+    case 5:
+        return launch_gemm_epilogue<5>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, packed, nullptr, scale, y_out, workspace,
+                                       workspace_bytes, stream);
+    case 6:
+        return launch_gemm_epilogue<6>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, packed, nullptr, scale, y_out, workspace,
+                                       workspace_bytes, stream);
+    case 8:
+        return launch_gemm_epilogue<8>(a_bf16, b_bf16, M, N, K, 1.0f, 1.0f, packed, nullptr, scale, y_out, workspace,
+                                       workspace_bytes, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace taco

@@ -15,11 +15,11 @@ struct DeviceInfo {
 };
 cudaError_t current_device_info(DeviceInfo *out);
 
-// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
-// Returns 0 on success.
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point
+// (128-byte swizzle unless asked otherwise).  Returns 0 on success.
 int encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t inner,
                          uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
-                         uint32_t box_rows);
+                         uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // Kernels working on the "128-view" of a TACO tensor: nrows rows of 128
 // elements; a block of n elements spans n / 128 consecutive rows.
@@ -79,6 +79,12 @@ cudaError_t launch_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t
 cudaError_t launch_gemm_agoq_accumulate(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
                                         uint8_t *main_codes, float *main_scale, float *y_out, void *workspace,
                                         uint64_t workspace_bytes, cudaStream_t stream);
+// The same GEMM with AGoQ's LAAQ activation quantisation of its output in
+// its epilogue: blocks of 128 along each row, `bits` (4, 5, 6 or 8) bits a
+// code, packed [M][N * bits / 8] and multipliers [M][N / 128].
+cudaError_t launch_gemm_laaq_quantize(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                      int bits, uint8_t *packed, float *scale, float *y_out, void *workspace,
+                                      uint64_t workspace_bytes, cudaStream_t stream);
 // Workspace the split tail of an M x N x K GEMM takes on the current device
 // (0 when it takes none).
 cudaError_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, uint64_t *bytes);

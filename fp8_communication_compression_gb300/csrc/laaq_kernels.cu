@@ -23,6 +23,7 @@
 
 #include "device_utils.cuh"
 #include "internal.h"
+#include "laaq_math.cuh"
 #include "reduce_math.cuh"
 
 namespace taco {
@@ -30,31 +31,6 @@ namespace taco {
 namespace {
 
 constexpr int kLThreads = 256;
-
-// Rounding to an integer without a conversion instruction: for |v| < 2^22,
-// the float sum v + 1.5 * 2^23 has a unit in the last place of 1, so the
-// addition rounds v to the nearest integer (ties to even), and the low
-// mantissa bits of the sum hold that integer in two's complement (the low 22
-// bits of 1.5 * 2^23 are zero).
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23, bits 0x4B400000
-
-// Packs the low BITS bits of each of 32 words (the rounded sums above) into
-// the lane's BITS-word stream segment.
-template <int BITS> __device__ __forceinline__ void pack32(const uint32_t (&c)[32], uint32_t (&w)[BITS])
-{
-    constexpr uint32_t kMask = (1u << BITS) - 1u;
-#pragma unroll
-    for (int j = 0; j < BITS; ++j)
-        w[j] = 0u;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t u = c[i] & kMask;
-        const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
-        w[wi] |= u << sh;
-        if (sh + BITS > 32)
-            w[wi + 1] |= u >> (32 - sh);
-    }
-}
 
 // The lane's BITS words go to byte offset 4 * BITS * (lane slot): 16-byte
 // aligned for 4 and 8 bits, 8-byte for 6, 4-byte for 5.
@@ -91,7 +67,6 @@ __global__ void __launch_bounds__(kLThreads)
 {
     constexpr int LPB = NB / 32;
     constexpr int U = kQuantSlots;
-    constexpr float kQmax = static_cast<float>((1 << (BITS - 1)) - 1);
     const uint64_t pol = WIDE ? policy_evict_first() : 0;  // the input is read once
     pdl_wait();
     const int64_t total = nblocks * LPB;
@@ -138,11 +113,8 @@ __global__ void __launch_bounds__(kLThreads)
                 }
             }
             const float amax = group_max<LPB>(mx);
-            float q = 1.0f, m = 1.0f;
-            if (amax > 0.0f) {
-                q = fminf(kQmax / amax, FLT_MAX);
-                m = amax / kQmax;
-            }
+            float q, m;
+            laaq_factors<BITS>(amax, q, m);
             // |x q| <= qmax up to one rounding, so the clamp to +-qmax never
             // binds: the nearest integer of qmax (1 + 2^-23) is qmax
             uint32_t c[32];

@@ -368,12 +368,12 @@ static bool gemm_shape_supported(int64_t M, int64_t N, int64_t K)
            K <= (int64_t(1) << 30) && (M / 128) * (N / 128) <= (int64_t(1) << 30);
 }
 
-// Shared checks of the two GEMM entry points.  alpha may be null (the AGoQ
-// epilogue has none); y_out may be null; a null workspace or one of 0 bytes
-// is none.
+// Shared checks of the GEMM entry points.  codes hold code_bits bits per
+// element of Y; alpha may be null (only the compressor has one); y_out may
+// be null; a null workspace or one of 0 bytes is none.
 static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
-                                   int32_t block, const uint8_t *codes, const float *alpha, bool need_alpha,
-                                   const float *scale, const float *y_out, const void *workspace,
+                                   int32_t block, const uint8_t *codes, int code_bits, const float *alpha,
+                                   bool need_alpha, const float *scale, const float *y_out, const void *workspace,
                                    uint64_t workspace_bytes)
 {
     if (M < 0 || N < 0 || K < 0)
@@ -392,7 +392,8 @@ static taco_status check_gemm_args(const void *a_bf16, const void *b_bf16, int64
         return TACO_ERR_MISALIGNED;
     const uint64_t mn = static_cast<uint64_t>(M) * N, nb = mn / 128;
     const void *outs[5] = {codes, alpha, scale, y_out, ws ? workspace : nullptr};
-    const uint64_t olen[5] = {mn, alpha ? 4 * nb : 0, 4 * nb, y_out ? 4 * mn : 0, ws ? workspace_bytes : 0};
+    const uint64_t olen[5] = {mn * code_bits / 8, alpha ? 4 * nb : 0, 4 * nb, y_out ? 4 * mn : 0,
+                              ws ? workspace_bytes : 0};
     const void *ins[2] = {a_bf16, b_bf16};
     const uint64_t ilen[2] = {2 * static_cast<uint64_t>(M) * K, 2 * static_cast<uint64_t>(N) * K};
     for (int i = 0; i < 5; ++i) {
@@ -425,8 +426,8 @@ taco_status taco_gemm_compress(const void *a_bf16, const void *b_bf16, int64_t M
 {
     if (!positive_finite(e_target) || !positive_finite(eps))
         return TACO_ERR_INVALID_ARG;
-    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, codes, alpha, true, scale, y_out, workspace,
-                                     workspace_bytes);
+    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, codes, 8, alpha, true, scale, y_out,
+                                     workspace, workspace_bytes);
     if (st != TACO_OK || M == 0 || N == 0)
         return st;
     return from_cuda(taco::launch_gemm_compress(a_bf16, b_bf16, M, N, K, e_target, eps, codes, alpha, scale, y_out,
@@ -437,13 +438,27 @@ taco_status agoq_gemm_accumulate(const void *a_bf16, const void *b_bf16, int64_t
                                  int32_t block, uint8_t *main_codes, float *main_scale, float *y_out,
                                  void *workspace, uint64_t workspace_bytes, taco_stream_t stream)
 {
-    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, main_codes, nullptr, false, main_scale, y_out,
-                                     workspace, workspace_bytes);
+    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, main_codes, 8, nullptr, false, main_scale,
+                                     y_out, workspace, workspace_bytes);
     if (st != TACO_OK || M == 0 || N == 0)
         return st;
     return from_cuda(taco::launch_gemm_agoq_accumulate(a_bf16, b_bf16, M, N, K, main_codes, main_scale, y_out,
                                                        workspace, workspace_bytes,
                                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_gemm_laaq_quantize(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                    int32_t block, int32_t bits, uint8_t *packed, float *scale, float *y_out,
+                                    void *workspace, uint64_t workspace_bytes, taco_stream_t stream)
+{
+    if (bits != 4 && bits != 5 && bits != 6 && bits != 8)
+        return TACO_ERR_UNSUPPORTED;
+    taco_status st = check_gemm_args(a_bf16, b_bf16, M, N, K, block, packed, bits, nullptr, false, scale, y_out,
+                                     workspace, workspace_bytes);
+    if (st != TACO_OK || M == 0 || N == 0)
+        return st;
+    return from_cuda(taco::launch_gemm_laaq_quantize(a_bf16, b_bf16, M, N, K, bits, packed, scale, y_out, workspace,
+                                                     workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 taco_status taco_e4m3_encode(const float *x, int64_t n, uint8_t *codes, taco_stream_t stream)

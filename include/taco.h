@@ -324,10 +324,35 @@ taco_status agoq_gemm_accumulate(const void *a_bf16, const void *b_bf16, int64_t
                                  void *workspace, uint64_t workspace_bytes, taco_stream_t stream);
 
 /*
- * taco_gemm_workspace_bytes - the workspace that taco_gemm_compress and
- * agoq_gemm_accumulate take for their split tail on an M x N x K product on
- * the current device (it depends on the SM count); 0 when the shape gets no
- * split.  No counterpart in the pages: a property of this implementation.
+ * agoq_gemm_laaq_quantize - the GEMM that produces an activation, with
+ * AGoQ's block-wise activation quantisation fused into its epilogue ([AGoQ]
+ * 2.C: quantisation in the adjacent GEMM kernel; 2.A: activations stored
+ * block-wise in 4 bits, or 5, 6 or 8).  Y = A B^T is accumulated in fp32 on
+ * the tensor cores (bf16 operands), and each 128-element block of each row
+ * of Y is quantised exactly as agoq_laaq_quantize quantises a block, from
+ * the fp32 values (no bf16 rounding of Y): amax = max|y|, q = qmax / amax,
+ * code = rint(y q), multiplier amax / qmax (1 for an all-zero block).  The
+ * packed stream and the multipliers have agoq_laaq_quantize's layout for the
+ * row-major [M][N] tensor, so agoq_laaq_dequantize reads them back.
+ *
+ *  a_bf16      in      bf16 [M][K], 16-byte aligned
+ *  b_bf16      in      bf16 [N][K], 16-byte aligned
+ *  M, N, K, block      as for taco_gemm_compress (block 128)
+ *  bits                4, 5, 6 or 8 (others return TACO_ERR_UNSUPPORTED)
+ *  packed      out     uint8 [M * N * bits / 8], 16-byte aligned
+ *  scale       out     fp32 [M][N / 128]
+ *  y_out       out     optional fp32 [M][N]: Y as accumulated (NULL: not written)
+ *  workspace, workspace_bytes  as for taco_gemm_compress (the split tail)
+ */
+taco_status agoq_gemm_laaq_quantize(const void *a_bf16, const void *b_bf16, int64_t M, int64_t N, int64_t K,
+                                    int32_t block, int32_t bits, uint8_t *packed, float *scale, float *y_out,
+                                    void *workspace, uint64_t workspace_bytes, taco_stream_t stream);
+
+/*
+ * taco_gemm_workspace_bytes - the workspace that taco_gemm_compress,
+ * agoq_gemm_accumulate and agoq_gemm_laaq_quantize take for their split
+ * tail on an M x N x K product on the current device (it depends on the SM
+ * count); 0 when the shape gets no split.  No counterpart in the pages: a property of this implementation.
  *
  *  bytes  out  the size; shapes as for taco_gemm_compress (M or N = 0: 0)
  */
@@ -430,7 +455,8 @@ taco_status taco_two_shot_host_noalloc(int32_t P, int64_t rows, int64_t d, int32
  * taco_device_error - watchdog flags of the kernels on the current device.
  * Every in-kernel wait gives up after about a second and sets a bit here
  * (bit 0: compressor, bit 1: decompressor, bit 4: taco_watchdog_selftest,
- * bit 5: taco_gemm_compress and agoq_gemm_accumulate).
+ * bit 5: the GEMMs taco_gemm_compress, agoq_gemm_accumulate and
+ * agoq_gemm_laaq_quantize).
  * Synchronises the device.  With clear != 0 the flags are reset to 0 after
  * reading.
  */

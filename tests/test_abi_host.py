@@ -222,6 +222,25 @@ def test_gemm_compress_validation(lib):
     assert gemm_compress(lib, ws=A * 63, ws_bytes=2 << 20) == INVALID         # over both operands
 
 
+def test_agoq_gemm_laaq_quantize_validation(lib):
+    f = lambda **k: lib.agoq_gemm_laaq_quantize(k.get("a", A), k.get("b", A * 64), k.get("M", 256),
+                                                k.get("N", 512), k.get("K", 128), k.get("block", 128),
+                                                k.get("bits", 4), k.get("packed", A * 128), k.get("scale", A * 200),
+                                                k.get("y", None), k.get("ws", None), k.get("ws_bytes", 0), None)
+    assert f(bits=3) == UNSUPPORTED and f(bits=7) == UNSUPPORTED and f(bits=16) == UNSUPPORTED
+    assert f(block=64) == UNSUPPORTED
+    assert f(M=100) == UNSUPPORTED and f(N=192) == UNSUPPORTED and f(K=32) == UNSUPPORTED
+    assert f(M=-1) == INVALID
+    assert f(M=0) == OK and f(N=0) == OK
+    assert f(packed=None) == INVALID and f(scale=None) == INVALID
+    assert f(packed=A * 128 + 8) == MISALIGNED
+    # the packed stream is M N bits / 8 bytes: 64 KB at 4 bits, 128 KB at 8
+    assert f(scale=A * 128 + 65532, bits=4) == INVALID       # multipliers inside the stream
+    assert f(scale=A * 128 + 65536 + 4096, bits=8) == INVALID
+    assert f(y=A * 64) == INVALID                              # output over an operand
+    assert f(ws=A * 400 + 16, ws_bytes=4096) == MISALIGNED
+
+
 def test_gemm_workspace_bytes_validation(lib):
     v = ctypes.c_uint64(7)
     assert lib.taco_gemm_workspace_bytes(256, 512, 128, None) == INVALID

@@ -272,3 +272,63 @@ def test_agoq_gemm_accumulate_full_size_weight_gradient():
     """A GPT-6.7B-shaped weight gradient, dW [4096, 4096] = dY^T X over 8192
     tokens, accumulated over two micro-batches: every block bit-exact."""
     check_agoq_gemm(4096, 4096, 8192, steps=2, seed=3)
+
+
+# ------------------------------------------ LAAQ quantisation epilogue --
+
+def check_laaq_gemm(M, N, K, bits, seed=0, split_tail=True):
+    """agoq_gemm_laaq_quantize: the packed codes and multipliers equal, bit
+    for bit, the oracle's fp32 quantisation of the kernel's own fp32 Y (the
+    quantisation is a fixed FP32 sequence); Y is checked against the float64
+    product within the accumulation bound; the call without the optional
+    output gives the same bits; the library's dequantizer reads the stream
+    back as the oracle's does."""
+    a, b = operands(M, N, K, seed)
+    ad, bd = to_dev_bf16(a), to_dev_bf16(b)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    p = torch.full((M * N * bits // 8,), 0xA5, dtype=torch.uint8, device="cuda")
+    s = torch.full((M * N // 128,), float("nan"), dtype=torch.float32, device="cuda")
+    api.agoq_gemm_laaq_quantize(ad, bd, bits, packed=p, scale=s, y_out=y, split_tail=split_tail)
+    p2, s2 = api.agoq_gemm_laaq_quantize(ad, bd, bits, split_tail=split_tail)
+    torch.cuda.synchronize()
+    assert torch.equal(p, p2) and torch.equal(s, s2)
+    yg = to_host(y)
+    ref = oracle.gemm_bt(a, b)
+    mag = np.abs(oracle.bf16_to_f64(a)) @ np.abs(oracle.bf16_to_f64(b)).T
+    assert np.all(np.abs(yg.astype(np.float64) - ref) <= (K / 16 + 2) * 2.0 ** -22 * mag)
+    rp, rs = oracle.laaq_quantize_f32(yg, 128, bits)
+    assert np.array_equal(to_host(p), rp), f"packed codes differ at {bits} bits"
+    assert np.array_equal(to_host(s), rs), f"multipliers differ at {bits} bits"
+    out = api.agoq_laaq_dequantize(p, s, M * N, 128, bits, out_dtype=torch.float32)
+    assert np.array_equal(to_host(out), oracle.laaq_dequantize(rp, rs, M * N, 128, bits))
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 384, 128), (2048, 4096, 512), (384, 768, 4096),
+                                   (128, 128, 6144)])
+def test_gemm_laaq_quantize_shapes(M, N, K, bits):
+    """One tile (256 and 128 wide), several tiles per SM, and split tails of 2
+    and 3 pieces, at every width."""
+    check_laaq_gemm(M, N, K, bits, seed=bits)
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_gemm_laaq_quantize_without_the_split_tail(bits):
+    check_laaq_gemm(384, 768, 4096, bits, seed=20 + bits, split_tail=False)
+
+
+def test_gemm_laaq_quantize_full_size_4_bits():
+    """A GPT-6.7B-sized activation, [8192 tokens, 4096] = X W^T with W [4096,
+    4096], stored in 4 bits: every block bit-exact against the oracle's
+    quantisation of the kernel's own fp32 Y."""
+    M, N, K = 8192, 4096, 4096
+    a, b = operands(M, N, K, 31)
+    ad, bd = to_dev_bf16(a), to_dev_bf16(b)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    p, s = api.agoq_gemm_laaq_quantize(ad, bd, 4, y_out=y)
+    cub = torch.matmul(ad.float(), bd.float().T)
+    mag = torch.matmul(ad.float().abs(), bd.float().abs().T)
+    assert bool(torch.all((y - cub).abs() <= 2 * (K / 16 + 2) * 2.0 ** -22 * mag))
+    del cub, mag
+    rp, rs = oracle.laaq_quantize_f32(to_host(y), 128, 4)
+    assert np.array_equal(to_host(p), rp) and np.array_equal(to_host(s), rs)
