@@ -871,6 +871,33 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
               "decompress": lambda: [ar.decompress(k) for k in range(ar.S)]}
     ns = max(2, args.kernel_samples)
     per_phase_ms = {k: time_launches(torch, fn, 10, stream, replays=max(1, ns // 10)) for k, fn in phases.items()}
+    # the AllReduce of a row-parallel layer fed by its GEMM (the GPT-6.7B
+    # MLP down-projection at TP = 4: [rows, 4096] x [d, 4096]^T): the GEMM
+    # with the compressor in its epilogue writing the send pieces
+    # (run_gemm), against cuBLAS (bf16 out) then the exchange of that output
+    layer = None
+    if not args.no_gemm and all((r1 - r0) % 128 == 0 for j in range(ar.W) for k in range(ar.S)
+                                for r0, r1 in [ar._piece(j, k)]):
+        kg = 4096
+        a_bits = pool.submit(_tp_shard, (100 + rank, rows, kg, True, False, block)).result()
+        a = torch.from_numpy(a_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        w_bits = W.f32_to_bf16_bits(np.random.default_rng(110 + rank).normal(0.0, 0.02, (d, kg))
+                                    .astype(np.float32))
+        wt = torch.from_numpy(w_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        y = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+        fused = lambda: ar.run_gemm(a, wt)
+
+        def unfused():
+            torch.matmul(a, wt.t(), out=y)
+            ar.run(y)
+
+        fused()
+        unfused()
+        f_ms = time_launches(torch, fused, 5, stream, replays=2)
+        u_ms = time_launches(torch, unfused, 5, stream, replays=2)
+        layer = {"shape": {"M": rows, "N": d, "K": kg}, "fused_gemm_then_exchange_us": f_ms * 1e3,
+                 "cublas_gemm_then_exchange_us": u_ms * 1e3, "speedup": u_ms / f_ms,
+                 "timed_as": "graph replays of whole steps (GEMM, kernels and NCCL collectives)"}
     # end to end: pinned host input in, result out, every step
     h_in = torch.empty((rows, d), dtype=torch.bfloat16, pin_memory=True)
     h_in.view(torch.int16).copy_(torch.from_numpy(bits.view(np.int16)))
@@ -912,6 +939,7 @@ def run_exchange(args, rank: int, world: int, local: int, pool) -> None:
                          "peak_source": peak_src, "spec_peak": spec, "spec_peak_source": spec_src,
                          "frac_of_spec": achieved / spec},
             "kernels": kern,
+            "row_parallel_layer": layer,
             "e2e": {"value": whole_job_gbs(step_bytes, E, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": 2 * rows * d, "d2h_bytes_per_step": 4 * rows * d,
                     "api": "TwoShotAllReduce.run with pinned host copies in and out"},
@@ -945,7 +973,9 @@ def main():
     ap.add_argument("--no-laaq", action="store_true", help="skip the LAAQ activation-codec leg")
     ap.add_argument("--no-gpt27b", action="store_true", help="skip the GPT-2.7B-shaped round-trip leg")
     ap.add_argument("--no-gpt13b", action="store_true", help="skip the GPT-13B-shaped leg")
-    ap.add_argument("--no-gemm", action="store_true", help="skip the fused GEMM legs (compress, AGoQ accumulate)")
+    ap.add_argument("--no-gemm", action="store_true",
+                    help="skip the fused GEMM legs (compress, AGoQ accumulate, LAAQ quantise; with --exchange, "
+                         "the GEMM-fed exchange)")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
     ap.add_argument("--replicas", action="store_true",

@@ -12,7 +12,9 @@ With W ranks, the rows (or, for a flat gradient buffer, the blocks) are cut
 into W contiguous chunks of equal size; rank j owns chunk j.  One call:
 
   1. compress the local tensor (one launch per chunk, into a packed send
-     buffer: each chunk's codes, alphas and scales as one byte run);
+     buffer: each chunk's codes, alphas and scales as one byte run), or, for
+     a row-parallel layer, compute the local partial sum with the GEMM that
+     compresses in its epilogue (``TwoShotAllReduce.run_gemm``);
   2. All-to-All of the packed chunks: chunk j of every rank lands on rank j,
      in the rank's own memory, in rank order;
   3. the shard reduce over the W received chunks (one launch);
@@ -56,6 +58,10 @@ class CudaOps:
     @staticmethod
     def compress(x, codes, alpha, scale, block, e_target, eps):
         api.taco_compress(x, block, e_target, eps, codes=codes, alpha=alpha, scale=scale)
+
+    @staticmethod
+    def gemm_compress(a, w, codes, alpha, scale, block, e_target, eps):
+        api.taco_gemm_compress(a, w, block, e_target, eps, codes=codes, alpha=alpha, scale=scale)
 
     @staticmethod
     def reduce(codes, alpha, scale, block, e_target, eps, out_codes, out_alpha, out_scale):
@@ -161,6 +167,19 @@ class TwoShotAllReduce:
                 self.ops.compress(x[r0:r1], self._codes_of(piece)[:n], self._alpha_of(piece)[:n * nbr],
                                   self._scale_of(piece)[:n * nbr], self.block, self.e_target, self.eps)
 
+    def compress_gemm(self, a: torch.Tensor, w: torch.Tensor, k: int = 0):
+        """Stage k's pieces of this rank's partial sum Y = a w^T, computed
+        and compressed by the GEMM with the compressor in its epilogue, one
+        launch per piece, straight into the send buffer."""
+        nbr = self.d // self.block
+        for j in range(self.W):
+            r0, r1 = self._piece(j, k)
+            if r1 > r0:
+                n = r1 - r0
+                piece = self.send[k, j]
+                self.ops.gemm_compress(a[r0:r1], w, self._codes_of(piece)[:n], self._alpha_of(piece)[:n * nbr],
+                                       self._scale_of(piece)[:n * nbr], self.block, self.e_target, self.eps)
+
     def exchange(self, k: int = 0, async_op: bool = False):
         """ReduceScatter in compressed form: piece k of chunk j of every rank
         to rank j (codes and both scalars in one collective)."""
@@ -188,15 +207,36 @@ class TwoShotAllReduce:
         ([rows, d] view of the output buffer)."""
         if tuple(x.shape) != (self.rows, self.d):
             raise ValueError(f"x must be [{self.rows}, {self.d}]")
+        return self._run(lambda k: self.compress(x, k))
+
+    def run_gemm(self, a: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
+        """The AllReduce of a row-parallel layer's output: this rank's partial
+        sum is Y = a w^T (a bf16 [rows, K], w bf16 [d, K], its slice of the
+        weight), produced already compressed by the GEMM's epilogue (AGoQ
+        2.C's fusion applied to the TACO compressor), then exchanged as in
+        ``run``.  Every piece must be a multiple of 128 rows (the GEMM's
+        tile): rows a multiple of 128 and of 128 x world size x stages
+        rows per chunk do it."""
+        if a.dim() != 2 or w.dim() != 2 or a.shape[0] != self.rows or w.shape[0] != self.d or \
+                a.shape[1] != w.shape[1]:
+            raise ValueError(f"a must be [{self.rows}, K] and w [{self.d}, K]")
+        for j in range(self.W):
+            for k in range(self.S):
+                r0, r1 = self._piece(j, k)
+                if (r1 - r0) % 128:
+                    raise ValueError(f"piece {k} of chunk {j} has {r1 - r0} rows, not a multiple of 128")
+        return self._run(lambda k: self.compress_gemm(a, w, k))
+
+    def _run(self, compress) -> torch.Tensor:
         if self.S == 1:
-            self.compress(x)
+            compress(0)
             self.exchange()
             self.reduce()
             self.gather()
             return self.decompress()
         a2a = []
         for k in range(self.S):  # compress k + 1 is queued while exchange k is in flight
-            self.compress(x, k)
+            compress(k)
             a2a.append(self.exchange(k, async_op=True))
         ag = []
         for k in range(self.S):

@@ -38,6 +38,15 @@ class OracleOps:
         scale.copy_(torch.from_numpy(s.reshape(-1)))
 
     @staticmethod
+    def gemm_compress(a, w, codes, alpha, scale, block, e_target, eps):
+        ab = a.contiguous().view(torch.int16).numpy().view(np.uint16)
+        wb = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+        c, al, sc = oracle.gemm_compress(ab, wb, block, e_target, eps)
+        codes.copy_(torch.from_numpy(c.reshape(codes.shape)))
+        alpha.copy_(torch.from_numpy(al.reshape(-1)))
+        scale.copy_(torch.from_numpy(sc.reshape(-1)))
+
+    @staticmethod
     def reduce(codes, alpha, scale, block, e_target, eps, out_codes, out_alpha, out_scale):
         c, a, s = oracle.reduce_shards([t.numpy() for t in codes], [t.numpy() for t in alpha],
                                        [t.numpy() for t in scale], block, e_target, eps)
@@ -67,6 +76,17 @@ def _taco_input(rank, rows, d, block):
     return W.tp_activation(50 + rank, rows, d, channel_scale=True, block=block)
 
 
+GEMM_K = 64
+
+
+def _gemm_operands(rank, rows, d):
+    """Rank r's slice of a row-parallel layer: its activations [rows, K] and
+    its slice of the weight [d, K], bf16."""
+    a = W.tp_activation(80 + rank, rows, GEMM_K, channel_scale=True)
+    w = W.f32_to_bf16_bits(np.random.default_rng(90 + rank).normal(0.0, 0.05, (d, GEMM_K)).astype(np.float32))
+    return a, w
+
+
 def _agoq_buffer(rank, n, block):
     c, s = np.zeros(n, np.uint8), np.ones(n // block, np.float32)
     for step in range(2):
@@ -79,7 +99,14 @@ def _worker(rank, world, port, case, q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         kind, a, b, block, stages = case
-        if kind == "taco":
+        if kind == "gemm":
+            rows, d = a, b
+            xa, xw = _gemm_operands(rank, rows, d)
+            ar = exchange.TwoShotAllReduce(rows, d, block, device="cpu", ops=OracleOps, stages=stages)
+            ta = torch.from_numpy(xa.view(np.int16)).view(torch.bfloat16)
+            tw = torch.from_numpy(xw.view(np.int16)).view(torch.bfloat16)
+            q.put((rank, ar.run_gemm(ta, tw).clone().numpy(), ar.R, None))
+        elif kind == "taco":
             rows, d = a, b
             x = torch.from_numpy(_taco_input(rank, rows, d, block).view(np.int16)).view(torch.bfloat16)
             ar = exchange.TwoShotAllReduce(rows, d, block, device="cpu", ops=OracleOps, stages=stages)
@@ -131,6 +158,42 @@ def test_two_shot_exchange_equals_the_reduce_of_all_ranks(world, rows, d, block,
         assert out.shape == (rows, d)
         assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), f"rank {rank}"
         assert sent == {"all_to_all": (world - 1) * chunk_bytes, "all_gather": (world - 1) * chunk_bytes}
+
+
+@pytest.mark.parametrize("world,rows,d,stages", [(2, 256, 256, 1), (3, 768, 128, 2)])
+def test_two_shot_exchange_of_gemm_outputs_equals_the_reduce_of_all_ranks(world, rows, d, stages):
+    """run_gemm: each rank's partial sum Y_r = A_r W_r^T is compressed by the
+    GEMM step piece by piece; the result equals the oracle's reduce of every
+    rank's fused GEMM + compress over the whole tensor (every block is
+    independent)."""
+    res = _run(world, ("gemm", rows, d, 128, stages))
+    comp = [oracle.gemm_compress(*_gemm_operands(r, rows, d), 128) for r in range(world)]
+    rc, ra, rs = oracle.reduce_shards(*zip(*comp), 128)
+    ref = oracle.decompress(rc, ra, rs, 128).astype(np.float32)
+    for rank, out, _, _ in res:
+        assert out.shape == (rows, d)
+        assert np.array_equal(out.view(np.uint32), ref.view(np.uint32)), f"rank {rank}"
+
+
+def test_run_gemm_rejects_pieces_that_are_not_whole_tiles():
+    """300 rows over 2 ranks are chunks of 150 rows: not whole 128-row tiles
+    of the GEMM, so run_gemm refuses before it launches anything."""
+    with pytest.raises(ValueError):
+        _check_pieces(300, 256, 2, 1)
+
+
+def _check_pieces(rows, d, world, stages):
+    """run_gemm's piece check without a process group: a one-rank gloo group
+    over a free port."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        ar = exchange.TwoShotAllReduce(rows, d, 128, device="cpu", ops=OracleOps, stages=stages)
+        a = torch.zeros((rows, 64), dtype=torch.bfloat16)
+        w = torch.zeros((d, 64), dtype=torch.bfloat16)
+        ar.run_gemm(a, w)
+    finally:
+        dist.destroy_process_group()
 
 
 def test_agoq_exchange_equals_the_reduce_of_all_ranks():

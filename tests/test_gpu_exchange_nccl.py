@@ -60,3 +60,27 @@ def test_agoq_exchange_on_one_rank_equals_the_local_reduce(nccl_group):
     rc, rs = api.agoq_reduce_shards([ar.codes], [ar.scale], block)
     torch.cuda.synchronize()
     assert torch.equal(c, rc) and torch.equal(s, rs)
+
+
+@pytest.mark.parametrize("rows,d,K,stages", [(512, 1024, 256, 1), (1024, 512, 512, 4)])
+def test_gemm_exchange_on_one_rank_equals_the_local_path(nccl_group, rows, d, K, stages):
+    """run_gemm: the row-parallel layer's partial sum Y = A W^T leaves the
+    GEMM compressed, piece by piece, into the send buffer.  With one rank the
+    result is the same pieces' taco_gemm_compress, reduced as one shard and
+    decompressed, bit for bit (the same shapes take the same tile plan)."""
+    a = to_dev_bf16(W.tp_activation(81, rows, K, channel_scale=True))
+    w = to_dev_bf16(W.f32_to_bf16_bits(np.random.default_rng(82).normal(0.0, 0.02, (d, K)).astype(np.float32)))
+    ar = exchange.TwoShotAllReduce(rows, d, 128, stages=stages)
+    out = ar.run_gemm(a, w).clone()
+    Rs, nbr = rows // stages, d // 128
+    codes = torch.empty((rows, d), dtype=torch.uint8, device="cuda")
+    alpha = torch.empty(rows * nbr, dtype=torch.float32, device="cuda")
+    scale = torch.empty_like(alpha)
+    for k in range(stages):
+        r0, r1 = k * Rs, (k + 1) * Rs
+        api.taco_gemm_compress(a[r0:r1], w, codes=codes[r0:r1], alpha=alpha[r0 * nbr:r1 * nbr],
+                               scale=scale[r0 * nbr:r1 * nbr])
+    rc, ra, rs = api.taco_reduce_shards([codes], [alpha], [scale], 128)
+    ref = api.taco_decompress(rc, ra, rs, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
