@@ -153,3 +153,63 @@ def test_host_pipeline_writes_stay_inside_the_host_output():
     for _ in range(2):
         pipe.run(h_in, h_out)
     assert gh.intact() and torch.equal(h_in.view(torch.int16), h0.view(torch.int16))
+
+
+def gemm_operands(M, N, K, seed):
+    a = to_dev_bf16(W.tp_activation(seed, M, K, channel_scale=True))
+    b = to_dev_bf16(W.f32_to_bf16_bits(np.random.default_rng(seed + 1).normal(0.0, 0.02, (N, K))
+                                       .astype(np.float32)))
+    return a, b
+
+
+def guarded_workspace(M, N, K):
+    """The split tail's workspace between guards (zeroed inside), or None."""
+    nb = api.gemm_workspace_bytes(M, N, K)
+    if nb == 0:
+        return None, None
+    g, ws = guarded(torch.uint8, (nb,))
+    ws.zero_()
+    return g, ws
+
+
+# (384, 768, 4096): 9 tiles split into 2 pieces; (256, 384, 128): 128-wide
+# tiles, no split; (2048, 4096, 512): several tiles per SM
+@pytest.mark.parametrize("M,N,K", [(384, 768, 4096), (256, 384, 128), (2048, 4096, 512)])
+def test_gemm_compress_writes_stay_inside_their_outputs(M, N, K):
+    a, b = gemm_operands(M, N, K, 60)
+    a0, b0 = a.clone(), b.clone()
+    gc, c = guarded(torch.uint8, (M, N))
+    ga, al = guarded(torch.float32, (M * N // 128,))
+    gs, sc = guarded(torch.float32, (M * N // 128,))
+    gy, y = guarded(torch.float32, (M, N))
+    gw, ws = guarded_workspace(M, N, K)
+    api.taco_gemm_compress(a, b, codes=c, alpha=al, scale=sc, y_out=y, workspace=ws)
+    assert gc.intact() and ga.intact() and gs.intact() and gy.intact() and (gw is None or gw.intact())
+    assert torch.equal(a, a0) and torch.equal(b, b0)
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 640, 4096), (2048, 4096, 512)])
+def test_agoq_gemm_accumulate_writes_stay_inside_their_buffers(M, N, K):
+    a, b = gemm_operands(M, N, K, 70)
+    a0, b0 = a.clone(), b.clone()
+    gc, c = guarded(torch.uint8, (M, N))
+    gs, sc = guarded(torch.float32, (M * N // 128,))
+    c.zero_()
+    sc.fill_(1.0)
+    gw, ws = guarded_workspace(M, N, K)
+    api.agoq_gemm_accumulate(a, b, c, sc, workspace=ws)
+    assert gc.intact() and gs.intact() and (gw is None or gw.intact())
+    assert torch.equal(a, a0) and torch.equal(b, b0)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("M,N,K", [(384, 768, 4096), (256, 384, 128)])
+def test_gemm_laaq_quantize_writes_stay_inside_their_outputs(M, N, K, bits):
+    a, b = gemm_operands(M, N, K, 80 + bits)
+    a0, b0 = a.clone(), b.clone()
+    gp, p = guarded(torch.uint8, (M * N * bits // 8,))
+    gs, sc = guarded(torch.float32, (M * N // 128,))
+    gw, ws = guarded_workspace(M, N, K)
+    api.agoq_gemm_laaq_quantize(a, b, bits, packed=p, scale=sc, workspace=ws)
+    assert gp.intact() and gs.intact() and (gw is None or gw.intact())
+    assert torch.equal(a, a0) and torch.equal(b, b0)
