@@ -1,37 +1,45 @@
-// The tensor-core GEMM that produces a tensor-parallel partial sum, with the
-// TACO compressor fused into its epilogue.
+// The tensor-core GEMM whose epilogue compresses or quantises its fp32
+// result before it leaves the SM.
 //
 // AGoQ (gist.science summary of arXiv 2605.00539), 2.C: the quantisation
 // runs inside the adjacent GEMM kernel, the tensor cores doing the matrix
-// product and the CUDA cores the quantisation.  Applied here to TACO's
-// compressor (gist.science summary of arXiv 2604.24088, 2.B.1-2.B.3): the
-// partial sum Y = A B^T of a row-parallel layer leaves the kernel already as
-// ASH + DS E4M3 codes with their two scalars per block, ready for the
-// two-shot exchange, instead of being written in bf16 and read back by the
-// compressor.
+// product and the CUDA cores the quantisation.  One kernel, three
+// epilogues:
+//  * TACO's compressor (gist.science summary of arXiv 2604.24088,
+//    2.B.1-2.B.3): the partial sum Y = A B^T of a row-parallel layer leaves
+//    the kernel already as ASH + DS E4M3 codes with their two scalars per
+//    block, ready for the two-shot exchange, instead of being written in
+//    bf16 and read back by the compressor;
+//  * AGoQ 2.B's accumulation of a weight gradient into the FP8 main
+//    gradient (dequantise, add, requantise, in place);
+//  * AGoQ 2.A's block-wise LAAQ quantisation of an activation (4, 5, 6 or 8
+//    bits a code, packed).
 //
 // Design (sm_103a):
 //  * A persistent grid, one CTA per SM, walks the 128 x 256 tiles of Y
-//    (128 x 128 where N % 256 != 0) in turn.  Warp 0 is the TMA producer: it streams 128 x 64 tiles of A and
-//    256 x 64 tiles of B (bf16, 128-byte swizzle) through a 4-stage mbarrier
-//    ring, from one output tile into the next without a gap.  Warp 1
-//    allocates 512 columns of tensor memory (two fp32 accumulators of 256
-//    columns) and one of its threads issues the tcgen05.mma steps (128 x 256
-//    x 16 each, four per 64-wide stage), frees each stage with
-//    tcgen05.commit, and signals a finished accumulator the same way.  Warps
-//    2-5 are the epilogue: while they compress tile i from one accumulator,
-//    the MMAs of tile i + 1 fill the other.
+//    (128 x 128 where N % 256 != 0) in turn.  Warp 0 is the TMA producer:
+//    it streams 128 x 64 tiles of A and 256 x 64 tiles of B (bf16, 128-byte
+//    swizzle) through a 4-stage mbarrier ring, from one output tile into
+//    the next without a gap.  Warp 1 allocates 512 columns of tensor memory
+//    (two fp32 accumulators of 256 columns) and one of its threads issues
+//    the tcgen05.mma steps (128 x 256 x 16 each, four per 64-wide stage),
+//    frees each stage with tcgen05.commit, and signals a finished
+//    accumulator the same way.  Warps 2-5 are the epilogue: while they
+//    process tile i from one accumulator, the MMAs of tile i + 1 fill the
+//    other.
 //  * The accumulator's lane is the tile row, so after tcgen05.ld each
 //    epilogue thread holds 128 consecutive fp32 values of one row: exactly
-//    one compression block, the layout the compress kernel gives a thread.
-//    The 128-point Walsh-Hadamard transform, the block energy, alpha, s and
-//    the E4M3 conversion run in that thread's registers; the codes go
-//    through the warp's swizzled staging rows and TMA stores.
+//    one block, the layout the stand-alone codec kernels give a thread.
+//    The block's arithmetic (the 128-point Walsh-Hadamard transform, alpha,
+//    s and E4M3; or the FP8 accumulation; or the LAAQ quantisation) runs in
+//    that thread's registers, and the codes go through the warp's staging
+//    rows and TMA stores.
 //  * Split tail: when the tiles do not fill whole rounds of SMs and K is
 //    long enough, the tiles of the last round are cut along K into 2-4
 //    pieces dealt out like tiles; their fp32 partial sums meet in a
 //    caller's workspace and the warp that stores a tile quarter's last
-//    piece adds them up in piece order, then compresses (no spin waits).
+//    piece adds them up in piece order, then runs the epilogue (no spin
+//    waits).
 //  * Every mbarrier wait is time-limited; a wait that runs out sets a flag
 //    readable through taco_device_error() and the CTA winds down.
 
