@@ -64,11 +64,14 @@ def _load():
             lib.oracle_laaq_quantize.argtypes = [P, i64, i32, i32, P, P]
             lib.oracle_laaq_dequantize.argtypes = [P, P, i64, i32, i32, P]
             lib.oracle_laaq_quantize_f32.argtypes = [P, i64, i32, i32, P, P]
+            lib.oracle_laaq_dequantize_silu.argtypes = [P, P, i64, i32, i32, P]
+            lib.oracle_laaq_dequantize_rmsnorm.argtypes = [P, P, i64, i64, i32, i32, P, ctypes.c_double, P]
             for f in ("oracle_compress", "oracle_compress_f64", "oracle_decompress",
                       "oracle_reduce_shards", "oracle_agoq_accumulate", "oracle_agoq_reduce",
                       "oracle_agoq_accumulate_f32",
                       "oracle_int8_roundtrip", "oracle_compress_int8", "oracle_decompress_int8",
-                      "oracle_laaq_quantize", "oracle_laaq_dequantize", "oracle_laaq_quantize_f32"):
+                      "oracle_laaq_quantize", "oracle_laaq_dequantize", "oracle_laaq_quantize_f32",
+                      "oracle_laaq_dequantize_silu", "oracle_laaq_dequantize_rmsnorm"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -309,3 +312,25 @@ def laaq_dequantize(packed: np.ndarray, scale: np.ndarray, n: int, block: int = 
     out = np.empty(n, dtype=np.float32)
     _check(_load().oracle_laaq_dequantize(_ptr(p), _ptr(s), n, block, bits, _ptr(out)))
     return out
+
+
+def laaq_dequantize_silu(packed: np.ndarray, scale: np.ndarray, n: int, block: int = 128, bits: int = 4):
+    """SiLU recomputed from the stored quantised input (AGoQ 2.A): float64 [n]."""
+    p = np.ascontiguousarray(packed, dtype=np.uint8).reshape(-1)
+    s = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
+    out = np.empty(n, dtype=np.float64)
+    _check(_load().oracle_laaq_dequantize_silu(_ptr(p), _ptr(s), n, block, bits, _ptr(out)))
+    return out
+
+
+def laaq_dequantize_rmsnorm(packed: np.ndarray, scale: np.ndarray, rows: int, d: int, gamma: np.ndarray,
+                            eps: float = 1e-6, block: int = 128, bits: int = 4):
+    """RMSNorm of each row of d values recomputed from the stored quantised
+    input (AGoQ 2.A): float64 [rows, d]."""
+    p = np.ascontiguousarray(packed, dtype=np.uint8).reshape(-1)
+    s = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
+    g = np.ascontiguousarray(gamma, dtype=np.float32).reshape(-1)
+    assert g.size == d
+    out = np.empty(rows * d, dtype=np.float64)
+    _check(_load().oracle_laaq_dequantize_rmsnorm(_ptr(p), _ptr(s), rows, d, block, bits, _ptr(g), eps, _ptr(out)))
+    return out.reshape(rows, d)

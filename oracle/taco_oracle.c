@@ -625,3 +625,45 @@ int oracle_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n,
     }
     return 0;
 }
+
+/* [AGoQ] 2.A, recomputation instead of caching: for RMSNorm and SiLU, AGoQ
+ * stores only the block-wise quantised input and recomputes the operator's
+ * output from it in the backward pass (a tighter error bound than caching a
+ * quantised output).  Reading (the page names the operators, not their
+ * formulas): SiLU(x) = x / (1 + exp(-x)); RMSNorm of a row of d values,
+ * y_i = x_i / sqrt(mean_j(x_j^2) + eps) * g_i.  The input x is the
+ * dequantised fp32 value exactly as oracle_laaq_dequantize gives it; the
+ * operator then runs in double. */
+int oracle_laaq_dequantize_silu(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
+                                double *out)
+{
+    int64_t i;
+    if (!laaq_args_ok(n, block, bits))
+        return -1;
+    for (i = 0; i < n; ++i) {
+        const double x = (double)((float)get_bits_signed(packed, i * (int64_t)bits, bits) * scale[i / block]);
+        out[i] = x / (1.0 + exp(-x));
+    }
+    return 0;
+}
+
+int oracle_laaq_dequantize_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, int block,
+                                   int bits, const float *gamma, double eps, double *out)
+{
+    int64_t r, j;
+    if (rows < 0 || d <= 0 || d % block != 0 || !laaq_args_ok(rows * d, block, bits) || !(eps >= 0.0))
+        return -1;
+    for (r = 0; r < rows; ++r) {
+        double ss = 0.0, inv;
+        for (j = 0; j < d; ++j) {
+            const int64_t i = r * d + j;
+            const double x = (double)((float)get_bits_signed(packed, i * (int64_t)bits, bits) * scale[i / block]);
+            out[i] = x;
+            ss += x * x;
+        }
+        inv = 1.0 / sqrt(ss / (double)d + eps);
+        for (j = 0; j < d; ++j)
+            out[r * d + j] = out[r * d + j] * inv * (double)gamma[j];
+    }
+    return 0;
+}

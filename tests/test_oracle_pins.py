@@ -722,3 +722,73 @@ def test_gemm_laaq_quantize_is_quantize_of_the_product():
         p, s = oracle.gemm_laaq_quantize(a, b, 128, bits)
         rp, rs = oracle.laaq_quantize(np.ascontiguousarray(b.T), 128, bits)
         assert np.array_equal(p, rp) and np.array_equal(s, rs)
+
+
+# ------------------------- RMSNorm / SiLU recomputed from the stored input --
+# AGoQ 2.A: for RMSNorm and SiLU, only the quantised input is stored and the
+# operator's output is recomputed from it in the backward pass.
+
+def _stored(seed, rows, d, bits, block=128):
+    x = W.tp_activation(seed, rows, d, channel_scale=True, zero_blocks=(2,), block=block)
+    packed, scale = oracle.laaq_quantize(x, block, bits)
+    xhat = oracle.laaq_dequantize(packed, scale, rows * d, block, bits).astype(np.float64)
+    return x, packed, scale, xhat
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_silu_recompute_odd_part_is_the_input(bits):
+    """SiLU(x) - SiLU(-x) = x (x sigma(x) + x sigma(-x) = x): the recompute of
+    the negated stream (codes -c with the same multipliers, what quantising
+    -x gives) subtracted from the recompute of the stream is the dequantised
+    input itself, to rounding."""
+    rows, d = 16, 1024
+    x, packed, scale, xhat = _stored(91, rows, d, bits)
+    neg_packed, neg_scale = oracle.laaq_quantize(x ^ np.uint16(0x8000), 128, bits)
+    assert np.array_equal(neg_scale, scale)
+    s_pos = oracle.laaq_dequantize_silu(packed, scale, rows * d, 128, bits)
+    s_neg = oracle.laaq_dequantize_silu(neg_packed, neg_scale, rows * d, 128, bits)
+    assert np.allclose(s_pos - s_neg, xhat, rtol=1e-14, atol=1e-300)
+
+
+def test_silu_recompute_equals_the_tanh_form():
+    """x sigma(x) = (x / 2) (1 + tanh(x / 2)), evaluated with numpy's tanh on
+    the dequantised input; zeros stay zeros."""
+    rows, d = 8, 512
+    _, packed, scale, xhat = _stored(92, rows, d, 5)
+    s = oracle.laaq_dequantize_silu(packed, scale, rows * d, 128, 5)
+    want = 0.5 * xhat * (1.0 + np.tanh(0.5 * xhat))
+    assert np.allclose(s, want, rtol=1e-13, atol=0)
+    assert np.all(s[xhat == 0] == 0)
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_rmsnorm_recompute_invariants(bits):
+    """Per row: y_i / (xhat_i g_i) is one constant r > 0, and mean(y^2 / g^2)
+    = r^2 mean(xhat^2) = mean(xhat^2) / (mean(xhat^2) + eps), so with the
+    row's mean square m: r = 1 / sqrt(m + eps).  A transposed index, a sum in
+    place of the mean or a dropped eps breaks one of these."""
+    rows, d, eps = 12, 1024, 1e-6
+    _, packed, scale, xhat = _stored(93 + bits, rows, d, bits)
+    xhat = xhat.reshape(rows, d)
+    g = (1.0 + 0.5 * np.sin(np.arange(d))).astype(np.float32)
+    y = oracle.laaq_dequantize_rmsnorm(packed, scale, rows, d, g, eps, 128, bits)
+    gd = g.astype(np.float64)
+    for r in range(rows):
+        nz = xhat[r] != 0
+        ratio = y[r][nz] / (xhat[r][nz] * gd[nz])
+        assert np.allclose(ratio, ratio[0], rtol=1e-13) and ratio[0] > 0
+        m = float(np.mean(xhat[r] ** 2))
+        assert abs(ratio[0] - 1.0 / math.sqrt(m + eps)) <= 1e-12 * ratio[0]
+        assert np.all(y[r][~nz] == 0)
+
+
+def test_rmsnorm_recompute_hand_worked_row():
+    """One row of 128 values, every code 7 at 4 bits with multiplier 0.5 (x =
+    3.5 everywhere, stored as amax 3.5): mean(x^2) = 12.25, so with eps = 0
+    y = 3.5 / 3.5 * g = g exactly."""
+    x = np.full(128, 0x4060, dtype=np.uint16)  # bf16 3.5
+    packed, scale = oracle.laaq_quantize(x, 128, 4)
+    assert scale.tolist() == [0.5] and packed.tolist() == [0x77] * 64
+    g = np.linspace(-2, 2, 128).astype(np.float32)
+    y = oracle.laaq_dequantize_rmsnorm(packed, scale, 1, 128, g, 0.0, 128, 4)
+    assert np.array_equal(y[0], g.astype(np.float64))
