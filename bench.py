@@ -502,7 +502,8 @@ def int8_leg(torch, api, x, P: int, rows: int, d: int, block: int, peak: float) 
 def laaq_leg(torch, api, peak: float) -> dict:
     """AGoQ LAAQ activation codec on a GPT-6.7B-shaped activation tensor
     (bf16 [8192, 4096]), block 128, 4/5/6/8 bits: quantize and dequantize to
-    bf16, timed per launch from graph replays.  One tensor is 67 MB, below the
+    bf16, and at 4 bits SiLU and RMSNorm recomputed from the stored input,
+    timed per launch from graph replays.  One tensor is 67 MB, below the
     129 MB L2, so launches rotate over a ring of three inputs and outputs
     (201 MB of inputs): each launch reads a tensor the previous two launches
     did not touch."""
@@ -513,6 +514,7 @@ def laaq_leg(torch, api, peak: float) -> dict:
     xs = [torch.from_numpy(W.tp_activation(600 + i, rows, d, channel_scale=True).view(np.int16))
           .cuda().view(torch.bfloat16).reshape(-1) for i in range(3)]
     stream = torch.cuda.current_stream()
+    gamma = torch.linspace(0.5, 1.5, d, device="cuda")
     res = {}
     for bits in (4, 5, 6, 8):
         packed = [torch.empty(n * bits // 8, dtype=torch.uint8, device="cuda") for _ in range(3)]
@@ -530,11 +532,26 @@ def laaq_leg(torch, api, peak: float) -> dict:
             it["d"] += 1
             api.agoq_laaq_dequantize(packed[i], scale[i], n, block, bits, out=out[i])
 
+        def silu():
+            i = it["d"] % 3
+            it["d"] += 1
+            api.agoq_laaq_dequantize_silu(packed[i], scale[i], n, block, bits, out=out[i])
+
+        def rmsnorm():
+            i = it["d"] % 3
+            it["d"] += 1
+            api.agoq_laaq_dequantize_rmsnorm(packed[i], scale[i], rows, d, gamma, 1e-6, block, bits,
+                                             out=out[i].view(rows, d))
+
         for _ in range(3):
             quant()
             dequant()
-        for name, fn, b in (("quantize", quant, 2 * n + n * bits // 8 + 4 * (n // block)),
-                            ("dequantize", dequant, n * bits // 8 + 4 * (n // block) + 2 * n)):
+        legs = [("quantize", quant, 2 * n + n * bits // 8 + 4 * (n // block)),
+                ("dequantize", dequant, n * bits // 8 + 4 * (n // block) + 2 * n)]
+        if bits == 4:  # the recomputations of AGoQ 2.A, from the 4-bit stored input
+            legs += [("dequantize_silu", silu, n * bits // 8 + 4 * (n // block) + 2 * n),
+                     ("dequantize_rmsnorm", rmsnorm, n * bits // 8 + 4 * (n // block) + 2 * n + 4 * d)]
+        for name, fn, b in legs:
             res[f"{name}_{bits}bit"] = kernel_entry(time_launches(torch, fn, 12, stream), b, peak)
     return res
 

@@ -38,6 +38,8 @@ SIGNATURES = {
     "agoq_reduce_shards": (ctypes.c_int, [_I32, _PP, _PP, _I64, _I32, _P, _P, _P]),
     "agoq_laaq_quantize": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
     "agoq_laaq_dequantize": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _I32, _P]),
+    "agoq_laaq_dequantize_silu": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _I32, _P]),
+    "agoq_laaq_dequantize_rmsnorm": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _I32, _P, _F32, _P, _I32, _P]),
     "taco_e4m3_encode": (ctypes.c_int, [_P, _I64, _P, _P]),
     "taco_gemm_compress": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _F32, _F32, _P, _P, _P, _P, _P, _U64,
                                           _P]),

@@ -263,6 +263,43 @@ def agoq_laaq_dequantize(packed: torch.Tensor, scale: torch.Tensor, n: int, bloc
     return out
 
 
+def agoq_laaq_dequantize_silu(packed: torch.Tensor, scale: torch.Tensor, n: int, block: int = 128,
+                              bits: int = 4, out_dtype: torch.dtype = torch.bfloat16,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """SiLU recomputed from the stored quantised input: x_hat / (1 + exp(-x_hat))
+    of the dequantised values, fp32 or bf16 [n] (AGoQ 2.A)."""
+    _need(packed, "packed", (torch.uint8,), n * bits // 8)
+    _need(scale, "scale", (torch.float32,))
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype, device=packed.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), n)
+    st = _lib.load().agoq_laaq_dequantize_silu(packed.data_ptr(), scale.data_ptr(), n, block, bits,
+                                               out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                               _stream_handle(stream))
+    _lib.check("agoq_laaq_dequantize_silu", st)
+    return out
+
+
+def agoq_laaq_dequantize_rmsnorm(packed: torch.Tensor, scale: torch.Tensor, rows: int, d: int,
+                                 gamma: torch.Tensor, eps: float = 1e-6, block: int = 128, bits: int = 4,
+                                 out_dtype: torch.dtype = torch.bfloat16, out: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """RMSNorm of each row of d values recomputed from the stored quantised
+    input: x_hat / sqrt(mean(x_hat^2) + eps) * gamma, fp32 or bf16 [rows, d]
+    (AGoQ 2.A)."""
+    _need(packed, "packed", (torch.uint8,), rows * d * bits // 8)
+    _need(scale, "scale", (torch.float32,))
+    _need(gamma, "gamma", (torch.float32,), d)
+    if out is None:
+        out = torch.empty((rows, d), dtype=out_dtype, device=packed.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), rows * d)
+    st = _lib.load().agoq_laaq_dequantize_rmsnorm(packed.data_ptr(), scale.data_ptr(), rows, d, block, bits,
+                                                  gamma.data_ptr(), eps, out.data_ptr(),
+                                                  int(out.dtype == torch.bfloat16), _stream_handle(stream))
+    _lib.check("agoq_laaq_dequantize_rmsnorm", st)
+    return out
+
+
 def taco_e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """fp32 [n] -> E4M3FN codes uint8 [n] (round to nearest even, saturating at +-448)."""
     _need(x, "x", (torch.float32,))

@@ -51,7 +51,12 @@ cudaError_t launch_agoq_reduce(int P, const ShardPtrs &in, int64_t n, int block,
 cudaError_t launch_laaq_quantize(const void *x_bf16, int64_t n, int block, int bits, uint8_t *packed,
                                  float *scale, cudaStream_t stream);
 cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
-                                   void *out, bool out_bf16, cudaStream_t stream);
+                                   void *out, bool out_bf16, bool silu, cudaStream_t stream);
+// RMSNorm of each row of d values (d % block == 0) recomputed from the
+// stored quantised input: y = x_hat / sqrt(mean(x_hat^2) + eps) * gamma.
+cudaError_t launch_laaq_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, int block,
+                                int bits, const float *gamma, float eps, void *out, bool out_bf16,
+                                cudaStream_t stream);
 
 cudaError_t launch_e4m3_encode(const float *x, int64_t n, uint8_t *codes, cudaStream_t stream);
 

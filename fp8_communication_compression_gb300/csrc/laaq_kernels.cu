@@ -170,17 +170,40 @@ template <int BITS> __device__ __forceinline__ float biased_code(const UnitBits 
 constexpr int kTileUnits = 128;                  // units of 8 codes per warp tile
 constexpr int kTileCodes = 8 * kTileUnits;       // 1024
 
-template <int BITS, bool BF16OUT>
-__device__ __forceinline__ void decode_store_unit(const UnitBits &u, float m, void *out, int64_t unit)
+// The operator applied after dequantisation: none, or SiLU recomputed from
+// the stored input (AGoQ 2.A: RMSNorm and SiLU keep only their quantised
+// input and recompute their output).
+constexpr int kOpNone = 0, kOpSilu = 1;
+
+// The unit's 8 values x_hat = code * m: an exact subtraction, then one
+// rounded multiply (two values at a time).
+template <int BITS> __device__ __forceinline__ void decode_unit(const UnitBits &u, float m, float2 (&v)[4])
 {
     constexpr float kBias = kRoundMagic + static_cast<float>(1 << (BITS - 1));
     const float2 nb2 = make_float2(-kBias, -kBias), m2 = make_float2(m, m);
-    float2 v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)  // x_hat = code * m: an exact subtraction, then one rounded multiply
+    for (int i = 0; i < 4; ++i)
         v[i] = __fmul2_rn(__fadd2_rn(make_float2(biased_code<BITS>(u, 2 * i), biased_code<BITS>(u, 2 * i + 1)),
                                      nb2),
                           m2);
+}
+
+// SiLU(x) = x sigma(x) in fp32, from e = exp(-|x|) <= 1 (expf, at most 2
+// units in the last place; it cannot overflow): sigma(|x|) = 1 / (1 + e) and
+// sigma(-|x|) = e / (1 + e).  The reciprocal of 1 + e, which lies in [1, 2],
+// is __fdividef's (at most 2 units in the last place there); the result is
+// then within about 6 units in the last place of x sigma(x).
+__device__ __forceinline__ float silu(float x)
+{
+    const float e = expf(-fabsf(x));
+    const float r = __fdividef(1.0f, 1.0f + e);
+    return x * (x >= 0.0f ? r : e * r);
+}
+
+// Stores 8 consecutive fp32 values at element 8 unit of `out`, as fp32 or
+// rounded to bf16 (nearest, ties to even).
+template <bool BF16OUT> __device__ __forceinline__ void store_unit(const float2 (&v)[4], void *out, int64_t unit)
+{
     if constexpr (BF16OUT) {
         stg128_stream(static_cast<uint16_t *>(out) + 8 * unit,
                       make_uint4(f32x2_to_bf16x2(v[0].x, v[0].y), f32x2_to_bf16x2(v[1].x, v[1].y),
@@ -194,7 +217,20 @@ __device__ __forceinline__ void decode_store_unit(const UnitBits &u, float m, vo
     }
 }
 
-template <int BITS, int NB, bool BF16OUT>
+template <int BITS, bool BF16OUT, int OP>
+__device__ __forceinline__ void decode_store_unit(const UnitBits &u, float m, void *out, int64_t unit)
+{
+    float2 v[4];
+    decode_unit<BITS>(u, m, v);
+    if constexpr (OP == kOpSilu) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = make_float2(silu(v[i].x), silu(v[i].y));
+    }
+    store_unit<BF16OUT>(v, out, unit);
+}
+
+template <int BITS, int NB, bool BF16OUT, int OP>
 __global__ void __launch_bounds__(kLThreads)
     laaq_dequantize_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale, int64_t n,
                            void *__restrict__ out)
@@ -276,7 +312,84 @@ __global__ void __launch_bounds__(kLThreads)
         for (int k = 0; k < 4; ++k) {
             const int64_t u = u0 + 32 * k + lane;
             if (full || u < units)
-                decode_store_unit<BITS, BF16OUT>(w[k], m[k], out, u);
+                decode_store_unit<BITS, BF16OUT, OP>(w[k], m[k], out, u);
+        }
+    }
+}
+
+// RMSNorm recomputed from the stored quantised input (AGoQ 2.A): rows of d
+// values (d a multiple of the block, so a row holds whole blocks), one warp
+// per row and two passes over the row's packed codes.  Pass 1: the sum of
+// x_hat^2, each 8-code unit as a chain of fused multiply-adds, the units of
+// a lane in a compensated (Kahan) sum, the lanes by shuffles; pass 2:
+// y = x_hat * (1 / sqrt(sum / d + eps)) * g, with IEEE square root and
+// division.  The row's codes are re-read in pass 2 from L1 / L2.
+//
+// A unit of 8 codes is BITS bytes at byte 8 BITS u / 8 of the stream: one
+// aligned word (4 bits) or two (8 bits); at 5 and 6 bits it starts inside a
+// word and spans at most two aligned words (the second read only while it is
+// inside the stream).
+template <int BITS> __device__ __forceinline__ UnitBits load_unit(const uint8_t *packed, int64_t u, int64_t nbytes)
+{
+    if constexpr (BITS == 4) {
+        return {__ldg(reinterpret_cast<const uint32_t *>(packed) + u), 0u};
+    } else if constexpr (BITS == 8) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(packed) + u);
+        return {v.x, v.y};
+    } else {
+        const int64_t byte = u * BITS, a = byte & ~int64_t(3);
+        const uint32_t sh = 8u * static_cast<uint32_t>(byte & 3);
+        const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(packed + a));
+        const uint32_t w1 = a + 4 < nbytes ? __ldg(reinterpret_cast<const uint32_t *>(packed + a + 4)) : 0u;
+        return {__funnelshift_r(w0, w1, sh), w1 >> sh};
+    }
+}
+
+template <int BITS, int NB, bool BF16OUT>
+__global__ void __launch_bounds__(kLThreads)
+    laaq_rmsnorm_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale, int64_t rows,
+                        int64_t d, const float *__restrict__ gamma, float eps, void *__restrict__ out)
+{
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t upr = d / 8;  // units per row
+    const int64_t nbytes = rows * d * BITS / 8;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kLThreads / 32);
+    const float inv_d = 1.0f / static_cast<float>(d);
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (kLThreads / 32) + (threadIdx.x >> 5); r < rows;
+         r += nwarps) {
+        const int64_t u0 = r * upr;
+        float sum = 0.0f, comp = 0.0f;  // Kahan: sum + comp carries the lane's total
+#pragma unroll 4
+        for (int64_t j = lane; j < upr; j += 32) {
+            float2 v[4];
+            decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+            float t = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                t = fmaf(v[i].x, v[i].x, t);
+                t = fmaf(v[i].y, v[i].y, t);
+            }
+            const float yk = t - comp;
+            const float tk = sum + yk;
+            comp = (tk - sum) - yk;
+            sum = tk;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const float inv = 1.0f / sqrtf(sum * inv_d + eps);
+#pragma unroll 4
+        for (int64_t j = lane; j < upr; j += 32) {
+            float2 v[4];
+            decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * j));
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * j + 4));
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = make_float2(v[i].x * inv * g[2 * i], v[i].y * inv * g[2 * i + 1]);
+            store_unit<BF16OUT>(v, out, u0 + j);
         }
     }
 }
@@ -316,22 +429,26 @@ cudaError_t run_quantize(const void *x, int64_t n, uint8_t *packed, float *scale
     return run_quantize_w<BITS, NB, false>(x, n, packed, scale, st);
 }
 
-template <int BITS, int NB>
-cudaError_t run_dequantize(const uint8_t *packed, const float *scale, int64_t n, void *out, bool bf16,
-                           cudaStream_t st)
+template <int BITS, int NB, bool BF16OUT, int OP>
+cudaError_t run_dequantize_k(const uint8_t *packed, const float *scale, int64_t n, void *out, cudaStream_t st)
 {
     int grid = 0;
     const int64_t lanes = (n / 8 + kTileUnits - 1) / kTileUnits * 32;  // one warp per tile
-    if (bf16) {
-        cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, true>, lanes, &grid);
-        if (e != cudaSuccess)
-            return e;
-        return launch_pdl(laaq_dequantize_kernel<BITS, NB, true>, grid, kLThreads, 0, st, packed, scale, n, out);
-    }
-    cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, false>, lanes, &grid);
+    cudaError_t e = laaq_grid(laaq_dequantize_kernel<BITS, NB, BF16OUT, OP>, lanes, &grid);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(laaq_dequantize_kernel<BITS, NB, false>, grid, kLThreads, 0, st, packed, scale, n, out);
+    return launch_pdl(laaq_dequantize_kernel<BITS, NB, BF16OUT, OP>, grid, kLThreads, 0, st, packed, scale, n, out);
+}
+
+template <int BITS, int NB>
+cudaError_t run_dequantize(const uint8_t *packed, const float *scale, int64_t n, void *out, bool bf16, int op,
+                           cudaStream_t st)
+{
+    if (op == kOpSilu)
+        return bf16 ? run_dequantize_k<BITS, NB, true, kOpSilu>(packed, scale, n, out, st)
+                    : run_dequantize_k<BITS, NB, false, kOpSilu>(packed, scale, n, out, st);
+    return bf16 ? run_dequantize_k<BITS, NB, true, kOpNone>(packed, scale, n, out, st)
+                : run_dequantize_k<BITS, NB, false, kOpNone>(packed, scale, n, out, st);
 }
 
 template <int BITS>
@@ -351,17 +468,17 @@ cudaError_t quantize_nb(int block, const void *x, int64_t n, uint8_t *packed, fl
 
 template <int BITS>
 cudaError_t dequantize_nb(int block, const uint8_t *packed, const float *scale, int64_t n, void *out, bool bf16,
-                          cudaStream_t st)
+                          int op, cudaStream_t st)
 {
     switch (block) {
     case 32:
-        return run_dequantize<BITS, 32>(packed, scale, n, out, bf16, st);
+        return run_dequantize<BITS, 32>(packed, scale, n, out, bf16, op, st);
     case 64:
-        return run_dequantize<BITS, 64>(packed, scale, n, out, bf16, st);
+        return run_dequantize<BITS, 64>(packed, scale, n, out, bf16, op, st);
     case 128:
-        return run_dequantize<BITS, 128>(packed, scale, n, out, bf16, st);
+        return run_dequantize<BITS, 128>(packed, scale, n, out, bf16, op, st);
     default:
-        return run_dequantize<BITS, 256>(packed, scale, n, out, bf16, st);
+        return run_dequantize<BITS, 256>(packed, scale, n, out, bf16, op, st);
     }
 }
 
@@ -382,18 +499,75 @@ cudaError_t launch_laaq_quantize(const void *x_bf16, int64_t n, int block, int b
     }
 }
 
-cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
-                                   void *out, bool out_bf16, cudaStream_t stream)
+namespace {
+
+template <int BITS, int NB, bool BF16OUT>
+cudaError_t run_rmsnorm_k(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, const float *gamma,
+                          float eps, void *out, cudaStream_t st)
+{
+    int grid = 0;
+    cudaError_t e = laaq_grid(laaq_rmsnorm_kernel<BITS, NB, BF16OUT>, rows * 32, &grid);  // a warp per row
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(laaq_rmsnorm_kernel<BITS, NB, BF16OUT>, grid, kLThreads, 0, st, packed, scale, rows, d, gamma,
+                      eps, out);
+}
+
+template <int BITS, int NB>
+cudaError_t run_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, const float *gamma,
+                        float eps, void *out, bool bf16, cudaStream_t st)
+{
+    return bf16 ? run_rmsnorm_k<BITS, NB, true>(packed, scale, rows, d, gamma, eps, out, st)
+                : run_rmsnorm_k<BITS, NB, false>(packed, scale, rows, d, gamma, eps, out, st);
+}
+
+template <int BITS>
+cudaError_t rmsnorm_nb(int block, const uint8_t *packed, const float *scale, int64_t rows, int64_t d,
+                       const float *gamma, float eps, void *out, bool bf16, cudaStream_t st)
+{
+    switch (block) {
+    case 32:
+        return run_rmsnorm<BITS, 32>(packed, scale, rows, d, gamma, eps, out, bf16, st);
+    case 64:
+        return run_rmsnorm<BITS, 64>(packed, scale, rows, d, gamma, eps, out, bf16, st);
+    case 128:
+        return run_rmsnorm<BITS, 128>(packed, scale, rows, d, gamma, eps, out, bf16, st);
+    default:
+        return run_rmsnorm<BITS, 256>(packed, scale, rows, d, gamma, eps, out, bf16, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_laaq_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, int block,
+                                int bits, const float *gamma, float eps, void *out, bool out_bf16,
+                                cudaStream_t stream)
 {
     switch (bits) {
     case 4:
-        return dequantize_nb<4>(block, packed, scale, n, out, out_bf16, stream);
+        return rmsnorm_nb<4>(block, packed, scale, rows, d, gamma, eps, out, out_bf16, stream);
     case 5:
-        return dequantize_nb<5>(block, packed, scale, n, out, out_bf16, stream);
+        return rmsnorm_nb<5>(block, packed, scale, rows, d, gamma, eps, out, out_bf16, stream);
     case 6:
-        return dequantize_nb<6>(block, packed, scale, n, out, out_bf16, stream);
+        return rmsnorm_nb<6>(block, packed, scale, rows, d, gamma, eps, out, out_bf16, stream);
     default:
-        return dequantize_nb<8>(block, packed, scale, n, out, out_bf16, stream);
+        return rmsnorm_nb<8>(block, packed, scale, rows, d, gamma, eps, out, out_bf16, stream);
+    }
+}
+
+cudaError_t launch_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int block, int bits,
+                                   void *out, bool out_bf16, bool silu, cudaStream_t stream)
+{
+    const int op = silu ? kOpSilu : kOpNone;
+    switch (bits) {
+    case 4:
+        return dequantize_nb<4>(block, packed, scale, n, out, out_bf16, op, stream);
+    case 5:
+        return dequantize_nb<5>(block, packed, scale, n, out, out_bf16, op, stream);
+    case 6:
+        return dequantize_nb<6>(block, packed, scale, n, out, out_bf16, op, stream);
+    default:
+        return dequantize_nb<8>(block, packed, scale, n, out, out_bf16, op, stream);
     }
 }
 

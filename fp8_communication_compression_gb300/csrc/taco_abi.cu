@@ -4,6 +4,7 @@
 // calls are the exception their declarations state: a pipeline owns CUDA
 // streams and events, and one run enqueues copies and launches per chunk.
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -343,12 +344,11 @@ taco_status agoq_laaq_quantize(const void *x_bf16, int64_t n, int32_t block, int
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
-taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
-                                 int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream)
+// Shared checks of the dequantizing entry points: the stream, its
+// multipliers and an output of n fp32 or bf16 values that overlaps neither.
+static taco_status check_laaq_out(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
+                                  int32_t bits, const void *out, int32_t out_is_bf16)
 {
-    taco_status st = check_laaq(n, block, bits);
-    if (st != TACO_OK || n == 0)
-        return st;
     if (!packed || !scale || !out)
         return TACO_ERR_INVALID_ARG;
     if (!aligned(packed, 16) || !aligned(scale, 4) || !aligned(out, 16))
@@ -357,8 +357,59 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
     const uint64_t ob = static_cast<uint64_t>(n) * (out_is_bf16 ? 2 : 4);
     if (overlap(out, ob, packed, pb) || overlap(out, ob, scale, 4 * nb))
         return TACO_ERR_INVALID_ARG;
-    return from_cuda(taco::launch_laaq_dequantize(packed, scale, n, block, bits, out, out_is_bf16 != 0,
+    return TACO_OK;
+}
+
+taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
+                                 int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream)
+{
+    taco_status st = check_laaq(n, block, bits);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if ((st = check_laaq_out(packed, scale, n, block, bits, out, out_is_bf16)) != TACO_OK)
+        return st;
+    return from_cuda(taco::launch_laaq_dequantize(packed, scale, n, block, bits, out, out_is_bf16 != 0, false,
                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_laaq_dequantize_silu(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
+                                      int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream)
+{
+    taco_status st = check_laaq(n, block, bits);
+    if (st != TACO_OK || n == 0)
+        return st;
+    if ((st = check_laaq_out(packed, scale, n, block, bits, out, out_is_bf16)) != TACO_OK)
+        return st;
+    return from_cuda(taco::launch_laaq_dequantize(packed, scale, n, block, bits, out, out_is_bf16 != 0, true,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+taco_status agoq_laaq_dequantize_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d,
+                                         int32_t block, int32_t bits, const float *gamma, float eps, void *out,
+                                         int32_t out_is_bf16, taco_stream_t stream)
+{
+    if (rows < 0 || d < 0 || !(eps >= 0.0f) || !(eps <= FLT_MAX))
+        return TACO_ERR_INVALID_ARG;
+    if (d > (int64_t(1) << 31) || (d > 0 && rows > INT64_MAX / 8 / d))
+        return TACO_ERR_UNSUPPORTED;
+    const int64_t n = rows * d;
+    taco_status st = check_laaq(n, block, bits);
+    if (st != TACO_OK)
+        return st;
+    if (rows == 0 || d == 0)
+        return TACO_OK;
+    if (d % block != 0)
+        return TACO_ERR_INVALID_ARG;
+    if ((st = check_laaq_out(packed, scale, n, block, bits, out, out_is_bf16)) != TACO_OK)
+        return st;
+    if (!gamma)
+        return TACO_ERR_INVALID_ARG;
+    if (!aligned(gamma, 16))
+        return TACO_ERR_MISALIGNED;
+    if (overlap(out, static_cast<uint64_t>(n) * (out_is_bf16 ? 2 : 4), gamma, 4 * static_cast<uint64_t>(d)))
+        return TACO_ERR_INVALID_ARG;
+    return from_cuda(taco::launch_laaq_rmsnorm(packed, scale, rows, d, block, bits, gamma, eps, out, out_is_bf16 != 0,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // The GEMM shapes the tensor-core kernel takes (M, N > 0).

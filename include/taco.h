@@ -236,6 +236,34 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
                                  taco_stream_t stream);
 
 /*
+ * agoq_laaq_dequantize_silu / agoq_laaq_dequantize_rmsnorm - an operator's
+ * output recomputed from its stored quantised input ([AGoQ] 2.A: for
+ * RMSNorm and SiLU, storing only the 4-bit input and recomputing the
+ * intermediate values in the backward pass bounds the error more tightly
+ * than caching quantised intermediates).  x_hat is the value
+ * agoq_laaq_dequantize gives (fp32); then, in fp32,
+ *   silu:     out = x_hat / (1 + exp(-x_hat)), computed as x_hat sigma(x_hat)
+ *             from exp(-|x_hat|) (no overflow)
+ *   rmsnorm:  per row of d values, out = x_hat / sqrt(mean(x_hat^2) + eps)
+ *             * gamma (the sum of squares taken with compensated fp32
+ *             addition)
+ * Results are within a few units in the last fp32 place of the exact
+ * operator on x_hat (not bit-reproducible against another implementation:
+ * exp and the order of the sum are the library's).
+ *
+ *  packed, scale, block, bits, out, out_is_bf16   as for agoq_laaq_dequantize
+ *  n                    (silu) elements, n % block == 0
+ *  rows, d              (rmsnorm) the tensor [rows][d]; d % block == 0
+ *  gamma        in      (rmsnorm) fp32 [d], 16-byte aligned
+ *  eps                  (rmsnorm) eps >= 0, finite
+ */
+taco_status agoq_laaq_dequantize_silu(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
+                                      int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream);
+taco_status agoq_laaq_dequantize_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d,
+                                         int32_t block, int32_t bits, const float *gamma, float eps, void *out,
+                                         int32_t out_is_bf16, taco_stream_t stream);
+
+/*
  * taco_e4m3_encode - the compressor's FP8 encoder on its own ([TACO] 2.A:
  * the E4M3 format of the codes; 2.B.2: codes are taken with saturation at
  * the largest finite value).  codes[i] = E4M3FN(x[i]): round to nearest,

@@ -161,6 +161,26 @@ def test_laaq_validation(lib):
     assert d(n=0) == OK
 
 
+def test_laaq_recompute_validation(lib):
+    s = lambda n=1024, block=128, bits=4, out=A * 16, bf=1: lib.agoq_laaq_dequantize_silu(
+        A * 4, A * 8, n, block, bits, out, bf, None)
+    assert s(bits=3) == UNSUPPORTED and s(block=16) == UNSUPPORTED
+    assert s(n=1000) == INVALID and s(n=-128) == INVALID
+    assert s(n=0) == OK
+    assert s(out=0) == INVALID and s(out=A * 16 + 8) == MISALIGNED
+    assert s(out=A * 4) == INVALID  # output over the packed codes
+    r = lambda rows=8, d=256, block=128, bits=4, g=A * 32, eps=1e-6, out=A * 16, bf=0: \
+        lib.agoq_laaq_dequantize_rmsnorm(A * 4, A * 8, rows, d, block, bits, g, eps, out, bf, None)
+    assert r(bits=7) == UNSUPPORTED and r(block=512) == UNSUPPORTED
+    assert r(d=192) == INVALID                     # rows of 192 hold 1.5 blocks of 128
+    assert r(rows=-1) == INVALID and r(eps=-1.0) == INVALID and r(eps=float("nan")) == INVALID
+    assert r(eps=float("inf")) == INVALID
+    assert r(rows=0) == OK and r(d=0) == OK
+    assert r(g=0) == INVALID and r(g=A * 32 + 4) == MISALIGNED
+    assert r(g=A * 16 + 64) == INVALID             # gamma inside the output
+    assert r(out=A * 8) == INVALID                 # output over the multipliers
+
+
 def test_e4m3_encode_validation(lib):
     f = lambda n=1024, x=A, c=A * 8: lib.taco_e4m3_encode(x, n, c, None)
     assert f(n=-1) == INVALID

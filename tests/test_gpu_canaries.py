@@ -213,3 +213,20 @@ def test_gemm_laaq_quantize_writes_stay_inside_their_outputs(M, N, K, bits):
     api.agoq_gemm_laaq_quantize(a, b, bits, packed=p, scale=sc, workspace=ws)
     assert gp.intact() and gs.intact() and (gw is None or gw.intact())
     assert torch.equal(a, a0) and torch.equal(b, b0)
+
+
+@pytest.mark.parametrize("bits,block,rows,d", [(4, 128, 37, 512), (5, 32, 9, 96), (6, 256, 5, 768)])
+def test_laaq_recompute_writes_stay_inside_their_outputs(bits, block, rows, d):
+    n = rows * d
+    x = activation(41, rows, d, block).reshape(-1)
+    packed, scale = api.agoq_laaq_quantize(x, block, bits)
+    p0, s0 = packed.clone(), scale.clone()
+    g = torch.linspace(0.5, 1.5, d, device="cuda")
+    for dt in (torch.float32, torch.bfloat16):
+        go, o = guarded(dt, (n,))
+        api.agoq_laaq_dequantize_silu(packed, scale, n, block, bits, out=o)
+        assert go.intact()
+        go, o = guarded(dt, (rows, d))
+        api.agoq_laaq_dequantize_rmsnorm(packed, scale, rows, d, g, 1e-6, block, bits, out=o)
+        assert go.intact()
+    assert torch.equal(packed, p0) and torch.equal(scale, s0)

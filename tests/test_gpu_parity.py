@@ -340,6 +340,93 @@ def test_laaq_quantize_of_an_input_16_but_not_32_byte_aligned(bits, block):
     assert np.array_equal(to_host(scale), rs)
 
 
+# SiLU and RMSNorm recomputed from the stored quantised input (AGoQ 2.A).
+# The GPU computes in fp32 (expf within 2 units in the last place, IEEE
+# division and square root; the RMSNorm sum of squares compensated), the
+# oracle in double on the same dequantised values, so the bar is the
+# reconstruction bar, 1e-6 relative per element; bf16 outputs within 2^-8
+# relative (half a bf16 step plus the fp32 error).
+RECOMPUTE_RTOL = 1e-6
+BF16_RTOL = 2.0 ** -8
+
+
+def _stored_on_gpu(x_bits, block, bits):
+    packed, scale = api.agoq_laaq_quantize(to_dev_bf16(x_bits).reshape(-1), block, bits)
+    rp, rs = oracle.laaq_quantize(x_bits, block, bits)
+    assert np.array_equal(to_host(packed), rp) and np.array_equal(to_host(scale), rs)
+    return packed, scale, rp, rs
+
+
+def _assert_close(got, ref, rtol, what):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    bad = err > rtol * np.abs(ref) + 1e-30
+    assert not bad.any(), f"{what}: {int(bad.sum())} values off, worst {float((err / np.maximum(np.abs(ref), 1e-300)).max()):.3g}"
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("block", [32, 128, 256])
+def test_laaq_silu_recompute_matches_the_oracle(bits, block):
+    n = 96 * 1024 + 3 * 256
+    x = W.tp_activation(560 + bits, n // 256, 256, channel_scale=True, zero_blocks=(2,), block=block)
+    packed, scale, rp, rs = _stored_on_gpu(x, block, bits)
+    ref = oracle.laaq_dequantize_silu(rp, rs, n, block, bits)
+    out32 = api.agoq_laaq_dequantize_silu(packed, scale, n, block, bits, out_dtype=torch.float32)
+    _assert_close(to_host(out32), ref, RECOMPUTE_RTOL, f"silu fp32, {bits} bits, block {block}")
+    out16 = api.agoq_laaq_dequantize_silu(packed, scale, n, block, bits, out_dtype=torch.bfloat16)
+    _assert_close(to_host(out16.float()), ref, BF16_RTOL, f"silu bf16, {bits} bits, block {block}")
+
+
+def test_laaq_silu_recompute_over_the_whole_range():
+    """Inputs spread over [-120, 120]: SiLU's saturation on both sides, and
+    values below -88 where exp(-x) overflows fp32 (the result is then -0,
+    within 1e-30 of the exact value)."""
+    n = 64 * 1024
+    v = np.random.default_rng(7).uniform(-120.0, 120.0, n).astype(np.float32)
+    x = W.f32_to_bf16_bits(v)
+    packed, scale, rp, rs = _stored_on_gpu(x, 128, 8)
+    ref = oracle.laaq_dequantize_silu(rp, rs, n, 128, 8)
+    out = api.agoq_laaq_dequantize_silu(packed, scale, n, 128, 8, out_dtype=torch.float32)
+    _assert_close(to_host(out), ref, RECOMPUTE_RTOL, "silu over [-120, 120]")
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("block,d", [(128, 4096), (32, 96), (256, 5120), (64, 1088)])
+def test_laaq_rmsnorm_recompute_matches_the_oracle(bits, block, d):
+    """37 rows (not a multiple of the 8 warps of a CTA), row lengths from 96
+    to 5120, rows that are all zero."""
+    rows = 37
+    x = W.tp_activation(580 + bits, rows, d, channel_scale=True, zero_blocks=(3,), block=block)
+    x[5] = 0
+    packed, scale, rp, rs = _stored_on_gpu(x, block, bits)
+    g = (1.0 + 0.5 * np.sin(np.arange(d))).astype(np.float32)
+    ref = oracle.laaq_dequantize_rmsnorm(rp, rs, rows, d, g, 1e-6, block, bits)
+    gd = torch.from_numpy(g).cuda()
+    out32 = api.agoq_laaq_dequantize_rmsnorm(packed, scale, rows, d, gd, 1e-6, block, bits,
+                                             out_dtype=torch.float32)
+    _assert_close(to_host(out32), ref, RECOMPUTE_RTOL, f"rmsnorm fp32, {bits} bits, block {block}, d {d}")
+    assert np.all(to_host(out32)[5] == 0)
+    out16 = api.agoq_laaq_dequantize_rmsnorm(packed, scale, rows, d, gd, 1e-6, block, bits,
+                                             out_dtype=torch.bfloat16)
+    _assert_close(to_host(out16.float()), ref, BF16_RTOL, f"rmsnorm bf16, {bits} bits")
+
+
+def test_laaq_recompute_full_size_4_bits():
+    """A GPT-6.7B-sized activation [8192, 4096] stored in 4 bits: SiLU and
+    RMSNorm recomputed, every element against the oracle."""
+    rows, d = 8192, 4096
+    x = W.tp_activation(599, rows, d, channel_scale=True, block=128)
+    packed, scale, rp, rs = _stored_on_gpu(x, 128, 4)
+    out = api.agoq_laaq_dequantize_silu(packed, scale, rows * d, 128, 4, out_dtype=torch.float32)
+    _assert_close(to_host(out), oracle.laaq_dequantize_silu(rp, rs, rows * d, 128, 4), RECOMPUTE_RTOL,
+                  "silu full size")
+    g = np.ones(d, np.float32)
+    out = api.agoq_laaq_dequantize_rmsnorm(packed, scale, rows, d, torch.from_numpy(g).cuda(), 1e-6, 128, 4,
+                                           out_dtype=torch.float32)
+    _assert_close(to_host(out), oracle.laaq_dequantize_rmsnorm(rp, rs, rows, d, g, 1e-6, 128, 4),
+                  RECOMPUTE_RTOL, "rmsnorm full size")
+
+
 @pytest.mark.parametrize("bits,block", [(4, 128), (5, 32), (6, 256), (8, 64)])
 def test_laaq_codec_many_slots_per_lane(bits, block):
     """8.4 M elements: more lanes than one grid holds, so each lane takes
