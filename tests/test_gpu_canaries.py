@@ -215,7 +215,7 @@ def test_gemm_laaq_quantize_writes_stay_inside_their_outputs(M, N, K, bits):
     assert torch.equal(a, a0) and torch.equal(b, b0)
 
 
-@pytest.mark.parametrize("bits,block,rows,d", [(4, 128, 37, 512), (5, 32, 9, 96), (6, 256, 5, 768)])
+@pytest.mark.parametrize("bits,block,rows,d", [(4, 128, 37, 512), (5, 32, 9, 96), (6, 256, 5, 768), (8, 128, 7, 2048)])
 def test_laaq_recompute_writes_stay_inside_their_outputs(bits, block, rows, d):
     n = rows * d
     x = activation(41, rows, d, block).reshape(-1)
