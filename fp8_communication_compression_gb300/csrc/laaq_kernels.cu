@@ -319,11 +319,13 @@ __global__ void __launch_bounds__(kLThreads)
 
 // RMSNorm recomputed from the stored quantised input (AGoQ 2.A): rows of d
 // values (d a multiple of the block, so a row holds whole blocks), one warp
-// per row and two passes over the row's packed codes.  Pass 1: the sum of
-// x_hat^2, each 8-code unit as a chain of fused multiply-adds, the units of
-// a lane in a compensated (Kahan) sum, the lanes by shuffles; pass 2:
+// per row and two passes over the row's values.  Pass 1: the sum of x_hat^2,
+// each 8-code unit as a chain of fused multiply-adds, the units of a lane in
+// a compensated (Kahan) sum, the lanes by shuffles; pass 2:
 // y = x_hat * (1 / sqrt(sum / d + eps)) * g, with IEEE square root and
-// division.  The row's codes are re-read in pass 2 from L1 / L2.
+// division.  A lane loads all its units of a row at once and keeps the
+// packed words for pass 2 (UPL units at most); longer rows re-read their
+// codes in pass 2 from L1 / L2 (UPL = 0).
 //
 // A unit of 8 codes is BITS bytes at byte 8 BITS u / 8 of the stream: one
 // aligned word (4 bits) or two (8 bits); at 5 and 6 bits it starts inside a
@@ -345,7 +347,7 @@ template <int BITS> __device__ __forceinline__ UnitBits load_unit(const uint8_t 
     }
 }
 
-template <int BITS, int NB, bool BF16OUT>
+template <int BITS, int NB, bool BF16OUT, int UPL>
 __global__ void __launch_bounds__(kLThreads)
     laaq_rmsnorm_kernel(const uint8_t *__restrict__ packed, const float *__restrict__ scale, int64_t rows,
                         int64_t d, const float *__restrict__ gamma, float eps, void *__restrict__ out)
@@ -360,10 +362,7 @@ __global__ void __launch_bounds__(kLThreads)
          r += nwarps) {
         const int64_t u0 = r * upr;
         float sum = 0.0f, comp = 0.0f;  // Kahan: sum + comp carries the lane's total
-#pragma unroll 4
-        for (int64_t j = lane; j < upr; j += 32) {
-            float2 v[4];
-            decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+        auto add_unit = [&](const float2 (&v)[4]) {
             float t = 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -374,15 +373,8 @@ __global__ void __launch_bounds__(kLThreads)
             const float tk = sum + yk;
             comp = (tk - sum) - yk;
             sum = tk;
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        const float inv = 1.0f / sqrtf(sum * inv_d + eps);
-#pragma unroll 4
-        for (int64_t j = lane; j < upr; j += 32) {
-            float2 v[4];
-            decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+        };
+        auto store_scaled = [&](float2 (&v)[4], int64_t j, float inv) {
             const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * j));
             const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + 8 * j + 4));
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
@@ -390,6 +382,61 @@ __global__ void __launch_bounds__(kLThreads)
             for (int i = 0; i < 4; ++i)
                 v[i] = make_float2(v[i].x * inv * g[2 * i], v[i].y * inv * g[2 * i + 1]);
             store_unit<BF16OUT>(v, out, u0 + j);
+        };
+        if constexpr (UPL > 0) {
+            // the lane's units of the row (at most UPL), loaded at once and
+            // kept as packed words for both passes
+            UnitBits w[UPL];
+            float m[UPL];
+#pragma unroll
+            for (int k = 0; k < UPL; ++k) {
+                const int64_t j = lane + 32 * k;
+                w[k] = {0u, 0u};
+                m[k] = 0.0f;
+                if (j < upr) {
+                    w[k] = load_unit<BITS>(packed, u0 + j, nbytes);
+                    m[k] = __ldg(scale + (u0 + j) / (NB / 8));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < UPL; ++k) {
+                if (lane + 32 * k < upr) {
+                    float2 v[4];
+                    decode_unit<BITS>(w[k], m[k], v);
+                    add_unit(v);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+            const float inv = 1.0f / sqrtf(sum * inv_d + eps);
+#pragma unroll
+            for (int k = 0; k < UPL; ++k) {
+                const int64_t j = lane + 32 * k;
+                if (j < upr) {
+                    float2 v[4];
+                    decode_unit<BITS>(w[k], m[k], v);
+                    store_scaled(v, j, inv);
+                }
+            }
+        } else {
+            // long rows: two passes over the row's codes (the second from L1 / L2)
+#pragma unroll 4
+            for (int64_t j = lane; j < upr; j += 32) {
+                float2 v[4];
+                decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+                add_unit(v);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+            const float inv = 1.0f / sqrtf(sum * inv_d + eps);
+#pragma unroll 4
+            for (int64_t j = lane; j < upr; j += 32) {
+                float2 v[4];
+                decode_unit<BITS>(load_unit<BITS>(packed, u0 + j, nbytes), __ldg(scale + (u0 + j) / (NB / 8)), v);
+                store_scaled(v, j, inv);
+            }
         }
     }
 }
@@ -501,24 +548,39 @@ cudaError_t launch_laaq_quantize(const void *x_bf16, int64_t n, int block, int b
 
 namespace {
 
-template <int BITS, int NB, bool BF16OUT>
+template <int BITS, int NB, bool BF16OUT, int UPL>
 cudaError_t run_rmsnorm_k(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, const float *gamma,
                           float eps, void *out, cudaStream_t st)
 {
     int grid = 0;
-    cudaError_t e = laaq_grid(laaq_rmsnorm_kernel<BITS, NB, BF16OUT>, rows * 32, &grid);  // a warp per row
+    cudaError_t e = laaq_grid(laaq_rmsnorm_kernel<BITS, NB, BF16OUT, UPL>, rows * 32, &grid);  // a warp per row
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(laaq_rmsnorm_kernel<BITS, NB, BF16OUT>, grid, kLThreads, 0, st, packed, scale, rows, d, gamma,
-                      eps, out);
+    return launch_pdl(laaq_rmsnorm_kernel<BITS, NB, BF16OUT, UPL>, grid, kLThreads, 0, st, packed, scale, rows, d,
+                      gamma, eps, out);
+}
+
+// Rows of up to 16 units a lane (4096 values) keep their packed words in
+// registers (4 or 16 units a lane); longer rows take two passes.  Measured
+// at [8192, 4096], 4 bits: 20.9 us, against 22.6 us in two passes.
+template <int BITS, int NB, bool BF16OUT>
+cudaError_t run_rmsnorm_b(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, const float *gamma,
+                          float eps, void *out, cudaStream_t st)
+{
+    const int64_t upl = (d / 8 + 31) / 32;
+    if (upl <= 4)
+        return run_rmsnorm_k<BITS, NB, BF16OUT, 4>(packed, scale, rows, d, gamma, eps, out, st);
+    if (upl <= 16)
+        return run_rmsnorm_k<BITS, NB, BF16OUT, 16>(packed, scale, rows, d, gamma, eps, out, st);
+    return run_rmsnorm_k<BITS, NB, BF16OUT, 0>(packed, scale, rows, d, gamma, eps, out, st);
 }
 
 template <int BITS, int NB>
 cudaError_t run_rmsnorm(const uint8_t *packed, const float *scale, int64_t rows, int64_t d, const float *gamma,
                         float eps, void *out, bool bf16, cudaStream_t st)
 {
-    return bf16 ? run_rmsnorm_k<BITS, NB, true>(packed, scale, rows, d, gamma, eps, out, st)
-                : run_rmsnorm_k<BITS, NB, false>(packed, scale, rows, d, gamma, eps, out, st);
+    return bf16 ? run_rmsnorm_b<BITS, NB, true>(packed, scale, rows, d, gamma, eps, out, st)
+                : run_rmsnorm_b<BITS, NB, false>(packed, scale, rows, d, gamma, eps, out, st);
 }
 
 template <int BITS>
