@@ -84,3 +84,23 @@ def test_gemm_exchange_on_one_rank_equals_the_local_path(nccl_group, rows, d, K,
     ref = api.taco_decompress(rc, ra, rs, 128)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+
+
+def test_agoq_exchange_of_gradients_accumulated_by_the_gemm(nccl_group):
+    """The AGoQ path end to end on one rank: two micro-batches' weight
+    gradients accumulated by the GEMM with the FP8 accumulation in its
+    epilogue, straight into the exchange's send buffer (AgoqAllReduce.codes
+    and .scale viewed as the [M, N] gradient), then the All-to-All, FP32
+    reduce and All-Gather.  With one rank the result is the reduce of that
+    buffer, bit for bit."""
+    M, N, K = 256, 512, 256
+    ar = exchange.AgoqAllReduce(M * N, 128)
+    for step in range(2):
+        a = to_dev_bf16(W.agoq_grad(40 + step, M * K).reshape(M, K))
+        b = to_dev_bf16(W.tp_activation(50 + step, N, K, channel_scale=True))
+        api.agoq_gemm_accumulate(a, b, ar.codes.view(M, N), ar.scale)
+    c, s = ar.run()
+    rc, rs = api.agoq_reduce_shards([ar.codes], [ar.scale], 128)
+    torch.cuda.synchronize()
+    assert torch.equal(c, rc) and torch.equal(s, rs)
+    assert int((rc != 0).sum()) > 0
