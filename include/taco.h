@@ -255,7 +255,8 @@ taco_status agoq_laaq_dequantize(const uint8_t *packed, const float *scale, int6
  *  n                    (silu) elements, n % block == 0
  *  rows, d              (rmsnorm) the tensor [rows][d]; d % block == 0
  *  gamma        in      (rmsnorm) fp32 [d], 16-byte aligned
- *  eps                  (rmsnorm) eps >= 0, finite
+ *  eps                  (rmsnorm) eps >= 0, finite; with eps = 0 a row of zeros
+ *                       gives NaN (0 / 0), as the formula does
  */
 taco_status agoq_laaq_dequantize_silu(const uint8_t *packed, const float *scale, int64_t n, int32_t block,
                                       int32_t bits, void *out, int32_t out_is_bf16, taco_stream_t stream);
