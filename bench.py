@@ -983,7 +983,7 @@ def main():
     ap.add_argument("--kernel-samples", type=int, default=60,
                     help="steps of the per-kernel sampling phase after the timed region")
     ap.add_argument("--e2e-chunks", type=int, default=4, help="row chunks of the host pipeline")
-    ap.add_argument("--e2e-blocks", type=int, default=5, help="timed blocks of the end-to-end leg (median reported)")
+    ap.add_argument("--e2e-blocks", type=int, default=9, help="timed blocks of the end-to-end leg (median reported)")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="single-thread oracle sample rows per shard")
     ap.add_argument("--ref-rows", type=int, default=1024, help="reference arm rows per shard per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
