@@ -196,13 +196,16 @@ def _check_pieces(rows, d, world, stages):
         dist.destroy_process_group()
 
 
-def test_agoq_exchange_equals_the_reduce_of_all_ranks():
-    world, n, block = 2, 37 * 128, 128  # 37 blocks: a padded last chunk
+@pytest.mark.parametrize("world,cb", [(2, 19), (3, 13)])
+def test_agoq_exchange_equals_the_reduce_of_all_ranks(world, cb):
+    """37 blocks: chunks of 19 (2 ranks) or 13 (3 ranks) blocks, the last one
+    padded with zero codes and multipliers of 1."""
+    n, block = 37 * 128, 128
     res = _run(world, ("agoq", n, None, block, 1))
     bufs = [_agoq_buffer(r, n, block) for r in range(world)]
     rc, rs = oracle.agoq_reduce([b[0] for b in bufs], [b[1] for b in bufs], block)
-    for rank, (c, s), cb, _ in res:
-        assert cb == 19
+    for rank, (c, s), got_cb, _ in res:
+        assert got_cb == cb
         assert np.array_equal(c, rc) and np.array_equal(s, rs), f"rank {rank}"
 
 
