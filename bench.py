@@ -12,14 +12,14 @@ L2 (268 MB of bf16 per step), so no L2 flush is needed between steps.
 
 Prints one JSON line (rank 0).  ``value`` is algorithmic HBM bytes moved per
 step (reads + writes of the three kernels) x steps x ranks / max-over-ranks
-time, in GB/s.  The measured path is the two-shot reduce on one GPU (P
-shards resident in its memory, the inter-GPU exchange left out), so under
-torchrun (N > 1) each rank runs an independent replica of it on its own
-data, with no data-path collective (weak scaling).  ``--exchange`` instead
-times the two-shot AllReduce across the ranks: each rank holds one
-activation of the same shape, and a step is compress, All-to-All of codes
-and scalars (NCCL), shard reduce of the received chunks, AllGather,
-decompress (on one GPU, an NCCL group of one).
+time, in GB/s.  On one GPU the step is the two-shot reduce with its P
+shards resident in that GPU's memory.  Under torchrun (N > 1), or with
+``--exchange`` on one GPU (an NCCL group of one), each rank holds one
+activation of the same shape and a step is the two-shot AllReduce across
+the ranks: compress, All-to-All of codes and scalars (NCCL), shard reduce of
+the received chunks, AllGather, decompress.  ``--replicas`` runs
+independent replicas of the one-GPU path under torchrun instead (no
+data-path collective).
 
 After the timed region, a sampling phase of a fixed number of steps (60 by
 default, whatever K is) records a CUDA event after every launch; the first
@@ -998,9 +998,10 @@ def main():
                          "the GEMM-fed exchange)")
     ap.add_argument("--fused", action="store_true",
                     help="run reduce and decompress through the one-call entry point (taco_reduce_decompress)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="under torchrun: independent replicas of the one-GPU path instead of the exchange")
     ap.add_argument("--exchange", action="store_true",
-                    help="time the two-shot AllReduce across the ranks (NCCL; one rank: a group of one) "
-                         "instead of the one-GPU path")
+                    help="run the exchange path even on one rank (an NCCL group of one)")
     ap.add_argument("--exchange-stages", type=int, default=4,
                     help="pieces per chunk in the exchange (compress and decompress overlap the collectives)")
     ap.add_argument("--rows", type=int, default=None,
@@ -1023,7 +1024,7 @@ def main():
 
     from fp8_communication_compression_gb300 import api
 
-    if args.exchange:
+    if (world > 1 and not args.replicas) or args.exchange:
         run_exchange(args, rank, world, local, pool)
         pool.shutdown()
         return
